@@ -1,0 +1,332 @@
+"""Checks that tie the fp64 oracle to something other than itself.
+
+Each ``pin_*`` function takes an oracle library handle (the real one, or a
+deliberately broken copy in the mutation test) and raises AssertionError if
+the oracle disagrees with:
+  - torch's own attention (scaled_dot_product_attention in fp64) and autograd
+    on the dense problem the sparse one reduces to when the indices list every
+    key row (the sink is an extra key column whose logit is sink_h and whose
+    value row is zero);
+  - central finite differences of L = sum(O * dO) in fp64;
+  - closed forms (one valid slot; all slots masked);
+  - invariants (slot order, masked slot == dropped slot, token-subset
+    linearity of dKV, duplicated slot == duplicated key row);
+  - brute force over every topk-subset of a tiny key set.
+The definition being pinned is that of the sparse MQA forward/backward
+interfaces on the DeepSeek-V4 kernel pages (tilelang_sparse_mla_fwd,
+tilelang_sparse_mla_bwd): per-head sink in the softmax denominator, slots
+outside [0, S_kv) masked, log2 LSE, gradients for q and the shared kv.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+import oracle
+
+LN2 = math.log(2.0)
+
+
+def _rand(shape, rng, scale=1.0):
+    return rng.standard_normal(shape) * scale
+
+
+def _perm_rows(S_kv, k, rng):
+    return rng.permutation(S_kv)[:k]
+
+
+def _dense_torch(q, kv, sink, idx, scale, need_grad=False, dout=None):
+    """Reference built from torch primitives: per token, gather the listed
+    valid key rows, append a zero key/value whose logit is forced to sink_h
+    through an additive mask, and call scaled_dot_product_attention (fp64).
+    Returns O [B,S,H,D], LSE2 [B,S,H] and, with need_grad, the gradients of
+    sum(O*dO) w.r.t. q, kv and sink (torch autograd)."""
+    B, S, H, D = q.shape
+    S_kv = kv.shape[1]
+    qt = torch.tensor(q, dtype=torch.float64, requires_grad=need_grad)
+    kvt = torch.tensor(kv, dtype=torch.float64, requires_grad=need_grad)
+    st = torch.tensor(sink, dtype=torch.float64, requires_grad=need_grad)
+    outs, lses = [], []
+    for b in range(B):
+        for s in range(S):
+            rows = [int(r) for r in idx[b, s] if 0 <= r < S_kv]
+            keys = kvt[b, rows] if rows else kvt.new_zeros((0, D))
+            keys = torch.cat([keys, kvt.new_zeros((1, D))], 0)            # [n+1, D]
+            n1 = keys.shape[0]
+            qq = qt[b, s].unsqueeze(1).unsqueeze(0)                          # [1,H,1,D]
+            kk = keys.unsqueeze(0).unsqueeze(0).expand(1, H, n1, D)
+            mask = torch.cat([kvt.new_zeros((H, n1 - 1)), st.unsqueeze(1)], 1)
+            mask = mask.unsqueeze(0).unsqueeze(2)                            # [1,H,1,n+1]
+            o = F.scaled_dot_product_attention(qq, kk, kk, attn_mask=mask, scale=scale)
+            outs.append(o[0, :, 0, :])
+            logits = torch.cat([scale * (qt[b, s] @ keys[:-1].T), st.unsqueeze(1)], 1)
+            lses.append(torch.logsumexp(logits, dim=1) / LN2)
+    O = torch.stack(outs).reshape(B, S, H, D)
+    L2 = torch.stack(lses).reshape(B, S, H)
+    grads = None
+    if need_grad:
+        loss = (O * torch.tensor(dout, dtype=torch.float64)).sum()
+        gq, gkv, gs = torch.autograd.grad(loss, [qt, kvt, st])
+        grads = (gq.numpy(), gkv.numpy(), gs.numpy())
+    return O.detach().numpy(), L2.detach().numpy(), grads
+
+
+def _close(a, b, rtol=1e-9, atol=1e-11, what=""):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    assert a.shape == b.shape, f"{what}: shape {a.shape} vs {b.shape}"
+    if not np.allclose(a, b, rtol=rtol, atol=atol):
+        err = np.max(np.abs(a - b))
+        raise AssertionError(f"{what}: max abs err {err:.3e}")
+
+
+def _tiny(rng, B=2, S=3, S_kv=5, H=2, D=4, topk=4, masked=True):
+    q = _rand((B, S, H, D), rng)
+    kv = _rand((B, S_kv, D), rng)
+    sink = _rand((H,), rng)
+    dout = _rand((B, S, H, D), rng)
+    idx = np.stack([np.stack([_perm_rows(S_kv, topk, rng) for _ in range(S)]) for _ in range(B)])
+    idx = idx.astype(np.int32)
+    if masked:
+        idx[0, 1, 0] = -1
+        idx[B - 1, S - 1, topk - 1] = S_kv
+    return q, kv, sink, idx, dout
+
+
+def pin_dense_sdpa_fwd(lib):
+    """All key rows listed, none masked: O and LSE2 equal torch's dense
+    attention with the sink column."""
+    rng = np.random.default_rng(11)
+    B, S, S_kv, H, D = 2, 3, 6, 3, 5
+    q, kv, sink = _rand((B, S, H, D), rng), _rand((B, S_kv, D), rng), _rand((H,), rng)
+    idx = np.stack([np.stack([rng.permutation(S_kv) for _ in range(S)]) for _ in range(B)])
+    idx = idx.astype(np.int32)
+    for scale in (D ** -0.5, 0.37):
+        o, l2 = oracle.fwd_f64(q, kv, sink, idx, sm_scale=scale, lib=lib)
+        O, L2, _ = _dense_torch(q, kv, sink, idx, scale)
+        _close(o.reshape(O.shape), O, what="dense O")
+        _close(l2.reshape(L2.shape), L2, what="dense LSE2")
+
+
+def pin_dense_autograd_bwd(lib):
+    """dQ, dKV and dsink equal torch autograd through the dense reference,
+    including masked slots and several tokens hitting the same rows."""
+    rng = np.random.default_rng(12)
+    q, kv, sink, idx, dout = _tiny(rng, B=2, S=4, S_kv=5, H=3, D=4, topk=4)
+    scale = 0.45
+    dq, dkv, dsink, _ = oracle.bwd_f64(q, kv, sink, idx, dout, sm_scale=scale, lib=lib)
+    _, _, (gq, gkv, gs) = _dense_torch(q, kv, sink, idx, scale, need_grad=True, dout=dout)
+    _close(dq.reshape(gq.shape), gq, what="dQ vs autograd")
+    _close(dkv, gkv, what="dKV vs autograd")
+    _close(dsink, gs, what="dsink vs autograd")
+
+
+def pin_permutation(lib):
+    """Reordering a token's slots changes nothing."""
+    rng = np.random.default_rng(13)
+    q, kv, sink, idx, dout = _tiny(rng)
+    perm = idx.copy()
+    for b in range(perm.shape[0]):
+        for s in range(perm.shape[1]):
+            perm[b, s] = perm[b, s][rng.permutation(perm.shape[2])]
+    o1, l1 = oracle.fwd_f64(q, kv, sink, idx, lib=lib)
+    o2, l2 = oracle.fwd_f64(q, kv, sink, perm, lib=lib)
+    _close(o1, o2, what="perm O")
+    _close(l1, l2, what="perm LSE")
+    r1 = oracle.bwd_f64(q, kv, sink, idx, dout, lib=lib)
+    r2 = oracle.bwd_f64(q, kv, sink, perm, dout, lib=lib)
+    for a, b, n in zip(r1, r2, ("dQ", "dKV", "dsink", "Delta")):
+        _close(a, b, what=f"perm {n}")
+
+
+def pin_masked_equals_dropped(lib):
+    """Slots with indices -1, -7, S_kv or S_kv+3 act as if absent: a row of
+    topk=6 with four masked slots equals the same two valid slots at topk=2."""
+    rng = np.random.default_rng(14)
+    B, S, S_kv, H, D = 1, 2, 5, 2, 3
+    q, kv, sink = _rand((B, S, H, D), rng), _rand((B, S_kv, D), rng), _rand((H,), rng)
+    dout = _rand((B, S, H, D), rng)
+    small = np.array([[[3, 1], [0, 4]]], np.int32)
+    big = np.array([[[-1, 3, S_kv, -7, 1, S_kv + 3], [0, S_kv, -1, 4, -2, S_kv + 9]]], np.int32)
+    a = oracle.fwd_f64(q, kv, sink, small, lib=lib)
+    b = oracle.fwd_f64(q, kv, sink, big, lib=lib)
+    _close(a[0], b[0], what="masked O")
+    _close(a[1], b[1], what="masked LSE")
+    ga = oracle.bwd_f64(q, kv, sink, small, dout, lib=lib)
+    gb = oracle.bwd_f64(q, kv, sink, big, dout, lib=lib)
+    for x, y, n in zip(ga, gb, ("dQ", "dKV", "dsink", "Delta")):
+        _close(x, y, what=f"masked {n}")
+
+
+def pin_all_masked(lib):
+    """No valid slot: O = 0, LSE2 = sink_h / ln 2, dQ = 0, nothing reaches
+    dKV, dsink = 0 (Delta = <dO, 0> = 0)."""
+    rng = np.random.default_rng(15)
+    B, S, S_kv, H, D = 1, 2, 4, 3, 5
+    q, kv, sink = _rand((B, S, H, D), rng), _rand((B, S_kv, D), rng), _rand((H,), rng) * 3
+    dout = _rand((B, S, H, D), rng)
+    idx = np.array([[[-1, S_kv, -3], [2, -1, S_kv]]], np.int32)
+    o, l2 = oracle.fwd_f64(q, kv, sink, idx, lib=lib)
+    _close(o[0], np.zeros((H, D)), what="all-masked O")
+    _close(l2[0], sink / LN2, what="all-masked LSE2")
+    dq, dkv, dsink, delta = oracle.bwd_f64(q, kv, sink, idx, dout, tokens=[0], lib=lib)
+    _close(dq, np.zeros_like(dq), what="all-masked dQ")
+    _close(dkv, np.zeros_like(dkv), what="all-masked dKV")
+    _close(dsink, np.zeros_like(dsink), what="all-masked dsink")
+    _close(delta, np.zeros_like(delta), what="all-masked Delta")
+
+
+def pin_single_slot_closed_form(lib):
+    """One valid slot r: z = c<q,k_r>, O = k_r * sigmoid(z - sink) and
+    LSE2 = log2(e^z + e^sink)."""
+    rng = np.random.default_rng(16)
+    B, S, S_kv, H, D = 1, 1, 4, 3, 6
+    q, kv, sink = _rand((B, S, H, D), rng), _rand((B, S_kv, D), rng), _rand((H,), rng)
+    r, scale = 2, 0.31
+    idx = np.array([[[-1, r, S_kv]]], np.int32)
+    o, l2 = oracle.fwd_f64(q, kv, sink, idx, sm_scale=scale, lib=lib)
+    for h in range(H):
+        z = scale * float(np.dot(q[0, 0, h], kv[0, r]))
+        sig = 1.0 / (1.0 + math.exp(-(z - sink[h])))
+        _close(o[0, h], kv[0, r] * sig, what="one-slot O")
+        _close(l2[0, h], math.log2(math.exp(z) + math.exp(sink[h])), what="one-slot LSE2")
+
+
+def pin_sink_limit(lib):
+    """sink -> -1e4 removes the sink: plain softmax over the valid logits
+    (torch.softmax) and LSE2 = log2 sum exp."""
+    rng = np.random.default_rng(17)
+    q, kv, _, idx, _ = _tiny(rng, B=1, S=3, S_kv=6, H=2, D=4, topk=5)
+    sink = np.full((2,), -1e4)
+    o, l2 = oracle.fwd_f64(q, kv, sink, idx, lib=lib)
+    D = q.shape[3]
+    for s in range(3):
+        rows = [int(r) for r in idx[0, s] if 0 <= r < 6]
+        K = torch.tensor(kv[0, rows])
+        for h in range(2):
+            z = (torch.tensor(q[0, s, h]) @ K.T) * D ** -0.5
+            p = torch.softmax(z, 0)
+            _close(o[s, h], (p @ K).numpy(), what="no-sink O")
+            _close(l2[s, h], float(torch.logsumexp(z, 0)) / LN2, what="no-sink LSE2")
+
+
+def pin_finite_differences(lib):
+    """dQ, dKV and dsink equal central differences of L = sum(O * dO)."""
+    rng = np.random.default_rng(18)
+    q, kv, sink, idx, dout = _tiny(rng, B=2, S=3, S_kv=4, H=2, D=3, topk=3)
+    scale = 0.52
+    dq, dkv, dsink, _ = oracle.bwd_f64(q, kv, sink, idx, dout, sm_scale=scale, lib=lib)
+
+    def loss(qq, kk, ss):
+        o, _ = oracle.fwd_f64(qq, kk, ss, idx, sm_scale=scale, lib=lib)
+        return float(np.sum(o.reshape(dout.shape) * dout))
+
+    eps = 1e-6
+    for arr, grad, name in ((q, dq.reshape(q.shape), "dQ"), (kv, dkv, "dKV"),
+                            (sink, dsink, "dsink")):
+        fd = np.zeros_like(arr)
+        for i in np.ndindex(arr.shape):
+            plus, minus = arr.copy(), arr.copy()
+            plus[i] += eps
+            minus[i] -= eps
+            args_p = [q, kv, sink]
+            args_m = [q, kv, sink]
+            k = {"dQ": 0, "dKV": 1, "dsink": 2}[name]
+            args_p[k], args_m[k] = plus, minus
+            fd[i] = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+        _close(grad, fd, rtol=1e-6, atol=1e-8, what=f"{name} vs finite differences")
+
+
+def pin_bruteforce_subsets(lib):
+    """Every 3-subset of 6 key rows, in a random slot order, equals dense
+    attention restricted to that subset (torch SDPA)."""
+    rng = np.random.default_rng(19)
+    B, S, S_kv, H, D = 1, 4, 6, 2, 3
+    q, kv, sink = _rand((B, S, H, D), rng), _rand((B, S_kv, D), rng), _rand((H,), rng)
+    for subset in itertools.combinations(range(S_kv), 3):
+        idx = np.stack([rng.permutation(np.array(subset)) for _ in range(S)])[None].astype(np.int32)
+        o, l2 = oracle.fwd_f64(q, kv, sink, idx, lib=lib)
+        O, L2, _ = _dense_torch(q, kv, sink, idx, D ** -0.5)
+        _close(o.reshape(O.shape), O, what=f"subset {subset} O")
+        _close(l2.reshape(L2.shape), L2, what=f"subset {subset} LSE2")
+
+
+def pin_token_subset_linearity(lib):
+    """dKV over all tokens = sum of the per-token dKVs, and a run with dO
+    zeroed outside a token sample gives the sample's dKV (the restricted-dO
+    check used for full-size parity)."""
+    rng = np.random.default_rng(20)
+    q, kv, sink, idx, dout = _tiny(rng, B=2, S=4, S_kv=5, H=2, D=3, topk=3)
+    _, dkv_all, dsink_all, _ = oracle.bwd_f64(q, kv, sink, idx, dout, lib=lib)
+    acc = np.zeros_like(dkv_all)
+    acc_s = np.zeros_like(dsink_all)
+    for t in range(8):
+        _, d1, s1, _ = oracle.bwd_f64(q, kv, sink, idx, dout, tokens=[t], lib=lib)
+        acc += d1
+        acc_s += s1
+    _close(acc, dkv_all, what="dKV linearity")
+    _close(acc_s, dsink_all, what="dsink linearity")
+    sample = [1, 6]
+    restricted = np.zeros_like(dout)
+    for t in sample:
+        restricted[t // 4, t % 4] = dout[t // 4, t % 4]
+    _, dkv_r, _, _ = oracle.bwd_f64(q, kv, sink, idx, restricted, lib=lib)
+    _, dkv_s, _, _ = oracle.bwd_f64(q, kv, sink, idx, dout, tokens=sample, lib=lib)
+    _close(dkv_r, dkv_s, what="restricted dO")
+
+
+def pin_duplicate_slot(lib):
+    """A row listed twice counts twice: equals dense attention over a key
+    list that holds that row twice; its dKV gets both slots' terms."""
+    rng = np.random.default_rng(21)
+    B, S, S_kv, H, D = 1, 1, 4, 2, 3
+    q, kv, sink = _rand((B, S, H, D), rng), _rand((B, S_kv, D), rng), _rand((H,), rng)
+    dout = _rand((B, S, H, D), rng)
+    idx = np.array([[[2, 0, 2]]], np.int32)
+    o, l2 = oracle.fwd_f64(q, kv, sink, idx, lib=lib)
+    O, L2, grads = _dense_torch(q, kv, sink, idx, D ** -0.5, need_grad=True, dout=dout)
+    _close(o.reshape(O.shape), O, what="dup O")
+    _close(l2.reshape(L2.shape), L2, what="dup LSE2")
+    dq, dkv, dsink, _ = oracle.bwd_f64(q, kv, sink, idx, dout, lib=lib)
+    _close(dq.reshape(q.shape), grads[0], what="dup dQ")
+    _close(dkv, grads[1], what="dup dKV")
+
+
+def pin_bf16_entry_matches_f64(lib):
+    """The bf16 entry points read bf16 bits exactly: on bf16-representable
+    inputs they equal the fp64 entry points bit for bit."""
+    rng = np.random.default_rng(22)
+    q, kv, sink, idx, dout = _tiny(rng)
+    tq = torch.tensor(q).to(torch.bfloat16)
+    tkv = torch.tensor(kv).to(torch.bfloat16)
+    tdo = torch.tensor(dout).to(torch.bfloat16)
+    ts = torch.tensor(sink, dtype=torch.float32)
+    o1, l1 = oracle.fwd(tq, tkv, ts, torch.tensor(idx), lib=lib)
+    o2, l2 = oracle.fwd_f64(tq.double().numpy(), tkv.double().numpy(), ts.double().numpy(), idx,
+                            lib=lib)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2), "bf16 entry differs from fp64"
+    g1 = oracle.bwd(tq, tkv, ts, torch.tensor(idx), tdo, lib=lib)
+    g2 = oracle.bwd_f64(tq.double().numpy(), tkv.double().numpy(), ts.double().numpy(), idx,
+                        tdo.double().numpy(), lib=lib)
+    for a, b in zip(g1, g2):
+        assert np.allclose(a, b, rtol=1e-14, atol=1e-15), "bf16 bwd entry differs from fp64"
+
+
+ALL_PINS = [
+    pin_dense_sdpa_fwd,
+    pin_dense_autograd_bwd,
+    pin_permutation,
+    pin_masked_equals_dropped,
+    pin_all_masked,
+    pin_single_slot_closed_form,
+    pin_sink_limit,
+    pin_finite_differences,
+    pin_bruteforce_subsets,
+    pin_token_subset_linearity,
+    pin_duplicate_slot,
+    pin_bf16_entry_matches_f64,
+]
