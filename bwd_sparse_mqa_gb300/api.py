@@ -1,0 +1,147 @@
+"""Python interface with the signatures of the DeepSeek-V4 sparse MQA pages
+(NeMo AutoModel, tilelang_sparse_mla_fwd: `sparse_mqa_fwd_interface`;
+tilelang_sparse_mla_bwd: `sparse_mqa_bwd_interface`).
+
+PyTorch only supplies device memory and the current stream; every step of the
+computation runs in libsparse_mqa.so's CUDA kernels, reached through the C ABI
+(include/sparse_mqa.h).  There is no CPU path: inputs must be contiguous CUDA
+tensors.  The TileLang tuning knobs of the pages (block_I, num_stages,
+threads) are accepted for signature compatibility and ignored.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional
+
+import torch
+
+from . import _lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _shape(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor,
+           topk_idxs: torch.Tensor) -> _lib.Shape:
+    _need(q, "q", torch.bfloat16, 4)
+    _need(kv, "kv", torch.bfloat16, 3)
+    _need(attn_sink, "attn_sink", torch.float32, 1)
+    _need(topk_idxs, "topk_idxs", torch.int32, 3)
+    B, S, H, D = q.shape
+    if kv.shape[0] != B or kv.shape[2] != D:
+        raise ValueError(f"kv shape {tuple(kv.shape)} does not match q {tuple(q.shape)}")
+    if attn_sink.shape[0] != H:
+        raise ValueError(f"attn_sink must have H={H} entries")
+    if topk_idxs.shape[0] != B or topk_idxs.shape[1] != S:
+        raise ValueError(f"topk_idxs shape {tuple(topk_idxs.shape)} does not match q")
+    devs = {q.device, kv.device, attn_sink.device, topk_idxs.device}
+    if len(devs) != 1:
+        raise ValueError("all tensors must be on the same device")
+    return _lib.Shape(B, S, kv.shape[1], H, D, topk_idxs.shape[2])
+
+
+def _scale(sm_scale: Optional[float], D: int) -> float:
+    """None selects D^-1/2 (the pages' default); a value is used as given."""
+    if sm_scale is None:
+        return 1.0 / math.sqrt(D)
+    s = float(sm_scale)
+    if not s > 0.0 or not math.isfinite(s):
+        raise ValueError("sm_scale must be a positive finite float or None")
+    return s
+
+
+def sparse_mqa_fwd_interface(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor,
+                             topk_idxs: torch.Tensor, sm_scale: Optional[float] = None,
+                             block_I: int = 64, num_stages: int = 2, threads: int = 256,
+                             reference_rounding: bool = False
+                             ) -> tuple[torch.Tensor, torch.Tensor]:
+    """Top-k sparse MQA forward.
+
+    q [B,S,H,D] bf16, kv [B,S_kv,D] bf16 (shared keys and values),
+    attn_sink [H] fp32, topk_idxs [B,S,topk] int32 (entries outside
+    [0,S_kv) are masked).  Returns freshly allocated O [B,S,H,D] bf16 and
+    LSE [B,S,H] fp32 = log2(sum_valid exp(sm_scale q.k) + exp(sink)).
+    """
+    shp = _shape(q, kv, attn_sink, topk_idxs)
+    scale = _scale(sm_scale, shp.D)
+    o = torch.empty_like(q)
+    lse = torch.empty((shp.B, shp.S, shp.H), dtype=torch.float32, device=q.device)
+    flags = _lib.FLAG_REFERENCE_ROUNDING if reference_rounding else 0
+    lib = _lib.load()
+    with torch.cuda.device(q.device):
+        _lib.check("smqa_fwd", lib.smqa_fwd(_ptr(q), _ptr(kv), _ptr(attn_sink), _ptr(topk_idxs),
+                                            shp, scale, _ptr(o), _ptr(lse), flags,
+                                            _stream(q.device)))
+    return o, lse
+
+
+def bwd_workspace_bytes(shape: _lib.Shape, return_dkv_accum_dtype: bool = False) -> int:
+    flags = _lib.FLAG_RETURN_DKV_FP32 if return_dkv_accum_dtype else 0
+    return int(_lib.load().smqa_bwd_workspace_bytes(shape, flags))
+
+
+def sparse_mqa_bwd_interface(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor,
+                             o: torch.Tensor, do: torch.Tensor, topk_idxs: torch.Tensor,
+                             lse: torch.Tensor, sm_scale: Optional[float] = None,
+                             return_dkv_accum_dtype: bool = False,
+                             workspace: Optional[torch.Tensor] = None
+                             ) -> tuple[torch.Tensor, torch.Tensor]:
+    """Top-k sparse MQA backward.
+
+    Takes the forward's inputs, its output o, the gradient do [B,S,H,D] bf16
+    and its log2 lse [B,S,H] fp32.  Returns freshly allocated dq [B,S,H,D]
+    bf16 and dkv [B,S_kv,D] (bf16, or fp32 with return_dkv_accum_dtype).
+    ``workspace`` (uint8 CUDA tensor) may be passed to reuse scratch memory
+    between calls; otherwise one is allocated.
+    """
+    shp = _shape(q, kv, attn_sink, topk_idxs)
+    _need(o, "o", torch.bfloat16, 4)
+    _need(do, "do", torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    if o.shape != q.shape or do.shape != q.shape:
+        raise ValueError("o and do must have q's shape")
+    if tuple(lse.shape) != (shp.B, shp.S, shp.H):
+        raise ValueError("lse must be [B,S,H]")
+    scale = _scale(sm_scale, shp.D)
+    flags = _lib.FLAG_RETURN_DKV_FP32 if return_dkv_accum_dtype else 0
+    lib = _lib.load()
+    need = int(lib.smqa_bwd_workspace_bytes(shp, flags))
+    if need == 0:
+        raise ValueError("unsupported shape for the backward")
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q)
+    dkv = torch.empty((shp.B, shp.S_kv, shp.D),
+                      dtype=torch.float32 if return_dkv_accum_dtype else torch.bfloat16,
+                      device=q.device)
+    with torch.cuda.device(q.device):
+        _lib.check("smqa_bwd", lib.smqa_bwd(_ptr(q), _ptr(kv), _ptr(attn_sink), _ptr(o), _ptr(do),
+                                            _ptr(topk_idxs), _ptr(lse), shp, scale, _ptr(dq),
+                                            _ptr(dkv), _ptr(workspace), workspace.numel(), flags,
+                                            _stream(q.device)))
+    return dq, dkv
+
+
+def device_status(clear: bool = True) -> int:
+    """The device status word (0, or SMQA_ERR_DEVICE_TIMEOUT after a kernel's
+    bounded wait ran out).  Synchronizes the device."""
+    return int(_lib.load().smqa_device_status(1 if clear else 0))

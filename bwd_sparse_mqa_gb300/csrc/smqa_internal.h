@@ -1,0 +1,49 @@
+// smqa_internal.h -- parameter blocks and launchers shared by the library's
+// translation units (not part of the public C ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace smqa {
+
+struct FwdParams {
+  const int32_t* idx;    // [B,S,topk]
+  const float* sink;     // [H]
+  __nv_bfloat16* o;      // [B,S,H,D]
+  float* lse;            // [B,S,H]
+  int S, S_kv, H, D, topk;
+  float scale;           // sm_scale
+  float scale_log2;      // sm_scale * log2(e)
+  int ref_round;         // 1: exp2 argument as (score * scale) * log2(e)
+  int* status;           // device status word
+  uint64_t limit_ns;     // bounded-wait limit
+};
+
+struct BwdParams {
+  const int32_t* idx;    // [B,S,topk]
+  const float* lse;      // [B,S,H]  log2 LSE from the forward
+  const float* delta;    // [B,S,H]  rowsum(O * dO)
+  __nv_bfloat16* dq;     // [B,S,H,D]
+  float* dkv_acc;        // [B,S_kv,D] fp32 accumulator (zeroed beforehand)
+  int S, S_kv, H, D, topk;
+  float scale;           // sm_scale
+  float scale_log2;      // sm_scale * log2(e)
+  int* status;
+  uint64_t limit_ns;
+};
+
+cudaError_t launch_fwd(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const FwdParams& p,
+                       int tokens, cudaStream_t stream);
+cudaError_t launch_bwd_main(const CUtensorMap& tm_q, const CUtensorMap& tm_do,
+                            const CUtensorMap& tm_kv, const BwdParams& p, int tokens,
+                            cudaStream_t stream);
+cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* dout,
+                                  float* delta, float* dkv_acc, int64_t rows, int D,
+                                  int64_t acc_elems, cudaStream_t stream);
+cudaError_t launch_bwd_postprocess(const float* acc, __nv_bfloat16* out, int64_t elems,
+                                   cudaStream_t stream);
+
+}  // namespace smqa

@@ -1,0 +1,161 @@
+/*
+ * sparse_mqa.h -- C ABI of the GB300 (sm_103a) top-k sparse multi-query
+ * attention library: forward and backward with a per-head attention sink.
+ *
+ * The operation is the one behind `sparse_mqa_fwd_interface` and
+ * `sparse_mqa_bwd_interface` on the DeepSeek-V4 kernel pages of NeMo
+ * AutoModel (tilelang_sparse_mla_fwd, tilelang_sparse_mla_bwd):
+ *
+ *   every query token (b, s) has H heads that attend only to the `topk` rows
+ *   of ONE shared kv tensor (used as both keys and values) listed in
+ *   topk_idxs[b, s, :]; a slot whose index lies outside [0, S_kv) is masked;
+ *   head h adds exp(attn_sink[h]) to its softmax denominator; the forward
+ *   returns O and the base-2 log of that denominator (sink included), which
+ *   the backward consumes together with dO to produce dQ and dKV.
+ *
+ * Conventions for every entry point
+ *   - Tensors are row-major and contiguous, in DEVICE memory of the current
+ *     CUDA device, with the shapes given below.  bf16 tensors are passed as
+ *     `const void*` and hold IEEE bfloat16 values.
+ *   - q, kv, o, dO, dq, dkv and the workspace must be 16-byte aligned; fp32
+ *     and int32 tensors 4-byte aligned.
+ *   - The caller allocates and owns every buffer; the library never allocates
+ *     and never frees.  Inputs are only read.
+ *   - Calls are asynchronous on `stream` (0 = the legacy default stream).
+ *     Argument checks happen on the host before anything is launched; a
+ *     rejected call launches nothing and leaves every output untouched.
+ *   - A kernel that waits longer than its bounded limit (4 s per wait, or
+ *     SMQA_WAIT_LIMIT_NS nanoseconds from the environment) records
+ *     SMQA_ERR_DEVICE_TIMEOUT in a per-device status word and exits cleanly;
+ *     read it with smqa_device_status().  The word is sticky: while it is set,
+ *     the forward and backward-main kernels skip their work (their outputs
+ *     are left undefined) until smqa_device_status(1) clears it.
+ *   - Supported shapes: 1 <= H <= 128, D in {64, 512}, topk >= 1, B, S,
+ *     S_kv >= 1, B*S_kv*D < 2^31, B*S*H < 2^31.  Anything else returns
+ *     SMQA_ERR_UNSUPPORTED.
+ */
+#ifndef SPARSE_MQA_H_
+#define SPARSE_MQA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SMQA_ABI_VERSION 1
+
+typedef enum {
+    SMQA_OK = 0,
+    SMQA_ERR_INVALID_ARG = 1,     /* null / misaligned pointer, non-positive size */
+    SMQA_ERR_UNSUPPORTED = 2,     /* shape outside the supported set, small workspace */
+    SMQA_ERR_CUDA = 3,            /* a CUDA runtime or driver call failed */
+    SMQA_ERR_DEVICE_TIMEOUT = 4   /* a kernel's bounded wait ran out (device status) */
+} smqa_status;
+
+typedef struct {
+    int32_t B;      /* batch                                  */
+    int32_t S;      /* query tokens per batch element         */
+    int32_t S_kv;   /* kv rows per batch element              */
+    int32_t H;      /* query heads sharing the one kv tensor  */
+    int32_t D;      /* head dim of q, of kv and of O          */
+    int32_t topk;   /* index slots per query token            */
+} smqa_shape;
+
+/* smqa_fwd: form the exp2 argument as (score * sm_scale) * log2(e), two fp32
+ * roundings, instead of score * (sm_scale * log2(e)).  The pages' forward
+ * interface has this switch (`reference_rounding`: the scaled-logit fp32
+ * arithmetic of the original inference kernel, LSE still in log2); both
+ * orders agree to within one fp32 rounding of the logit. */
+#define SMQA_FLAG_REFERENCE_ROUNDING 2u
+
+/* smqa_bwd: write dkv as fp32 (the raw accumulator) instead of bf16.  The
+ * pages' backward interface has the same switch (`return_dkv_accum_dtype`). */
+#define SMQA_FLAG_RETURN_DKV_FP32 1u
+
+/*
+ * Forward (tilelang_sparse_mla_fwd: `sparse_mqa_fwd_interface`, the kernel
+ * factory `sparse_mqa_fwd`).
+ *   q         [B,S,H,D]    bf16  queries
+ *   kv        [B,S_kv,D]   bf16  shared keys/values
+ *   attn_sink [H]          fp32  per-head denominator bias (enters as exp)
+ *   topk_idxs [B,S,topk]   int32 kv row per slot; outside [0,S_kv) = masked
+ *   sm_scale               score multiplier; <= 0 (or NaN) selects D^-1/2
+ *   o         [B,S,H,D]    bf16  output (written)
+ *   lse       [B,S,H]      fp32  log2(sum_valid exp(sm_scale*q.k) + exp(sink))
+ *   flags                  0 or SMQA_FLAG_REFERENCE_ROUNDING
+ * A token whose slots are all masked gets O = 0 and lse = sink/ln 2.
+ */
+smqa_status smqa_fwd(const void* q, const void* kv, const float* attn_sink,
+                     const int32_t* topk_idxs, smqa_shape shape, float sm_scale,
+                     void* o, float* lse, unsigned flags, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace smqa_bwd needs for `shape` and `flags`: the fp32
+ * dKV accumulator [B,S_kv,D] (absent with SMQA_FLAG_RETURN_DKV_FP32, where
+ * dkv itself accumulates) and Delta [B,S,H] fp32, each 256-byte aligned.
+ * Returns 0 for an unsupported shape.
+ */
+size_t smqa_bwd_workspace_bytes(smqa_shape shape, unsigned flags);
+
+/*
+ * Backward (tilelang_sparse_mla_bwd: `sparse_mqa_bwd_interface`, which runs
+ * its `preprocess`, `bwd` and `postprocess` kernels in that order).
+ *   q, kv, attn_sink, topk_idxs, sm_scale   as in smqa_fwd
+ *   o         [B,S,H,D]  bf16  the forward's output
+ *   dout      [B,S,H,D]  bf16  gradient of the loss w.r.t. o
+ *   lse       [B,S,H]    fp32  the forward's log2 LSE
+ *   dq        [B,S,H,D]  bf16  written
+ *   dkv       [B,S_kv,D] bf16 written, or fp32 with SMQA_FLAG_RETURN_DKV_FP32;
+ *                              rows no slot names are 0
+ *   workspace, workspace_bytes  >= smqa_bwd_workspace_bytes(shape, flags)
+ * dkv sums contributions with fp32 atomics, so its low bits may differ from
+ * run to run; dq is deterministic.
+ */
+smqa_status smqa_bwd(const void* q, const void* kv, const float* attn_sink, const void* o,
+                     const void* dout, const int32_t* topk_idxs, const float* lse,
+                     smqa_shape shape, float sm_scale, void* dq, void* dkv,
+                     void* workspace, size_t workspace_bytes, unsigned flags,
+                     cudaStream_t stream);
+
+/*
+ * The three backward stages one at a time (same arguments as smqa_bwd; used
+ * to time and profile them separately).
+ *   preprocess  : delta[B,S,H] = rowsum(o * dout) in fp32, and dkv_accum
+ *                 [B,S_kv,D] fp32 set to zero
+ *   main        : dq, and dkv_accum += every slot's dKV contribution
+ *   postprocess : dkv_bf16 = round-to-nearest-even(dkv_accum)
+ */
+smqa_status smqa_bwd_preprocess(const void* o, const void* dout, smqa_shape shape,
+                                float* delta, float* dkv_accum, cudaStream_t stream);
+smqa_status smqa_bwd_main(const void* q, const void* kv, const float* attn_sink,
+                          const void* dout, const int32_t* topk_idxs, const float* lse,
+                          const float* delta, smqa_shape shape, float sm_scale, void* dq,
+                          float* dkv_accum, cudaStream_t stream);
+smqa_status smqa_bwd_postprocess(const float* dkv_accum, smqa_shape shape, void* dkv_bf16,
+                                 cudaStream_t stream);
+
+/*
+ * Reads the device status word that kernels set when a bounded wait runs out
+ * (SMQA_OK if none did).  Synchronizes the current device first.  A nonzero
+ * `clear` resets the word afterwards.
+ */
+smqa_status smqa_device_status(int clear);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* smqa_status_string(smqa_status status);
+
+/* Text describing the last failure seen by this thread's calls (a rejected
+ * argument or a failing CUDA call); static thread-local storage. */
+const char* smqa_last_error(void);
+
+/* SMQA_ABI_VERSION of the built library. */
+int smqa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_MQA_H_ */

@@ -1,0 +1,102 @@
+"""The C-ABI library: it loads, exports every symbol include/sparse_mqa.h
+declares, and rejects bad arguments on the host before touching a GPU
+(these calls return before any CUDA call, so they run without a device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from bwd_sparse_mqa_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _lib.load()
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "sparse_mqa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(smqa_\w+)\s*\(", text)))
+
+
+def test_exports_match_header(lib):
+    declared = _header_functions()
+    assert declared, "no declarations parsed"
+    assert sorted(_lib.EXPORTS) == declared
+    for name in declared:
+        assert hasattr(lib, name), f"{name} not exported"
+
+
+def test_version_and_strings(lib):
+    assert lib.smqa_abi_version() == 1
+    assert lib.smqa_status_string(0) == b"SMQA_OK"
+    assert lib.smqa_status_string(4) == b"SMQA_ERR_DEVICE_TIMEOUT"
+    assert lib.smqa_status_string(99) == b"SMQA_ERR_UNKNOWN"
+
+
+def _fake(addr=0x10000):
+    return ctypes.c_void_p(addr)
+
+
+def test_fwd_rejects_bad_shapes(lib):
+    p = _fake()
+    bad = [(_lib.Shape(0, 1, 1, 1, 64, 1), _lib.SMQA_ERR_INVALID_ARG),
+           (_lib.Shape(1, 1, 1, 1, 64, 0), _lib.SMQA_ERR_INVALID_ARG),
+           (_lib.Shape(1, 1, 1, 129, 64, 1), _lib.SMQA_ERR_UNSUPPORTED),
+           (_lib.Shape(1, 1, 1, 16, 128, 1), _lib.SMQA_ERR_UNSUPPORTED),
+           (_lib.Shape(1, 1, 1 << 23, 16, 512, 1), _lib.SMQA_ERR_UNSUPPORTED)]
+    for shp, want in bad:
+        assert lib.smqa_fwd(p, p, p, p, shp, 0.0, p, p, 0, None) == want
+
+
+def test_fwd_rejects_null_misaligned_and_flags(lib):
+    shp = _lib.Shape(1, 4, 4, 16, 64, 4)
+    p = _fake()
+    assert lib.smqa_fwd(None, p, p, p, shp, 0.0, p, p, 0, None) == _lib.SMQA_ERR_INVALID_ARG
+    assert lib.smqa_fwd(_fake(0x10008), p, p, p, shp, 0.0, p, p, 0, None) == \
+        _lib.SMQA_ERR_INVALID_ARG
+    assert lib.smqa_fwd(p, p, p, p, shp, 0.0, p, p, 8, None) == _lib.SMQA_ERR_INVALID_ARG
+    assert b"misaligned" in lib.smqa_last_error()
+
+
+def test_bwd_workspace_and_checks(lib):
+    shp = _lib.Shape(2, 8, 16, 16, 64, 4)
+    ws = lib.smqa_bwd_workspace_bytes(shp, 0)
+    ws32 = lib.smqa_bwd_workspace_bytes(shp, _lib.FLAG_RETURN_DKV_FP32)
+    acc = 2 * 16 * 64 * 4
+    delta = 2 * 8 * 16 * 4
+    r = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert ws == r(acc) + r(delta)
+    assert ws32 == r(delta)
+    assert lib.smqa_bwd_workspace_bytes(_lib.Shape(1, 1, 1, 1, 100, 1), 0) == 0
+    p = _fake()
+    args = [p] * 7 + [shp, 0.0, p, p, p]
+    assert lib.smqa_bwd(*args, ws - 1, 0, None) == _lib.SMQA_ERR_UNSUPPORTED
+    assert lib.smqa_bwd(*args, ws, 4, None) == _lib.SMQA_ERR_INVALID_ARG
+    args_null = [p] * 6 + [None, shp, 0.0, p, p, p]
+    assert lib.smqa_bwd(*args_null, ws, 0, None) == _lib.SMQA_ERR_INVALID_ARG
+
+
+def test_python_interface_rejects_cpu_tensors():
+    import torch
+    from bwd_sparse_mqa_gb300 import sparse_mqa_fwd_interface
+    q = torch.zeros(1, 4, 16, 64, dtype=torch.bfloat16)
+    kv = torch.zeros(1, 4, 64, dtype=torch.bfloat16)
+    sink = torch.zeros(16)
+    idx = torch.zeros(1, 4, 4, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        sparse_mqa_fwd_interface(q, kv, sink, idx)
+
+
+def test_product_package_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "bwd_sparse_mqa_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "smqa_oracle" not in text, f
