@@ -1,0 +1,398 @@
+#!/usr/bin/env python
+"""Benchmark: top-k sparse MQA forward + backward on GB300.
+
+One step = the whole hot path over one batch: forward (O, log2 LSE), then the
+backward's preprocess (Delta and zeroing of the fp32 dKV accumulator), main
+kernel (dQ, dKV scatter) and postprocess (dKV to bf16).  Workload: B=1,
+S=S_kv=8192, H=128, D=512, topk=2048, indices causal and biased to the
+newest 512 keys (the H=128 D=512 topk=2048 configuration).  Inputs are
+synthetic and seeded; q, o, dO and dq are 1 GiB each (larger than L2), kv
+(8 MiB) stays L2-resident as it would in the real workload.
+
+Metric: TFLOP/s of the step, FLOPs counted on valid slots only
+(4*H*D per valid slot forward, 10*H*D backward).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own replica
+(the op shards by tokens with no data-path collective) and the timed region
+is bracketed by barriers; value = all ranks' FLOPs / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bwd_sparse_mqa_gb300 import _lib, inputs  # noqa: E402
+from bwd_sparse_mqa_gb300 import sparse_mqa_bwd_interface, sparse_mqa_fwd_interface  # noqa: E402
+
+WORKLOAD = "h128_d512_k2048_s8192"
+METRIC = "sparse MQA fwd/bwd TFLOP/s + % BF16 roofline, 1×GB300, H=128 D=512 topk=2048"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_bwd_main_h128_d512_k2048.json")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("smqa_bwd.cu", "smqa_ptx.cuh"):
+        with open(os.path.join(ROOT, "bwd_sparse_mqa_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the backward main kernel from the committed
+    ncu summary, or None if the kernel source changed since it was taken."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def flops_of(idx: torch.Tensor, S_kv: int, H: int, D: int):
+    nv = int(((idx >= 0) & (idx < S_kv)).sum().item())
+    return 4.0 * H * D * nv, 10.0 * H * D * nv, nv
+
+
+def cpu_baseline(x: dict, cfg, target_s: float = 15.0, max_tokens: int = 512):
+    """The fp64 oracle as it stands, on the host cores, fwd+bwd over a seeded
+    token sample of the workload sized to ~target_s seconds."""
+    import numpy as np
+
+    import oracle
+    q, kv, sink, idx, dout = (x["q"].cpu(), x["kv"].cpu(), x["attn_sink"].cpu(),
+                              x["topk_idxs"].cpu(), x["do"].cpu())
+    rng = np.random.default_rng(1234)
+    T = cfg.B * cfg.S
+
+    def run(n):
+        toks = np.sort(rng.choice(T, size=n, replace=False))
+        sel = idx.reshape(T, -1)[torch.as_tensor(toks)]
+        nv = int(((sel >= 0) & (sel < cfg.S_kv)).sum())
+        t0 = time.perf_counter()
+        oracle.fwd(q, kv, sink, idx, tokens=toks)
+        oracle.bwd(q, kv, sink, idx, dout, tokens=toks)
+        return time.perf_counter() - t0, nv
+
+    probe_n = 4
+    dt, _ = run(probe_n)
+    n = int(max(probe_n, min(max_tokens, probe_n * target_s / max(dt, 1e-3))))
+    dt, nv = run(n)
+    fl = 14.0 * cfg.H * cfg.D * nv
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{n} seeded tokens of {WORKLOAD} (fwd+bwd, fp64, {nv} valid slots), "
+                      f"{dt:.1f} s"}
+
+
+def reference_arm(args, rank: int):
+    """--impl reference: the fp64 oracle timed on the host cores, each step a
+    bounded token sample of the same workload."""
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    cfg = inputs.by_name(WORKLOAD)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    x = inputs.make_inputs(cfg, device=dev)
+    q, kv, sink, idx, dout = (x["q"].cpu(), x["kv"].cpu(), x["attn_sink"].cpu(),
+                              x["topk_idxs"].cpu(), x["do"].cpu())
+    T = cfg.B * cfg.S
+    per_step = int(os.environ.get("SMQA_REF_TOKENS_PER_STEP", "8"))
+    rng = np.random.default_rng(99)
+
+    def step():
+        toks = np.sort(rng.choice(T, size=per_step, replace=False))
+        sel = idx.reshape(T, -1)[torch.as_tensor(toks)]
+        nv = int(((sel >= 0) & (sel < cfg.S_kv)).sum())
+        oracle.fwd(q, kv, sink, idx, tokens=toks)
+        oracle.bwd(q, kv, sink, idx, dout, tokens=toks)
+        return 14.0 * cfg.H * cfg.D * nv
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    total = sum(step() for _ in range(args.steps))
+    dt = time.perf_counter() - t0
+    v = total / dt / 1e12
+    line = {"metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD, "B": cfg.B, "S": cfg.S, "S_kv": cfg.S_kv,
+                       "H": cfg.H, "D": cfg.D, "topk": cfg.topk,
+                       "sample_tokens_per_step": per_step},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": f"{per_step} seeded tokens per step (fwd+bwd, fp64)"},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "gb300" else "gloo")
+    if args.impl == "reference":
+        reference_arm(args, rank)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = inputs.by_name(WORKLOAD)
+    x = inputs.make_inputs(cfg, device=str(dev))
+    q, kv, sink, idx, dout = x["q"], x["kv"], x["attn_sink"], x["topk_idxs"], x["do"]
+    B, S, S_kv, H, D, K = cfg.B, cfg.S, cfg.S_kv, cfg.H, cfg.D, cfg.topk
+    f_fwd, f_bwd, n_valid = flops_of(idx, S_kv, H, D)
+    lib = _lib.load()
+    shp = _lib.Shape(B, S, S_kv, H, D, K)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, S, H), dtype=torch.float32, device=dev)
+    dq = torch.empty_like(q)
+    dkv = torch.empty((B, S_kv, D), dtype=torch.bfloat16, device=dev)
+    acc = torch.empty((B, S_kv, D), dtype=torch.float32, device=dev)
+    delta = torch.empty((B, S, H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    scale = D ** -0.5
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        _lib.check("smqa_fwd", lib.smqa_fwd(P(q), P(kv), P(sink), P(idx), shp, scale, P(o), P(lse),
+                                            0, sp))
+        if ev is not None:
+            ev[1].record(stream)
+        _lib.check("pre", lib.smqa_bwd_preprocess(P(o), P(dout), shp, P(delta), P(acc), sp))
+        if ev is not None:
+            ev[2].record(stream)
+        _lib.check("main", lib.smqa_bwd_main(P(q), P(kv), P(sink), P(dout), P(idx), P(lse),
+                                             P(delta), shp, scale, P(dq), P(acc), sp))
+        if ev is not None:
+            ev[3].record(stream)
+        _lib.check("post", lib.smqa_bwd_postprocess(P(acc), shp, P(dkv), sp))
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if lib.smqa_device_status(1) != 0:
+        raise RuntimeError("device timeout during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier(device_ids=[local])
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier(device_ids=[local])
+    torch.cuda.synchronize(dev)
+    elapsed_ms = start.elapsed_time(end)
+    if lib.smqa_device_status(1) != 0:
+        raise RuntimeError("device timeout during the timed region")
+    t_fwd = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    t_pre = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    t_main = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    t_post = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_step = elapsed_ms / args.steps
+    value = world * (f_fwd + f_bwd) * args.steps / (elapsed_ms * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs -> device, fwd,
+    # bwd, results -> pinned host, every step
+    host = {k: v.cpu().pin_memory() for k, v in (("q", q), ("kv", kv), ("sink", sink),
+                                                 ("idx", idx), ("do", dout))}
+    outs = {"o": torch.empty_like(host["q"]).pin_memory(),
+            "lse": torch.empty((B, S, H), dtype=torch.float32).pin_memory(),
+            "dq": torch.empty_like(host["q"]).pin_memory(),
+            "dkv": torch.empty((B, S_kv, D), dtype=torch.bfloat16).pin_memory()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in outs.values())
+    ws = torch.empty((int(lib.smqa_bwd_workspace_bytes(shp, 0)),), dtype=torch.uint8, device=dev)
+
+    def e2e_step():
+        g = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
+        oo, ll = sparse_mqa_fwd_interface(g["q"], g["kv"], g["sink"], g["idx"])
+        gq, gkv = sparse_mqa_bwd_interface(g["q"], g["kv"], g["sink"], oo, g["do"], g["idx"], ll,
+                                           workspace=ws)
+        outs["o"].copy_(oo, non_blocking=True)
+        outs["lse"].copy_(ll, non_blocking=True)
+        outs["dq"].copy_(gq, non_blocking=True)
+        outs["dkv"].copy_(gkv, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier(device_ids=[local])
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * (f_fwd + f_bwd) * args.e2e_steps / (e2e_ms * 1e-3) / 1e12
+
+    if rank == 0:
+        pk, src = peaks()
+        peak_tf = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
+        hbm = float(pk.get("hbm_gbs"))
+        ach_main = f_bwd / (t_main * 1e-3) / 1e12
+        ach_fwd = f_fwd / (t_fwd * 1e-3) / 1e12
+        T = B * S
+        # bytes per the op's algorithmic accounting (valid slots)
+        fwd_bytes = 2 * D * n_valid + 4 * H * D * T + 4 * K * T + 4 * H * T
+        bwd_bytes = 6 * D * n_valid + 8 * H * D * T + 4 * K * T + 8 * H * T + 10 * B * S_kv * D
+        bwd_ms = t_pre + t_main + t_post
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "B": B, "S": S, "S_kv": S_kv, "H": H, "D": D,
+                       "topk": K, "index_recipe": cfg.recipe, "valid_slots": n_valid,
+                       "l2": "inputs larger than L2 (q, o, dO, dq 1 GiB each); kv 8 MiB stays "
+                             "L2-resident by design",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "tensor", "kernel": "smqa_bwd_kernel<256,2> (bwd main)",
+                         "achieved": ach_main, "peak": peak_tf, "unit": "TFLOP/s",
+                         "frac": ach_main / peak_tf, "peak_source":
+                         f"{src} bf16 sustained (kernel timed inside a long step)",
+                         "traffic": recorded_traffic()},
+            "kernels_ms": {"fwd": t_fwd, "bwd_pre": t_pre, "bwd_main": t_main,
+                           "bwd_post": t_post},
+            "fwd": {"tflops": ach_fwd, "ms": t_fwd, "frac_tensor": ach_fwd / peak_tf,
+                    "frac_roofline_slower_of":
+                        max(f_fwd / (peak_tf * 1e12), fwd_bytes / (hbm * 1e9)) / (t_fwd * 1e-3)},
+            "bwd": {"tflops": f_bwd / (bwd_ms * 1e-3) / 1e12, "ms": bwd_ms,
+                    "frac_tensor": f_bwd / (bwd_ms * 1e-3) / 1e12 / peak_tf,
+                    "frac_roofline_slower_of":
+                        max(f_bwd / (peak_tf * 1e12), bwd_bytes / (hbm * 1e9)) / (bwd_ms * 1e-3)},
+            "tokens_per_s": world * T * args.steps / (elapsed_ms * 1e-3),
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+            "gpu_launches": 4 * args.steps,
+            "clocks": clk.summary(),
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(x, cfg)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
