@@ -215,6 +215,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--seq", type=int, default=None,
+                    help="profiling only: override S = S_kv (the bench line then names the "
+                         "smaller workload)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -235,6 +238,11 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     cfg = inputs.by_name(WORKLOAD)
+    workload = WORKLOAD
+    if args.seq:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, S=args.seq, S_kv=args.seq)
+        workload = f"{WORKLOAD} with S=S_kv={args.seq} (profiling size)"
     x = inputs.make_inputs(cfg, device=str(dev))
     q, kv, sink, idx, dout = x["q"], x["kv"], x["attn_sink"], x["topk_idxs"], x["do"]
     B, S, S_kv, H, D, K = cfg.B, cfg.S, cfg.S_kv, cfg.H, cfg.D, cfg.topk
@@ -327,23 +335,25 @@ def main():
         outs["dq"].copy_(gq, non_blocking=True)
         outs["dkv"].copy_(gkv, non_blocking=True)
 
-    e2e_step()
-    torch.cuda.synchronize(dev)
-    if dist is not None:
-        dist.barrier(device_ids=[local])
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
+    e2e_value = None
+    if args.e2e_steps > 0:
         e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * (f_fwd + f_bwd) * args.e2e_steps / (e2e_ms * 1e-3) / 1e12
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier(device_ids=[local])
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1)
+        if dist is not None:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e_value = world * (f_fwd + f_bwd) * args.e2e_steps / (e2e_ms * 1e-3) / 1e12
 
     if rank == 0:
         pk, src = peaks()
@@ -361,7 +371,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "B": B, "S": S, "S_kv": S_kv, "H": H, "D": D,
+            "config": {"workload": workload, "B": B, "S": S, "S_kv": S_kv, "H": H, "D": D,
                        "topk": K, "index_recipe": cfg.recipe, "valid_slots": n_valid,
                        "l2": "inputs larger than L2 (q, o, dO, dq 1 GiB each); kv 8 MiB stays "
                              "L2-resident by design",
