@@ -27,8 +27,9 @@ FLAG_REFERENCE_ROUNDING = 2
 EXPORTS = [
     "smqa_fwd", "smqa_bwd_workspace_bytes", "smqa_bwd", "smqa_bwd_preprocess", "smqa_bwd_main",
     "smqa_bwd_postprocess", "smqa_device_status", "smqa_status_string", "smqa_last_error",
-    "smqa_abi_version",
+    "smqa_abi_version", "smqa_bwd_static_scratch",
 ]
+STATIC_SCRATCH_BYTES = 24 << 20
 
 
 class Shape(ctypes.Structure):
@@ -57,6 +58,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.smqa_bwd_main.restype = st
     lib.smqa_bwd_postprocess.argtypes = [P, S, P, P]
     lib.smqa_bwd_postprocess.restype = st
+    lib.smqa_bwd_static_scratch.argtypes = [P, P, P, P, P, P, P, S, F, P, P, U, P]
+    lib.smqa_bwd_static_scratch.restype = st
     lib.smqa_device_status.argtypes = [ctypes.c_int]
     lib.smqa_device_status.restype = st
     lib.smqa_status_string.argtypes = [st]

@@ -162,6 +162,10 @@ smqa_status bwd_main_impl(const void* q, const void* kv, const void* dout, const
 
 }  // namespace
 
+namespace smqa {
+void set_last_error(const char* msg) { std::snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+}  // namespace smqa
+
 extern "C" {
 
 int smqa_abi_version(void) { return SMQA_ABI_VERSION; }

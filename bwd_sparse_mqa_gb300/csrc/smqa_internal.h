@@ -35,6 +35,9 @@ struct BwdParams {
   uint64_t limit_ns;
 };
 
+// Records `msg` as the text smqa_last_error() returns on this thread.
+void set_last_error(const char* msg);
+
 cudaError_t launch_fwd(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const FwdParams& p,
                        int tokens, cudaStream_t stream);
 cudaError_t launch_bwd_main(const CUtensorMap& tm_q, const CUtensorMap& tm_do,

@@ -121,6 +121,39 @@ smqa_status smqa_bwd(const void* q, const void* kv, const float* attn_sink, cons
                      cudaStream_t stream);
 
 /*
+ * Backward for callers that cannot allocate device memory.  (The sparse MQA
+ * pages have no counterpart: this entry point exists for this library's
+ * users, not for parity with the pages.)
+ *
+ * smqa_bwd needs a device workspace of smqa_bwd_workspace_bytes() bytes.  Some
+ * callers cannot provide one: code running under a memory planner that has
+ * already handed every byte of device memory to its own pool, plugins that
+ * get only the tensors they are given, or hot paths that must not take the
+ * device-wide synchronisation cudaMalloc/cudaFree may imply.  This entry
+ * point computes exactly what smqa_bwd computes, with the same arguments
+ * minus the workspace, and allocates nothing: its scratch is a static device
+ * buffer of SMQA_STATIC_SCRATCH_BYTES inside the library, which every GPU that
+ * loads the library holds until the process exits.
+ *   - Shapes whose smqa_bwd_workspace_bytes(shape, flags) exceeds
+ *     SMQA_STATIC_SCRATCH_BYTES are rejected with SMQA_ERR_UNSUPPORTED before
+ *     anything runs (smqa_last_error() gives both sizes).  With
+ *     SMQA_FLAG_RETURN_DKV_FP32 only Delta (B*S*H floats) needs the buffer.
+ *   - The first call on a device looks up the buffer's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls share the one buffer per device, and it keeps the previous
+ *     call's contents (each call re-zeroes what must start at zero).  Calls
+ *     whose kernels may overlap on the GPU -- different streams without
+ *     ordering between them, or several host threads -- race on it and give
+ *     wrong results; order them on one stream.
+ */
+#define SMQA_STATIC_SCRATCH_BYTES (24u << 20)
+smqa_status smqa_bwd_static_scratch(const void* q, const void* kv, const float* attn_sink,
+                                    const void* o, const void* dout, const int32_t* topk_idxs,
+                                    const float* lse, smqa_shape shape, float sm_scale, void* dq,
+                                    void* dkv, unsigned flags, cudaStream_t stream);
+
+/*
  * The three backward stages one at a time (same arguments as smqa_bwd; used
  * to time and profile them separately).
  *   preprocess  : delta[B,S,H] = rowsum(o * dout) in fp32, and dkv_accum
