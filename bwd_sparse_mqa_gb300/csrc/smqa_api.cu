@@ -134,13 +134,13 @@ smqa_status bwd_main_impl(const void* q, const void* kv, const void* dout, const
   cudaError_t e;
   int* st = status_ptr(&e);
   if (!st) return cuda_fail(e, "status word");
-  CUtensorMap tq, tdo, tkv;
+  CUtensorMap tq, tdo;
   const uint64_t T = static_cast<uint64_t>(s.B) * s.S;
   if (!encode_bf16_2d(&tq, q, s.D, T * s.H, 64, static_cast<uint32_t>(s.H)) ||
-      !encode_bf16_2d(&tdo, dout, s.D, T * s.H, 64, static_cast<uint32_t>(s.H)) ||
-      !encode_bf16_2d(&tkv, kv, s.D, static_cast<uint64_t>(s.B) * s.S_kv, 64, 1))
+      !encode_bf16_2d(&tdo, dout, s.D, T * s.H, 64, static_cast<uint32_t>(s.H)))
     return SMQA_ERR_CUDA;
   smqa::BwdParams p{};
+  p.kv = static_cast<const __nv_bfloat16*>(kv);
   p.idx = idx;
   p.lse = lse;
   p.delta = delta;
@@ -155,7 +155,7 @@ smqa_status bwd_main_impl(const void* q, const void* kv, const void* dout, const
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = st;
   p.limit_ns = wait_limit_ns();
-  e = smqa::launch_bwd_main(tq, tdo, tkv, p, static_cast<int>(T), stream);
+  e = smqa::launch_bwd_main(tq, tdo, p, static_cast<int>(T), stream);
   if (e != cudaSuccess) return cuda_fail(e, "bwd main launch");
   return SMQA_OK;
 }
@@ -197,13 +197,14 @@ smqa_status smqa_fwd(const void* q, const void* kv, const float* attn_sink,
   cudaError_t e;
   int* st = status_ptr(&e);
   if (!st) return cuda_fail(e, "status word");
-  CUtensorMap tq, tkv;
+  CUtensorMap tq;
   const uint64_t T = static_cast<uint64_t>(shape.B) * shape.S;
-  if (!encode_bf16_2d(&tq, q, shape.D, T * shape.H, 64, static_cast<uint32_t>(shape.H)) ||
-      !encode_bf16_2d(&tkv, kv, shape.D, static_cast<uint64_t>(shape.B) * shape.S_kv, 64, 1))
+  if (!encode_bf16_2d(&tq, q, shape.D, T * shape.H, 64, static_cast<uint32_t>(shape.H)))
     return SMQA_ERR_CUDA;
   const float scale = effective_scale(sm_scale, shape.D);
   smqa::FwdParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.kv = static_cast<const __nv_bfloat16*>(kv);
   p.idx = topk_idxs;
   p.sink = attn_sink;
   p.o = static_cast<__nv_bfloat16*>(o);
@@ -218,7 +219,7 @@ smqa_status smqa_fwd(const void* q, const void* kv, const float* attn_sink,
   p.ref_round = (flags & SMQA_FLAG_REFERENCE_ROUNDING) ? 1 : 0;
   p.status = st;
   p.limit_ns = wait_limit_ns();
-  e = smqa::launch_fwd(tq, tkv, p, static_cast<int>(T), stream);
+  e = smqa::launch_fwd(tq, p, static_cast<int>(T), stream);
   if (e != cudaSuccess) return cuda_fail(e, "fwd launch");
   return SMQA_OK;
 }

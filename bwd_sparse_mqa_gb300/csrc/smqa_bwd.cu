@@ -100,7 +100,8 @@ struct BwdLayout {
   static constexpr uint32_t kKvChunkBytes = kBI * 128;           // 4 KB
   static constexpr uint32_t kKvStageBytes = kChunks * kKvChunkBytes;
   static constexpr uint32_t kPBytes = kHPad * kBI * 2;           // 8 KB (64-byte rows)
-  static constexpr uint32_t kRecvBytes = NC == 2 ? kHPad * 2 * kBI * 4 : 0;  // S and dP
+  // peer's partial S and dP, fp16 (see the exchange in the P / dS role)
+  static constexpr uint32_t kRecvBytes = NC == 2 ? kHPad * 2 * kBI * 2 : 0;
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffDo = kOffQ + kQBytes;
   // For DC = 64 the 128-row M-major views of Q^T / dO^T read one chunk past
@@ -136,14 +137,17 @@ struct BwdLayout {
   static constexpr uint32_t kTmemDkv = DC + 2 * kBI;  // + buf * kNE * kBI + e * kBI
   static constexpr uint32_t kTmemUsed = kTmemDkv + 2 * kNE * kBI;
   static constexpr uint32_t kTmemCols = kTmemUsed <= 256 ? 256 : 512;
-  static constexpr int kThreads = 320;
+  // warps 0-3: P / dS (thread = head row); 4-7: dKV drain (thread = head-dim
+  // row); 8-9: gather; 10: TMEM owner + MMA issuer
+  static constexpr int kProducerWarp0 = 8;
+  static constexpr int kMmaWarp = 10;
+  static constexpr int kThreads = 352;
 };
 
 template <int DC, int NC>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     smqa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
-                    const __grid_constant__ CUtensorMap tm_do,
-                    const __grid_constant__ CUtensorMap tm_kv, const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
   using L = BwdLayout<DC, NC>;
   extern __shared__ uint8_t smem_raw[];
   uint32_t base = smem_u32(smem_raw);
@@ -165,7 +169,7 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(bar(L::kBarKvFull + s), 1);
+      mbar_init(bar(L::kBarKvFull + s), 64);  // every gather thread arrives
       mbar_init(bar(L::kBarKvEmpty + s), 1);
     }
     mbar_init(bar(L::kBarSdpFull), 1);
@@ -176,7 +180,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(bar(L::kBarDkvFull + i), 1);
       mbar_init(bar(L::kBarDkvFree + i), 128);
     }
-    mbar_init(bar(L::kBarRecvFull), 1);
+    mbar_init(bar(L::kBarRecvFull), 128);
     mbar_init(bar(L::kBarSendOk), 128);
     mbar_init(bar(L::kBarQdoFull), 1);
     mbar_init(bar(L::kBarDqDone), 1);
@@ -184,12 +188,13 @@ __global__ void __launch_bounds__(320, 1)
     *abort_flag = *reinterpret_cast<volatile int*>(p.status) != 0 ? 1 : 0;
     fence_mbar_init();
   }
-  if (warp == 8 && lane == 0) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_do);
-    tma_prefetch_desc(&tm_kv);
+  if (warp == L::kMmaWarp) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+    }
+    tmem_alloc(base + L::kOffTmemHolder, L::kTmemCols);
   }
-  if (warp == 9) tmem_alloc(base + L::kOffTmemHolder, L::kTmemCols);
   if (threadIdx.x < L::kHPad && static_cast<int>(threadIdx.x) >= p.H) {
     const uint32_t h = threadIdx.x;
 #pragma unroll
@@ -207,11 +212,28 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    int issued = 0;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar(L::kBarQdoFull), 2u * static_cast<uint32_t>(p.H) * 128u * L::kChunks);
+  if (warp >= L::kProducerWarp0 && warp < L::kMmaWarp) {
+    // ------------------------------------------------------------ gather
+    // Warp pw copies slots [16 pw, 16 pw + 16) of each 32-slot block; one warp
+    // instruction moves kRpi whole rows of this CTA's D slice (32 lanes x 16
+    // bytes, coalesced) into the 128-byte-swizzled tile with cp.async.
+    const int pw = warp - L::kProducerWarp0;
+    constexpr int kCpr = DC / 8;
+    constexpr int kRpi = 32 / kCpr;
+    const int rsub = lane / kCpr;
+    const int cc = lane % kCpr;
+    const uint32_t lane_off = static_cast<uint32_t>(cc / 8) * L::kKvChunkBytes;
+    const uint32_t c16 = static_cast<uint32_t>(cc % 8);
+    const __nv_bfloat16* kv_col = p.kv + static_cast<size_t>(rank) * DC + cc * 8;
+    const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
+    auto load_idx = [&](int blk) -> int {
+      const int j = blk * L::kBI + lane;
+      return j < p.topk ? __ldg(idx_row + j) : -1;
+    };
+    int r_next = load_idx(0);
+    if (warp == L::kProducerWarp0 && lane == 0) {
+      mbar_arrive_expect_tx(bar(L::kBarQdoFull),
+                            2u * static_cast<uint32_t>(p.H) * 128u * L::kChunks);
       for (int c = 0; c < L::kChunks; ++c) {
         const int x = static_cast<int>(rank) * DC + c * 64;
         tma_load_2d(base + L::kOffQ + c * L::kQChunkBytes, &tm_q, x, t * p.H, bar(L::kBarQdoFull));
@@ -219,41 +241,40 @@ __global__ void __launch_bounds__(320, 1)
                     bar(L::kBarQdoFull));
       }
     }
-    const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
-    for (int i = 0; i < nblk; ++i) {
+    int i = 0;
+    for (; i < nblk; ++i) {
       const int s = i % L::kStages;
-      if (i >= L::kStages) {
-        bool ok = mbar_wait(bar(L::kBarKvEmpty + s), ((i / L::kStages) - 1) & 1, ctl);
-        if (!__all_sync(0xffffffffu, ok)) break;
-      }
-      const int j = i * L::kBI + lane;
-      const int r = j < p.topk ? __ldg(idx_row + j) : -1;
+      const int r = r_next;
+      if (i + 1 < nblk) r_next = load_idx(i + 1);
       const bool v = static_cast<unsigned>(r) < static_cast<unsigned>(p.S_kv);
       const int row = b * p.S_kv + (v ? r : 0);
       const uint32_t m = __ballot_sync(0xffffffffu, v);
-      int gy[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) gy[k] = __shfl_sync(0xffffffffu, row, (4 * (lane & 7) + k) & 31);
-      if (lane == 0) {
-        masks[s] = m;
-        mbar_arrive_expect_tx(bar(L::kBarKvFull + s), L::kKvStageBytes);
+      if (i >= L::kStages) {
+        const bool ok = mbar_wait(bar(L::kBarKvEmpty + s), ((i / L::kStages) - 1) & 1, ctl);
+        if (!__all_sync(0xffffffffu, ok)) break;
       }
-      __syncwarp();
-      if (lane < 8) {
-        const uint32_t dst0 = base + L::kOffKv + s * L::kKvStageBytes + lane * 4u * 128u;
+      if (pw == 0 && lane == 0) masks[s] = m;
+      const uint32_t stage = base + L::kOffKv + s * L::kKvStageBytes + lane_off;
 #pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_gather4(dst0 + c * L::kKvChunkBytes, &tm_kv, static_cast<int>(rank) * DC + c * 64,
-                      gy[0], gy[1], gy[2], gy[3], bar(L::kBarKvFull + s));
+      for (int k = 0; k < 16 / kRpi; ++k) {
+        const int rloc = 16 * pw + k * kRpi + rsub;
+        const int rr = __shfl_sync(0xffffffffu, row, rloc);
+        const uint32_t srow = static_cast<uint32_t>(rloc);
+        cp_async_16(stage + srow * 128u + ((c16 ^ (srow & 7u)) << 4),
+                    kv_col + static_cast<size_t>(rr) * p.D);
       }
-      issued = i + 1;
+      cp_async_commit();
+      if (i >= 1) {
+        cp_async_wait_group<1>();
+        fence_proxy_async_smem();
+        mbar_arrive(bar(L::kBarKvFull + (i - 1) % L::kStages));
+      }
     }
-    if (lane == 0) {
-      mbar_wait_drain(bar(L::kBarQdoFull), 0);
-      for (int i = issued - L::kStages; i < issued; ++i)
-        if (i >= 0) mbar_wait_drain(bar(L::kBarKvFull + i % L::kStages), (i / L::kStages) & 1);
-    }
-  } else if (warp == 9) {
+    cp_async_wait_group<0>();
+    fence_proxy_async_smem();
+    if (i == nblk) mbar_arrive(bar(L::kBarKvFull + (nblk - 1) % L::kStages));
+    if (warp == L::kProducerWarp0 && lane == 0) mbar_wait_drain(bar(L::kBarQdoFull), 0);
+  } else if (warp == L::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_sdp = idesc_bf16_f32(128, L::kBI, false, false);
@@ -365,7 +386,8 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const float cl2 = p.scale_log2;
     const float lse2 = h < p.H ? __ldg(p.lse + static_cast<size_t>(t) * p.H + h) : INFINITY;
-    const float dlt = h < p.H ? __ldg(p.delta + static_cast<size_t>(t) * p.H + h) : 0.f;
+    const float dlt_s =
+        h < p.H ? __ldg(p.delta + static_cast<size_t>(t) * p.H + h) * p.scale : 0.f;
     uint32_t peer_recv = 0, peer_recv_bar = 0, peer_sendok = 0;
     if (NC == 2) {
       peer_recv = mapa_shared(base + L::kOffRecv, rank ^ 1u);
@@ -383,38 +405,59 @@ __global__ void __launch_bounds__(320, 1)
       tmem_ld32(tmem + lane_base + L::kTmemDp, xp);
       tc_fence_before();
       mbar_arrive(bar(L::kBarSdpFree));
+      // zs: score in the exp2 domain; zp: sm_scale * dP (so that
+      // dS' = P (zp - sm_scale Delta) already carries the scale).
       if (NC == 2) {
+        // Exchange partial S and dP with the peer CTA (the other half of D),
+        // both rounded to fp16 first and summed in the same order on both
+        // sides; fp16 halves the bytes on the CTA-to-CTA network.
+        uint32_t hs[16], hp[16];
+#pragma unroll
+        for (int w = 0; w < 16; ++w) {
+          hs[w] = pack_f16x2_sat(xs[2 * w] * cl2, xs[2 * w + 1] * cl2);
+          hp[w] = pack_f16x2_sat(xp[2 * w] * p.scale, xp[2 * w + 1] * p.scale);
+        }
         if (i >= 1) {
           ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarSendOk), (i - 1) & 1, ctl));
           if (!ok) break;
         }
-        const uint32_t row_off = static_cast<uint32_t>(h) * 256u;
+        const uint32_t row_off = static_cast<uint32_t>(h) * 128u;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_async_v4(peer_recv + row_off + ((c ^ (h & 7)) << 4), xs[4 * c], xs[4 * c + 1],
-                      xs[4 * c + 2], xs[4 * c + 3], peer_recv_bar);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_async_v4(peer_recv + row_off + (((c + 8) ^ (h & 7)) << 4), xp[4 * c], xp[4 * c + 1],
-                      xp[4 * c + 2], xp[4 * c + 3], peer_recv_bar);
-        if (h == 0) mbar_arrive_expect_tx(bar(L::kBarRecvFull), L::kRecvBytes);
+        for (int c = 0; c < 4; ++c) {
+          st_cluster_v4u(peer_recv + row_off + ((c ^ (h & 7)) << 4), hs[4 * c], hs[4 * c + 1],
+                         hs[4 * c + 2], hs[4 * c + 3]);
+          st_cluster_v4u(peer_recv + row_off + (((c + 4) ^ (h & 7)) << 4), hp[4 * c],
+                         hp[4 * c + 1], hp[4 * c + 2], hp[4 * c + 3]);
+        }
+        mbar_arrive_remote(peer_recv_bar);
         ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull), i & 1, ctl));
         if (!ok) break;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          float y0, y1, y2, y3;
-          ld_shared_v4f(base + L::kOffRecv + row_off + ((c ^ (h & 7)) << 4), y0, y1, y2, y3);
-          xs[4 * c] += y0;
-          xs[4 * c + 1] += y1;
-          xs[4 * c + 2] += y2;
-          xs[4 * c + 3] += y3;
-          ld_shared_v4f(base + L::kOffRecv + row_off + (((c + 8) ^ (h & 7)) << 4), y0, y1, y2, y3);
-          xp[4 * c] += y0;
-          xp[4 * c + 1] += y1;
-          xp[4 * c + 2] += y2;
-          xp[4 * c + 3] += y3;
+        for (int c = 0; c < 4; ++c) {
+          uint32_t ys[4], yp[4];
+          ld_shared_v4u(base + L::kOffRecv + row_off + ((c ^ (h & 7)) << 4), ys[0], ys[1], ys[2],
+                        ys[3]);
+          ld_shared_v4u(base + L::kOffRecv + row_off + (((c + 4) ^ (h & 7)) << 4), yp[0], yp[1],
+                        yp[2], yp[3]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 ms = unpack_f16x2(hs[4 * c + k]);
+            const float2 ps = unpack_f16x2(ys[k]);
+            const float2 mp = unpack_f16x2(hp[4 * c + k]);
+            const float2 pp2 = unpack_f16x2(yp[k]);
+            xs[8 * c + 2 * k] = ms.x + ps.x;
+            xs[8 * c + 2 * k + 1] = ms.y + ps.y;
+            xp[8 * c + 2 * k] = mp.x + pp2.x;
+            xp[8 * c + 2 * k + 1] = mp.y + pp2.y;
+          }
         }
         if (i + 1 < nblk) mbar_arrive_remote(peer_sendok);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          xs[j] *= cl2;
+          xp[j] *= p.scale;
+        }
       }
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarKvFull + s), (i / L::kStages) & 1, ctl));
       if (!ok) break;
@@ -426,9 +469,9 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int jj = 2 * w + u;
-          const float pr = ((msk >> jj) & 1u) ? fast_exp2(fmaf(xs[jj], cl2, -lse2)) : 0.f;
+          const float pr = ((msk >> jj) & 1u) ? fast_exp2(xs[jj] - lse2) : 0.f;
           pv[u] = pr;
-          dv[u] = pr * (xp[jj] - dlt) * p.scale;
+          dv[u] = pr * (xp[jj] - dlt_s);
         }
         pp[w] = pack_bf16x2(pv[0], pv[1]);
         pd[w] = pack_bf16x2(dv[0], dv[1]);
@@ -475,7 +518,7 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_before();
   __syncthreads();
   if (NC == 2) cluster_sync();
-  if (warp == 9) {
+  if (warp == L::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
   }
@@ -483,8 +526,7 @@ __global__ void __launch_bounds__(320, 1)
 
 template <int DC, int NC>
 static cudaError_t launch_bwd_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_do,
-                                   const CUtensorMap& tm_kv, const BwdParams& p, int tokens,
-                                   cudaStream_t stream) {
+                                   const BwdParams& p, int tokens, cudaStream_t stream) {
   using L = BwdLayout<DC, NC>;
   auto kern = smqa_bwd_kernel<DC, NC>;
   cudaError_t e =
@@ -502,14 +544,13 @@ static cudaError_t launch_bwd_impl(const CUtensorMap& tm_q, const CUtensorMap& t
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tm_q, tm_do, tm_kv, p);
+  return cudaLaunchKernelEx(&cfg, kern, tm_q, tm_do, p);
 }
 
 cudaError_t launch_bwd_main(const CUtensorMap& tm_q, const CUtensorMap& tm_do,
-                            const CUtensorMap& tm_kv, const BwdParams& p, int tokens,
-                            cudaStream_t stream) {
-  if (p.D == 512) return launch_bwd_impl<256, 2>(tm_q, tm_do, tm_kv, p, tokens, stream);
-  if (p.D == 64) return launch_bwd_impl<64, 1>(tm_q, tm_do, tm_kv, p, tokens, stream);
+                            const BwdParams& p, int tokens, cudaStream_t stream) {
+  if (p.D == 512) return launch_bwd_impl<256, 2>(tm_q, tm_do, p, tokens, stream);
+  if (p.D == 64) return launch_bwd_impl<64, 1>(tm_q, tm_do, p, tokens, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -8,78 +8,100 @@
 //   lse[t,h] = log2 of that denominator,
 // over the slots j whose index lies in [0, S_kv).
 //
-// Design (one token per CTA, or per CTA pair when D = 512):
-//   * The token's H heads form the M = 128 rows of every MMA (heads beyond H
-//     are zero rows), so the H heads sharing one gathered kv block make a
-//     real GEMM for the tcgen05 tensor core.
-//   * D = 512: a 2-CTA cluster splits the head dim; CTA r holds columns
-//     [256r, 256r+256) of q, of every gathered kv row and of O.  Its O
-//     accumulator (128 x 256 fp32) takes half of TMEM, the score tiles the
-//     rest.  Each CTA computes partial scores over its half of D, sends them
-//     to its peer with st.async into the peer's shared memory, and adds the
-//     peer's half; both CTAs then run the same softmax on identical scores.
-//   * Warp roles: warp 4 gathers kv rows with TMA gather4 (4 rows x 128 B
-//     per instruction, 128-byte swizzle, multi-stage ring); warp 5 owns TMEM
-//     and issues the MMAs from one thread; warps 0-3 (thread = head row =
-//     TMEM lane) run the masked online softmax in the exp2 domain, rescale O
-//     lazily (only when the running max grows by more than 2^8), write P as
+// Design.  The token's H heads are the M = 128 rows of every MMA (heads
+// beyond H are zero rows), so the heads sharing one gathered kv block form a
+// real GEMM for the tcgen05 tensor core.
+//   * D = 512: two independent CTAs per token.  CTA r owns O columns
+//     [256r, 256r+256): its O accumulator (128 x 256 fp32) is half of TMEM.
+//     Both CTAs compute the FULL score tile S = Q.K^T over all 512 columns,
+//     so no partial sums cross between SMs (the CTA-to-CTA network moves
+//     only ~8 B/clk per SM, far too little for a per-block exchange).  Q's
+//     own half is an smem operand; the other half sits in TMEM as the A
+//     operand of `tcgen05.mma ... [a_tmem]` (TMEM: O 256 + two 64-column
+//     score tiles + Q 128 = 512 columns).  Both CTAs issue the K steps in the
+//     same order, so their scores, softmax and LSE are bit-identical.
+//   * D = 64: one CTA per token; Q is an smem operand.
+//   * Warp roles: warps 8-11 gather full kv rows with 16-byte cp.async
+//     (coalesced 512-byte row pieces, written into the 128-byte-swizzled
+//     K-major tile; completion signalled per block by cp.async mbarrier
+//     arrivals); warp 12 owns TMEM and issues the MMAs from one thread;
+//     warps 0-7 (two warpgroups; thread = head row = TMEM lane, 32 score
+//     columns each) run the masked online softmax in the exp2 domain, rescale
+//     O lazily (only when the running max grows by more than 2^8), write P as
 //     bf16 for the P.V MMA and finish with the sink and the log2 LSE.
 //   * Masked slots load a real (finite) row and get a -inf score, so their
 //     probability is exactly 0.
 #include <cuda_runtime.h>
+
+#include <type_traits>
 
 #include "smqa_internal.h"
 #include "smqa_ptx.cuh"
 
 namespace smqa {
 
-template <int DC, int NC>
+template <int D, int NSPLIT>
 struct FwdLayout {
-  static constexpr int kHPad = 128;         // MMA M: heads padded to 128
-  static constexpr int kBI = 64;            // slots per block
-  static constexpr int kChunks = DC / 64;   // 64-column (128-byte) swizzle chunks
-  static constexpr int kStages = NC == 2 ? 3 : 4;
-  static constexpr uint32_t kQBytes = kHPad * DC * 2;
+  static constexpr int kDC = D / NSPLIT;      // O columns (and own Q columns) per CTA
+  static constexpr int kHPad = 128;           // MMA M: heads padded to 128
+  static constexpr int kBI = 64;              // slots per block
+  static constexpr int kChunks = D / 64;      // 64-column (128-byte) swizzle chunks per row
+  static constexpr int kOwnChunks = kDC / 64;
+  static constexpr int kStages = D >= 512 ? 2 : 4;
   static constexpr uint32_t kQChunkBytes = kHPad * 128;
+  static constexpr uint32_t kQBytes = kOwnChunks * kQChunkBytes;
   static constexpr uint32_t kKvChunkBytes = kBI * 128;
   static constexpr uint32_t kKvStageBytes = kChunks * kKvChunkBytes;
   static constexpr uint32_t kPBytes = kHPad * kBI * 2;
-  static constexpr uint32_t kRecvBytes = NC == 2 ? kHPad * kBI * 4 : 0;
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffKv = kOffQ + kQBytes;
   static constexpr uint32_t kOffP = kOffKv + kStages * kKvStageBytes;
-  static constexpr uint32_t kOffRecv = kOffP + 2 * kPBytes;
-  static constexpr uint32_t kOffCtrl = kOffRecv + kRecvBytes;
-  // barrier indices
+  static constexpr uint32_t kOffCtrl = kOffP + kPBytes;
   static constexpr int kBarKvFull = 0;
   static constexpr int kBarKvEmpty = kBarKvFull + kStages;
-  static constexpr int kBarSFull = kBarKvEmpty + kStages;
-  static constexpr int kBarSFree = kBarSFull + 2;
-  static constexpr int kBarPFull = kBarSFree + 2;
-  static constexpr int kBarODone = kBarPFull + 2;
-  static constexpr int kBarRecvFull = kBarODone + 2;
-  static constexpr int kBarSendOk = kBarRecvFull + 1;
-  static constexpr int kBarQFull = kBarSendOk + 1;
-  static constexpr int kBarDrain = kBarQFull + 1;
-  static constexpr int kNumBars = kBarDrain + 1;
-  static constexpr uint32_t kOffMask = kOffCtrl + 8 * kNumBars;
-  static constexpr uint32_t kOffTmemHolder = kOffMask + 8 * kStages;
+  static constexpr int kBarSFull = kBarKvEmpty + kStages;  // phase i: S of block i ready
+  static constexpr int kBarSFree = kBarSFull + 1;          // phase i: S of block i read
+  static constexpr int kBarPFull = kBarSFree + 1;          // phase i: P of block i written
+  static constexpr int kBarODone = kBarPFull + 1;          // phase i: P.V of block i done
+  static constexpr int kBarQFull = kBarODone + 1;
+  static constexpr int kBarQtFull = kBarQFull + 1;  // other half of Q stored in TMEM
+  static constexpr int kBarDrain = kBarQtFull + 1;
+  static constexpr int kBarXmax = kBarDrain + 1;    // [2], by block parity
+  static constexpr int kBarLsum = kBarXmax + 2;
+  static constexpr int kNumBars = kBarLsum + 1;
+  static constexpr uint32_t kOffMask = kOffCtrl + 8 * kNumBars;     // uint64 [stages]
+  static constexpr uint32_t kOffXmax = kOffMask + 8 * kStages;      // float [2][2][128]
+  static constexpr uint32_t kOffLsum = kOffXmax + 2 * 2 * 128 * 4;  // float [2][128]
+  static constexpr uint32_t kOffTmemHolder = kOffLsum + 2 * 128 * 4;
   static constexpr uint32_t kOffAbort = kOffTmemHolder + 4;
-  static constexpr uint32_t kCtrlBytes = 512;
+  static constexpr uint32_t kCtrlBytes = 4096;
   static_assert(kOffAbort + 4 - kOffCtrl <= kCtrlBytes, "control block overflow");
-  // +1024 so the dynamic buffer can be realigned to 1024 bytes (swizzle atoms)
-  static constexpr uint32_t kSmemBytes = kOffCtrl + kCtrlBytes + 1024;
+  static constexpr uint32_t kSmemBytes = kOffCtrl + kCtrlBytes + 1024;  // +1024: realignment
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  // The score tile is accumulated as kChains independent partial sums (even
+  // and odd 64-column chunks of D): a chain of MMAs into one accumulator
+  // waits ~95 cycles per instruction, so two chains in flight halve the time.
+  static constexpr int kChains = kChunks >= 2 ? 2 : 1;
   static constexpr uint32_t kTmemO = 0;
-  static constexpr uint32_t kTmemS = DC;
-  static constexpr uint32_t kTmemCols = (DC + 2 * kBI) <= 256 ? 256 : 512;
-  static constexpr int kThreads = 192;
+  static constexpr uint32_t kTmemQt = kDC;                    // other half of Q, bf16 pairs
+  static constexpr uint32_t kTmemS = kDC + (D - kDC) / 2;     // kChains x kBI columns
+  static constexpr uint32_t kTmemUsed = kTmemS + kChains * kBI;
+  static constexpr uint32_t kTmemCols = kTmemUsed <= 256 ? 256 : 512;
+  static_assert(kTmemUsed <= 512, "TMEM budget");
+  static constexpr int kSoftmaxThreads = 256;
+  static constexpr int kProducerWarp0 = 8;
+  static constexpr int kProducerWarps = 4;
+  static constexpr int kMmaWarp = 12;
+  static constexpr int kThreads = 416;
+  static constexpr int kCpr = D / 8;                          // 16-byte chunks per row
+  static constexpr int kInstrPerBlock = kBI * kCpr / 32;      // warp instructions per block
 };
 
-template <int DC, int NC>
-__global__ void __launch_bounds__(192, 1)
-    smqa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
-                    const __grid_constant__ CUtensorMap tm_kv, const FwdParams p) {
-  using L = FwdLayout<DC, NC>;
+template <int D, int NSPLIT>
+__global__ void __launch_bounds__(416, 1)
+    smqa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const FwdParams p) {
+  using L = FwdLayout<D, NSPLIT>;
+  constexpr int DC = L::kDC;
   extern __shared__ uint8_t smem_raw[];
   uint32_t base = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (base & 1023u)) & 1023u;
@@ -88,44 +110,46 @@ __global__ void __launch_bounds__(192, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x / NC;
-  const uint32_t rank = NC == 2 ? cluster_ctarank() : 0u;
+  const int t = blockIdx.x / NSPLIT;
+  const int rank = NSPLIT == 2 ? static_cast<int>(blockIdx.x % NSPLIT) : 0;
   const int b = t / p.S;
   const int nblk = (p.topk + L::kBI - 1) / L::kBI;
   auto bar = [&](int i) -> uint32_t { return base + L::kOffCtrl + 8u * static_cast<uint32_t>(i); };
   volatile uint64_t* masks = reinterpret_cast<volatile uint64_t*>(smem + L::kOffMask);
+  volatile float* xmax = reinterpret_cast<volatile float*>(smem + L::kOffXmax);
+  volatile float* lsum = reinterpret_cast<volatile float*>(smem + L::kOffLsum);
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(smem + L::kOffTmemHolder);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
   const WaitCtl ctl{abort_flag, p.status, p.limit_ns};
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(bar(L::kBarKvFull + s), 1);
+      // one cp.async arrival per gather thread + one plain arrival (masks)
+      mbar_init(bar(L::kBarKvFull + s), 32 * L::kProducerWarps + 1);
       mbar_init(bar(L::kBarKvEmpty + s), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(L::kBarSFull + i), 1);
-      mbar_init(bar(L::kBarSFree + i), 128);
-      mbar_init(bar(L::kBarPFull + i), 128);
-      mbar_init(bar(L::kBarODone + i), 1);
-    }
-    mbar_init(bar(L::kBarRecvFull), 1);
-    mbar_init(bar(L::kBarSendOk), 128);
+    mbar_init(bar(L::kBarSFull), 1);
+    mbar_init(bar(L::kBarSFree), L::kSoftmaxThreads);
+    mbar_init(bar(L::kBarPFull), L::kSoftmaxThreads);
+    mbar_init(bar(L::kBarODone), 1);
+    mbar_init(bar(L::kBarXmax), L::kSoftmaxThreads);
+    mbar_init(bar(L::kBarXmax + 1), L::kSoftmaxThreads);
     mbar_init(bar(L::kBarQFull), 1);
+    mbar_init(bar(L::kBarQtFull), L::kSoftmaxThreads);
     mbar_init(bar(L::kBarDrain), 1);
+    mbar_init(bar(L::kBarLsum), L::kSoftmaxThreads);
     *abort_flag = *reinterpret_cast<volatile int*>(p.status) != 0 ? 1 : 0;
     fence_mbar_init();
   }
-  if (warp == 4 && lane == 0) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_kv);
+  if (warp == L::kMmaWarp) {
+    if (lane == 0) tma_prefetch_desc(&tm_q);
+    tmem_alloc(base + L::kOffTmemHolder, L::kTmemCols);
   }
-  if (warp == 5) tmem_alloc(base + L::kOffTmemHolder, L::kTmemCols);
-  // Heads beyond H are zero rows of the A operand (the TMA box covers H rows).
+  // Heads beyond H are zero rows of the smem A operand (the TMA box covers H rows).
   if (threadIdx.x < L::kHPad && static_cast<int>(threadIdx.x) >= p.H) {
     const uint32_t h = threadIdx.x;
 #pragma unroll
-    for (int c = 0; c < L::kChunks; ++c)
+    for (int c = 0; c < L::kOwnChunks; ++c)
 #pragma unroll
       for (int k = 0; k < 8; ++k)
         st_shared_v4(base + L::kOffQ + c * L::kQChunkBytes + h * 128u + k * 16u, 0u, 0u, 0u, 0u);
@@ -133,112 +157,157 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (NC == 2) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
-    int issued = 0;  // blocks whose gather was issued
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar(L::kBarQFull), static_cast<uint32_t>(p.H) * 128u * L::kChunks);
-      for (int c = 0; c < L::kChunks; ++c)
-        tma_load_2d(base + L::kOffQ + c * L::kQChunkBytes, &tm_q,
-                    static_cast<int>(rank) * DC + c * 64, t * p.H, bar(L::kBarQFull));
-    }
+  if (warp >= L::kProducerWarp0 && warp < L::kMmaWarp) {
+    // ------------------------------------------------------------ gather
+    // Full kv rows (all D columns) into the 128-byte-swizzled K-major tile.
+    // Instruction k of a block moves 16-byte chunks q = 32k + lane; chunk q
+    // is column chunk q % kCpr of slot row q / kCpr.
+    const int pw = warp - L::kProducerWarp0;
     const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
+    auto load_idx = [&](int blk, int half) -> int {
+      const int j = blk * L::kBI + 32 * half + lane;
+      return j < p.topk ? __ldg(idx_row + j) : -1;
+    };
+    int n0 = load_idx(0, 0), n1 = load_idx(0, 1);
+    if (pw == 0 && lane == 0) {
+      mbar_arrive_expect_tx(bar(L::kBarQFull), static_cast<uint32_t>(p.H) * 128u * L::kOwnChunks);
+      for (int c = 0; c < L::kOwnChunks; ++c)
+        tma_load_2d(base + L::kOffQ + c * L::kQChunkBytes, &tm_q, rank * DC + c * 64, t * p.H,
+                    bar(L::kBarQFull));
+    }
     for (int i = 0; i < nblk; ++i) {
       const int s = i % L::kStages;
-      if (i >= L::kStages) {
-        bool ok = mbar_wait(bar(L::kBarKvEmpty + s), ((i / L::kStages) - 1) & 1, ctl);
-        if (!__all_sync(0xffffffffu, ok)) break;
+      const int r0 = n0, r1 = n1;
+      if (i + 1 < nblk) {
+        n0 = load_idx(i + 1, 0);
+        n1 = load_idx(i + 1, 1);
       }
-      const int j0 = i * L::kBI + lane;
-      const int j1 = j0 + 32;
-      const int r0 = j0 < p.topk ? __ldg(idx_row + j0) : -1;
-      const int r1 = j1 < p.topk ? __ldg(idx_row + j1) : -1;
       const bool v0 = static_cast<unsigned>(r0) < static_cast<unsigned>(p.S_kv);
       const bool v1 = static_cast<unsigned>(r1) < static_cast<unsigned>(p.S_kv);
       const int row0 = b * p.S_kv + (v0 ? r0 : 0);
       const int row1 = b * p.S_kv + (v1 ? r1 : 0);
+      if (i >= L::kStages) {
+        const bool ok = mbar_wait(bar(L::kBarKvEmpty + s), ((i / L::kStages) - 1) & 1, ctl);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+      const uint32_t stage = base + L::kOffKv + s * L::kKvStageBytes;
+#pragma unroll 4
+      for (int k = pw; k < L::kInstrPerBlock; k += L::kProducerWarps) {
+        const int q = 32 * k + lane;
+        const int r = q / L::kCpr;
+        const int cc = q % L::kCpr;
+        const int a = __shfl_sync(0xffffffffu, row0, r & 31);
+        const int c2 = __shfl_sync(0xffffffffu, row1, r & 31);
+        const int rr = r < 32 ? a : c2;
+        cp_async_16(stage + static_cast<uint32_t>(cc / 8) * L::kKvChunkBytes +
+                        static_cast<uint32_t>(r) * 128u +
+                        ((static_cast<uint32_t>(cc % 8) ^ (static_cast<uint32_t>(r) & 7u)) << 4),
+                    p.kv + static_cast<size_t>(rr) * D + cc * 8);
+      }
+      cp_async_arrive_noinc(bar(L::kBarKvFull + s));
       const uint32_t m_lo = __ballot_sync(0xffffffffu, v0);
       const uint32_t m_hi = __ballot_sync(0xffffffffu, v1);
-      int gy[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int src = 4 * (lane & 15) + k;
-        const int a = __shfl_sync(0xffffffffu, row0, src & 31);
-        const int c = __shfl_sync(0xffffffffu, row1, src & 31);
-        gy[k] = src < 32 ? a : c;
-      }
-      if (lane == 0) {
+      if (pw == 0 && lane == 0) {
         masks[s] = static_cast<uint64_t>(m_lo) | (static_cast<uint64_t>(m_hi) << 32);
-        mbar_arrive_expect_tx(bar(L::kBarKvFull + s), L::kKvStageBytes);
+        mbar_arrive(bar(L::kBarKvFull + s));
       }
-      __syncwarp();
-      if (lane < 16) {
-        const uint32_t dst0 = base + L::kOffKv + s * L::kKvStageBytes + lane * 4u * 128u;
-#pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_gather4(dst0 + c * L::kKvChunkBytes, &tm_kv, static_cast<int>(rank) * DC + c * 64,
-                      gy[0], gy[1], gy[2], gy[3], bar(L::kBarKvFull + s));
-      }
-      issued = i + 1;
     }
     // Let every copy this warp started land before the CTA can exit.
-    if (lane == 0) {
-      mbar_wait_drain(bar(L::kBarQFull), 0);
-      for (int i = issued - L::kStages; i < issued; ++i)
-        if (i >= 0) mbar_wait_drain(bar(L::kBarKvFull + i % L::kStages), (i / L::kStages) & 1);
-    }
-  } else if (warp == 5) {
+    cp_async_wait_group<0>();
+    if (pw == 0 && lane == 0) mbar_wait_drain(bar(L::kBarQFull), 0);
+  } else if (warp == L::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, L::kBI, false, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, DC, false, true);
-      auto issue_pv = [&](int j) -> bool {
-        const int bj = j & 1;
+      // Descriptors are built once; per MMA only the start-address field
+      // (bits 0-13, in 16-byte units) moves, by compile-time offsets.
+      const uint64_t d_q = smem_desc(base + L::kOffQ, 16u, 1024u, kSwizzle128B);
+      const uint64_t d_p = smem_desc(base + L::kOffP, 16u, 1024u, kSwizzle128B);
+      const uint64_t d_kv0 = smem_desc(base + L::kOffKv, 16u, 1024u, kSwizzle128B);
+      const uint64_t d_v0 = smem_desc(base + L::kOffKv, L::kKvChunkBytes, 1024u, kSwizzle128B) +
+                            ((static_cast<uint32_t>(rank * L::kOwnChunks) * L::kKvChunkBytes) >> 4);
+      const uint32_t t_s = tmem + L::kTmemS;
+      const uint32_t t_qt = tmem + L::kTmemQt;
+      // O += P.V for block j (P ready, kv stage still resident); V = this
+      // CTA's column half of the gathered rows, read MN-major.
+      auto issue_pv = [&](int j) {
         const int sj = j % L::kStages;
-        if (!mbar_wait(bar(L::kBarPFull + bj), (j >> 1) & 1, ctl)) return false;
-        tc_fence_after();
-        const uint32_t p_base = base + L::kOffP + bj * L::kPBytes;
-        const uint32_t v_base = base + L::kOffKv + sj * L::kKvStageBytes;
+        const uint64_t d_v = d_v0 + ((static_cast<uint32_t>(sj) * L::kKvStageBytes) >> 4);
 #pragma unroll
-        for (int k = 0; k < L::kBI / 16; ++k) {
-          const uint64_t a = smem_desc(p_base + k * 32u, 16u, 1024u, kSwizzle128B);
-          const uint64_t bd = smem_desc(v_base + k * 2048u, L::kKvChunkBytes, 1024u, kSwizzle128B);
-          mma_ss(tmem + L::kTmemO, a, bd, idesc_o, (j > 0 || k > 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < L::kBI / 16; ++k)
+          mma_ss(tmem + L::kTmemO, d_p + (k * 32u >> 4), d_v + (k * 2048u >> 4), idesc_o,
+                 (j > 0 || k > 0) ? 1u : 0u);
         mma_commit(bar(L::kBarKvEmpty + sj));
-        mma_commit(bar(L::kBarODone + bj));
-        return true;
+        mma_commit(bar(L::kBarODone));
       };
-      bool ok = mbar_wait(bar(L::kBarQFull), 0, ctl);
-      for (int i = 0; ok && i < nblk; ++i) {
-        const int s = i % L::kStages;
-        const int bb = i & 1;
-        if (!mbar_wait(bar(L::kBarKvFull + s), (i / L::kStages) & 1, ctl)) { ok = false; break; }
-        if (i >= 2 && !mbar_wait(bar(L::kBarSFree + bb), ((i >> 1) - 1) & 1, ctl)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t kv_base = base + L::kOffKv + s * L::kKvStageBytes;
+      // S = Q.K^T for block i over all D columns, in the same chunk order on
+      // both CTAs: own chunks from smem Q, the other half from TMEM Q; chunk
+      // c accumulates into chain c % kChains.  The rank is made a compile-time
+      // value so the whole sequence is straight-line code.
+      auto issue_s_rank = [&](auto rank_c, int i) {
+        constexpr int kRank = decltype(rank_c)::value;
+        const uint64_t d_kv = d_kv0 + ((static_cast<uint32_t>(i % L::kStages) * L::kKvStageBytes) >> 4);
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c) {
+          const uint32_t d_tm = t_s + (c % L::kChains) * L::kBI;
+          const int sub = c % L::kOwnChunks;  // chunk index within its half
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint64_t a = smem_desc(base + L::kOffQ + c * L::kQChunkBytes + k * 32u, 16u,
-                                         1024u, kSwizzle128B);
-            const uint64_t bd = smem_desc(kv_base + c * L::kKvChunkBytes + k * 32u, 16u, 1024u,
-                                          kSwizzle128B);
-            mma_ss(tmem + L::kTmemS + bb * L::kBI, a, bd, idesc_s, (c | k) != 0 ? 1u : 0u);
+            const uint64_t bd = d_kv + ((c * L::kKvChunkBytes + k * 32u) >> 4);
+            const uint32_t acc = (c >= L::kChains || k > 0) ? 1u : 0u;
+            if ((c / L::kOwnChunks) == kRank)
+              mma_ss(d_tm, d_q + ((sub * L::kQChunkBytes + k * 32u) >> 4), bd, idesc_s, acc);
+            else
+              mma_ts(d_tm, t_qt + (sub * 4 + k) * 8, bd, idesc_s, acc);
           }
         }
-        mma_commit(bar(L::kBarSFull + bb));
-        if (i >= 1 && !issue_pv(i - 1)) { ok = false; break; }
+        mma_commit(bar(L::kBarSFull));
+      };
+      auto issue_s = [&](int i) {
+        if (NSPLIT == 2 && rank == 1)
+          issue_s_rank(std::integral_constant<int, 1>{}, i);
+        else
+          issue_s_rank(std::integral_constant<int, 0>{}, i);
+      };
+      bool ok = mbar_wait(bar(L::kBarQFull), 0, ctl);
+      if (ok && NSPLIT == 2) ok = mbar_wait(bar(L::kBarQtFull), 0, ctl);
+      // Event loop: issue P.V of the oldest block whose P is ready, else S of
+      // the next block once its kv stage has landed and the score tile has
+      // been read; both chains share the tensor pipe in issue order.
+      int ns = 0, npv = 0;
+      uint64_t t_last = globaltimer_ns();
+      uint32_t spins = 0;
+      while (ok && npv < nblk) {
+        if (npv < ns && mbar_test(bar(L::kBarPFull), npv & 1)) {
+          tc_fence_after();
+          issue_pv(npv);
+          ++npv;
+        } else if (ns < nblk && ns <= npv + 1 &&
+                   (ns == 0 || mbar_test(bar(L::kBarSFree), (ns - 1) & 1)) &&
+                   mbar_test(bar(L::kBarKvFull + ns % L::kStages), (ns / L::kStages) & 1)) {
+          // The kv tile was written by cp.async (generic proxy): order it
+          // before the tensor core's (async proxy) reads.
+          fence_proxy_async_smem();
+          tc_fence_after();
+          issue_s(ns);
+          ++ns;
+        } else {
+          if ((++spins & 63u) == 0u) {
+            if (ctl_aborted(ctl)) { ok = false; break; }
+            if (globaltimer_ns() - t_last > ctl.limit_ns) {
+              ctl_abort(ctl);
+              ok = false;
+              break;
+            }
+          }
+          continue;
+        }
+        t_last = globaltimer_ns();
       }
-      if (ok) issue_pv(nblk - 1);
       // No MMA may still be running when TMEM is released.
       mma_commit(bar(L::kBarDrain));
       mbar_wait_drain(bar(L::kBarDrain), 0);
@@ -246,142 +315,144 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int h = threadIdx.x;  // head row == TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // Thread (h, g): head row h (TMEM lane), score columns [32g, 32g+32) of
+    // every block, O columns [DC/2 g, DC/2 (g+1)) for rescaling and output.
+    const int g = warp >> 2;
+    const int h = threadIdx.x & 127;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     // exp2 argument: score * (c log2 e), or (score * c) * log2 e with the
     // reference-rounding flag (x * s1 * 1 is exact when the flag is off).
     const float s1 = p.ref_round ? p.scale : p.scale_log2;
     const float s2 = p.ref_round ? 1.4426950408889634f : 1.f;
-    float m_run = -INFINITY;
-    float l_run = 0.f;
-    uint32_t peer_recv = 0, peer_recv_bar = 0, peer_sendok = 0;
-    if (NC == 2) {
-      peer_recv = mapa_shared(base + L::kOffRecv, rank ^ 1u);
-      peer_recv_bar = mapa_shared(bar(L::kBarRecvFull), rank ^ 1u);
-      peer_sendok = mapa_shared(bar(L::kBarSendOk), rank ^ 1u);
+    constexpr int kOHalf = DC / 2;
+    if (NSPLIT == 2) {
+      // The other column half of this head's q row -> TMEM (A operand of the
+      // score MMA), as bf16 pairs: this thread stores words [64g, 64g+64).
+      const int ocol = (1 - rank) * DC + g * 128;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + (static_cast<size_t>(t) * p.H + (h < p.H ? h : 0)) * D + ocol);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float v[32];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 w = h < p.H ? __ldg(src + half * 8 + k) : make_uint4(0u, 0u, 0u, 0u);
+          v[4 * k] = __uint_as_float(w.x);
+          v[4 * k + 1] = __uint_as_float(w.y);
+          v[4 * k + 2] = __uint_as_float(w.z);
+          v[4 * k + 3] = __uint_as_float(w.w);
+        }
+        tmem_st32(tmem + lane_base + L::kTmemQt + 64 * g + 32 * half, v);
+      }
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarQtFull));
     }
+    float m_run = -INFINITY;
+    float l_part = 0.f;
     bool ok = true;
     for (int i = 0; i < nblk; ++i) {
       const int bb = i & 1;
       const int s = i % L::kStages;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + bb), (i >> 1) & 1, ctl));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull), i & 1, ctl));
       if (!ok) break;
       tc_fence_after();
-      float x[64];
-      {
-        float* x0 = x;
-        tmem_ld32(tmem + lane_base + L::kTmemS + bb * L::kBI,
-                  *reinterpret_cast<float(*)[32]>(x0));
-        tmem_ld32(tmem + lane_base + L::kTmemS + bb * L::kBI + 32,
-                  *reinterpret_cast<float(*)[32]>(x0 + 32));
+      float x[32];
+      tmem_ld32(tmem + lane_base + L::kTmemS + 32 * g, x);
+      if (L::kChains == 2) {
+        float x2[32];
+        tmem_ld32(tmem + lane_base + L::kTmemS + L::kBI + 32 * g, x2);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] += x2[j];
       }
       tc_fence_before();
-      mbar_arrive(bar(L::kBarSFree + bb));
-      if (NC == 2) {
-        // Exchange partial scores with the peer CTA (the other half of D).
-        if (i >= 1) {
-          ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarSendOk), (i - 1) & 1, ctl));
-          if (!ok) break;
-        }
-        const uint32_t row_off = static_cast<uint32_t>(h) * 256u;
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          st_async_v4(peer_recv + row_off + ((c ^ (h & 7)) << 4), x[4 * c], x[4 * c + 1],
-                      x[4 * c + 2], x[4 * c + 3], peer_recv_bar);
-        if (h == 0) mbar_arrive_expect_tx(bar(L::kBarRecvFull), L::kRecvBytes);
-        ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull), i & 1, ctl));
-        if (!ok) break;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          float y0, y1, y2, y3;
-          ld_shared_v4f(base + L::kOffRecv + row_off + ((c ^ (h & 7)) << 4), y0, y1, y2, y3);
-          x[4 * c] += y0;
-          x[4 * c + 1] += y1;
-          x[4 * c + 2] += y2;
-          x[4 * c + 3] += y3;
-        }
-        if (i + 1 < nblk) mbar_arrive_remote(peer_sendok);
-      }
+      mbar_arrive(bar(L::kBarSFree));
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarKvFull + s), (i / L::kStages) & 1, ctl));
       if (!ok) break;
-      const uint64_t msk = masks[s];
-      float mx = -INFINITY;
+      const uint32_t msk = static_cast<uint32_t>(masks[s] >> (32 * g));
+      float mq[8];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        x[j] = ((msk >> j) & 1ull) ? (x[j] * s1) * s2 : -INFINITY;
-        mx = fmaxf(mx, x[j]);
-      }
+      for (int j = 0; j < 32; ++j) x[j] = ((msk >> j) & 1u) ? (x[j] * s1) * s2 : -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        mq[j] = fmaxf(fmaxf(x[4 * j], x[4 * j + 1]), fmaxf(x[4 * j + 2], x[4 * j + 3]));
+      const float mloc = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])),
+                               fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
+      // Combine with the other half of the row (the thread of the other
+      // warpgroup with the same h); buffers alternate by block parity.
+      xmax[(bb * 2 + g) * 128 + h] = mloc;
+      mbar_arrive(bar(L::kBarXmax + bb));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarXmax + bb), (i >> 1) & 1, ctl));
+      if (!ok) break;
+      const float mx = fmaxf(mloc, xmax[(bb * 2 + (g ^ 1)) * 128 + h]);
       const float m_new = fmaxf(m_run, mx);
       const bool bump = (m_run == -INFINITY) ? (m_new != -INFINITY) : (m_new > m_run + 8.f);
       float alpha = 1.f;
       if (bump) {
         alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_new);
-        l_run *= alpha;
+        l_part *= alpha;
         m_run = m_new;
       }
-      // O was accumulated against the old max: rescale it (whole warp, since
-      // the TMEM accesses are warp-collective; rows without a bump use 1).
-      const bool need_rescale = bump && alpha != 0.f && i > 0;
-      if (__any_sync(0xffffffffu, need_rescale)) {
-        const int jp = i - 1;
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(bar(L::kBarODone + (jp & 1)), (jp >> 1) & 1, ctl));
+      // The P buffer and the O accumulator are free once P.V of block i-1
+      // has completed.
+      if (i >= 1) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone), (i - 1) & 1, ctl));
         if (!ok) break;
         tc_fence_after();
+      }
+      // O was accumulated against the old max: rescale this thread's half of
+      // the row (whole warp, since TMEM accesses are warp-collective; rows
+      // without a bump use 1).
+      const bool need_rescale = bump && alpha != 0.f && i > 0;
+      if (__any_sync(0xffffffffu, need_rescale)) {
         const float a = need_rescale ? alpha : 1.f;
 #pragma unroll 1
-        for (int c = 0; c < DC / 32; ++c) {
+        for (int c = 0; c < kOHalf / 32; ++c) {
           float v[32];
-          tmem_ld32(tmem + lane_base + L::kTmemO + c * 32, v);
+          tmem_ld32(tmem + lane_base + L::kTmemO + g * kOHalf + c * 32, v);
 #pragma unroll
           for (int k = 0; k < 32; ++k) v[k] *= a;
-          tmem_st32(tmem + lane_base + L::kTmemO + c * 32, v);
+          tmem_st32(tmem + lane_base + L::kTmemO + g * kOHalf + c * 32, v);
         }
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      // P buffer `bb` was last read by the P.V MMA of block i-2.
-      if (i >= 2) {
-        const int jp = i - 2;
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(bar(L::kBarODone + (jp & 1)), (jp >> 1) & 1, ctl));
-        if (!ok) break;
-      }
-      uint32_t pk[32];
-      float rs = 0.f;
+      uint32_t pk[16];
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int w = 0; w < 32; ++w) {
+      for (int w = 0; w < 16; ++w) {
         const float p0 = fast_exp2(x[2 * w] - m_use);
         const float p1 = fast_exp2(x[2 * w + 1] - m_use);
         pk[w] = pack_bf16x2(p0, p1);
-        rs += p0 + p1;  // fp32 probabilities: the LSE must not carry bf16 rounding
+        rs[w & 3] += p0 + p1;  // fp32 probabilities: the LSE must not carry bf16 rounding
       }
-      l_run += rs;
-      const uint32_t p_row = base + L::kOffP + bb * L::kPBytes + static_cast<uint32_t>(h) * 128u;
+      l_part += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+      const uint32_t p_row = base + L::kOffP + static_cast<uint32_t>(h) * 128u;
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_shared_v4(p_row + ((c ^ (h & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                     pk[4 * c + 3]);
+      for (int c = 0; c < 4; ++c)
+        st_shared_v4(p_row + (((4 * g + c) ^ (h & 7)) << 4), pk[4 * c], pk[4 * c + 1],
+                     pk[4 * c + 2], pk[4 * c + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(L::kBarPFull + bb));
+      mbar_arrive(bar(L::kBarPFull));
     }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone), (nblk - 1) & 1, ctl));
+    // Row sums: the two halves of each row meet here.
+    lsum[g * 128 + h] = l_part;
+    mbar_arrive(bar(L::kBarLsum));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarLsum), 0, ctl));
     if (ok) {
-      const int jl = nblk - 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + (jl & 1)), (jl >> 1) & 1, ctl));
-    }
-    if (ok) {
+      const float l_run = lsum[h] + lsum[128 + h];
       tc_fence_after();
       const float sink2 = h < p.H ? __ldg(p.sink + h) * 1.4426950408889634f : 0.f;
       const float m_fin = fmaxf(m_run, sink2);
       const float so = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_fin);
       const float Z = l_run * so + fast_exp2(sink2 - m_fin);
       const float inv = so / Z;
-      __nv_bfloat16* orow = p.o + (static_cast<size_t>(t) * p.H + h) * p.D +
-                            static_cast<size_t>(rank) * DC;
+      __nv_bfloat16* orow = p.o + (static_cast<size_t>(t) * p.H + h) * D +
+                            static_cast<size_t>(rank) * DC + g * kOHalf;
 #pragma unroll 1
-      for (int c = 0; c < DC / 32; ++c) {
+      for (int c = 0; c < kOHalf / 32; ++c) {
         float v[32];
-        tmem_ld32(tmem + lane_base + L::kTmemO + c * 32, v);
+        tmem_ld32(tmem + lane_base + L::kTmemO + g * kOHalf + c * 32, v);
         if (h < p.H) {
           uint32_t w[16];
 #pragma unroll
@@ -392,46 +463,35 @@ __global__ void __launch_bounds__(192, 1)
             dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
         }
       }
-      if (rank == 0 && h < p.H) p.lse[static_cast<size_t>(t) * p.H + h] = m_fin + log2f(Z);
+      if (rank == 0 && g == 0 && h < p.H)
+        p.lse[static_cast<size_t>(t) * p.H + h] = m_fin + log2f(Z);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (NC == 2) cluster_sync();
-  if (warp == 5) {
+  if (warp == L::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
   }
 }
 
-template <int DC, int NC>
-static cudaError_t launch_fwd_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
-                                   const FwdParams& p, int tokens, cudaStream_t stream) {
-  using L = FwdLayout<DC, NC>;
-  auto kern = smqa_fwd_kernel<DC, NC>;
+template <int D, int NSPLIT>
+static cudaError_t launch_fwd_impl(const CUtensorMap& tm_q, const FwdParams& p, int tokens,
+                                   cudaStream_t stream) {
+  using L = FwdLayout<D, NSPLIT>;
+  auto kern = smqa_fwd_kernel<D, NSPLIT>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(tokens) * NC, 1, 1);
-  cfg.blockDim = dim3(L::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = L::kSmemBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = NC;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tm_q, tm_kv, p);
+  kern<<<static_cast<unsigned>(tokens) * NSPLIT, L::kThreads, L::kSmemBytes, stream>>>(tm_q, p);
+  return cudaGetLastError();
 }
 
-cudaError_t launch_fwd(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const FwdParams& p,
-                       int tokens, cudaStream_t stream) {
-  if (p.D == 512) return launch_fwd_impl<256, 2>(tm_q, tm_kv, p, tokens, stream);
-  if (p.D == 64) return launch_fwd_impl<64, 1>(tm_q, tm_kv, p, tokens, stream);
+cudaError_t launch_fwd(const CUtensorMap& tm_q, const FwdParams& p, int tokens,
+                       cudaStream_t stream) {
+  if (p.D == 512) return launch_fwd_impl<512, 2>(tm_q, p, tokens, stream);
+  if (p.D == 64) return launch_fwd_impl<64, 1>(tm_q, p, tokens, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -10,6 +10,8 @@
 namespace smqa {
 
 struct FwdParams {
+  const __nv_bfloat16* q;   // [B,S,H,D]
+  const __nv_bfloat16* kv;  // [B,S_kv,D]
   const int32_t* idx;    // [B,S,topk]
   const float* sink;     // [H]
   __nv_bfloat16* o;      // [B,S,H,D]
@@ -23,6 +25,7 @@ struct FwdParams {
 };
 
 struct BwdParams {
+  const __nv_bfloat16* kv;  // [B,S_kv,D]
   const int32_t* idx;    // [B,S,topk]
   const float* lse;      // [B,S,H]  log2 LSE from the forward
   const float* delta;    // [B,S,H]  rowsum(O * dO)
@@ -38,11 +41,10 @@ struct BwdParams {
 // Records `msg` as the text smqa_last_error() returns on this thread.
 void set_last_error(const char* msg);
 
-cudaError_t launch_fwd(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const FwdParams& p,
-                       int tokens, cudaStream_t stream);
+cudaError_t launch_fwd(const CUtensorMap& tm_q, const FwdParams& p, int tokens,
+                       cudaStream_t stream);
 cudaError_t launch_bwd_main(const CUtensorMap& tm_q, const CUtensorMap& tm_do,
-                            const CUtensorMap& tm_kv, const BwdParams& p, int tokens,
-                            cudaStream_t stream);
+                            const BwdParams& p, int tokens, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* dout,
                                   float* delta, float* dkv_acc, int64_t rows, int D,
                                   int64_t acc_elems, cudaStream_t stream);
