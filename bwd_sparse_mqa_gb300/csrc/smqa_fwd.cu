@@ -33,8 +33,6 @@
 //     probability is exactly 0.
 #include <cuda_runtime.h>
 
-#include <type_traits>
-
 #include "smqa_internal.h"
 #include "smqa_ptx.cuh"
 
@@ -44,58 +42,86 @@ template <int D, int NSPLIT>
 struct FwdLayout {
   static constexpr int kDC = D / NSPLIT;      // O columns (and own Q columns) per CTA
   static constexpr int kHPad = 128;           // MMA M: heads padded to 128
-  static constexpr int kBI = 64;              // slots per block
+  static constexpr int kBI = 64;              // slots per block (MMA N of the scores)
   static constexpr int kChunks = D / 64;      // 64-column (128-byte) swizzle chunks per row
   static constexpr int kOwnChunks = kDC / 64;
-  static constexpr int kStages = D >= 512 ? 2 : 4;
+  static constexpr int kOthChunks = kChunks - kOwnChunks;
+  static constexpr int kStages = D >= 512 ? 2 : 4;   // slots of each ring
   static constexpr uint32_t kQChunkBytes = kHPad * 128;
   static constexpr uint32_t kQBytes = kOwnChunks * kQChunkBytes;
-  static constexpr uint32_t kKvChunkBytes = kBI * 128;
-  static constexpr uint32_t kKvStageBytes = kChunks * kKvChunkBytes;
+  static constexpr uint32_t kKvChunkBytes = kBI * 128;   // kBI rows x 128 B
+  static constexpr uint32_t kOwnStageBytes = kOwnChunks * kKvChunkBytes;
+  static constexpr uint32_t kOthStageBytes = kOthChunks * kKvChunkBytes;
   static constexpr uint32_t kPBytes = kHPad * kBI * 2;
   static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffKv = kOffQ + kQBytes;
-  static constexpr uint32_t kOffP = kOffKv + kStages * kKvStageBytes;
+  static constexpr uint32_t kOffOwn = kOffQ + kQBytes;
+  static constexpr uint32_t kOffOth = kOffOwn + kStages * kOwnStageBytes;
+  static constexpr uint32_t kOffP = kOffOth + kStages * kOthStageBytes;
   static constexpr uint32_t kOffCtrl = kOffP + kPBytes;
-  static constexpr int kBarKvFull = 0;
-  static constexpr int kBarKvEmpty = kBarKvFull + kStages;
-  static constexpr int kBarSFull = kBarKvEmpty + kStages;  // phase i: S of block i ready
-  static constexpr int kBarSFree = kBarSFull + 1;          // phase i: S of block i read
-  static constexpr int kBarPFull = kBarSFree + 1;          // phase i: P of block i written
-  static constexpr int kBarODone = kBarPFull + 1;          // phase i: P.V of block i done
+  static constexpr int kBarOwnFull = 0;
+  static constexpr int kBarOwnEmpty = kBarOwnFull + kStages;
+  static constexpr int kBarOthFull = kBarOwnEmpty + kStages;
+  static constexpr int kBarOthEmpty = kBarOthFull + kStages;
+  static constexpr int kBarSFull = kBarOthEmpty + kStages;  // phase i: S of block i ready
+  static constexpr int kBarSFree = kBarSFull + 1;           // phase i: S of block i read
+  static constexpr int kBarPFull = kBarSFree + 1;           // phase i: P of block i written
+  static constexpr int kBarODone = kBarPFull + 1;           // phase i: P.V of block i done
   static constexpr int kBarQFull = kBarODone + 1;
-  static constexpr int kBarQtFull = kBarQFull + 1;  // other half of Q stored in TMEM
+  static constexpr int kBarQtFull = kBarQFull + 1;   // other half of Q stored in TMEM
   static constexpr int kBarDrain = kBarQtFull + 1;
-  static constexpr int kBarXmax = kBarDrain + 1;    // [2], by block parity
+  static constexpr int kBarXmax = kBarDrain + 1;     // [2], by block parity
   static constexpr int kBarLsum = kBarXmax + 2;
   static constexpr int kNumBars = kBarLsum + 1;
-  static constexpr uint32_t kOffMask = kOffCtrl + 8 * kNumBars;     // uint64 [stages]
-  static constexpr uint32_t kOffXmax = kOffMask + 8 * kStages;      // float [2][2][128]
-  static constexpr uint32_t kOffLsum = kOffXmax + 2 * 2 * 128 * 4;  // float [2][128]
+  static constexpr uint32_t kOffXmax = kOffCtrl + 8 * kNumBars;    // float [2][2][128]
+  static constexpr uint32_t kOffLsum = kOffXmax + 2 * 2 * 128 * 4; // float [2][128]
   static constexpr uint32_t kOffTmemHolder = kOffLsum + 2 * 128 * 4;
   static constexpr uint32_t kOffAbort = kOffTmemHolder + 4;
   static constexpr uint32_t kCtrlBytes = 4096;
   static_assert(kOffAbort + 4 - kOffCtrl <= kCtrlBytes, "control block overflow");
   static constexpr uint32_t kSmemBytes = kOffCtrl + kCtrlBytes + 1024;  // +1024: realignment
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  // The score tile is accumulated as kChains independent partial sums (even
-  // and odd 64-column chunks of D): a chain of MMAs into one accumulator
-  // waits ~95 cycles per instruction, so two chains in flight halve the time.
-  static constexpr int kChains = kChunks >= 2 ? 2 : 1;
+  // TMEM: O, the other half of Q (bf16 pairs), then the score tile as two
+  // partial sums: chain A over the own column half, chain B over the other.
   static constexpr uint32_t kTmemO = 0;
-  static constexpr uint32_t kTmemQt = kDC;                    // other half of Q, bf16 pairs
-  static constexpr uint32_t kTmemS = kDC + (D - kDC) / 2;     // kChains x kBI columns
-  static constexpr uint32_t kTmemUsed = kTmemS + kChains * kBI;
+  static constexpr uint32_t kTmemQt = kDC;
+  static constexpr uint32_t kTmemSA = kDC + (D - kDC) / 2;
+  static constexpr uint32_t kTmemSB = kTmemSA + kBI;
+  static constexpr uint32_t kTmemUsed = kTmemSA + (kOthChunks > 0 ? 2 : 1) * kBI;
   static constexpr uint32_t kTmemCols = kTmemUsed <= 256 ? 256 : 512;
   static_assert(kTmemUsed <= 512, "TMEM budget");
+  // warps 0-7: softmax; 8-9: gather own column half; 10-11: gather the other
+  // half; 12: TMEM owner + MMA issuer
   static constexpr int kSoftmaxThreads = 256;
-  static constexpr int kProducerWarp0 = 8;
-  static constexpr int kProducerWarps = 4;
+  static constexpr int kOwnWarp0 = 8;
+  static constexpr int kOthWarp0 = 10;
   static constexpr int kMmaWarp = 12;
   static constexpr int kThreads = 416;
-  static constexpr int kCpr = D / 8;                          // 16-byte chunks per row
-  static constexpr int kInstrPerBlock = kBI * kCpr / 32;      // warp instructions per block
 };
+
+// Gathers one column half of a block's kv rows into a 128-byte-swizzled
+// K-major tile of `nchunks` 64-column chunks.  Warp w (0 or 1) of the pair
+// issues instructions w, w+2, ...; instruction k moves 16-byte pieces
+// q = 32k + lane, piece q being column piece q % (8 nchunks) of slot row
+// q / (8 nchunks).
+template <int NCHUNKS, int D>
+__device__ __forceinline__ void gather_half(uint32_t stage, const __nv_bfloat16* kv, int col0,
+                                            int row0, int row1, int w, int lane) {
+  constexpr int kRcpr = NCHUNKS * 8;
+  constexpr int kInstr = 64 * kRcpr / 32;
+#pragma unroll 4
+  for (int k = w; k < kInstr; k += 2) {
+    const int q = 32 * k + lane;
+    const int r = q / kRcpr;
+    const int cc = q % kRcpr;
+    const int a = __shfl_sync(0xffffffffu, row0, r & 31);
+    const int c2 = __shfl_sync(0xffffffffu, row1, r & 31);
+    const int rr = r < 32 ? a : c2;
+    cp_async_16(stage + static_cast<uint32_t>(cc / 8) * (64u * 128u) +
+                    static_cast<uint32_t>(r) * 128u +
+                    ((static_cast<uint32_t>(cc % 8) ^ (static_cast<uint32_t>(r) & 7u)) << 4),
+                kv + static_cast<size_t>(rr) * D + col0 + cc * 8);
+  }
+}
 
 template <int D, int NSPLIT>
 __global__ void __launch_bounds__(416, 1)
@@ -114,8 +140,8 @@ __global__ void __launch_bounds__(416, 1)
   const int rank = NSPLIT == 2 ? static_cast<int>(blockIdx.x % NSPLIT) : 0;
   const int b = t / p.S;
   const int nblk = (p.topk + L::kBI - 1) / L::kBI;
+  const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
   auto bar = [&](int i) -> uint32_t { return base + L::kOffCtrl + 8u * static_cast<uint32_t>(i); };
-  volatile uint64_t* masks = reinterpret_cast<volatile uint64_t*>(smem + L::kOffMask);
   volatile float* xmax = reinterpret_cast<volatile float*>(smem + L::kOffXmax);
   volatile float* lsum = reinterpret_cast<volatile float*>(smem + L::kOffLsum);
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(smem + L::kOffTmemHolder);
@@ -124,19 +150,20 @@ __global__ void __launch_bounds__(416, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < L::kStages; ++s) {
-      // one cp.async arrival per gather thread + one plain arrival (masks)
-      mbar_init(bar(L::kBarKvFull + s), 32 * L::kProducerWarps + 1);
-      mbar_init(bar(L::kBarKvEmpty + s), 1);
+      mbar_init(bar(L::kBarOwnFull + s), 64);  // one cp.async arrival per gather thread
+      mbar_init(bar(L::kBarOwnEmpty + s), 1);
+      mbar_init(bar(L::kBarOthFull + s), 64);
+      mbar_init(bar(L::kBarOthEmpty + s), 1);
     }
     mbar_init(bar(L::kBarSFull), 1);
     mbar_init(bar(L::kBarSFree), L::kSoftmaxThreads);
     mbar_init(bar(L::kBarPFull), L::kSoftmaxThreads);
     mbar_init(bar(L::kBarODone), 1);
-    mbar_init(bar(L::kBarXmax), L::kSoftmaxThreads);
-    mbar_init(bar(L::kBarXmax + 1), L::kSoftmaxThreads);
     mbar_init(bar(L::kBarQFull), 1);
     mbar_init(bar(L::kBarQtFull), L::kSoftmaxThreads);
     mbar_init(bar(L::kBarDrain), 1);
+    mbar_init(bar(L::kBarXmax), L::kSoftmaxThreads);
+    mbar_init(bar(L::kBarXmax + 1), L::kSoftmaxThreads);
     mbar_init(bar(L::kBarLsum), L::kSoftmaxThreads);
     *abort_flag = *reinterpret_cast<volatile int*>(p.status) != 0 ? 1 : 0;
     fence_mbar_init();
@@ -160,64 +187,56 @@ __global__ void __launch_bounds__(416, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp >= L::kProducerWarp0 && warp < L::kMmaWarp) {
+  if (warp >= L::kOwnWarp0 && warp < L::kMmaWarp) {
     // ------------------------------------------------------------ gather
-    // Full kv rows (all D columns) into the 128-byte-swizzled K-major tile.
-    // Instruction k of a block moves 16-byte chunks q = 32k + lane; chunk q
-    // is column chunk q % kCpr of slot row q / kCpr.
-    const int pw = warp - L::kProducerWarp0;
-    const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
-    auto load_idx = [&](int blk, int half) -> int {
-      const int j = blk * L::kBI + 32 * half + lane;
-      return j < p.topk ? __ldg(idx_row + j) : -1;
-    };
-    int n0 = load_idx(0, 0), n1 = load_idx(0, 1);
-    if (pw == 0 && lane == 0) {
-      mbar_arrive_expect_tx(bar(L::kBarQFull), static_cast<uint32_t>(p.H) * 128u * L::kOwnChunks);
-      for (int c = 0; c < L::kOwnChunks; ++c)
-        tma_load_2d(base + L::kOffQ + c * L::kQChunkBytes, &tm_q, rank * DC + c * 64, t * p.H,
-                    bar(L::kBarQFull));
+    // Warps 8-9 fill the own-column-half ring (needed until P.V), warps
+    // 10-11 the other-half ring (needed only by the scores), so the other
+    // half of block i+2 can land as soon as the scores of block i are done.
+    const bool own = warp < L::kOthWarp0;
+    const int w = (warp - L::kOwnWarp0) & 1;
+    if (own || L::kOthChunks > 0) {
+      auto load_idx = [&](int blk, int half) -> int {
+        const int j = blk * L::kBI + 32 * half + lane;
+        return j < p.topk ? __ldg(idx_row + j) : -1;
+      };
+      if (own && w == 0 && lane == 0) {
+        mbar_arrive_expect_tx(bar(L::kBarQFull),
+                              static_cast<uint32_t>(p.H) * 128u * L::kOwnChunks);
+        for (int c = 0; c < L::kOwnChunks; ++c)
+          tma_load_2d(base + L::kOffQ + c * L::kQChunkBytes, &tm_q, rank * DC + c * 64, t * p.H,
+                      bar(L::kBarQFull));
+      }
+      const int full0 = own ? L::kBarOwnFull : L::kBarOthFull;
+      const int empty0 = own ? L::kBarOwnEmpty : L::kBarOthEmpty;
+      const uint32_t ring = base + (own ? L::kOffOwn : L::kOffOth);
+      const uint32_t stage_bytes = own ? L::kOwnStageBytes : L::kOthStageBytes;
+      const int col0 = (own ? rank : 1 - rank) * DC;
+      int n0 = load_idx(0, 0), n1 = load_idx(0, 1);
+      for (int i = 0; i < nblk; ++i) {
+        const int s = i % L::kStages;
+        const int r0 = n0, r1 = n1;
+        if (i + 1 < nblk) {
+          n0 = load_idx(i + 1, 0);
+          n1 = load_idx(i + 1, 1);
+        }
+        const int row0 = b * p.S_kv + (static_cast<unsigned>(r0) < static_cast<unsigned>(p.S_kv) ? r0 : 0);
+        const int row1 = b * p.S_kv + (static_cast<unsigned>(r1) < static_cast<unsigned>(p.S_kv) ? r1 : 0);
+        if (i >= L::kStages) {
+          const bool ok = mbar_wait(bar(empty0 + s), ((i / L::kStages) - 1) & 1, ctl);
+          if (!__all_sync(0xffffffffu, ok)) break;
+        }
+        const uint32_t stage = ring + static_cast<uint32_t>(s) * stage_bytes;
+        if (own)
+          gather_half<L::kOwnChunks, D>(stage, p.kv, col0, row0, row1, w, lane);
+        else
+          gather_half<(L::kOthChunks > 0 ? L::kOthChunks : 1), D>(stage, p.kv, col0, row0, row1,
+                                                                  w, lane);
+        cp_async_arrive_noinc(bar(full0 + s));
+      }
+      // Let every copy this warp started land before the CTA can exit.
+      cp_async_wait_group<0>();
+      if (own && w == 0 && lane == 0) mbar_wait_drain(bar(L::kBarQFull), 0);
     }
-    for (int i = 0; i < nblk; ++i) {
-      const int s = i % L::kStages;
-      const int r0 = n0, r1 = n1;
-      if (i + 1 < nblk) {
-        n0 = load_idx(i + 1, 0);
-        n1 = load_idx(i + 1, 1);
-      }
-      const bool v0 = static_cast<unsigned>(r0) < static_cast<unsigned>(p.S_kv);
-      const bool v1 = static_cast<unsigned>(r1) < static_cast<unsigned>(p.S_kv);
-      const int row0 = b * p.S_kv + (v0 ? r0 : 0);
-      const int row1 = b * p.S_kv + (v1 ? r1 : 0);
-      if (i >= L::kStages) {
-        const bool ok = mbar_wait(bar(L::kBarKvEmpty + s), ((i / L::kStages) - 1) & 1, ctl);
-        if (!__all_sync(0xffffffffu, ok)) break;
-      }
-      const uint32_t stage = base + L::kOffKv + s * L::kKvStageBytes;
-#pragma unroll 4
-      for (int k = pw; k < L::kInstrPerBlock; k += L::kProducerWarps) {
-        const int q = 32 * k + lane;
-        const int r = q / L::kCpr;
-        const int cc = q % L::kCpr;
-        const int a = __shfl_sync(0xffffffffu, row0, r & 31);
-        const int c2 = __shfl_sync(0xffffffffu, row1, r & 31);
-        const int rr = r < 32 ? a : c2;
-        cp_async_16(stage + static_cast<uint32_t>(cc / 8) * L::kKvChunkBytes +
-                        static_cast<uint32_t>(r) * 128u +
-                        ((static_cast<uint32_t>(cc % 8) ^ (static_cast<uint32_t>(r) & 7u)) << 4),
-                    p.kv + static_cast<size_t>(rr) * D + cc * 8);
-      }
-      cp_async_arrive_noinc(bar(L::kBarKvFull + s));
-      const uint32_t m_lo = __ballot_sync(0xffffffffu, v0);
-      const uint32_t m_hi = __ballot_sync(0xffffffffu, v1);
-      if (pw == 0 && lane == 0) {
-        masks[s] = static_cast<uint64_t>(m_lo) | (static_cast<uint64_t>(m_hi) << 32);
-        mbar_arrive(bar(L::kBarKvFull + s));
-      }
-    }
-    // Let every copy this warp started land before the CTA can exit.
-    cp_async_wait_group<0>();
-    if (pw == 0 && lane == 0) mbar_wait_drain(bar(L::kBarQFull), 0);
   } else if (warp == L::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -227,74 +246,76 @@ __global__ void __launch_bounds__(416, 1)
       // (bits 0-13, in 16-byte units) moves, by compile-time offsets.
       const uint64_t d_q = smem_desc(base + L::kOffQ, 16u, 1024u, kSwizzle128B);
       const uint64_t d_p = smem_desc(base + L::kOffP, 16u, 1024u, kSwizzle128B);
-      const uint64_t d_kv0 = smem_desc(base + L::kOffKv, 16u, 1024u, kSwizzle128B);
-      const uint64_t d_v0 = smem_desc(base + L::kOffKv, L::kKvChunkBytes, 1024u, kSwizzle128B) +
-                            ((static_cast<uint32_t>(rank * L::kOwnChunks) * L::kKvChunkBytes) >> 4);
-      const uint32_t t_s = tmem + L::kTmemS;
-      const uint32_t t_qt = tmem + L::kTmemQt;
-      // O += P.V for block j (P ready, kv stage still resident); V = this
-      // CTA's column half of the gathered rows, read MN-major.
+      const uint64_t d_own = smem_desc(base + L::kOffOwn, 16u, 1024u, kSwizzle128B);
+      const uint64_t d_oth = smem_desc(base + L::kOffOth, 16u, 1024u, kSwizzle128B);
+      const uint64_t d_v = smem_desc(base + L::kOffOwn, L::kKvChunkBytes, 1024u, kSwizzle128B);
+      // Chain A: own column half, Q from smem.  Chain B: the other half, Q
+      // from TMEM.  Chunk j of a half is chunk j of that half on both CTAs,
+      // so each chain sums the same products in the same order everywhere.
+      auto issue_a = [&](int i) {
+        const uint64_t dk = d_own + ((static_cast<uint32_t>(i % L::kStages) * L::kOwnStageBytes) >> 4);
+#pragma unroll
+        for (int c = 0; c < L::kOwnChunks; ++c)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem + L::kTmemSA, d_q + ((c * L::kQChunkBytes + k * 32u) >> 4),
+                   dk + ((c * L::kKvChunkBytes + k * 32u) >> 4), idesc_s, (c | k) ? 1u : 0u);
+      };
+      auto issue_b = [&](int i) {
+        const uint64_t dk = d_oth + ((static_cast<uint32_t>(i % L::kStages) * L::kOthStageBytes) >> 4);
+#pragma unroll
+        for (int c = 0; c < L::kOthChunks; ++c)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ts(tmem + L::kTmemSB, tmem + L::kTmemQt + (c * 4 + k) * 8,
+                   dk + ((c * L::kKvChunkBytes + k * 32u) >> 4), idesc_s, (c | k) ? 1u : 0u);
+      };
+      // O += P.V for block j; V = the own column half, read MN-major.
       auto issue_pv = [&](int j) {
         const int sj = j % L::kStages;
-        const uint64_t d_v = d_v0 + ((static_cast<uint32_t>(sj) * L::kKvStageBytes) >> 4);
+        const uint64_t dv = d_v + ((static_cast<uint32_t>(sj) * L::kOwnStageBytes) >> 4);
 #pragma unroll
         for (int k = 0; k < L::kBI / 16; ++k)
-          mma_ss(tmem + L::kTmemO, d_p + (k * 32u >> 4), d_v + (k * 2048u >> 4), idesc_o,
+          mma_ss(tmem + L::kTmemO, d_p + (k * 32u >> 4), dv + (k * 2048u >> 4), idesc_o,
                  (j > 0 || k > 0) ? 1u : 0u);
-        mma_commit(bar(L::kBarKvEmpty + sj));
+        mma_commit(bar(L::kBarOwnEmpty + sj));
         mma_commit(bar(L::kBarODone));
-      };
-      // S = Q.K^T for block i over all D columns, in the same chunk order on
-      // both CTAs: own chunks from smem Q, the other half from TMEM Q; chunk
-      // c accumulates into chain c % kChains.  The rank is made a compile-time
-      // value so the whole sequence is straight-line code.
-      auto issue_s_rank = [&](auto rank_c, int i) {
-        constexpr int kRank = decltype(rank_c)::value;
-        const uint64_t d_kv = d_kv0 + ((static_cast<uint32_t>(i % L::kStages) * L::kKvStageBytes) >> 4);
-#pragma unroll
-        for (int c = 0; c < L::kChunks; ++c) {
-          const uint32_t d_tm = t_s + (c % L::kChains) * L::kBI;
-          const int sub = c % L::kOwnChunks;  // chunk index within its half
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t bd = d_kv + ((c * L::kKvChunkBytes + k * 32u) >> 4);
-            const uint32_t acc = (c >= L::kChains || k > 0) ? 1u : 0u;
-            if ((c / L::kOwnChunks) == kRank)
-              mma_ss(d_tm, d_q + ((sub * L::kQChunkBytes + k * 32u) >> 4), bd, idesc_s, acc);
-            else
-              mma_ts(d_tm, t_qt + (sub * 4 + k) * 8, bd, idesc_s, acc);
-          }
-        }
-        mma_commit(bar(L::kBarSFull));
-      };
-      auto issue_s = [&](int i) {
-        if (NSPLIT == 2 && rank == 1)
-          issue_s_rank(std::integral_constant<int, 1>{}, i);
-        else
-          issue_s_rank(std::integral_constant<int, 0>{}, i);
       };
       bool ok = mbar_wait(bar(L::kBarQFull), 0, ctl);
       if (ok && NSPLIT == 2) ok = mbar_wait(bar(L::kBarQtFull), 0, ctl);
-      // Event loop: issue P.V of the oldest block whose P is ready, else S of
-      // the next block once its kv stage has landed and the score tile has
-      // been read; both chains share the tensor pipe in issue order.
-      int ns = 0, npv = 0;
+      // Event loop over three kinds of work, oldest first: P.V of block npv
+      // once its P is written; chain A (+ completion of S) of block na once
+      // the own half has landed; chain B of block nb once the other half has
+      // landed.  Both score chains of a block need the previous block's
+      // scores to have been read (one score tile in TMEM), and a block's
+      // scores may complete at most one block ahead of P.V.
+      constexpr bool kHasB = L::kOthChunks > 0;
+      int nb = 0, na = 0, npv = 0;
       uint64_t t_last = globaltimer_ns();
       uint32_t spins = 0;
       while (ok && npv < nblk) {
-        if (npv < ns && mbar_test(bar(L::kBarPFull), npv & 1)) {
+        if (npv < na && mbar_test(bar(L::kBarPFull), npv & 1)) {
           tc_fence_after();
           issue_pv(npv);
           ++npv;
-        } else if (ns < nblk && ns <= npv + 1 &&
-                   (ns == 0 || mbar_test(bar(L::kBarSFree), (ns - 1) & 1)) &&
-                   mbar_test(bar(L::kBarKvFull + ns % L::kStages), (ns / L::kStages) & 1)) {
+        } else if (na < nblk && (!kHasB || nb > na) && na <= npv + 1 &&
+                   (na == 0 || mbar_test(bar(L::kBarSFree), (na - 1) & 1)) &&
+                   mbar_test(bar(L::kBarOwnFull + na % L::kStages), (na / L::kStages) & 1)) {
           // The kv tile was written by cp.async (generic proxy): order it
           // before the tensor core's (async proxy) reads.
           fence_proxy_async_smem();
           tc_fence_after();
-          issue_s(ns);
-          ++ns;
+          issue_a(na);
+          mma_commit(bar(L::kBarSFull));
+          if (kHasB) mma_commit(bar(L::kBarOthEmpty + na % L::kStages));
+          ++na;
+        } else if (kHasB && nb < nblk && nb <= na &&
+                   (nb == 0 || mbar_test(bar(L::kBarSFree), (nb - 1) & 1)) &&
+                   mbar_test(bar(L::kBarOthFull + nb % L::kStages), (nb / L::kStages) & 1)) {
+          fence_proxy_async_smem();
+          tc_fence_after();
+          issue_b(nb);
+          ++nb;
         } else {
           if ((++spins & 63u) == 0u) {
             if (ctl_aborted(ctl)) { ok = false; break; }
@@ -326,8 +347,8 @@ __global__ void __launch_bounds__(416, 1)
     const float s2 = p.ref_round ? 1.4426950408889634f : 1.f;
     constexpr int kOHalf = DC / 2;
     if (NSPLIT == 2) {
-      // The other column half of this head's q row -> TMEM (A operand of the
-      // score MMA), as bf16 pairs: this thread stores words [64g, 64g+64).
+      // The other column half of this head's q row -> TMEM (A operand of
+      // score chain B), as bf16 pairs: this thread stores words [64g, 64g+64).
       const int ocol = (1 - rank) * DC + g * 128;
       const uint4* src = reinterpret_cast<const uint4*>(
           p.q + (static_cast<size_t>(t) * p.H + (h < p.H ? h : 0)) * D + ocol);
@@ -347,28 +368,36 @@ __global__ void __launch_bounds__(416, 1)
       tc_fence_before();
       mbar_arrive(bar(L::kBarQtFull));
     }
+    // Slot validity: lane j of each warp holds slot 32g + j of the block;
+    // the warp's ballot is this thread's 32-bit column mask (read one block
+    // ahead from L2).
+    auto slot_ok = [&](int blk) -> bool {
+      const int j = blk * L::kBI + 32 * g + lane;
+      if (j >= p.topk) return false;
+      const int r = __ldg(idx_row + j);
+      return static_cast<unsigned>(r) < static_cast<unsigned>(p.S_kv);
+    };
+    bool v_next = slot_ok(0);
     float m_run = -INFINITY;
     float l_part = 0.f;
     bool ok = true;
     for (int i = 0; i < nblk; ++i) {
       const int bb = i & 1;
-      const int s = i % L::kStages;
+      const uint32_t msk = __ballot_sync(0xffffffffu, v_next);
+      if (i + 1 < nblk) v_next = slot_ok(i + 1);
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull), i & 1, ctl));
       if (!ok) break;
       tc_fence_after();
       float x[32];
-      tmem_ld32(tmem + lane_base + L::kTmemS + 32 * g, x);
-      if (L::kChains == 2) {
+      tmem_ld32(tmem + lane_base + L::kTmemSA + 32 * g, x);
+      if (L::kOthChunks > 0) {
         float x2[32];
-        tmem_ld32(tmem + lane_base + L::kTmemS + L::kBI + 32 * g, x2);
+        tmem_ld32(tmem + lane_base + L::kTmemSB + 32 * g, x2);
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[j] += x2[j];
       }
       tc_fence_before();
       mbar_arrive(bar(L::kBarSFree));
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarKvFull + s), (i / L::kStages) & 1, ctl));
-      if (!ok) break;
-      const uint32_t msk = static_cast<uint32_t>(masks[s] >> (32 * g));
       float mq[8];
 #pragma unroll
       for (int j = 0; j < 32; ++j) x[j] = ((msk >> j) & 1u) ? (x[j] * s1) * s2 : -INFINITY;
