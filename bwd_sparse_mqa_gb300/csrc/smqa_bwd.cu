@@ -280,38 +280,41 @@ __global__ void __launch_bounds__(352, 1)
       constexpr uint32_t idesc_sdp = idesc_bf16_f32(128, L::kBI, false, false);
       constexpr uint32_t idesc_dq = idesc_bf16_f32(128, DC, false, true);
       constexpr uint32_t idesc_dkv = idesc_bf16_f32(128, L::kBI, true, true);
+      // Descriptors are built once; per MMA only the start-address field
+      // (bits 0-13, in 16-byte units) moves, by compile-time offsets.
+      const uint64_t d_q = smem_desc(base + L::kOffQ, 16u, 1024u, kSwizzle128B);
+      const uint64_t d_do = smem_desc(base + L::kOffDo, 16u, 1024u, kSwizzle128B);
+      const uint64_t d_kv = smem_desc(base + L::kOffKv, 16u, 1024u, kSwizzle128B);
+      const uint64_t d_kvmn = smem_desc(base + L::kOffKv, L::kKvChunkBytes, 1024u, kSwizzle128B);
+      const uint64_t d_ds = smem_desc(base + L::kOffDs, 16u, 512u, kSwizzle64B);
+      const uint64_t d_qt = smem_desc(base + L::kOffQ, L::kQChunkBytes, 1024u, kSwizzle128B);
+      const uint64_t d_dot = smem_desc(base + L::kOffDo, L::kQChunkBytes, 1024u, kSwizzle128B);
+      const uint64_t d_dsmn = smem_desc(base + L::kOffDs, 8192u, 512u, kSwizzle64B);
+      const uint64_t d_pmn = smem_desc(base + L::kOffP, 8192u, 512u, kSwizzle64B);
       auto issue_grad = [&](int j) -> bool {
         const int bk = j & 1;
         const int sj = j % L::kStages;
         if (!mbar_wait(bar(L::kBarPdsFull), j & 1, ctl)) return false;
         if (j >= 2 && !mbar_wait(bar(L::kBarDkvFree + bk), ((j >> 1) - 1) & 1, ctl)) return false;
         tc_fence_after();
-        const uint32_t kv_base = base + L::kOffKv + sj * L::kKvStageBytes;
+        const uint64_t dkv = d_kvmn + ((static_cast<uint32_t>(sj) * L::kKvStageBytes) >> 4);
         // dQ += dS' . K   (M = 128 heads, N = DC, K = 32 slots)
 #pragma unroll
-        for (int k = 0; k < L::kBI / 16; ++k) {
-          const uint64_t a = smem_desc(base + L::kOffDs + k * 32u, 16u, 512u, kSwizzle64B);
-          const uint64_t bd = smem_desc(kv_base + k * 2048u, L::kKvChunkBytes, 1024u, kSwizzle128B);
-          mma_ss(tmem + L::kTmemDq, a, bd, idesc_dq, (j > 0 || k > 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < L::kBI / 16; ++k)
+          mma_ss(tmem + L::kTmemDq, d_ds + (k * 32u >> 4), dkv + (k * 2048u >> 4), idesc_dq,
+                 (j > 0 || k > 0) ? 1u : 0u);
         // dKV^T[e] = Q^T[e] . dS' + dO^T[e] . P   (M = 128 dims, N = 32 slots, K = 128 heads)
 #pragma unroll
         for (int e = 0; e < L::kNE; ++e) {
           const uint32_t d_tm = tmem + L::kTmemDkv + (bk * L::kNE + e) * L::kBI;
 #pragma unroll
-          for (int k = 0; k < L::kHPad / 16; ++k) {
-            const uint64_t a = smem_desc(base + L::kOffQ + 2 * e * L::kQChunkBytes + k * 2048u,
-                                         L::kQChunkBytes, 1024u, kSwizzle128B);
-            const uint64_t bd = smem_desc(base + L::kOffDs + k * 1024u, 8192u, 512u, kSwizzle64B);
-            mma_ss(d_tm, a, bd, idesc_dkv, k > 0 ? 1u : 0u);
-          }
+          for (int k = 0; k < L::kHPad / 16; ++k)
+            mma_ss(d_tm, d_qt + ((2 * e * L::kQChunkBytes + k * 2048u) >> 4),
+                   d_dsmn + (k * 1024u >> 4), idesc_dkv, k > 0 ? 1u : 0u);
 #pragma unroll
-          for (int k = 0; k < L::kHPad / 16; ++k) {
-            const uint64_t a = smem_desc(base + L::kOffDo + 2 * e * L::kQChunkBytes + k * 2048u,
-                                         L::kQChunkBytes, 1024u, kSwizzle128B);
-            const uint64_t bd = smem_desc(base + L::kOffP + k * 1024u, 8192u, 512u, kSwizzle64B);
-            mma_ss(d_tm, a, bd, idesc_dkv, 1u);
-          }
+          for (int k = 0; k < L::kHPad / 16; ++k)
+            mma_ss(d_tm, d_dot + ((2 * e * L::kQChunkBytes + k * 2048u) >> 4),
+                   d_pmn + (k * 1024u >> 4), idesc_dkv, 1u);
         }
         mma_commit(bar(L::kBarPdsFree));
         mma_commit(bar(L::kBarKvEmpty + sj));
@@ -324,19 +327,17 @@ __global__ void __launch_bounds__(352, 1)
         if (!mbar_wait(bar(L::kBarKvFull + s), (i / L::kStages) & 1, ctl)) { ok = false; break; }
         if (i >= 1 && !mbar_wait(bar(L::kBarSdpFree), (i - 1) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kv_base = base + L::kOffKv + s * L::kKvStageBytes;
+        const uint64_t dk = d_kv + ((static_cast<uint32_t>(s) * L::kKvStageBytes) >> 4);
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint64_t bd = smem_desc(kv_base + c * L::kKvChunkBytes + k * 32u, 16u, 1024u,
-                                          kSwizzle128B);
-            const uint64_t aq = smem_desc(base + L::kOffQ + c * L::kQChunkBytes + k * 32u, 16u,
-                                          1024u, kSwizzle128B);
-            const uint64_t ad = smem_desc(base + L::kOffDo + c * L::kQChunkBytes + k * 32u, 16u,
-                                          1024u, kSwizzle128B);
-            mma_ss(tmem + L::kTmemS, aq, bd, idesc_sdp, (c | k) != 0 ? 1u : 0u);
-            mma_ss(tmem + L::kTmemDp, ad, bd, idesc_sdp, (c | k) != 0 ? 1u : 0u);
+            const uint64_t bd = dk + ((c * L::kKvChunkBytes + k * 32u) >> 4);
+            const uint32_t acc = (c | k) != 0 ? 1u : 0u;
+            mma_ss(tmem + L::kTmemS, d_q + ((c * L::kQChunkBytes + k * 32u) >> 4), bd, idesc_sdp,
+                   acc);
+            mma_ss(tmem + L::kTmemDp, d_do + ((c * L::kQChunkBytes + k * 32u) >> 4), bd,
+                   idesc_sdp, acc);
           }
         }
         mma_commit(bar(L::kBarSdpFull));
