@@ -100,7 +100,7 @@ struct BwdLayout {
   static constexpr uint32_t kKvChunkBytes = kBI * 128;           // 4 KB
   static constexpr uint32_t kKvStageBytes = kChunks * kKvChunkBytes;
   static constexpr uint32_t kPBytes = kHPad * kBI * 2;           // 8 KB (64-byte rows)
-  // peer's partial S and dP, fp16 (see the exchange in the P / dS role)
+  // peer's partial S and dP of one block, fp16; two buffers (block parity)
   static constexpr uint32_t kRecvBytes = NC == 2 ? kHPad * 2 * kBI * 2 : 0;
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffDo = kOffQ + kQBytes;
@@ -110,42 +110,46 @@ struct BwdLayout {
   static constexpr uint32_t kOffP = kOffKv + kStages * kKvStageBytes;
   static constexpr uint32_t kOffDs = kOffP + kPBytes;
   static constexpr uint32_t kOffRecv = kOffDs + kPBytes;
-  static constexpr uint32_t kOffCtrl = kOffRecv + kRecvBytes;
+  static constexpr uint32_t kOffCtrl = kOffRecv + 2 * kRecvBytes;
   static constexpr int kBarKvFull = 0;
   static constexpr int kBarKvEmpty = kBarKvFull + kStages;
-  static constexpr int kBarSdpFull = kBarKvEmpty + kStages;
-  static constexpr int kBarSdpFree = kBarSdpFull + 1;
-  static constexpr int kBarPdsFull = kBarSdpFree + 1;
+  static constexpr int kBarSdpFull = kBarKvEmpty + kStages;  // [2], by block parity
+  static constexpr int kBarSdpFree = kBarSdpFull + 2;         // [2]
+  static constexpr int kBarPdsFull = kBarSdpFree + 2;
   static constexpr int kBarPdsFree = kBarPdsFull + 1;
   static constexpr int kBarDkvFull = kBarPdsFree + 1;  // [2]
   static constexpr int kBarDkvFree = kBarDkvFull + 2;  // [2]
-  static constexpr int kBarRecvFull = kBarDkvFree + 2;
-  static constexpr int kBarSendOk = kBarRecvFull + 1;
-  static constexpr int kBarQdoFull = kBarSendOk + 1;
+  static constexpr int kBarRecvFull = kBarDkvFree + 2;  // [2]
+  static constexpr int kBarSendOk = kBarRecvFull + 2;    // [2]
+  static constexpr int kBarQdoFull = kBarSendOk + 2;
   static constexpr int kBarDqDone = kBarQdoFull + 1;
   static constexpr int kBarDrain = kBarDqDone + 1;
   static constexpr int kNumBars = kBarDrain + 1;
-  static constexpr uint32_t kOffMask = kOffCtrl + 8 * kNumBars;
-  static constexpr uint32_t kOffTmemHolder = kOffMask + 8 * kStages;
+  static constexpr uint32_t kOffTmemHolder = kOffCtrl + 8 * kNumBars;
   static constexpr uint32_t kOffAbort = kOffTmemHolder + 4;
   static constexpr uint32_t kCtrlBytes = 512;
   static_assert(kOffAbort + 4 - kOffCtrl <= kCtrlBytes, "control block overflow");
   static constexpr uint32_t kSmemBytes = kOffCtrl + kCtrlBytes + 1024;
+  // TMEM: dQ, then two S/dP buffers (block parity), then two dKV^T buffers.
   static constexpr uint32_t kTmemDq = 0;
-  static constexpr uint32_t kTmemS = DC;
-  static constexpr uint32_t kTmemDp = DC + kBI;
-  static constexpr uint32_t kTmemDkv = DC + 2 * kBI;  // + buf * kNE * kBI + e * kBI
+  static constexpr uint32_t kTmemS = DC;              // + buf * 2 kBI
+  static constexpr uint32_t kTmemDp = DC + kBI;       // + buf * 2 kBI
+  static constexpr uint32_t kTmemDkv = DC + 4 * kBI;  // + buf * kNE * kBI + e * kBI
   static constexpr uint32_t kTmemUsed = kTmemDkv + 2 * kNE * kBI;
   static constexpr uint32_t kTmemCols = kTmemUsed <= 256 ? 256 : 512;
   // warps 0-3: P / dS (thread = head row); 4-7: dKV drain (thread = head-dim
-  // row); 8-9: gather; 10: TMEM owner + MMA issuer
+  // row); 8-9: gather; 10: TMEM owner + MMA issuer; 11-14 (D split across
+  // the pair only): send this CTA's partial S / dP to the peer.
   static constexpr int kProducerWarp0 = 8;
   static constexpr int kMmaWarp = 10;
-  static constexpr int kThreads = 352;
+  static constexpr int kSenderWarp0 = 11;
+  static constexpr int kThreads = NC == 2 ? 480 : 352;
+  // Readers of a S / dP buffer: the P / dS warps and the senders.
+  static constexpr int kSdpReaders = NC == 2 ? 256 : 128;
 };
 
 template <int DC, int NC>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
     smqa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
   using L = BwdLayout<DC, NC>;
@@ -162,7 +166,6 @@ __global__ void __launch_bounds__(352, 1)
   const int b = t / p.S;
   const int nblk = (p.topk + L::kBI - 1) / L::kBI;
   auto bar = [&](int i) -> uint32_t { return base + L::kOffCtrl + 8u * static_cast<uint32_t>(i); };
-  volatile uint64_t* masks = reinterpret_cast<volatile uint64_t*>(smem + L::kOffMask);
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(smem + L::kOffTmemHolder);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
   const WaitCtl ctl{abort_flag, p.status, p.limit_ns};
@@ -172,21 +175,32 @@ __global__ void __launch_bounds__(352, 1)
       mbar_init(bar(L::kBarKvFull + s), 64);  // every gather thread arrives
       mbar_init(bar(L::kBarKvEmpty + s), 1);
     }
-    mbar_init(bar(L::kBarSdpFull), 1);
-    mbar_init(bar(L::kBarSdpFree), 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(L::kBarSdpFull + i), 1);
+      mbar_init(bar(L::kBarSdpFree + i), L::kSdpReaders);
+    }
     mbar_init(bar(L::kBarPdsFull), 128);
     mbar_init(bar(L::kBarPdsFree), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(L::kBarDkvFull + i), 1);
       mbar_init(bar(L::kBarDkvFree + i), 128);
     }
-    mbar_init(bar(L::kBarRecvFull), 128);
-    mbar_init(bar(L::kBarSendOk), 128);
+    // Receive buffers: one local arrival (with the expected bytes) per
+    // phase, the bytes counted by the peer's st.async; the peer's four P / dS
+    // warps each free a buffer once.
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(L::kBarRecvFull + i), 1);
+      mbar_init(bar(L::kBarSendOk + i), 4);
+    }
     mbar_init(bar(L::kBarQdoFull), 1);
     mbar_init(bar(L::kBarDqDone), 1);
     mbar_init(bar(L::kBarDrain), 1);
     *abort_flag = *reinterpret_cast<volatile int*>(p.status) != 0 ? 1 : 0;
     fence_mbar_init();
+    if (NC == 2) {
+      mbar_arrive_expect_tx(bar(L::kBarRecvFull), L::kRecvBytes);
+      if (nblk > 1) mbar_arrive_expect_tx(bar(L::kBarRecvFull + 1), L::kRecvBytes);
+    }
   }
   if (warp == L::kMmaWarp) {
     if (lane == 0) {
@@ -241,19 +255,16 @@ __global__ void __launch_bounds__(352, 1)
                     bar(L::kBarQdoFull));
       }
     }
-    int i = 0;
-    for (; i < nblk; ++i) {
+    for (int i = 0; i < nblk; ++i) {
       const int s = i % L::kStages;
       const int r = r_next;
       if (i + 1 < nblk) r_next = load_idx(i + 1);
       const bool v = static_cast<unsigned>(r) < static_cast<unsigned>(p.S_kv);
       const int row = b * p.S_kv + (v ? r : 0);
-      const uint32_t m = __ballot_sync(0xffffffffu, v);
       if (i >= L::kStages) {
         const bool ok = mbar_wait(bar(L::kBarKvEmpty + s), ((i / L::kStages) - 1) & 1, ctl);
         if (!__all_sync(0xffffffffu, ok)) break;
       }
-      if (pw == 0 && lane == 0) masks[s] = m;
       const uint32_t stage = base + L::kOffKv + s * L::kKvStageBytes + lane_off;
 #pragma unroll
       for (int k = 0; k < 16 / kRpi; ++k) {
@@ -263,16 +274,12 @@ __global__ void __launch_bounds__(352, 1)
         cp_async_16(stage + srow * 128u + ((c16 ^ (srow & 7u)) << 4),
                     kv_col + static_cast<size_t>(rr) * p.D);
       }
-      cp_async_commit();
-      if (i >= 1) {
-        cp_async_wait_group<1>();
-        fence_proxy_async_smem();
-        mbar_arrive(bar(L::kBarKvFull + (i - 1) % L::kStages));
-      }
+      // Arrives on the stage's full barrier once this thread's copies of the
+      // block have landed; the MMA thread fences them into the async proxy.
+      cp_async_arrive_noinc(bar(L::kBarKvFull + s));
     }
-    cp_async_wait_group<0>();
-    fence_proxy_async_smem();
-    if (i == nblk) mbar_arrive(bar(L::kBarKvFull + (nblk - 1) % L::kStages));
+    // Let every copy this warp started land before the CTA can exit.
+    cp_async_wait_all();
     if (warp == L::kProducerWarp0 && lane == 0) mbar_wait_drain(bar(L::kBarQdoFull), 0);
   } else if (warp == L::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -321,34 +328,93 @@ __global__ void __launch_bounds__(352, 1)
         mma_commit(bar(L::kBarDkvFull + bk));
         return true;
       };
-      bool ok = mbar_wait(bar(L::kBarQdoFull), 0, ctl);
-      for (int i = 0; ok && i < nblk; ++i) {
+      // S and dP of block i into TMEM buffer i & 1 (M = 128 heads, N = 32
+      // slots, K = this CTA's D slice).
+      auto issue_sdp = [&](int i) -> bool {
         const int s = i % L::kStages;
-        if (!mbar_wait(bar(L::kBarKvFull + s), (i / L::kStages) & 1, ctl)) { ok = false; break; }
-        if (i >= 1 && !mbar_wait(bar(L::kBarSdpFree), (i - 1) & 1, ctl)) { ok = false; break; }
+        const int sb = i & 1;
+        if (!mbar_wait(bar(L::kBarKvFull + s), (i / L::kStages) & 1, ctl)) return false;
+        // Both buffers: the tile of block i-2 (same buffer) and of block i-1
+        // must have been read.  Waiting for block i-1 keeps the S / dP MMAs
+        // from competing for shared memory with the exchange of block i-1.
+        if (i >= 1 && !mbar_wait(bar(L::kBarSdpFree + (sb ^ 1)), ((i - 1) >> 1) & 1, ctl))
+          return false;
+        // The kv tile was written by cp.async (generic proxy): order it before
+        // the tensor core's (async proxy) reads.
+        fence_proxy_async_smem();
         tc_fence_after();
         const uint64_t dk = d_kv + ((static_cast<uint32_t>(s) * L::kKvStageBytes) >> 4);
+        const uint32_t t_s = tmem + L::kTmemS + sb * 2 * L::kBI;
+        const uint32_t t_dp = tmem + L::kTmemDp + sb * 2 * L::kBI;
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t bd = dk + ((c * L::kKvChunkBytes + k * 32u) >> 4);
             const uint32_t acc = (c | k) != 0 ? 1u : 0u;
-            mma_ss(tmem + L::kTmemS, d_q + ((c * L::kQChunkBytes + k * 32u) >> 4), bd, idesc_sdp,
-                   acc);
-            mma_ss(tmem + L::kTmemDp, d_do + ((c * L::kQChunkBytes + k * 32u) >> 4), bd,
-                   idesc_sdp, acc);
+            mma_ss(t_s, d_q + ((c * L::kQChunkBytes + k * 32u) >> 4), bd, idesc_sdp, acc);
+            mma_ss(t_dp, d_do + ((c * L::kQChunkBytes + k * 32u) >> 4), bd, idesc_sdp, acc);
           }
         }
-        mma_commit(bar(L::kBarSdpFull));
-        if (i >= 1 && !issue_grad(i - 1)) { ok = false; break; }
+        mma_commit(bar(L::kBarSdpFull + sb));
+        return true;
+      };
+      // S/dP of block i + 1 go to the tensor core ahead of the gradients of
+      // block i, so they run while block i's P / dS are being formed.
+      bool ok = mbar_wait(bar(L::kBarQdoFull), 0, ctl) && issue_sdp(0);
+      for (int i = 0; ok && i < nblk; ++i) {
+        if (i + 1 < nblk && !issue_sdp(i + 1)) { ok = false; break; }
+        if (!issue_grad(i)) { ok = false; break; }
       }
-      if (ok) ok = issue_grad(nblk - 1);
       mma_commit(bar(L::kBarDqDone));
       mma_commit(bar(L::kBarDrain));
       mbar_wait_drain(bar(L::kBarDrain), 0);
     }
     __syncwarp();
+  } else if (NC == 2 && warp >= L::kSenderWarp0) {
+    // ------------------------------------------------------------ sender
+    // Thread = head row h: this CTA's partial S (exp2 domain) and sm_scale
+    // dP over its half of D, rounded to fp16, into the peer's receive buffer
+    // of the block's parity.  The P / dS warps round the same TMEM values the
+    // same way, so both CTAs add identical halves.
+    const int sq = warp & 3;  // TMEM lane quarter
+    const int h = sq * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(sq * 32) << 16;
+    const uint32_t peer_recv = mapa_shared(base + L::kOffRecv, rank ^ 1u);
+    const uint32_t peer_full = mapa_shared(bar(L::kBarRecvFull), rank ^ 1u);
+    const uint32_t row_off = static_cast<uint32_t>(h) * 128u;
+    for (int i = 0; i < nblk; ++i) {
+      const int sb = i & 1;
+      bool ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSdpFull + sb), (i >> 1) & 1, ctl));
+      if (!ok) break;
+      tc_fence_after();
+      float xs[32], xp[32];
+      tmem_ld32(tmem + lane_base + L::kTmemS + sb * 2 * L::kBI, xs);
+      tmem_ld32(tmem + lane_base + L::kTmemDp + sb * 2 * L::kBI, xp);
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarSdpFree + sb));
+      uint32_t hs[16], hp[16];
+#pragma unroll
+      for (int w = 0; w < 16; ++w) {
+        hs[w] = pack_f16x2_sat(xs[2 * w] * p.scale_log2, xs[2 * w + 1] * p.scale_log2);
+        hp[w] = pack_f16x2_sat(xp[2 * w] * p.scale, xp[2 * w + 1] * p.scale);
+      }
+      // The peer's buffer of this parity is free once it has combined block i-2.
+      if (i >= 2) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait<true>(bar(L::kBarSendOk + sb), ((i >> 1) - 1) & 1, ctl));
+        if (!ok) break;
+      }
+      const uint32_t dst = peer_recv + static_cast<uint32_t>(sb) * L::kRecvBytes + row_off;
+      const uint32_t rbar = peer_full + 8u * static_cast<uint32_t>(sb);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        st_async_v4u(dst + ((c ^ (h & 7)) << 4), hs[4 * c], hs[4 * c + 1], hs[4 * c + 2],
+                     hs[4 * c + 3], rbar);
+        st_async_v4u(dst + (((c + 4) ^ (h & 7)) << 4), hp[4 * c], hp[4 * c + 1], hp[4 * c + 2],
+                     hp[4 * c + 3], rbar);
+      }
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ dKV drain
     const int wq = warp - 4;  // TMEM lane quarter
@@ -366,15 +432,22 @@ __global__ void __launch_bounds__(352, 1)
       const uint32_t vm = __ballot_sync(0xffffffffu, v);
       const int row = b * p.S_kv + (v ? r : 0);
       if (active) {
-#pragma unroll 1
-        for (int e = 0; e < L::kNE; ++e) {
-          float x[32];
-          tmem_ld32(tmem + lane_base + L::kTmemDkv + (bk * L::kNE + e) * L::kBI, x);
-          float* col = p.dkv_acc + static_cast<size_t>(rank) * DC + e * 128 + wq * 32 + lane;
+        // Both 128-row halves of the tile in one TMEM round trip; each slot's
+        // row index is shuffled once for both.
+        float x[L::kNE][32];
+        const uint32_t t0 = tmem + lane_base + L::kTmemDkv + bk * L::kNE * L::kBI;
+        if constexpr (L::kNE == 2)
+          tmem_ld32x2(t0, t0 + L::kBI, x[0], x[L::kNE - 1]);
+        else
+          tmem_ld32(t0, x[0]);
+        float* col = p.dkv_acc + static_cast<size_t>(rank) * DC + wq * 32 + lane;
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int rk = __shfl_sync(0xffffffffu, row, k);
-            if ((vm >> k) & 1u) red_add_f32(col + static_cast<size_t>(rk) * p.D, x[k]);
+        for (int k = 0; k < 32; ++k) {
+          const int rk = __shfl_sync(0xffffffffu, row, k);
+          if ((vm >> k) & 1u) {
+#pragma unroll
+            for (int e = 0; e < L::kNE; ++e)
+              red_add_f32(col + static_cast<size_t>(rk) * p.D + e * 128, x[e][k]);
           }
         }
       }
@@ -383,113 +456,108 @@ __global__ void __launch_bounds__(352, 1)
     }
   } else {
     // ------------------------------------------------------------ P / dS
+    // Thread = head row h.  Per block: the full S and dP of the row (own
+    // partial + the peer's, both fp16-rounded, for D = 512), then
+    //   P = 2^(S - lse2),  dS' = P (sm_scale dP - sm_scale Delta),
+    // written bf16 for the gradient MMAs, 8 slots at a time.
     const int h = threadIdx.x;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const float cl2 = p.scale_log2;
     const float lse2 = h < p.H ? __ldg(p.lse + static_cast<size_t>(t) * p.H + h) : INFINITY;
     const float dlt_s =
         h < p.H ? __ldg(p.delta + static_cast<size_t>(t) * p.H + h) * p.scale : 0.f;
-    uint32_t peer_recv = 0, peer_recv_bar = 0, peer_sendok = 0;
-    if (NC == 2) {
-      peer_recv = mapa_shared(base + L::kOffRecv, rank ^ 1u);
-      peer_recv_bar = mapa_shared(bar(L::kBarRecvFull), rank ^ 1u);
-      peer_sendok = mapa_shared(bar(L::kBarSendOk), rank ^ 1u);
-    }
-    bool ok = true;
-    for (int i = 0; i < nblk; ++i) {
-      const int s = i % L::kStages;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSdpFull), i & 1, ctl));
-      if (!ok) break;
-      tc_fence_after();
-      float xs[32], xp[32];
-      tmem_ld32(tmem + lane_base + L::kTmemS, xs);
-      tmem_ld32(tmem + lane_base + L::kTmemDp, xp);
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarSdpFree));
-      // zs: score in the exp2 domain; zp: sm_scale * dP (so that
-      // dS' = P (zp - sm_scale Delta) already carries the scale).
-      if (NC == 2) {
-        // Exchange partial S and dP with the peer CTA (the other half of D),
-        // both rounded to fp16 first and summed in the same order on both
-        // sides; fp16 halves the bytes on the CTA-to-CTA network.
-        uint32_t hs[16], hp[16];
+    const uint32_t peer_sendok = NC == 2 ? mapa_shared(bar(L::kBarSendOk), rank ^ 1u) : 0u;
+    const uint32_t row64 = static_cast<uint32_t>(h) * 64u;
+    const uint32_t sw = static_cast<uint32_t>((h >> 1) & 3);
+    const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
+    auto load_idx = [&](int blk) -> int {
+      const int j = blk * L::kBI + lane;
+      return j < p.topk ? __ldg(idx_row + j) : -1;
+    };
+    // P and dS' of slots 8c .. 8c+7 from their scores zs and scaled dP zp.
+    auto emit = [&](int c, uint32_t msk, const float* zs, const float* zp) {
+      uint32_t pp[4], pd[4];
 #pragma unroll
-        for (int w = 0; w < 16; ++w) {
-          hs[w] = pack_f16x2_sat(xs[2 * w] * cl2, xs[2 * w + 1] * cl2);
-          hp[w] = pack_f16x2_sat(xp[2 * w] * p.scale, xp[2 * w + 1] * p.scale);
-        }
-        if (i >= 1) {
-          ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarSendOk), (i - 1) & 1, ctl));
-          if (!ok) break;
-        }
-        const uint32_t row_off = static_cast<uint32_t>(h) * 128u;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          st_cluster_v4u(peer_recv + row_off + ((c ^ (h & 7)) << 4), hs[4 * c], hs[4 * c + 1],
-                         hs[4 * c + 2], hs[4 * c + 3]);
-          st_cluster_v4u(peer_recv + row_off + (((c + 4) ^ (h & 7)) << 4), hp[4 * c],
-                         hp[4 * c + 1], hp[4 * c + 2], hp[4 * c + 3]);
-        }
-        mbar_arrive_remote(peer_recv_bar);
-        ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull), i & 1, ctl));
-        if (!ok) break;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t ys[4], yp[4];
-          ld_shared_v4u(base + L::kOffRecv + row_off + ((c ^ (h & 7)) << 4), ys[0], ys[1], ys[2],
-                        ys[3]);
-          ld_shared_v4u(base + L::kOffRecv + row_off + (((c + 4) ^ (h & 7)) << 4), yp[0], yp[1],
-                        yp[2], yp[3]);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 ms = unpack_f16x2(hs[4 * c + k]);
-            const float2 ps = unpack_f16x2(ys[k]);
-            const float2 mp = unpack_f16x2(hp[4 * c + k]);
-            const float2 pp2 = unpack_f16x2(yp[k]);
-            xs[8 * c + 2 * k] = ms.x + ps.x;
-            xs[8 * c + 2 * k + 1] = ms.y + ps.y;
-            xp[8 * c + 2 * k] = mp.x + pp2.x;
-            xp[8 * c + 2 * k + 1] = mp.y + pp2.y;
-          }
-        }
-        if (i + 1 < nblk) mbar_arrive_remote(peer_sendok);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          xs[j] *= cl2;
-          xp[j] *= p.scale;
-        }
-      }
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarKvFull + s), (i / L::kStages) & 1, ctl));
-      if (!ok) break;
-      const uint32_t msk = static_cast<uint32_t>(masks[s]);
-      uint32_t pp[16], pd[16];
-#pragma unroll
-      for (int w = 0; w < 16; ++w) {
+      for (int k = 0; k < 4; ++k) {
         float pv[2], dv[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const int jj = 2 * w + u;
-          const float pr = ((msk >> jj) & 1u) ? fast_exp2(xs[jj] - lse2) : 0.f;
+          const int jj = 8 * c + 2 * k + u;
+          const float pr = ((msk >> jj) & 1u) ? fast_exp2(zs[2 * k + u] - lse2) : 0.f;
           pv[u] = pr;
-          dv[u] = pr * (xp[jj] - dlt_s);
+          dv[u] = pr * (zp[2 * k + u] - dlt_s);
         }
-        pp[w] = pack_bf16x2(pv[0], pv[1]);
-        pd[w] = pack_bf16x2(dv[0], dv[1]);
+        pp[k] = pack_bf16x2(pv[0], pv[1]);
+        pd[k] = pack_bf16x2(dv[0], dv[1]);
       }
+      st_shared_v4(base + L::kOffP + row64 + ((c ^ sw) << 4), pp[0], pp[1], pp[2], pp[3]);
+      st_shared_v4(base + L::kOffDs + row64 + ((c ^ sw) << 4), pd[0], pd[1], pd[2], pd[3]);
+    };
+    int r_next = load_idx(0);
+    bool ok = true;
+    for (int i = 0; i < nblk; ++i) {
+      const int sb = i & 1;
+      // Valid-slot mask of the block, from the index row (prefetched).
+      const uint32_t msk =
+          __ballot_sync(0xffffffffu, static_cast<unsigned>(r_next) < static_cast<unsigned>(p.S_kv));
+      if (i + 1 < nblk) r_next = load_idx(i + 1);
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSdpFull + sb), (i >> 1) & 1, ctl));
+      if (!ok) break;
+      tc_fence_after();
+      float xs[32], xp[32];
+      tmem_ld32(tmem + lane_base + L::kTmemS + sb * 2 * L::kBI, xs);
+      tmem_ld32(tmem + lane_base + L::kTmemDp + sb * 2 * L::kBI, xp);
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarSdpFree + sb));
       // P / dS buffers were last read by the gradient MMAs of block i-1.
       if (i >= 1) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarPdsFree), (i - 1) & 1, ctl));
         if (!ok) break;
       }
-      const uint32_t row64 = static_cast<uint32_t>(h) * 64u;
-      const uint32_t sw = static_cast<uint32_t>((h >> 1) & 3);
+      if constexpr (NC == 2) {
+        uint32_t hs[16], hp[16];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        st_shared_v4(base + L::kOffP + row64 + ((c ^ sw) << 4), pp[4 * c], pp[4 * c + 1],
-                     pp[4 * c + 2], pp[4 * c + 3]);
-        st_shared_v4(base + L::kOffDs + row64 + ((c ^ sw) << 4), pd[4 * c], pd[4 * c + 1],
-                     pd[4 * c + 2], pd[4 * c + 3]);
+        for (int w = 0; w < 16; ++w) {
+          hs[w] = pack_f16x2_sat(xs[2 * w] * p.scale_log2, xs[2 * w + 1] * p.scale_log2);
+          hp[w] = pack_f16x2_sat(xp[2 * w] * p.scale, xp[2 * w + 1] * p.scale);
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull + sb), (i >> 1) & 1, ctl));
+        if (!ok) break;
+        // Post the byte count of this buffer's next block (i + 2).
+        if (h == 0 && i + 2 < nblk) mbar_arrive_expect_tx(bar(L::kBarRecvFull + sb), L::kRecvBytes);
+        const uint32_t src = base + L::kOffRecv + static_cast<uint32_t>(sb) * L::kRecvBytes +
+                             static_cast<uint32_t>(h) * 128u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t ys[4], yp[4];
+          ld_shared_v4u(src + ((c ^ (h & 7)) << 4), ys[0], ys[1], ys[2], ys[3]);
+          ld_shared_v4u(src + (((c + 4) ^ (h & 7)) << 4), yp[0], yp[1], yp[2], yp[3]);
+          float zs[8], zp[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 a = add_f16x2_f32(hs[4 * c + k], ys[k]);
+            const float2 d = add_f16x2_f32(hp[4 * c + k], yp[k]);
+            zs[2 * k] = a.x;
+            zs[2 * k + 1] = a.y;
+            zp[2 * k] = d.x;
+            zp[2 * k + 1] = d.y;
+          }
+          emit(c, msk, zs, zp);
+        }
+        // Our receive buffer of this parity may take the peer's block i+2.
+        __syncwarp();
+        if (lane == 0 && i + 2 < nblk)
+          mbar_arrive_remote(peer_sendok + 8u * static_cast<uint32_t>(sb));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float zs[8], zp[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            zs[k] = xs[8 * c + k] * p.scale_log2;
+            zp[k] = xp[8 * c + k] * p.scale;
+          }
+          emit(c, msk, zs, zp);
+        }
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(L::kBarPdsFull));

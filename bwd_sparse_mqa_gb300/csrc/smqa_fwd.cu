@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(416, 1)
         cp_async_arrive_noinc(bar(full0 + s));
       }
       // Let every copy this warp started land before the CTA can exit.
-      cp_async_wait_group<0>();
+      cp_async_wait_all();
       if (own && w == 0 && lane == 0) mbar_wait_drain(bar(L::kBarQFull), 0);
     }
   } else if (warp == L::kMmaWarp) {
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(416, 1)
       // scores may complete at most one block ahead of P.V.
       constexpr bool kHasB = L::kOthChunks > 0;
       int nb = 0, na = 0, npv = 0;
-      uint64_t t_last = globaltimer_ns();
+      PollState ps = poll_start();
       uint32_t spins = 0;
       while (ok && npv < nblk) {
         if (npv < na && mbar_test(bar(L::kBarPFull), npv & 1)) {
@@ -317,17 +317,14 @@ __global__ void __launch_bounds__(416, 1)
           issue_b(nb);
           ++nb;
         } else {
-          if ((++spins & 63u) == 0u) {
-            if (ctl_aborted(ctl)) { ok = false; break; }
-            if (globaltimer_ns() - t_last > ctl.limit_ns) {
-              ctl_abort(ctl);
-              ok = false;
-              break;
-            }
+          if ((++spins & 63u) == 0u && !poll_check(ctl, ps)) {
+            ok = false;
+            break;
           }
           continue;
         }
-        t_last = globaltimer_ns();
+        // Progress: the limit counts from the last issued work.
+        ps.t0 = globaltimer_ns();
       }
       // No MMA may still be running when TMEM is released.
       mma_commit(bar(L::kBarDrain));

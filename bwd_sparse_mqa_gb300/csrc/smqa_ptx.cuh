@@ -88,20 +88,37 @@ struct WaitCtl {
   uint64_t limit_ns;
 };
 
-__device__ __forceinline__ bool ctl_aborted(const WaitCtl& c) {
-  if (*c.abort_flag) return true;
-  if (*reinterpret_cast<volatile int*>(c.status) != 0) {
-    *c.abort_flag = 1;
-    return true;
-  }
-  return false;
-}
-
 __device__ __forceinline__ void ctl_abort(const WaitCtl& c) {
   if (*c.abort_flag == 0) {
     *c.abort_flag = 1;
     atomicOr(c.status, kStatusTimeout);
   }
+}
+
+// Polling state of one bounded wait.  Every 64 polls the shared abort flag
+// and the wall clock are checked and the global status word is loaded; that
+// load is examined only at the next check, so its L2 latency never delays
+// noticing a completed phase.
+struct PollState {
+  uint64_t t0;
+  int status_seen;
+};
+
+__device__ __forceinline__ PollState poll_start() { return PollState{globaltimer_ns(), 0}; }
+
+// False once the CTA must give up (limit reached, or an abort seen here or
+// in the status word).
+__device__ __forceinline__ bool poll_check(const WaitCtl& c, PollState& ps) {
+  if (*c.abort_flag || ps.status_seen != 0) {
+    *c.abort_flag = 1;
+    return false;
+  }
+  ps.status_seen = *reinterpret_cast<volatile int*>(c.status);
+  if (globaltimer_ns() - ps.t0 > c.limit_ns) {
+    ctl_abort(c);
+    return false;
+  }
+  return true;
 }
 
 // Waits until the phase with parity `parity` of `bar` has completed.
@@ -110,16 +127,10 @@ __device__ __forceinline__ void ctl_abort(const WaitCtl& c) {
 template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& c) {
   if (kCluster ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  PollState ps = poll_start();
   for (uint32_t it = 1;; ++it) {
     if (kCluster ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
-    if ((it & 63u) == 0u) {
-      if (ctl_aborted(c)) return false;
-      if (globaltimer_ns() - t0 > c.limit_ns) {
-        ctl_abort(c);
-        return false;
-      }
-    }
+    if ((it & 63u) == 0u && !poll_check(c, ps)) return false;
   }
 }
 
@@ -168,6 +179,18 @@ __device__ __forceinline__ void cluster_sync() {
 
 // 16-byte store into another CTA's shared memory that counts its bytes on
 // that CTA's barrier (`remote_bar`) when it lands.
+// 16-byte store into another CTA's shared memory that counts its bytes
+// toward that CTA's barrier `remote_bar` (complete_tx); the receiver posts the
+// expected byte count.
+__device__ __forceinline__ void st_async_v4u(uint32_t remote_addr, uint32_t a, uint32_t b,
+                                             uint32_t c, uint32_t d, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
+      "[%5];" ::"r"(remote_addr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float a, float b, float c,
                                             float d, uint32_t remote_bar) {
   asm volatile(
@@ -206,6 +229,10 @@ __device__ __forceinline__ void cp_async_commit() {
 // landed (the arrival is counted in the barrier's expected count).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+// Waits for every cp.async this thread started (committed or not).
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 template <int N>
 __device__ __forceinline__ void cp_async_wait_group() {
@@ -346,6 +373,26 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Two 32-column loads issued together, one wait: v0 from taddr0, v1 from
+// taddr1 (same lane mapping as tmem_ld32).
+__device__ __forceinline__ void tmem_ld32x2(uint32_t taddr0, uint32_t taddr1, float (&v0)[32],
+                                            float (&v1)[32]) {
+  uint32_t r0[32], r1[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r0[0]), "=r"(r0[1]), "=r"(r0[2]), "=r"(r0[3]), "=r"(r0[4]), "=r"(r0[5]), "=r"(r0[6]), "=r"(r0[7]), "=r"(r0[8]), "=r"(r0[9]), "=r"(r0[10]), "=r"(r0[11]), "=r"(r0[12]), "=r"(r0[13]), "=r"(r0[14]), "=r"(r0[15]), "=r"(r0[16]), "=r"(r0[17]), "=r"(r0[18]), "=r"(r0[19]), "=r"(r0[20]), "=r"(r0[21]), "=r"(r0[22]), "=r"(r0[23]), "=r"(r0[24]), "=r"(r0[25]), "=r"(r0[26]), "=r"(r0[27]), "=r"(r0[28]), "=r"(r0[29]), "=r"(r0[30]), "=r"(r0[31]),
+        "=r"(r1[0]), "=r"(r1[1]), "=r"(r1[2]), "=r"(r1[3]), "=r"(r1[4]), "=r"(r1[5]), "=r"(r1[6]), "=r"(r1[7]), "=r"(r1[8]), "=r"(r1[9]), "=r"(r1[10]), "=r"(r1[11]), "=r"(r1[12]), "=r"(r1[13]), "=r"(r1[14]), "=r"(r1[15]), "=r"(r1[16]), "=r"(r1[17]), "=r"(r1[18]), "=r"(r1[19]), "=r"(r1[20]), "=r"(r1[21]), "=r"(r1[22]), "=r"(r1[23]), "=r"(r1[24]), "=r"(r1[25]), "=r"(r1[26]), "=r"(r1[27]), "=r"(r1[28]), "=r"(r1[29]), "=r"(r1[30]), "=r"(r1[31])
+      : "r"(taddr0), "r"(taddr1)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v0[i] = __uint_as_float(r0[i]);
+    v1[i] = __uint_as_float(r1[i]);
+  }
+}
+
 // 32 lanes x 16 / 8 consecutive fp32 columns (same mapping as tmem_ld32).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   uint32_t r[16];
@@ -418,8 +465,26 @@ __device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
 }
 
 // Packed fp16x2 -> the two floats (exact).
-__device__ __forceinline__ float2 unpack_f16x2(uint32_t w) {
-  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+// Sum of two fp16 pairs in fp32 with one rounding per element:
+// {float(a.lo) + float(b.lo), float(a.hi) + float(b.hi)}.  Uses the sm_100
+// mixed-precision add (fp16 operand, fp32 operand and result), which runs on
+// the FMA pipe instead of the conversion unit.  The result does not depend on
+// the order of a and b (both conversions are exact, the addition commutes).
+__device__ __forceinline__ float2 add_f16x2_f32(uint32_t a, uint32_t b) {
+  float2 r;
+  asm("{\n"
+      ".reg .b16 alo, ahi, blo, bhi;\n"
+      ".reg .f32 t0, t1;\n"
+      "mov.b32 {alo, ahi}, %2;\n"
+      "mov.b32 {blo, bhi}, %3;\n"
+      "add.rn.f32.f16 t0, alo, 0f00000000;\n"
+      "add.rn.f32.f16 t1, ahi, 0f00000000;\n"
+      "add.rn.f32.f16 %0, blo, t0;\n"
+      "add.rn.f32.f16 %1, bhi, t1;\n"
+      "}"
+      : "=f"(r.x), "=f"(r.y)
+      : "r"(a), "r"(b));
+  return r;
 }
 
 __device__ __forceinline__ void ld_shared_v4u(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c,
