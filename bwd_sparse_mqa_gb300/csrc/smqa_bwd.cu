@@ -127,8 +127,9 @@ struct BwdLayout {
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr uint32_t kOffTmemHolder = kOffCtrl + 8 * kNumBars;
   static constexpr uint32_t kOffAbort = kOffTmemHolder + 4;
+  static constexpr uint32_t kOffWarpLast = kOffAbort + 4;  // int [16]
   static constexpr uint32_t kCtrlBytes = 512;
-  static_assert(kOffAbort + 4 - kOffCtrl <= kCtrlBytes, "control block overflow");
+  static_assert(kOffWarpLast + 64 - kOffCtrl <= kCtrlBytes, "control block overflow");
   static constexpr uint32_t kSmemBytes = kOffCtrl + kCtrlBytes + 1024;
   // TMEM: dQ, then two S/dP buffers (block parity), then two dKV^T buffers.
   static constexpr uint32_t kTmemDq = 0;
@@ -164,7 +165,6 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
   const int t = blockIdx.x / NC;
   const uint32_t rank = NC == 2 ? cluster_ctarank() : 0u;
   const int b = t / p.S;
-  const int nblk = (p.topk + L::kBI - 1) / L::kBI;
   auto bar = [&](int i) -> uint32_t { return base + L::kOffCtrl + 8u * static_cast<uint32_t>(i); };
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(smem + L::kOffTmemHolder);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
     fence_mbar_init();
     if (NC == 2) {
       mbar_arrive_expect_tx(bar(L::kBarRecvFull), L::kRecvBytes);
-      if (nblk > 1) mbar_arrive_expect_tx(bar(L::kBarRecvFull + 1), L::kRecvBytes);
+      mbar_arrive_expect_tx(bar(L::kBarRecvFull + 1), L::kRecvBytes);
     }
   }
   if (warp == L::kMmaWarp) {
@@ -220,11 +220,15 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
       }
     fence_proxy_async_smem();
   }
+  volatile int* warp_last = reinterpret_cast<volatile int*>(smem + L::kOffWarpLast);
+  scan_last_valid(p.idx + static_cast<size_t>(t) * p.topk, p.topk, p.S_kv, warp_last);
   tc_fence_before();
   __syncthreads();
   if (NC == 2) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  // Blocks up to the last one holding a valid slot (0: no valid slot).
+  const int nblk = live_blocks(warp_last, L::kBI);
 
   if (warp >= L::kProducerWarp0 && warp < L::kMmaWarp) {
     // ------------------------------------------------------------ gather
@@ -361,7 +365,7 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
       };
       // S/dP of block i + 1 go to the tensor core ahead of the gradients of
       // block i, so they run while block i's P / dS are being formed.
-      bool ok = mbar_wait(bar(L::kBarQdoFull), 0, ctl) && issue_sdp(0);
+      bool ok = mbar_wait(bar(L::kBarQdoFull), 0, ctl) && (nblk == 0 || issue_sdp(0));
       for (int i = 0; ok && i < nblk; ++i) {
         if (i + 1 < nblk && !issue_sdp(i + 1)) { ok = false; break; }
         if (!issue_grad(i)) { ok = false; break; }
@@ -571,6 +575,10 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
       for (int c = 0; c < DC / 32; ++c) {
         float v[32];
         tmem_ld32(tmem + lane_base + L::kTmemDq + c * 32, v);
+        if (nblk == 0) {  // no valid slot: dQ was never written, the gradient is 0
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = 0.f;
+        }
         if (h < p.H) {
           uint32_t w[16];
 #pragma unroll

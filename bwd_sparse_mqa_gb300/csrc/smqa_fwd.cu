@@ -76,8 +76,9 @@ struct FwdLayout {
   static constexpr uint32_t kOffLsum = kOffXmax + 2 * 2 * 128 * 4; // float [2][128]
   static constexpr uint32_t kOffTmemHolder = kOffLsum + 2 * 128 * 4;
   static constexpr uint32_t kOffAbort = kOffTmemHolder + 4;
+  static constexpr uint32_t kOffWarpLast = kOffAbort + 4;  // int [16]
   static constexpr uint32_t kCtrlBytes = 4096;
-  static_assert(kOffAbort + 4 - kOffCtrl <= kCtrlBytes, "control block overflow");
+  static_assert(kOffWarpLast + 64 - kOffCtrl <= kCtrlBytes, "control block overflow");
   static constexpr uint32_t kSmemBytes = kOffCtrl + kCtrlBytes + 1024;  // +1024: realignment
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   // TMEM: O, the other half of Q (bf16 pairs), then the score tile as two
@@ -139,7 +140,6 @@ __global__ void __launch_bounds__(416, 1)
   const int t = blockIdx.x / NSPLIT;
   const int rank = NSPLIT == 2 ? static_cast<int>(blockIdx.x % NSPLIT) : 0;
   const int b = t / p.S;
-  const int nblk = (p.topk + L::kBI - 1) / L::kBI;
   const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
   auto bar = [&](int i) -> uint32_t { return base + L::kOffCtrl + 8u * static_cast<uint32_t>(i); };
   volatile float* xmax = reinterpret_cast<volatile float*>(smem + L::kOffXmax);
@@ -182,10 +182,14 @@ __global__ void __launch_bounds__(416, 1)
         st_shared_v4(base + L::kOffQ + c * L::kQChunkBytes + h * 128u + k * 16u, 0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
   }
+  volatile int* warp_last = reinterpret_cast<volatile int*>(smem + L::kOffWarpLast);
+  scan_last_valid(idx_row, p.topk, p.S_kv, warp_last);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  // Blocks up to the last one holding a valid slot (0: no valid slot).
+  const int nblk = live_blocks(warp_last, L::kBI);
 
   if (warp >= L::kOwnWarp0 && warp < L::kMmaWarp) {
     // ------------------------------------------------------------ gather
@@ -283,7 +287,8 @@ __global__ void __launch_bounds__(416, 1)
       };
       bool ok = mbar_wait(bar(L::kBarQFull), 0, ctl);
       if (ok && NSPLIT == 2) ok = mbar_wait(bar(L::kBarQtFull), 0, ctl);
-      // Event loop over three kinds of work, oldest first: P.V of block npv
+      // Event loop over three kinds of work, oldest first (polled with
+      // non-blocking tests, so that waiting on one never delays another): P.V of block npv
       // once its P is written; chain A (+ completion of S) of block na once
       // the own half has landed; chain B of block nb once the other half has
       // landed.  Both score chains of a block need the previous block's
@@ -294,27 +299,28 @@ __global__ void __launch_bounds__(416, 1)
       PollState ps = poll_start();
       uint32_t spins = 0;
       while (ok && npv < nblk) {
-        if (npv < na && mbar_test(bar(L::kBarPFull), npv & 1)) {
+        if (npv < na && mbar_probe(bar(L::kBarPFull), npv & 1)) {
           tc_fence_after();
           issue_pv(npv);
           ++npv;
         } else if (na < nblk && (!kHasB || nb > na) && na <= npv + 1 &&
-                   (na == 0 || mbar_test(bar(L::kBarSFree), (na - 1) & 1)) &&
-                   mbar_test(bar(L::kBarOwnFull + na % L::kStages), (na / L::kStages) & 1)) {
+                   (na == 0 || mbar_probe(bar(L::kBarSFree), (na - 1) & 1)) &&
+                   mbar_probe(bar(L::kBarOwnFull + na % L::kStages), (na / L::kStages) & 1)) {
           // The kv tile was written by cp.async (generic proxy): order it
           // before the tensor core's (async proxy) reads.
           fence_proxy_async_smem();
           tc_fence_after();
           issue_a(na);
           mma_commit(bar(L::kBarSFull));
-          if (kHasB) mma_commit(bar(L::kBarOthEmpty + na % L::kStages));
           ++na;
         } else if (kHasB && nb < nblk && nb <= na &&
-                   (nb == 0 || mbar_test(bar(L::kBarSFree), (nb - 1) & 1)) &&
-                   mbar_test(bar(L::kBarOthFull + nb % L::kStages), (nb / L::kStages) & 1)) {
+                   (nb == 0 || mbar_probe(bar(L::kBarSFree), (nb - 1) & 1)) &&
+                   mbar_probe(bar(L::kBarOthFull + nb % L::kStages), (nb / L::kStages) & 1)) {
           fence_proxy_async_smem();
           tc_fence_after();
           issue_b(nb);
+          // Only chain B reads the other column half: free its stage.
+          mma_commit(bar(L::kBarOthEmpty + nb % L::kStages));
           ++nb;
         } else {
           if ((++spins & 63u) == 0u && !poll_check(ctl, ps)) {
@@ -460,7 +466,7 @@ __global__ void __launch_bounds__(416, 1)
       tc_fence_before();
       mbar_arrive(bar(L::kBarPFull));
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone), (nblk - 1) & 1, ctl));
+    if (ok && nblk > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone), (nblk - 1) & 1, ctl));
     // Row sums: the two halves of each row meet here.
     lsum[g * 128 + h] = l_part;
     mbar_arrive(bar(L::kBarLsum));
@@ -479,6 +485,10 @@ __global__ void __launch_bounds__(416, 1)
       for (int c = 0; c < kOHalf / 32; ++c) {
         float v[32];
         tmem_ld32(tmem + lane_base + L::kTmemO + g * kOHalf + c * 32, v);
+        if (nblk == 0) {  // no valid slot: O was never written, the output is 0
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = 0.f;
+        }
         if (h < p.H) {
           uint32_t w[16];
 #pragma unroll

@@ -69,6 +69,21 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test (never suspends the thread): for loops that poll
+// several barriers, where a suspending try_wait on one would delay noticing
+// another.
+__device__ __forceinline__ bool mbar_probe(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -142,6 +157,32 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
   while (!mbar_test(bar, parity))
     if (globaltimer_ns() - t0 > limit_ns) return false;
   return true;
+}
+
+// ---------------------------------------------------------------------------
+// Live slot range of a token
+// ---------------------------------------------------------------------------
+// Every thread of the CTA calls this before the CTA's first barrier: the
+// warp's largest slot j < topk whose index names a row in [0, S_kv) (or -1)
+// goes to warp_last[warp].  After the barrier, live_blocks() turns the
+// per-warp values into the number of slot blocks that hold any valid slot;
+// blocks past the last valid slot contribute nothing and are skipped.
+__device__ __forceinline__ void scan_last_valid(const int32_t* idx_row, int topk, int S_kv,
+                                                volatile int* warp_last) {
+  int last = -1;
+#pragma unroll 4
+  for (int j = static_cast<int>(threadIdx.x); j < topk; j += static_cast<int>(blockDim.x))
+    if (static_cast<unsigned>(__ldg(idx_row + j)) < static_cast<unsigned>(S_kv)) last = j;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, off));
+  if ((threadIdx.x & 31) == 0) warp_last[threadIdx.x >> 5] = last;
+}
+
+__device__ __forceinline__ int live_blocks(const volatile int* warp_last, int block_slots) {
+  int last = -1;
+  const int nwarps = static_cast<int>(blockDim.x >> 5);
+  for (int w = 0; w < nwarps; ++w) last = max(last, warp_last[w]);
+  return last < 0 ? 0 : last / block_slots + 1;
 }
 
 // ---------------------------------------------------------------------------

@@ -50,6 +50,21 @@ def test_all_masked_rows_and_duplicates():
     assert torch.allclose(lse[0, 3], sink2, rtol=1e-5, atol=1e-6)
 
 
+def test_masked_tails_and_gaps():
+    """Both kernels stop after the last slot block holding a valid slot;
+    rows whose valid slots end early, sit only at the end, or straddle a
+    fully masked block must still match the oracle."""
+    x = inputs.custom(1, 24, 300, 128, 512, 256, seed=12)
+    idx = x["topk_idxs"]
+    idx[0, 0, 1:] = -1                  # only slot 0 valid: one block
+    idx[0, 1, 64:128] = -1              # a fully masked 64-slot block, valid slots after it
+    idx[0, 2, :255] = 300               # only the last slot valid
+    idx[0, 3, 130:] = -1                # tail ends inside a block
+    idx[0, 4, 64:] = -1                 # exactly one full 64-slot block
+    idx[0, 5, 32:] = -1                 # exactly one full 32-slot block
+    print(P.check_full(x))
+
+
 def test_return_dkv_fp32_and_reference_rounding():
     x = inputs.custom(1, 24, 100, 128, 512, 80, recipe="causal_masked10", seed=11)
     g = P.to_dev(x)
