@@ -255,6 +255,8 @@ def main():
     dkv = torch.empty((B, S_kv, D), dtype=torch.bfloat16, device=dev)
     acc = torch.empty((B, S_kv, D), dtype=torch.float32, device=dev)
     delta = torch.empty((B, S, H), dtype=torch.float32, device=dev)
+    exch_bytes = int(lib.smqa_bwd_exchange_bytes(shp))
+    exch = torch.empty((max(exch_bytes, 256),), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = ctypes.c_void_p(stream.cuda_stream)
     P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
@@ -271,7 +273,8 @@ def main():
         if ev is not None:
             ev[2].record(stream)
         _lib.check("main", lib.smqa_bwd_main(P(q), P(kv), P(sink), P(dout), P(idx), P(lse),
-                                             P(delta), shp, scale, P(dq), P(acc), sp))
+                                             P(delta), shp, scale, P(dq), P(acc), P(exch),
+                                             exch_bytes, sp))
         if ev is not None:
             ev[3].record(stream)
         _lib.check("post", lib.smqa_bwd_postprocess(P(acc), shp, P(dkv), sp))

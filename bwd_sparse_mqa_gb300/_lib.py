@@ -27,7 +27,7 @@ FLAG_REFERENCE_ROUNDING = 2
 EXPORTS = [
     "smqa_fwd", "smqa_bwd_workspace_bytes", "smqa_bwd", "smqa_bwd_preprocess", "smqa_bwd_main",
     "smqa_bwd_postprocess", "smqa_device_status", "smqa_status_string", "smqa_last_error",
-    "smqa_abi_version", "smqa_bwd_static_scratch",
+    "smqa_abi_version", "smqa_bwd_static_scratch", "smqa_bwd_exchange_bytes",
 ]
 STATIC_SCRATCH_BYTES = 24 << 20
 
@@ -54,7 +54,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.smqa_bwd.restype = st
     lib.smqa_bwd_preprocess.argtypes = [P, P, S, P, P, P]
     lib.smqa_bwd_preprocess.restype = st
-    lib.smqa_bwd_main.argtypes = [P, P, P, P, P, P, P, S, F, P, P, P]
+    lib.smqa_bwd_main.argtypes = [P, P, P, P, P, P, P, S, F, P, P, P, ctypes.c_size_t, P]
+    lib.smqa_bwd_exchange_bytes.argtypes = [S]
+    lib.smqa_bwd_exchange_bytes.restype = ctypes.c_size_t
     lib.smqa_bwd_main.restype = st
     lib.smqa_bwd_postprocess.argtypes = [P, S, P, P]
     lib.smqa_bwd_postprocess.restype = st

@@ -128,12 +128,25 @@ float effective_scale(float sm_scale, int D) {
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Exchange pool of the D = 512 backward: slot flags, then the slots.
+constexpr size_t kExchFlagBytes = 4096;
+constexpr int kExchSlots = 96;
+
+size_t exchange_bytes(const smqa_shape& s) {
+  return s.D == 512 ? kExchFlagBytes + static_cast<size_t>(kExchSlots) * smqa::kBwdSlotBytes : 0;
+}
+
 smqa_status bwd_main_impl(const void* q, const void* kv, const void* dout, const int32_t* idx,
                           const float* lse, const float* delta, const smqa_shape& s, float scale,
-                          void* dq, float* acc, cudaStream_t stream) {
+                          void* dq, float* acc, void* exch, cudaStream_t stream) {
   cudaError_t e;
   int* st = status_ptr(&e);
   if (!st) return cuda_fail(e, "status word");
+  if (exchange_bytes(s) != 0) {
+    // Every slot free at launch (the kernel's pairs claim and release them).
+    e = cudaMemsetAsync(exch, 0, kExchSlots * sizeof(int), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "exchange flags clear");
+  }
   CUtensorMap tq, tdo;
   const uint64_t T = static_cast<uint64_t>(s.B) * s.S;
   if (!encode_bf16_2d(&tq, q, s.D, T * s.H, 64, static_cast<uint32_t>(s.H)) ||
@@ -155,6 +168,11 @@ smqa_status bwd_main_impl(const void* q, const void* kv, const void* dout, const
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = st;
   p.limit_ns = wait_limit_ns();
+  if (exchange_bytes(s) != 0) {
+    p.slot_flags = static_cast<int*>(exch);
+    p.exch = static_cast<uint8_t*>(exch) + kExchFlagBytes;
+    p.nslots = kExchSlots;
+  }
   e = smqa::launch_bwd_main(tq, tdo, p, static_cast<int>(T), stream);
   if (e != cudaSuccess) return cuda_fail(e, "bwd main launch");
   return SMQA_OK;
@@ -230,7 +248,13 @@ size_t smqa_bwd_workspace_bytes(smqa_shape shape, unsigned flags) {
   if (!(flags & SMQA_FLAG_RETURN_DKV_FP32))
     bytes += round256(static_cast<size_t>(shape.B) * shape.S_kv * shape.D * sizeof(float));
   bytes += round256(static_cast<size_t>(shape.B) * shape.S * shape.H * sizeof(float));
+  bytes += round256(exchange_bytes(shape));
   return bytes;
+}
+
+size_t smqa_bwd_exchange_bytes(smqa_shape shape) {
+  if (check_shape(shape) != SMQA_OK) return 0;
+  return exchange_bytes(shape);
 }
 
 smqa_status smqa_bwd_preprocess(const void* o, const void* dout, smqa_shape shape, float* delta,
@@ -254,17 +278,24 @@ smqa_status smqa_bwd_preprocess(const void* o, const void* dout, smqa_shape shap
 smqa_status smqa_bwd_main(const void* q, const void* kv, const float* attn_sink, const void* dout,
                           const int32_t* topk_idxs, const float* lse, const float* delta,
                           smqa_shape shape, float sm_scale, void* dq, float* dkv_accum,
-                          cudaStream_t stream) {
+                          void* exchange, size_t exchange_bytes_given, cudaStream_t stream) {
   const smqa_status sc = check_shape(shape);
   if (sc != SMQA_OK) return sc;
+  const size_t need = exchange_bytes(shape);
   if (!q || !kv || !attn_sink || !dout || !topk_idxs || !lse || !delta || !dq || !dkv_accum ||
-      !aligned(q, 16) || !aligned(kv, 16) || !aligned(dout, 16) || !aligned(dq, 16) ||
-      !aligned(topk_idxs, 4) || !aligned(lse, 4) || !aligned(delta, 4) || !aligned(dkv_accum, 16)) {
+      (need != 0 && !exchange) || !aligned(q, 16) || !aligned(kv, 16) || !aligned(dout, 16) ||
+      !aligned(dq, 16) || !aligned(topk_idxs, 4) || !aligned(lse, 4) || !aligned(delta, 4) ||
+      !aligned(dkv_accum, 16) || !aligned(exchange, 256)) {
     std::snprintf(g_last_error, sizeof g_last_error, "null or misaligned pointer");
     return SMQA_ERR_INVALID_ARG;
   }
+  if (exchange_bytes_given < need) {
+    std::snprintf(g_last_error, sizeof g_last_error, "exchange pool too small (%zu < %zu bytes)",
+                  exchange_bytes_given, need);
+    return SMQA_ERR_UNSUPPORTED;
+  }
   return bwd_main_impl(q, kv, dout, topk_idxs, lse, delta, shape,
-                       effective_scale(sm_scale, shape.D), dq, dkv_accum, stream);
+                       effective_scale(sm_scale, shape.D), dq, dkv_accum, exchange, stream);
 }
 
 smqa_status smqa_bwd_postprocess(const float* dkv_accum, smqa_shape shape, void* dkv_bf16,
@@ -306,10 +337,12 @@ smqa_status smqa_bwd(const void* q, const void* kv, const float* attn_sink, cons
   const size_t acc_bytes =
       fp32_out ? 0 : round256(static_cast<size_t>(shape.B) * shape.S_kv * shape.D * sizeof(float));
   float* delta = reinterpret_cast<float*>(ws + acc_bytes);
+  void* exch = ws + acc_bytes +
+               round256(static_cast<size_t>(shape.B) * shape.S * shape.H * sizeof(float));
   smqa_status r = smqa_bwd_preprocess(o, dout, shape, delta, acc, stream);
   if (r != SMQA_OK) return r;
   r = bwd_main_impl(q, kv, dout, topk_idxs, lse, delta, shape, effective_scale(sm_scale, shape.D),
-                    dq, acc, stream);
+                    dq, acc, exch, stream);
   if (r != SMQA_OK) return r;
   if (!fp32_out) return smqa_bwd_postprocess(acc, shape, dkv, stream);
   return SMQA_OK;

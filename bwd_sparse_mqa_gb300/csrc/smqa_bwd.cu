@@ -91,17 +91,15 @@ __global__ void __launch_bounds__(256)
 template <int DC, int NC>
 struct BwdLayout {
   static constexpr int kHPad = 128;
-  static constexpr int kBI = 32;                 // slots per block
+  static constexpr int kBI = 64;                 // slots per block (MMA N of S, dP, dKV^T)
   static constexpr int kChunks = DC / 64;
   static constexpr int kNE = DC >= 128 ? DC / 128 : 1;  // 128-row halves of dKV^T
-  static constexpr int kStages = NC == 2 ? 3 : 4;
+  static constexpr int kStages = NC == 2 ? 2 : 4;
   static constexpr uint32_t kQChunkBytes = kHPad * 128;          // 16 KB
   static constexpr uint32_t kQBytes = kChunks * kQChunkBytes;
-  static constexpr uint32_t kKvChunkBytes = kBI * 128;           // 4 KB
+  static constexpr uint32_t kKvChunkBytes = kBI * 128;           // 8 KB
   static constexpr uint32_t kKvStageBytes = kChunks * kKvChunkBytes;
-  static constexpr uint32_t kPBytes = kHPad * kBI * 2;           // 8 KB (64-byte rows)
-  // peer's partial S and dP of one block, fp16; two buffers (block parity)
-  static constexpr uint32_t kRecvBytes = NC == 2 ? kHPad * 2 * kBI * 2 : 0;
+  static constexpr uint32_t kPBytes = kHPad * kBI * 2;           // 16 KB (128-byte rows)
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffDo = kOffQ + kQBytes;
   // For DC = 64 the 128-row M-major views of Q^T / dO^T read one chunk past
@@ -109,17 +107,16 @@ struct BwdLayout {
   static constexpr uint32_t kOffKv = kOffDo + (kChunks >= 2 ? kQBytes : 2 * kQChunkBytes);
   static constexpr uint32_t kOffP = kOffKv + kStages * kKvStageBytes;
   static constexpr uint32_t kOffDs = kOffP + kPBytes;
-  static constexpr uint32_t kOffRecv = kOffDs + kPBytes;
-  static constexpr uint32_t kOffCtrl = kOffRecv + 2 * kRecvBytes;
+  static constexpr uint32_t kOffCtrl = kOffDs + kPBytes;
   static constexpr int kBarKvFull = 0;
   static constexpr int kBarKvEmpty = kBarKvFull + kStages;
-  static constexpr int kBarSdpFull = kBarKvEmpty + kStages;  // [2], by block parity
-  static constexpr int kBarSdpFree = kBarSdpFull + 2;         // [2]
-  static constexpr int kBarPdsFull = kBarSdpFree + 2;
+  static constexpr int kBarSdpFull = kBarKvEmpty + kStages;
+  static constexpr int kBarSdpFree = kBarSdpFull + 1;
+  static constexpr int kBarPdsFull = kBarSdpFree + 1;
   static constexpr int kBarPdsFree = kBarPdsFull + 1;
-  static constexpr int kBarDkvFull = kBarPdsFree + 1;  // [2]
-  static constexpr int kBarDkvFree = kBarDkvFull + 2;  // [2]
-  static constexpr int kBarRecvFull = kBarDkvFree + 2;  // [2]
+  static constexpr int kBarDkvFull = kBarPdsFree + 1;
+  static constexpr int kBarDkvFree = kBarDkvFull + 1;
+  static constexpr int kBarRecvFull = kBarDkvFree + 1;  // [2], by block parity
   static constexpr int kBarSendOk = kBarRecvFull + 2;    // [2]
   static constexpr int kBarQdoFull = kBarSendOk + 2;
   static constexpr int kBarDqDone = kBarQdoFull + 1;
@@ -127,17 +124,20 @@ struct BwdLayout {
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr uint32_t kOffTmemHolder = kOffCtrl + 8 * kNumBars;
   static constexpr uint32_t kOffAbort = kOffTmemHolder + 4;
-  static constexpr uint32_t kOffWarpLast = kOffAbort + 4;  // int [16]
+  static constexpr uint32_t kOffSlot = kOffAbort + 4;
+  static constexpr uint32_t kOffWarpLast = kOffSlot + 4;  // int [16]
   static constexpr uint32_t kCtrlBytes = 512;
   static_assert(kOffWarpLast + 64 - kOffCtrl <= kCtrlBytes, "control block overflow");
   static constexpr uint32_t kSmemBytes = kOffCtrl + kCtrlBytes + 1024;
-  // TMEM: dQ, then two S/dP buffers (block parity), then two dKV^T buffers.
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  // TMEM: dQ, S, dP, dKV^T (one tile each).
   static constexpr uint32_t kTmemDq = 0;
-  static constexpr uint32_t kTmemS = DC;              // + buf * 2 kBI
-  static constexpr uint32_t kTmemDp = DC + kBI;       // + buf * 2 kBI
-  static constexpr uint32_t kTmemDkv = DC + 4 * kBI;  // + buf * kNE * kBI + e * kBI
-  static constexpr uint32_t kTmemUsed = kTmemDkv + 2 * kNE * kBI;
+  static constexpr uint32_t kTmemS = DC;
+  static constexpr uint32_t kTmemDp = DC + kBI;
+  static constexpr uint32_t kTmemDkv = DC + 2 * kBI;  // + e * kBI
+  static constexpr uint32_t kTmemUsed = kTmemDkv + kNE * kBI;
   static constexpr uint32_t kTmemCols = kTmemUsed <= 256 ? 256 : 512;
+  static_assert(kTmemUsed <= 512, "TMEM budget");
   // warps 0-3: P / dS (thread = head row); 4-7: dKV drain (thread = head-dim
   // row); 8-9: gather; 10: TMEM owner + MMA issuer; 11-14 (D split across
   // the pair only): send this CTA's partial S / dP to the peer.
@@ -145,9 +145,32 @@ struct BwdLayout {
   static constexpr int kMmaWarp = 10;
   static constexpr int kSenderWarp0 = 11;
   static constexpr int kThreads = NC == 2 ? 480 : 352;
-  // Readers of a S / dP buffer: the P / dS warps and the senders.
+  // Readers of the S / dP tile: the P / dS warps and the senders.
   static constexpr int kSdpReaders = NC == 2 ? 256 : 128;
+  // Exchange buffer of one receiver and block parity: 16 pieces of 16 bytes
+  // per head (8 of S, 8 of dP, each 8 slots of fp16), piece-major.
+  static constexpr uint32_t kXchgBytes = 16u * 16u * kHPad;
+  static_assert(2 * 2 * kXchgBytes == kBwdSlotBytes, "exchange slot size");
 };
+
+// Partial S (exp2 domain) and sm_scale dP of one head row over the block's
+// 64 slots, rounded to fp16 pairs: hs[w] / hp[w] hold slots 2w, 2w+1.  The
+// sender and the P / dS warps round the same TMEM values the same way.
+template <int DC, int NC>
+__device__ __forceinline__ void load_own_partials(uint32_t t_s, uint32_t t_dp, float scale_log2,
+                                                  float scale, uint32_t (&hs)[32],
+                                                  uint32_t (&hp)[32]) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    float xs[32], xp[32];
+    tmem_ld32x2(t_s + 32 * half, t_dp + 32 * half, xs, xp);
+#pragma unroll
+    for (int w = 0; w < 16; ++w) {
+      hs[16 * half + w] = pack_f16x2_sat(xs[2 * w] * scale_log2, xs[2 * w + 1] * scale_log2);
+      hp[16 * half + w] = pack_f16x2_sat(xp[2 * w] * scale, xp[2 * w + 1] * scale);
+    }
+  }
+}
 
 template <int DC, int NC>
 __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
@@ -168,6 +191,7 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
   auto bar = [&](int i) -> uint32_t { return base + L::kOffCtrl + 8u * static_cast<uint32_t>(i); };
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(smem + L::kOffTmemHolder);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
+  volatile int* slot_smem = reinterpret_cast<volatile int*>(smem + L::kOffSlot);
   const WaitCtl ctl{abort_flag, p.status, p.limit_ns};
 
   if (threadIdx.x == 0) {
@@ -175,32 +199,42 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
       mbar_init(bar(L::kBarKvFull + s), 64);  // every gather thread arrives
       mbar_init(bar(L::kBarKvEmpty + s), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(L::kBarSdpFull + i), 1);
-      mbar_init(bar(L::kBarSdpFree + i), L::kSdpReaders);
-    }
+    mbar_init(bar(L::kBarSdpFull), 1);
+    mbar_init(bar(L::kBarSdpFree), L::kSdpReaders);
     mbar_init(bar(L::kBarPdsFull), 128);
     mbar_init(bar(L::kBarPdsFree), 1);
+    mbar_init(bar(L::kBarDkvFull), 1);
+    mbar_init(bar(L::kBarDkvFree), 128);
+    // Exchange: the peer's four sender warps each signal a filled buffer,
+    // the peer's four P / dS warps each signal a consumed one.
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(L::kBarDkvFull + i), 1);
-      mbar_init(bar(L::kBarDkvFree + i), 128);
-    }
-    // Receive buffers: one local arrival (with the expected bytes) per
-    // phase, the bytes counted by the peer's st.async; the peer's four P / dS
-    // warps each free a buffer once.
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(L::kBarRecvFull + i), 1);
+      mbar_init(bar(L::kBarRecvFull + i), 4);
       mbar_init(bar(L::kBarSendOk + i), 4);
     }
     mbar_init(bar(L::kBarQdoFull), 1);
     mbar_init(bar(L::kBarDqDone), 1);
     mbar_init(bar(L::kBarDrain), 1);
     *abort_flag = *reinterpret_cast<volatile int*>(p.status) != 0 ? 1 : 0;
-    fence_mbar_init();
-    if (NC == 2) {
-      mbar_arrive_expect_tx(bar(L::kBarRecvFull), L::kRecvBytes);
-      mbar_arrive_expect_tx(bar(L::kBarRecvFull + 1), L::kRecvBytes);
+    *slot_smem = -1;
+    if (NC == 2 && rank == 0 && *abort_flag == 0) {
+      // Claim an exchange slot for the pair (bounded; released at exit).
+      const int c = static_cast<int>(blockIdx.x / NC);
+      const uint64_t t0 = globaltimer_ns();
+      int got = -1;
+      for (uint32_t it = 0; got < 0; ++it) {
+        const int s = static_cast<int>((static_cast<uint32_t>(c) + it) % static_cast<uint32_t>(p.nslots));
+        if (atomicCAS(p.slot_flags + s, 0, 1) == 0) {
+          got = s;
+        } else if ((it % static_cast<uint32_t>(p.nslots)) == static_cast<uint32_t>(p.nslots) - 1u &&
+                   globaltimer_ns() - t0 > p.limit_ns) {
+          *abort_flag = 1;
+          atomicOr(p.status, kStatusTimeout);
+          break;
+        }
+      }
+      *slot_smem = got;
     }
+    fence_mbar_init();
   }
   if (warp == L::kMmaWarp) {
     if (lane == 0) {
@@ -229,12 +263,18 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
   const uint32_t tmem = *tmem_holder;
   // Blocks up to the last one holding a valid slot (0: no valid slot).
   const int nblk = live_blocks(warp_last, L::kBI);
+  // The pair's exchange slot (claimed by rank 0); without one, nothing runs.
+  int slot = -1;
+  if (NC == 2) {
+    slot = rank == 0 ? *slot_smem : ld_shared_cluster_s32(mapa_shared(base + L::kOffSlot, 0u));
+    if (slot < 0) *abort_flag = 1;
+  }
 
   if (warp >= L::kProducerWarp0 && warp < L::kMmaWarp) {
     // ------------------------------------------------------------ gather
-    // Warp pw copies slots [16 pw, 16 pw + 16) of each 32-slot block; one warp
-    // instruction moves kRpi whole rows of this CTA's D slice (32 lanes x 16
-    // bytes, coalesced) into the 128-byte-swizzled tile with cp.async.
+    // Warp pw copies slots [32 pw, 32 pw + 32) of each 64-slot block; one
+    // warp instruction moves kRpi whole rows of this CTA's D slice (32 lanes
+    // x 16 bytes, coalesced) into the 128-byte-swizzled tile with cp.async.
     const int pw = warp - L::kProducerWarp0;
     constexpr int kCpr = DC / 8;
     constexpr int kRpi = 32 / kCpr;
@@ -245,11 +285,11 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
     const __nv_bfloat16* kv_col = p.kv + static_cast<size_t>(rank) * DC + cc * 8;
     const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
     auto load_idx = [&](int blk) -> int {
-      const int j = blk * L::kBI + lane;
+      const int j = blk * L::kBI + 32 * pw + lane;
       return j < p.topk ? __ldg(idx_row + j) : -1;
     };
     int r_next = load_idx(0);
-    if (warp == L::kProducerWarp0 && lane == 0) {
+    if (warp == L::kProducerWarp0 && lane == 0 && *abort_flag == 0) {
       mbar_arrive_expect_tx(bar(L::kBarQdoFull),
                             2u * static_cast<uint32_t>(p.H) * 128u * L::kChunks);
       for (int c = 0; c < L::kChunks; ++c) {
@@ -268,13 +308,15 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
       if (i >= L::kStages) {
         const bool ok = mbar_wait(bar(L::kBarKvEmpty + s), ((i / L::kStages) - 1) & 1, ctl);
         if (!__all_sync(0xffffffffu, ok)) break;
+      } else if (*abort_flag) {
+        break;
       }
       const uint32_t stage = base + L::kOffKv + s * L::kKvStageBytes + lane_off;
 #pragma unroll
-      for (int k = 0; k < 16 / kRpi; ++k) {
-        const int rloc = 16 * pw + k * kRpi + rsub;
-        const int rr = __shfl_sync(0xffffffffu, row, rloc);
-        const uint32_t srow = static_cast<uint32_t>(rloc);
+      for (int k = 0; k < 32 / kRpi; ++k) {
+        const int rw = k * kRpi + rsub;  // row within this warp's 32
+        const int rr = __shfl_sync(0xffffffffu, row, rw);
+        const uint32_t srow = static_cast<uint32_t>(32 * pw + rw);
         cp_async_16(stage + srow * 128u + ((c16 ^ (srow & 7u)) << 4),
                     kv_col + static_cast<size_t>(rr) * p.D);
       }
@@ -297,78 +339,86 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
       const uint64_t d_do = smem_desc(base + L::kOffDo, 16u, 1024u, kSwizzle128B);
       const uint64_t d_kv = smem_desc(base + L::kOffKv, 16u, 1024u, kSwizzle128B);
       const uint64_t d_kvmn = smem_desc(base + L::kOffKv, L::kKvChunkBytes, 1024u, kSwizzle128B);
-      const uint64_t d_ds = smem_desc(base + L::kOffDs, 16u, 512u, kSwizzle64B);
+      const uint64_t d_ds = smem_desc(base + L::kOffDs, 16u, 1024u, kSwizzle128B);
       const uint64_t d_qt = smem_desc(base + L::kOffQ, L::kQChunkBytes, 1024u, kSwizzle128B);
       const uint64_t d_dot = smem_desc(base + L::kOffDo, L::kQChunkBytes, 1024u, kSwizzle128B);
-      const uint64_t d_dsmn = smem_desc(base + L::kOffDs, 8192u, 512u, kSwizzle64B);
-      const uint64_t d_pmn = smem_desc(base + L::kOffP, 8192u, 512u, kSwizzle64B);
-      auto issue_grad = [&](int j) -> bool {
-        const int bk = j & 1;
-        const int sj = j % L::kStages;
-        if (!mbar_wait(bar(L::kBarPdsFull), j & 1, ctl)) return false;
-        if (j >= 2 && !mbar_wait(bar(L::kBarDkvFree + bk), ((j >> 1) - 1) & 1, ctl)) return false;
-        tc_fence_after();
-        const uint64_t dkv = d_kvmn + ((static_cast<uint32_t>(sj) * L::kKvStageBytes) >> 4);
-        // dQ += dS' . K   (M = 128 heads, N = DC, K = 32 slots)
-#pragma unroll
-        for (int k = 0; k < L::kBI / 16; ++k)
-          mma_ss(tmem + L::kTmemDq, d_ds + (k * 32u >> 4), dkv + (k * 2048u >> 4), idesc_dq,
-                 (j > 0 || k > 0) ? 1u : 0u);
-        // dKV^T[e] = Q^T[e] . dS' + dO^T[e] . P   (M = 128 dims, N = 32 slots, K = 128 heads)
-#pragma unroll
-        for (int e = 0; e < L::kNE; ++e) {
-          const uint32_t d_tm = tmem + L::kTmemDkv + (bk * L::kNE + e) * L::kBI;
-#pragma unroll
-          for (int k = 0; k < L::kHPad / 16; ++k)
-            mma_ss(d_tm, d_qt + ((2 * e * L::kQChunkBytes + k * 2048u) >> 4),
-                   d_dsmn + (k * 1024u >> 4), idesc_dkv, k > 0 ? 1u : 0u);
-#pragma unroll
-          for (int k = 0; k < L::kHPad / 16; ++k)
-            mma_ss(d_tm, d_dot + ((2 * e * L::kQChunkBytes + k * 2048u) >> 4),
-                   d_pmn + (k * 1024u >> 4), idesc_dkv, 1u);
-        }
-        mma_commit(bar(L::kBarPdsFree));
-        mma_commit(bar(L::kBarKvEmpty + sj));
-        mma_commit(bar(L::kBarDkvFull + bk));
-        return true;
-      };
-      // S and dP of block i into TMEM buffer i & 1 (M = 128 heads, N = 32
-      // slots, K = this CTA's D slice).
-      auto issue_sdp = [&](int i) -> bool {
+      const uint64_t d_dsmn = smem_desc(base + L::kOffDs, L::kPBytes, 1024u, kSwizzle128B);
+      const uint64_t d_pmn = smem_desc(base + L::kOffP, L::kPBytes, 1024u, kSwizzle128B);
+      // S and dP of block i (M = 128 heads, N = 64 slots, K = this CTA's D slice).
+      auto issue_sdp = [&](int i) {
         const int s = i % L::kStages;
-        const int sb = i & 1;
-        if (!mbar_wait(bar(L::kBarKvFull + s), (i / L::kStages) & 1, ctl)) return false;
-        // Both buffers: the tile of block i-2 (same buffer) and of block i-1
-        // must have been read.  Waiting for block i-1 keeps the S / dP MMAs
-        // from competing for shared memory with the exchange of block i-1.
-        if (i >= 1 && !mbar_wait(bar(L::kBarSdpFree + (sb ^ 1)), ((i - 1) >> 1) & 1, ctl))
-          return false;
-        // The kv tile was written by cp.async (generic proxy): order it before
-        // the tensor core's (async proxy) reads.
-        fence_proxy_async_smem();
-        tc_fence_after();
         const uint64_t dk = d_kv + ((static_cast<uint32_t>(s) * L::kKvStageBytes) >> 4);
-        const uint32_t t_s = tmem + L::kTmemS + sb * 2 * L::kBI;
-        const uint32_t t_dp = tmem + L::kTmemDp + sb * 2 * L::kBI;
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t bd = dk + ((c * L::kKvChunkBytes + k * 32u) >> 4);
             const uint32_t acc = (c | k) != 0 ? 1u : 0u;
-            mma_ss(t_s, d_q + ((c * L::kQChunkBytes + k * 32u) >> 4), bd, idesc_sdp, acc);
-            mma_ss(t_dp, d_do + ((c * L::kQChunkBytes + k * 32u) >> 4), bd, idesc_sdp, acc);
+            mma_ss(tmem + L::kTmemS, d_q + ((c * L::kQChunkBytes + k * 32u) >> 4), bd,
+                   idesc_sdp, acc);
+            mma_ss(tmem + L::kTmemDp, d_do + ((c * L::kQChunkBytes + k * 32u) >> 4), bd,
+                   idesc_sdp, acc);
           }
         }
-        mma_commit(bar(L::kBarSdpFull + sb));
-        return true;
+        mma_commit(bar(L::kBarSdpFull));
       };
-      // S/dP of block i + 1 go to the tensor core ahead of the gradients of
-      // block i, so they run while block i's P / dS are being formed.
-      bool ok = mbar_wait(bar(L::kBarQdoFull), 0, ctl) && (nblk == 0 || issue_sdp(0));
-      for (int i = 0; ok && i < nblk; ++i) {
-        if (i + 1 < nblk && !issue_sdp(i + 1)) { ok = false; break; }
-        if (!issue_grad(i)) { ok = false; break; }
+      // Gradients of block j: dQ += dS'.K (M = 128 heads, N = DC, K = 64
+      // slots); dKV^T[e] = Q^T[e].dS' + dO^T[e].P (M = 128 dims, N = 64
+      // slots, K = 128 heads).
+      auto issue_grad = [&](int j) {
+        const int sj = j % L::kStages;
+        const uint64_t dkv = d_kvmn + ((static_cast<uint32_t>(sj) * L::kKvStageBytes) >> 4);
+#pragma unroll
+        for (int k = 0; k < L::kBI / 16; ++k)
+          mma_ss(tmem + L::kTmemDq, d_ds + (k * 32u >> 4), dkv + (k * 2048u >> 4), idesc_dq,
+                 (j > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+        for (int e = 0; e < L::kNE; ++e) {
+          const uint32_t d_tm = tmem + L::kTmemDkv + e * L::kBI;
+#pragma unroll
+          for (int k = 0; k < L::kHPad / 16; ++k)
+            mma_ss(d_tm, d_qt + ((2 * e * L::kQChunkBytes + k * 2048u) >> 4),
+                   d_dsmn + (k * 2048u >> 4), idesc_dkv, k > 0 ? 1u : 0u);
+#pragma unroll
+          for (int k = 0; k < L::kHPad / 16; ++k)
+            mma_ss(d_tm, d_dot + ((2 * e * L::kQChunkBytes + k * 2048u) >> 4),
+                   d_pmn + (k * 2048u >> 4), idesc_dkv, 1u);
+        }
+        mma_commit(bar(L::kBarPdsFree));
+        mma_commit(bar(L::kBarKvEmpty + sj));
+        mma_commit(bar(L::kBarDkvFull));
+      };
+      // Event loop (non-blocking tests), oldest work first: the gradients
+      // of block ng once its P / dS are written and the drain has read the
+      // previous dKV^T tile; S / dP of block ns once its kv rows have landed
+      // and the previous S / dP tile has been read.
+      bool ok = mbar_wait(bar(L::kBarQdoFull), 0, ctl);
+      int ns = 0, ng = 0;
+      PollState ps = poll_start();
+      uint32_t spins = 0;
+      while (ok && ng < nblk) {
+        if (ng < ns && mbar_probe(bar(L::kBarPdsFull), ng & 1) &&
+            (ng == 0 || mbar_probe(bar(L::kBarDkvFree), (ng - 1) & 1))) {
+          tc_fence_after();
+          issue_grad(ng);
+          ++ng;
+        } else if (ns < nblk &&
+                   mbar_probe(bar(L::kBarKvFull + ns % L::kStages), (ns / L::kStages) & 1) &&
+                   (ns == 0 || mbar_probe(bar(L::kBarSdpFree), (ns - 1) & 1))) {
+          // The kv tile was written by cp.async (generic proxy): order it
+          // before the tensor core's (async proxy) reads.
+          fence_proxy_async_smem();
+          tc_fence_after();
+          issue_sdp(ns);
+          ++ns;
+        } else {
+          if ((++spins & 63u) == 0u && !poll_check(ctl, ps)) {
+            ok = false;
+            break;
+          }
+          continue;
+        }
+        ps.t0 = globaltimer_ns();  // progress: the limit counts from the last issue
       }
       mma_commit(bar(L::kBarDqDone));
       mma_commit(bar(L::kBarDrain));
@@ -377,86 +427,99 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
     __syncwarp();
   } else if (NC == 2 && warp >= L::kSenderWarp0) {
     // ------------------------------------------------------------ sender
-    // Thread = head row h: this CTA's partial S (exp2 domain) and sm_scale
-    // dP over its half of D, rounded to fp16, into the peer's receive buffer
-    // of the block's parity.  The P / dS warps round the same TMEM values the
-    // same way, so both CTAs add identical halves.
+    // Thread = head row h: this CTA's fp16 partial S / dP of each block into
+    // the peer's exchange buffer of the block's parity (L2), then one
+    // release-arrive per warp on the peer's barrier.
     const int sq = warp & 3;  // TMEM lane quarter
     const int h = sq * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(sq * 32) << 16;
-    const uint32_t peer_recv = mapa_shared(base + L::kOffRecv, rank ^ 1u);
     const uint32_t peer_full = mapa_shared(bar(L::kBarRecvFull), rank ^ 1u);
-    const uint32_t row_off = static_cast<uint32_t>(h) * 128u;
+    uint8_t* dst0 = p.exch + (static_cast<size_t>(slot) * 2 + (rank ^ 1u)) * (2 * L::kXchgBytes);
     for (int i = 0; i < nblk; ++i) {
       const int sb = i & 1;
-      bool ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSdpFull + sb), (i >> 1) & 1, ctl));
+      bool ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSdpFull), i & 1, ctl));
       if (!ok) break;
       tc_fence_after();
-      float xs[32], xp[32];
-      tmem_ld32(tmem + lane_base + L::kTmemS + sb * 2 * L::kBI, xs);
-      tmem_ld32(tmem + lane_base + L::kTmemDp + sb * 2 * L::kBI, xp);
+      uint32_t hs[32], hp[32];
+      load_own_partials<DC, NC>(tmem + lane_base + L::kTmemS, tmem + lane_base + L::kTmemDp,
+                                p.scale_log2, p.scale, hs, hp);
       tc_fence_before();
-      mbar_arrive(bar(L::kBarSdpFree + sb));
-      uint32_t hs[16], hp[16];
-#pragma unroll
-      for (int w = 0; w < 16; ++w) {
-        hs[w] = pack_f16x2_sat(xs[2 * w] * p.scale_log2, xs[2 * w + 1] * p.scale_log2);
-        hp[w] = pack_f16x2_sat(xp[2 * w] * p.scale, xp[2 * w + 1] * p.scale);
-      }
-      // The peer's buffer of this parity is free once it has combined block i-2.
+      mbar_arrive(bar(L::kBarSdpFree));
+      // The peer has consumed block i-2 from this buffer.
       if (i >= 2) {
         ok = __all_sync(0xffffffffu,
                         mbar_wait<true>(bar(L::kBarSendOk + sb), ((i >> 1) - 1) & 1, ctl));
         if (!ok) break;
       }
-      const uint32_t dst = peer_recv + static_cast<uint32_t>(sb) * L::kRecvBytes + row_off;
-      const uint32_t rbar = peer_full + 8u * static_cast<uint32_t>(sb);
+      uint4* dst = reinterpret_cast<uint4*>(dst0 + sb * L::kXchgBytes) + h;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        st_async_v4u(dst + ((c ^ (h & 7)) << 4), hs[4 * c], hs[4 * c + 1], hs[4 * c + 2],
-                     hs[4 * c + 3], rbar);
-        st_async_v4u(dst + (((c + 4) ^ (h & 7)) << 4), hp[4 * c], hp[4 * c + 1], hp[4 * c + 2],
-                     hp[4 * c + 3], rbar);
+      for (int j = 0; j < 8; ++j) {
+        dst[j * L::kHPad] = make_uint4(hs[4 * j], hs[4 * j + 1], hs[4 * j + 2], hs[4 * j + 3]);
+        dst[(8 + j) * L::kHPad] =
+            make_uint4(hp[4 * j], hp[4 * j + 1], hp[4 * j + 2], hp[4 * j + 3]);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(peer_full + 8u * static_cast<uint32_t>(sb));
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ dKV drain
+    // Thread = head-dim row of one lane quarter; per block 64 slots, read as
+    // two 32-slot halves (both 128-row halves of the tile per TMEM trip).
     const int wq = warp - 4;  // TMEM lane quarter
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
     const bool active = (wq * 32) < DC;  // DC = 64: rows 64..127 are padding
+    float* col = p.dkv_acc + static_cast<size_t>(rank) * DC + wq * 32 + lane;
     for (int j = 0; j < nblk; ++j) {
-      const int bk = j & 1;
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDkvFull + bk), (j >> 1) & 1, ctl));
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDkvFull), j & 1, ctl));
       if (!ok) break;
       tc_fence_after();
-      const int slot = j * L::kBI + lane;
-      const int r = slot < p.topk ? __ldg(idx_row + slot) : -1;
-      const bool v = static_cast<unsigned>(r) < static_cast<unsigned>(p.S_kv);
-      const uint32_t vm = __ballot_sync(0xffffffffu, v);
-      const int row = b * p.S_kv + (v ? r : 0);
-      if (active) {
-        // Both 128-row halves of the tile in one TMEM round trip; each slot's
-        // row index is shuffled once for both.
-        float x[L::kNE][32];
-        const uint32_t t0 = tmem + lane_base + L::kTmemDkv + bk * L::kNE * L::kBI;
-        if constexpr (L::kNE == 2)
-          tmem_ld32x2(t0, t0 + L::kBI, x[0], x[L::kNE - 1]);
-        else
-          tmem_ld32(t0, x[0]);
-        float* col = p.dkv_acc + static_cast<size_t>(rank) * DC + wq * 32 + lane;
+      int row[2];
+      uint32_t vm[2];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int rk = __shfl_sync(0xffffffffu, row, k);
-          if ((vm >> k) & 1u) {
+      for (int half = 0; half < 2; ++half) {
+        const int slot_j = j * L::kBI + 32 * half + lane;
+        const int r = slot_j < p.topk ? __ldg(idx_row + slot_j) : -1;
+        const bool v = static_cast<unsigned>(r) < static_cast<unsigned>(p.S_kv);
+        vm[half] = __ballot_sync(0xffffffffu, v);
+        row[half] = b * p.S_kv + (v ? r : 0);
+      }
+      const uint32_t t0 = tmem + lane_base + L::kTmemDkv;
+      if constexpr (L::kNE == 2) {
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          float x[2][32];
+          tmem_ld32x2(t0 + 32 * half, t0 + L::kBI + 32 * half, x[0], x[1]);
+          if (half == 1) {  // the whole tile is in registers: let the MMAs reuse it
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarDkvFree));
+          }
+          if (active) {
 #pragma unroll
-            for (int e = 0; e < L::kNE; ++e)
-              red_add_f32(col + static_cast<size_t>(rk) * p.D + e * 128, x[e][k]);
+            for (int k = 0; k < 32; ++k) {
+              const int rk = __shfl_sync(0xffffffffu, row[half], k);
+              if ((vm[half] >> k) & 1u) {
+                red_add_f32(col + static_cast<size_t>(rk) * p.D, x[0][k]);
+                red_add_f32(col + static_cast<size_t>(rk) * p.D + 128, x[1][k]);
+              }
+            }
           }
         }
+      } else {
+        float x[2][32];
+        tmem_ld32x2(t0, t0 + 32, x[0], x[1]);
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarDkvFree));
+        if (active) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half)
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int rk = __shfl_sync(0xffffffffu, row[half], k);
+              if ((vm[half] >> k) & 1u) red_add_f32(col + static_cast<size_t>(rk) * p.D, x[half][k]);
+            }
+        }
       }
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarDkvFree + bk));
     }
   } else {
     // ------------------------------------------------------------ P / dS
@@ -470,14 +533,18 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
     const float dlt_s =
         h < p.H ? __ldg(p.delta + static_cast<size_t>(t) * p.H + h) * p.scale : 0.f;
     const uint32_t peer_sendok = NC == 2 ? mapa_shared(bar(L::kBarSendOk), rank ^ 1u) : 0u;
-    const uint32_t row64 = static_cast<uint32_t>(h) * 64u;
-    const uint32_t sw = static_cast<uint32_t>((h >> 1) & 3);
+    const uint4* src0 = NC == 2 ? reinterpret_cast<const uint4*>(
+                                      p.exch + (static_cast<size_t>(slot) * 2 + rank) *
+                                                   (2 * L::kXchgBytes)) + h
+                                : nullptr;
+    const uint32_t row128 = static_cast<uint32_t>(h) * 128u;
     const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
-    auto load_idx = [&](int blk) -> int {
-      const int j = blk * L::kBI + lane;
+    auto load_idx = [&](int blk, int half) -> int {
+      const int j = blk * L::kBI + 32 * half + lane;
       return j < p.topk ? __ldg(idx_row + j) : -1;
     };
-    // P and dS' of slots 8c .. 8c+7 from their scores zs and scaled dP zp.
+    // P and dS' of slots 8c .. 8c+7 from their scores zs and scaled dP zp
+    // (slot validity: bit (8c + k) % 32 of msk).
     auto emit = [&](int c, uint32_t msk, const float* zs, const float* zp) {
       uint32_t pp[4], pd[4];
 #pragma unroll
@@ -485,7 +552,7 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
         float pv[2], dv[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const int jj = 8 * c + 2 * k + u;
+          const int jj = (8 * c + 2 * k + u) & 31;
           const float pr = ((msk >> jj) & 1u) ? fast_exp2(zs[2 * k + u] - lse2) : 0.f;
           pv[u] = pr;
           dv[u] = pr * (zp[2 * k + u] - dlt_s);
@@ -493,75 +560,83 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
         pp[k] = pack_bf16x2(pv[0], pv[1]);
         pd[k] = pack_bf16x2(dv[0], dv[1]);
       }
-      st_shared_v4(base + L::kOffP + row64 + ((c ^ sw) << 4), pp[0], pp[1], pp[2], pp[3]);
-      st_shared_v4(base + L::kOffDs + row64 + ((c ^ sw) << 4), pd[0], pd[1], pd[2], pd[3]);
+      const uint32_t off = row128 + ((static_cast<uint32_t>(c) ^ static_cast<uint32_t>(h & 7)) << 4);
+      st_shared_v4(base + L::kOffP + off, pp[0], pp[1], pp[2], pp[3]);
+      st_shared_v4(base + L::kOffDs + off, pd[0], pd[1], pd[2], pd[3]);
     };
-    int r_next = load_idx(0);
-    bool ok = true;
-    for (int i = 0; i < nblk; ++i) {
+    int r0 = load_idx(0, 0), r1 = load_idx(0, 1);
+    bool ok = *abort_flag == 0;
+    for (int i = 0; ok && i < nblk; ++i) {
       const int sb = i & 1;
-      // Valid-slot mask of the block, from the index row (prefetched).
-      const uint32_t msk =
-          __ballot_sync(0xffffffffu, static_cast<unsigned>(r_next) < static_cast<unsigned>(p.S_kv));
-      if (i + 1 < nblk) r_next = load_idx(i + 1);
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSdpFull + sb), (i >> 1) & 1, ctl));
+      // Valid-slot masks of the block's two 32-slot halves (prefetched).
+      const uint32_t m0 = __ballot_sync(0xffffffffu, static_cast<unsigned>(r0) < static_cast<unsigned>(p.S_kv));
+      const uint32_t m1 = __ballot_sync(0xffffffffu, static_cast<unsigned>(r1) < static_cast<unsigned>(p.S_kv));
+      if (i + 1 < nblk) {
+        r0 = load_idx(i + 1, 0);
+        r1 = load_idx(i + 1, 1);
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSdpFull), i & 1, ctl));
       if (!ok) break;
       tc_fence_after();
-      float xs[32], xp[32];
-      tmem_ld32(tmem + lane_base + L::kTmemS + sb * 2 * L::kBI, xs);
-      tmem_ld32(tmem + lane_base + L::kTmemDp + sb * 2 * L::kBI, xp);
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarSdpFree + sb));
-      // P / dS buffers were last read by the gradient MMAs of block i-1.
-      if (i >= 1) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarPdsFree), (i - 1) & 1, ctl));
-        if (!ok) break;
-      }
       if constexpr (NC == 2) {
-        uint32_t hs[16], hp[16];
-#pragma unroll
-        for (int w = 0; w < 16; ++w) {
-          hs[w] = pack_f16x2_sat(xs[2 * w] * p.scale_log2, xs[2 * w + 1] * p.scale_log2);
-          hp[w] = pack_f16x2_sat(xp[2 * w] * p.scale, xp[2 * w + 1] * p.scale);
+        uint32_t hs[32], hp[32];
+        load_own_partials<DC, NC>(tmem + lane_base + L::kTmemS, tmem + lane_base + L::kTmemDp,
+                                  p.scale_log2, p.scale, hs, hp);
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarSdpFree));
+        // P / dS buffers were last read by the gradient MMAs of block i-1.
+        if (i >= 1) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarPdsFree), (i - 1) & 1, ctl));
+          if (!ok) break;
         }
         ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull + sb), (i >> 1) & 1, ctl));
         if (!ok) break;
-        // Post the byte count of this buffer's next block (i + 2).
-        if (h == 0 && i + 2 < nblk) mbar_arrive_expect_tx(bar(L::kBarRecvFull + sb), L::kRecvBytes);
-        const uint32_t src = base + L::kOffRecv + static_cast<uint32_t>(sb) * L::kRecvBytes +
-                             static_cast<uint32_t>(h) * 128u;
+        const uint4* src = src0 + sb * (L::kXchgBytes / 16);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t ys[4], yp[4];
-          ld_shared_v4u(src + ((c ^ (h & 7)) << 4), ys[0], ys[1], ys[2], ys[3]);
-          ld_shared_v4u(src + (((c + 4) ^ (h & 7)) << 4), yp[0], yp[1], yp[2], yp[3]);
+        for (int c = 0; c < 8; ++c) {
+          const uint4 ys = __ldcg(src + c * L::kHPad);
+          const uint4 yp = __ldcg(src + (8 + c) * L::kHPad);
+          const uint32_t ysa[4] = {ys.x, ys.y, ys.z, ys.w};
+          const uint32_t ypa[4] = {yp.x, yp.y, yp.z, yp.w};
           float zs[8], zp[8];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const float2 a = add_f16x2_f32(hs[4 * c + k], ys[k]);
-            const float2 d = add_f16x2_f32(hp[4 * c + k], yp[k]);
+            const float2 a = add_f16x2_f32(hs[4 * c + k], ysa[k]);
+            const float2 d = add_f16x2_f32(hp[4 * c + k], ypa[k]);
             zs[2 * k] = a.x;
             zs[2 * k + 1] = a.y;
             zp[2 * k] = d.x;
             zp[2 * k + 1] = d.y;
           }
-          emit(c, msk, zs, zp);
+          emit(c, c < 4 ? m0 : m1, zs, zp);
         }
-        // Our receive buffer of this parity may take the peer's block i+2.
+        // This exchange buffer may take the peer's block i+2.
         __syncwarp();
         if (lane == 0 && i + 2 < nblk)
           mbar_arrive_remote(peer_sendok + 8u * static_cast<uint32_t>(sb));
       } else {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float zs[8], zp[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            zs[k] = xs[8 * c + k] * p.scale_log2;
-            zp[k] = xp[8 * c + k] * p.scale;
-          }
-          emit(c, msk, zs, zp);
+        if (i >= 1) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarPdsFree), (i - 1) & 1, ctl));
+          if (!ok) break;
         }
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          float xs[32], xp[32];
+          tmem_ld32x2(tmem + lane_base + L::kTmemS + 32 * half,
+                      tmem + lane_base + L::kTmemDp + 32 * half, xs, xp);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float zs[8], zp[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              zs[k] = xs[8 * c + k] * p.scale_log2;
+              zp[k] = xp[8 * c + k] * p.scale;
+            }
+            emit(4 * half + c, half == 0 ? m0 : m1, zs, zp);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarSdpFree));
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(L::kBarPdsFull));
@@ -598,6 +673,11 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
   if (warp == L::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
+  }
+  // Release the pair's exchange slot once both CTAs are done with it.
+  if (NC == 2 && rank == 0 && threadIdx.x == 0 && slot >= 0) {
+    __threadfence();
+    atomicExch(p.slot_flags + slot, 0);
   }
 }
 

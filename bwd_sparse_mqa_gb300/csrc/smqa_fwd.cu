@@ -392,12 +392,15 @@ __global__ void __launch_bounds__(416, 1)
       if (!ok) break;
       tc_fence_after();
       float x[32];
-      tmem_ld32(tmem + lane_base + L::kTmemSA + 32 * g, x);
-      if (L::kOthChunks > 0) {
+      if constexpr (L::kOthChunks > 0) {
+        // Both partial tiles in one TMEM round trip.
         float x2[32];
-        tmem_ld32(tmem + lane_base + L::kTmemSB + 32 * g, x2);
+        tmem_ld32x2(tmem + lane_base + L::kTmemSA + 32 * g, tmem + lane_base + L::kTmemSB + 32 * g,
+                    x, x2);
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[j] += x2[j];
+      } else {
+        tmem_ld32(tmem + lane_base + L::kTmemSA + 32 * g, x);
       }
       tc_fence_before();
       mbar_arrive(bar(L::kBarSFree));

@@ -36,7 +36,17 @@ struct BwdParams {
   float scale_log2;      // sm_scale * log2(e)
   int* status;
   uint64_t limit_ns;
+  // D split across a CTA pair: the pairs trade their partial S / dP through
+  // an L2-resident pool of nslots slots (kBwdSlotBytes each); slot_flags[s]
+  // is 1 while a pair holds slot s (all zero before the launch).
+  uint8_t* exch;
+  int* slot_flags;
+  int nslots;
 };
+
+// One exchange slot: two receivers x two block parities x 32 KB (the fp16
+// partial S and dP of 128 heads x 64 slots).
+constexpr size_t kBwdSlotBytes = 2 * 2 * 32768;
 
 // Records `msg` as the text smqa_last_error() returns on this thread.
 void set_last_error(const char* msg);

@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define SMQA_ABI_VERSION 1
+#define SMQA_ABI_VERSION 2
 
 typedef enum {
     SMQA_OK = 0,
@@ -95,10 +95,22 @@ smqa_status smqa_fwd(const void* q, const void* kv, const float* attn_sink,
 /*
  * Bytes of device workspace smqa_bwd needs for `shape` and `flags`: the fp32
  * dKV accumulator [B,S_kv,D] (absent with SMQA_FLAG_RETURN_DKV_FP32, where
- * dkv itself accumulates) and Delta [B,S,H] fp32, each 256-byte aligned.
+ * dkv itself accumulates), Delta [B,S,H] fp32, and for D = 512 the exchange
+ * pool of smqa_bwd_exchange_bytes(shape), each 256-byte aligned.
  * Returns 0 for an unsupported shape.
  */
 size_t smqa_bwd_workspace_bytes(smqa_shape shape, unsigned flags);
+
+/*
+ * Bytes of the exchange pool the main backward kernel uses for `shape`
+ * (0 when D = 64; 4 KB of slot flags + 96 slots of 128 KB when D = 512).
+ * For D = 512 each token is handled by a pair of CTAs that own one half of D
+ * each; every 64-slot block they trade their fp16 partial scores and dP
+ * through a slot of this pool (it stays in L2).  The pool's contents need no
+ * initialisation: smqa_bwd_main clears the slot flags on its stream.
+ * Returns 0 for an unsupported shape.
+ */
+size_t smqa_bwd_exchange_bytes(smqa_shape shape);
 
 /*
  * Backward (tilelang_sparse_mla_bwd: `sparse_mqa_bwd_interface`, which runs
@@ -137,7 +149,8 @@ smqa_status smqa_bwd(const void* q, const void* kv, const float* attn_sink, cons
  *   - Shapes whose smqa_bwd_workspace_bytes(shape, flags) exceeds
  *     SMQA_STATIC_SCRATCH_BYTES are rejected with SMQA_ERR_UNSUPPORTED before
  *     anything runs (smqa_last_error() gives both sizes).  With
- *     SMQA_FLAG_RETURN_DKV_FP32 only Delta (B*S*H floats) needs the buffer.
+ *     SMQA_FLAG_RETURN_DKV_FP32 only Delta (B*S*H floats) and, for D = 512,
+ *     the exchange pool need the buffer.
  *   - The first call on a device looks up the buffer's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.
@@ -160,13 +173,18 @@ smqa_status smqa_bwd_static_scratch(const void* q, const void* kv, const float* 
  *                 [B,S_kv,D] fp32 set to zero
  *   main        : dq, and dkv_accum += every slot's dKV contribution
  *   postprocess : dkv_bf16 = round-to-nearest-even(dkv_accum)
+ * smqa_bwd_main also takes the exchange pool: a 256-byte-aligned device
+ * buffer of at least smqa_bwd_exchange_bytes(shape) bytes (may be NULL with
+ * size 0 when that is 0); a smaller pool is rejected with
+ * SMQA_ERR_UNSUPPORTED.  Calls whose kernels may overlap must not share it.
  */
 smqa_status smqa_bwd_preprocess(const void* o, const void* dout, smqa_shape shape,
                                 float* delta, float* dkv_accum, cudaStream_t stream);
 smqa_status smqa_bwd_main(const void* q, const void* kv, const float* attn_sink,
                           const void* dout, const int32_t* topk_idxs, const float* lse,
                           const float* delta, smqa_shape shape, float sm_scale, void* dq,
-                          float* dkv_accum, cudaStream_t stream);
+                          float* dkv_accum, void* exchange, size_t exchange_bytes,
+                          cudaStream_t stream);
 smqa_status smqa_bwd_postprocess(const float* dkv_accum, smqa_shape shape, void* dkv_bf16,
                                  cudaStream_t stream);
 

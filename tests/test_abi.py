@@ -32,7 +32,7 @@ def test_exports_match_header(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.smqa_abi_version() == 1
+    assert lib.smqa_abi_version() == 2
     assert lib.smqa_status_string(0) == b"SMQA_OK"
     assert lib.smqa_status_string(4) == b"SMQA_ERR_DEVICE_TIMEOUT"
     assert lib.smqa_status_string(99) == b"SMQA_ERR_UNKNOWN"
@@ -79,6 +79,26 @@ def test_bwd_workspace_and_checks(lib):
     assert lib.smqa_bwd(*args, ws, 4, None) == _lib.SMQA_ERR_INVALID_ARG
     args_null = [p] * 6 + [None, shp, 0.0, p, p, p]
     assert lib.smqa_bwd(*args_null, ws, 0, None) == _lib.SMQA_ERR_INVALID_ARG
+
+
+def test_bwd_exchange_pool_size_and_checks(lib):
+    """D = 512: the workspace carries the CTA-pair exchange pool (4 KB of slot
+    flags + 96 slots of 128 KB); D = 64 needs none.  smqa_bwd_main rejects a
+    pool that is too small, or missing, before any GPU work."""
+    r = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    s512 = _lib.Shape(1, 8, 16, 16, 512, 4)
+    ex = lib.smqa_bwd_exchange_bytes(s512)
+    assert ex == 4096 + 96 * 128 * 1024
+    acc, delta = 16 * 512 * 4, 8 * 16 * 4
+    assert lib.smqa_bwd_workspace_bytes(s512, 0) == r(acc) + r(delta) + r(ex)
+    assert lib.smqa_bwd_exchange_bytes(_lib.Shape(1, 8, 16, 16, 64, 4)) == 0
+    assert lib.smqa_bwd_exchange_bytes(_lib.Shape(1, 8, 16, 16, 100, 4)) == 0
+    p = _fake()
+    args = [p] * 7 + [s512, 0.0, p, p]
+    assert lib.smqa_bwd_main(*args, p, ex - 1, None) == _lib.SMQA_ERR_UNSUPPORTED
+    assert b"exchange pool too small" in lib.smqa_last_error()
+    assert lib.smqa_bwd_main(*args, None, ex, None) == _lib.SMQA_ERR_INVALID_ARG
+    assert lib.smqa_bwd_main(*args, _fake(0x10010), ex, None) == _lib.SMQA_ERR_INVALID_ARG
 
 
 def test_python_interface_rejects_cpu_tensors():
