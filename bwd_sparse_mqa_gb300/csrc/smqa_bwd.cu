@@ -235,6 +235,13 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
       *slot_smem = got;
     }
     fence_mbar_init();
+    // Q and dO slices, issued before the index scan so the loads overlap.
+    mbar_arrive_expect_tx(bar(L::kBarQdoFull), 2u * static_cast<uint32_t>(p.H) * 128u * L::kChunks);
+    for (int c = 0; c < L::kChunks; ++c) {
+      const int x = static_cast<int>(rank) * DC + c * 64;
+      tma_load_2d(base + L::kOffQ + c * L::kQChunkBytes, &tm_q, x, t * p.H, bar(L::kBarQdoFull));
+      tma_load_2d(base + L::kOffDo + c * L::kQChunkBytes, &tm_do, x, t * p.H, bar(L::kBarQdoFull));
+    }
   }
   if (warp == L::kMmaWarp) {
     if (lane == 0) {
@@ -289,16 +296,6 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
       return j < p.topk ? __ldg(idx_row + j) : -1;
     };
     int r_next = load_idx(0);
-    if (warp == L::kProducerWarp0 && lane == 0 && *abort_flag == 0) {
-      mbar_arrive_expect_tx(bar(L::kBarQdoFull),
-                            2u * static_cast<uint32_t>(p.H) * 128u * L::kChunks);
-      for (int c = 0; c < L::kChunks; ++c) {
-        const int x = static_cast<int>(rank) * DC + c * 64;
-        tma_load_2d(base + L::kOffQ + c * L::kQChunkBytes, &tm_q, x, t * p.H, bar(L::kBarQdoFull));
-        tma_load_2d(base + L::kOffDo + c * L::kQChunkBytes, &tm_do, x, t * p.H,
-                    bar(L::kBarQdoFull));
-      }
-    }
     for (int i = 0; i < nblk; ++i) {
       const int s = i % L::kStages;
       const int r = r_next;
@@ -610,10 +607,14 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
           }
           emit(c, c < 4 ? m0 : m1, zs, zp);
         }
-        // This exchange buffer may take the peer's block i+2.
+        fence_proxy_async_smem();
+        mbar_arrive(bar(L::kBarPdsFull));
+        // The exchange buffer may take the peer's block i+2 (a cluster-scope
+        // release: signalled after P / dS so the gradients need not wait).
         __syncwarp();
         if (lane == 0 && i + 2 < nblk)
           mbar_arrive_remote(peer_sendok + 8u * static_cast<uint32_t>(sb));
+        continue;
       } else {
         if (i >= 1) {
           ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarPdsFree), (i - 1) & 1, ctl));

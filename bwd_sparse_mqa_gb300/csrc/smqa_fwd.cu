@@ -167,10 +167,24 @@ __global__ void __launch_bounds__(416, 1)
     mbar_init(bar(L::kBarLsum), L::kSoftmaxThreads);
     *abort_flag = *reinterpret_cast<volatile int*>(p.status) != 0 ? 1 : 0;
     fence_mbar_init();
+    // This CTA's column half of Q, issued before anything else waits on
+    // memory (the index scan below and the other half's loads overlap it).
+    mbar_arrive_expect_tx(bar(L::kBarQFull), static_cast<uint32_t>(p.H) * 128u * L::kOwnChunks);
+    for (int c = 0; c < L::kOwnChunks; ++c)
+      tma_load_2d(base + L::kOffQ + c * L::kQChunkBytes, &tm_q, rank * DC + c * 64, t * p.H,
+                  bar(L::kBarQFull));
   }
-  if (warp == L::kMmaWarp) {
-    if (lane == 0) tma_prefetch_desc(&tm_q);
-    tmem_alloc(base + L::kOffTmemHolder, L::kTmemCols);
+  if (warp == L::kMmaWarp) tmem_alloc(base + L::kOffTmemHolder, L::kTmemCols);
+  // Softmax threads (h, g) start loading their part of the other column half
+  // of Q (stored into TMEM once it is allocated).
+  uint4 qt_pre[16];
+  if (NSPLIT == 2 && warp < L::kOwnWarp0) {
+    const int hq = threadIdx.x & 127;
+    const uint4* src = reinterpret_cast<const uint4*>(
+        p.q + (static_cast<size_t>(t) * p.H + (hq < p.H ? hq : 0)) * D + (1 - rank) * DC +
+        (warp >> 2) * 128);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) qt_pre[k] = hq < p.H ? __ldg(src + k) : make_uint4(0u, 0u, 0u, 0u);
   }
   // Heads beyond H are zero rows of the smem A operand (the TMA box covers H rows).
   if (threadIdx.x < L::kHPad && static_cast<int>(threadIdx.x) >= p.H) {
@@ -203,13 +217,6 @@ __global__ void __launch_bounds__(416, 1)
         const int j = blk * L::kBI + 32 * half + lane;
         return j < p.topk ? __ldg(idx_row + j) : -1;
       };
-      if (own && w == 0 && lane == 0) {
-        mbar_arrive_expect_tx(bar(L::kBarQFull),
-                              static_cast<uint32_t>(p.H) * 128u * L::kOwnChunks);
-        for (int c = 0; c < L::kOwnChunks; ++c)
-          tma_load_2d(base + L::kOffQ + c * L::kQChunkBytes, &tm_q, rank * DC + c * 64, t * p.H,
-                      bar(L::kBarQFull));
-      }
       const int full0 = own ? L::kBarOwnFull : L::kBarOthFull;
       const int empty0 = own ? L::kBarOwnEmpty : L::kBarOthEmpty;
       const uint32_t ring = base + (own ? L::kOffOwn : L::kOffOth);
@@ -351,16 +358,14 @@ __global__ void __launch_bounds__(416, 1)
     constexpr int kOHalf = DC / 2;
     if (NSPLIT == 2) {
       // The other column half of this head's q row -> TMEM (A operand of
-      // score chain B), as bf16 pairs: this thread stores words [64g, 64g+64).
-      const int ocol = (1 - rank) * DC + g * 128;
-      const uint4* src = reinterpret_cast<const uint4*>(
-          p.q + (static_cast<size_t>(t) * p.H + (h < p.H ? h : 0)) * D + ocol);
+      // score chain B), as bf16 pairs: this thread stores words [64g, 64g+64)
+      // (loaded into qt_pre during the prologue).
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         float v[32];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint4 w = h < p.H ? __ldg(src + half * 8 + k) : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 w = qt_pre[half * 8 + k];
           v[4 * k] = __uint_as_float(w.x);
           v[4 * k + 1] = __uint_as_float(w.y);
           v[4 * k + 2] = __uint_as_float(w.z);

@@ -213,6 +213,16 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t local, uint32_t rank) {
   return r;
 }
 
+// 16-byte global load cached in L2 only (never a stale L1 line), kept in
+// program order so that callers control how many are in flight.
+__device__ __forceinline__ uint4 ld_global_cg_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
 // 32-bit load from another CTA's shared memory (`remote` from mapa).
 __device__ __forceinline__ int ld_shared_cluster_s32(uint32_t remote) {
   int v;
