@@ -29,7 +29,7 @@ EXPORTS = [
     "smqa_bwd_postprocess", "smqa_device_status", "smqa_status_string", "smqa_last_error",
     "smqa_abi_version", "smqa_bwd_static_scratch", "smqa_bwd_exchange_bytes",
 ]
-STATIC_SCRATCH_BYTES = 24 << 20
+STATIC_SCRATCH_BYTES = 40 << 20
 
 
 class Shape(ctypes.Structure):

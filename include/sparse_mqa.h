@@ -160,7 +160,7 @@ smqa_status smqa_bwd(const void* q, const void* kv, const float* attn_sink, cons
  *     ordering between them, or several host threads -- race on it and give
  *     wrong results; order them on one stream.
  */
-#define SMQA_STATIC_SCRATCH_BYTES (24u << 20)
+#define SMQA_STATIC_SCRATCH_BYTES (40u << 20)
 smqa_status smqa_bwd_static_scratch(const void* q, const void* kv, const float* attn_sink,
                                     const void* o, const void* dout, const int32_t* topk_idxs,
                                     const float* lse, smqa_shape shape, float sm_scale, void* dq,
