@@ -255,7 +255,9 @@ def main():
     dkv = torch.empty((B, S_kv, D), dtype=torch.bfloat16, device=dev)
     acc = torch.empty((B, S_kv, D), dtype=torch.float32, device=dev)
     delta = torch.empty((B, S, H), dtype=torch.float32, device=dev)
-    exch_bytes = int(lib.smqa_bwd_exchange_bytes(shp))
+    # One exchange pool serves the forward and the backward main kernel (they
+    # run one after the other on the stream).
+    exch_bytes = max(int(lib.smqa_fwd_workspace_bytes(shp)), int(lib.smqa_bwd_exchange_bytes(shp)))
     exch = torch.empty((max(exch_bytes, 256),), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = ctypes.c_void_p(stream.cuda_stream)
@@ -266,7 +268,7 @@ def main():
         if ev is not None:
             ev[0].record(stream)
         _lib.check("smqa_fwd", lib.smqa_fwd(P(q), P(kv), P(sink), P(idx), shp, scale, P(o), P(lse),
-                                            0, sp))
+                                            P(exch), exch_bytes, 0, sp))
         if ev is not None:
             ev[1].record(stream)
         _lib.check("pre", lib.smqa_bwd_preprocess(P(o), P(dout), shp, P(delta), P(acc), sp))
@@ -327,10 +329,12 @@ def main():
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = sum(v.numel() * v.element_size() for v in outs.values())
     ws = torch.empty((int(lib.smqa_bwd_workspace_bytes(shp, 0)),), dtype=torch.uint8, device=dev)
+    fws = torch.empty((max(int(lib.smqa_fwd_workspace_bytes(shp)), 1),), dtype=torch.uint8,
+                      device=dev)
 
     def e2e_step():
         g = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
-        oo, ll = sparse_mqa_fwd_interface(g["q"], g["kv"], g["sink"], g["idx"])
+        oo, ll = sparse_mqa_fwd_interface(g["q"], g["kv"], g["sink"], g["idx"], workspace=fws)
         gq, gkv = sparse_mqa_bwd_interface(g["q"], g["kv"], g["sink"], oo, g["do"], g["idx"], ll,
                                            workspace=ws)
         outs["o"].copy_(oo, non_blocking=True)

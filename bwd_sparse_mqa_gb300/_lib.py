@@ -28,6 +28,7 @@ EXPORTS = [
     "smqa_fwd", "smqa_bwd_workspace_bytes", "smqa_bwd", "smqa_bwd_preprocess", "smqa_bwd_main",
     "smqa_bwd_postprocess", "smqa_device_status", "smqa_status_string", "smqa_last_error",
     "smqa_abi_version", "smqa_bwd_static_scratch", "smqa_bwd_exchange_bytes",
+    "smqa_fwd_workspace_bytes", "smqa_fwd_static_scratch",
 ]
 STATIC_SCRATCH_BYTES = 40 << 20
 
@@ -46,8 +47,12 @@ class SMQAError(RuntimeError):
 def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     P, S, F, U = ctypes.c_void_p, Shape, ctypes.c_float, ctypes.c_uint
     st = ctypes.c_int
-    lib.smqa_fwd.argtypes = [P, P, P, P, S, F, P, P, U, P]
+    lib.smqa_fwd.argtypes = [P, P, P, P, S, F, P, P, P, ctypes.c_size_t, U, P]
     lib.smqa_fwd.restype = st
+    lib.smqa_fwd_workspace_bytes.argtypes = [S]
+    lib.smqa_fwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.smqa_fwd_static_scratch.argtypes = [P, P, P, P, S, F, P, P, U, P]
+    lib.smqa_fwd_static_scratch.restype = st
     lib.smqa_bwd_workspace_bytes.argtypes = [S, U]
     lib.smqa_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.smqa_bwd.argtypes = [P, P, P, P, P, P, P, S, F, P, P, P, ctypes.c_size_t, U, P]

@@ -72,7 +72,8 @@ def _scale(sm_scale: Optional[float], D: int) -> float:
 def sparse_mqa_fwd_interface(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor,
                              topk_idxs: torch.Tensor, sm_scale: Optional[float] = None,
                              block_I: int = 64, num_stages: int = 2, threads: int = 256,
-                             reference_rounding: bool = False
+                             reference_rounding: bool = False,
+                             workspace: Optional[torch.Tensor] = None
                              ) -> tuple[torch.Tensor, torch.Tensor]:
     """Top-k sparse MQA forward.
 
@@ -80,18 +81,32 @@ def sparse_mqa_fwd_interface(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch
     attn_sink [H] fp32, topk_idxs [B,S,topk] int32 (entries outside
     [0,S_kv) are masked).  Returns freshly allocated O [B,S,H,D] bf16 and
     LSE [B,S,H] fp32 = log2(sum_valid exp(sm_scale q.k) + exp(sink)).
+    ``workspace`` (uint8 CUDA tensor, D = 512 only) may be passed to reuse
+    the exchange pool between calls; otherwise one is allocated.
     """
     shp = _shape(q, kv, attn_sink, topk_idxs)
     scale = _scale(sm_scale, shp.D)
-    o = torch.empty_like(q)
-    lse = torch.empty((shp.B, shp.S, shp.H), dtype=torch.float32, device=q.device)
     flags = _lib.FLAG_REFERENCE_ROUNDING if reference_rounding else 0
     lib = _lib.load()
+    need = int(lib.smqa_fwd_workspace_bytes(shp))
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8, 1)
+    if need > 0 and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty((need,), dtype=torch.uint8, device=q.device)
+    if need == 0:
+        workspace = None
+    o = torch.empty_like(q)
+    lse = torch.empty((shp.B, shp.S, shp.H), dtype=torch.float32, device=q.device)
     with torch.cuda.device(q.device):
         _lib.check("smqa_fwd", lib.smqa_fwd(_ptr(q), _ptr(kv), _ptr(attn_sink), _ptr(topk_idxs),
-                                            shp, scale, _ptr(o), _ptr(lse), flags,
+                                            shp, scale, _ptr(o), _ptr(lse), _ptr(workspace),
+                                            0 if workspace is None else workspace.numel(), flags,
                                             _stream(q.device)))
     return o, lse
+
+
+def fwd_workspace_bytes(shape: _lib.Shape) -> int:
+    return int(_lib.load().smqa_fwd_workspace_bytes(shape))
 
 
 def bwd_workspace_bytes(shape: _lib.Shape, return_dkv_accum_dtype: bool = False) -> int:
@@ -127,6 +142,8 @@ def sparse_mqa_bwd_interface(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch
     need = int(lib.smqa_bwd_workspace_bytes(shp, flags))
     if need == 0:
         raise ValueError("unsupported shape for the backward")
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8, 1)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty((need,), dtype=torch.uint8, device=q.device)
     dq = torch.empty_like(q)

@@ -128,12 +128,17 @@ float effective_scale(float sm_scale, int D) {
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Exchange pool of the D = 512 backward: slot flags, then the slots.
+// Exchange pool of the D = 512 forward and backward: slot flags, then the
+// slots.
 constexpr size_t kExchFlagBytes = 4096;
 constexpr int kExchSlots = 96;
 
 size_t exchange_bytes(const smqa_shape& s) {
   return s.D == 512 ? kExchFlagBytes + static_cast<size_t>(kExchSlots) * smqa::kBwdSlotBytes : 0;
+}
+
+size_t fwd_exchange_bytes(const smqa_shape& s) {
+  return s.D == 512 ? kExchFlagBytes + static_cast<size_t>(kExchSlots) * smqa::kFwdSlotBytes : 0;
 }
 
 smqa_status bwd_main_impl(const void* q, const void* kv, const void* dout, const int32_t* idx,
@@ -203,14 +208,22 @@ const char* smqa_last_error(void) { return g_last_error; }
 
 smqa_status smqa_fwd(const void* q, const void* kv, const float* attn_sink,
                      const int32_t* topk_idxs, smqa_shape shape, float sm_scale, void* o,
-                     float* lse, unsigned flags, cudaStream_t stream) {
+                     float* lse, void* workspace, size_t workspace_bytes, unsigned flags,
+                     cudaStream_t stream) {
   const smqa_status sc = check_shape(shape);
   if (sc != SMQA_OK) return sc;
-  if (!q || !kv || !attn_sink || !topk_idxs || !o || !lse || (flags & ~SMQA_FLAG_REFERENCE_ROUNDING) ||
-      !aligned(q, 16) || !aligned(kv, 16) || !aligned(o, 16) || !aligned(attn_sink, 4) ||
-      !aligned(topk_idxs, 4) || !aligned(lse, 4)) {
+  const size_t need = fwd_exchange_bytes(shape);
+  if (!q || !kv || !attn_sink || !topk_idxs || !o || !lse || (need != 0 && !workspace) ||
+      (flags & ~SMQA_FLAG_REFERENCE_ROUNDING) || !aligned(q, 16) || !aligned(kv, 16) ||
+      !aligned(o, 16) || !aligned(attn_sink, 4) || !aligned(topk_idxs, 4) || !aligned(lse, 4) ||
+      !aligned(workspace, 256)) {
     std::snprintf(g_last_error, sizeof g_last_error, "null/misaligned pointer or bad flags");
     return SMQA_ERR_INVALID_ARG;
+  }
+  if (workspace_bytes < need) {
+    std::snprintf(g_last_error, sizeof g_last_error, "workspace too small (%zu < %zu bytes)",
+                  workspace_bytes, need);
+    return SMQA_ERR_UNSUPPORTED;
   }
   cudaError_t e;
   int* st = status_ptr(&e);
@@ -219,6 +232,11 @@ smqa_status smqa_fwd(const void* q, const void* kv, const float* attn_sink,
   const uint64_t T = static_cast<uint64_t>(shape.B) * shape.S;
   if (!encode_bf16_2d(&tq, q, shape.D, T * shape.H, 64, static_cast<uint32_t>(shape.H)))
     return SMQA_ERR_CUDA;
+  if (need != 0) {
+    // Every slot free at launch (the kernel's pairs claim and release them).
+    e = cudaMemsetAsync(workspace, 0, kExchSlots * sizeof(int), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "exchange flags clear");
+  }
   const float scale = effective_scale(sm_scale, shape.D);
   smqa::FwdParams p{};
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -237,9 +255,19 @@ smqa_status smqa_fwd(const void* q, const void* kv, const float* attn_sink,
   p.ref_round = (flags & SMQA_FLAG_REFERENCE_ROUNDING) ? 1 : 0;
   p.status = st;
   p.limit_ns = wait_limit_ns();
+  if (need != 0) {
+    p.slot_flags = static_cast<int*>(workspace);
+    p.exch = static_cast<uint8_t*>(workspace) + kExchFlagBytes;
+    p.nslots = kExchSlots;
+  }
   e = smqa::launch_fwd(tq, p, static_cast<int>(T), stream);
   if (e != cudaSuccess) return cuda_fail(e, "fwd launch");
   return SMQA_OK;
+}
+
+size_t smqa_fwd_workspace_bytes(smqa_shape shape) {
+  if (check_shape(shape) != SMQA_OK) return 0;
+  return fwd_exchange_bytes(shape);
 }
 
 size_t smqa_bwd_workspace_bytes(smqa_shape shape, unsigned flags) {

@@ -10,27 +10,42 @@
 //
 // Design.  The token's H heads are the M = 128 rows of every MMA (heads
 // beyond H are zero rows), so the heads sharing one gathered kv block form a
-// real GEMM for the tcgen05 tensor core.
-//   * D = 512: two independent CTAs per token.  CTA r owns O columns
-//     [256r, 256r+256): its O accumulator (128 x 256 fp32) is half of TMEM.
-//     Both CTAs compute the FULL score tile S = Q.K^T over all 512 columns,
-//     so no partial sums cross between SMs (the CTA-to-CTA network moves
-//     only ~8 B/clk per SM, far too little for a per-block exchange).  Q's
-//     own half is an smem operand; the other half sits in TMEM as the A
-//     operand of `tcgen05.mma ... [a_tmem]` (TMEM: O 256 + two 64-column
-//     score tiles + Q 128 = 512 columns).  Both CTAs issue the K steps in the
-//     same order, so their scores, softmax and LSE are bit-identical.
-//   * D = 64: one CTA per token; Q is an smem operand.
-//   * Warp roles: warps 8-11 gather full kv rows with 16-byte cp.async
-//     (coalesced 512-byte row pieces, written into the 128-byte-swizzled
-//     K-major tile; completion signalled per block by cp.async mbarrier
-//     arrivals); warp 12 owns TMEM and issues the MMAs from one thread;
-//     warps 0-7 (two warpgroups; thread = head row = TMEM lane, 32 score
-//     columns each) run the masked online softmax in the exp2 domain, rescale
-//     O lazily (only when the running max grows by more than 2^8), write P as
-//     bf16 for the P.V MMA and finish with the sink and the log2 LSE.
+// real GEMM for the tcgen05 tensor core.  Slots go in blocks of 64.
+//   * D = 512: a cluster of two CTAs per token.  CTA r owns the column half
+//     [256r, 256r+256) of Q, of every gathered kv row and of O (its O
+//     accumulator, 128 x 256 fp32, is half of TMEM).  Per block it computes
+//     the partial scores over its half, S_r = Q_r.K_r^T, and the pair trades
+//     them: each CTA scales its fp32 partial into the exp2 domain and writes
+//     it into the peer's receive buffer in an L2-resident exchange slot, and
+//     both CTAs form S = S_0 + S_1 from the same two fp32 values (so the
+//     pair's probabilities and LSE are bit-identical).  fp16 partials would
+//     halve the exchange but put up to ~2^-8 of a score's magnitude into a
+//     single-slot LSE.  Each CTA then runs the same online softmax and
+//     accumulates O_r += P.V_r.  The exchange slot (two receivers x four
+//     block buffers x 32 KB) is claimed from a pool by the pair's rank 0 and
+//     released at exit.
+//   * Exchange flow control without a consumed-signal: a CTA frees score
+//     tile i % 3 only after its softmax has read the peer's partial of block
+//     i, and it computes (and sends) block i + 3 only into a freed tile, so
+//     the arrival of the peer's block j + 3 proves that the peer has read
+//     block j; a sender writes block j + 4 into the buffer of block j only
+//     after its own CTA has received block j + 3.
+//   * D = 64: one CTA per token, no exchange.
+//   * Warp roles: warps 8-10 gather this CTA's half of the kv rows with
+//     16-byte cp.async (coalesced 512-byte row pieces written into the
+//     128-byte-swizzled K-major tile; completion signalled per block by
+//     cp.async mbarrier arrivals) into a four-stage ring; warp 11 owns TMEM
+//     and issues the MMAs from one thread (scores into a ring of three
+//     64-column TMEM tiles; P.V with P, bf16, from a two-buffer ring in TMEM
+//     as the A operand); warps 12-15 (D = 512) read each score
+//     tile and send it to the peer; warps 0-7 (two warpgroups; thread = head
+//     row = TMEM lane, 32 score columns each) add the peer's partial, run the
+//     masked online softmax in the exp2 domain, rescale O lazily (only when
+//     the running max grows by more than 2^8), write P as bf16 into TMEM for
+//     the P.V MMA and finish with the sink and the log2 LSE.
 //   * Masked slots load a real (finite) row and get a -inf score, so their
-//     probability is exactly 0.
+//     probability is exactly 0; blocks past a token's last valid slot are
+//     skipped.
 #include <cuda_runtime.h>
 
 #include "smqa_internal.h"
@@ -40,35 +55,29 @@ namespace smqa {
 
 template <int D, int NSPLIT>
 struct FwdLayout {
-  static constexpr int kDC = D / NSPLIT;      // O columns (and own Q columns) per CTA
+  static constexpr int kDC = D / NSPLIT;      // columns of Q, kv and O per CTA
   static constexpr int kHPad = 128;           // MMA M: heads padded to 128
   static constexpr int kBI = 64;              // slots per block (MMA N of the scores)
-  static constexpr int kChunks = D / 64;      // 64-column (128-byte) swizzle chunks per row
-  static constexpr int kOwnChunks = kDC / 64;
-  static constexpr int kOthChunks = kChunks - kOwnChunks;
-  static constexpr int kStages = D >= 512 ? 2 : 4;   // slots of each ring
+  static constexpr int kChunks = kDC / 64;    // 64-column (128-byte) swizzle chunks per row
+  static constexpr int kStages = 4;           // kv ring
+  static constexpr int kSBufs = 3;            // score tiles in TMEM
+  static constexpr int kXBufs = kSBufs + 1;   // exchange buffers per receiver
   static constexpr uint32_t kQChunkBytes = kHPad * 128;
-  static constexpr uint32_t kQBytes = kOwnChunks * kQChunkBytes;
+  static constexpr uint32_t kQBytes = kChunks * kQChunkBytes;
   static constexpr uint32_t kKvChunkBytes = kBI * 128;   // kBI rows x 128 B
-  static constexpr uint32_t kOwnStageBytes = kOwnChunks * kKvChunkBytes;
-  static constexpr uint32_t kOthStageBytes = kOthChunks * kKvChunkBytes;
-  static constexpr uint32_t kPBytes = kHPad * kBI * 2;
+  static constexpr uint32_t kStageBytes = kChunks * kKvChunkBytes;
   static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffOwn = kOffQ + kQBytes;
-  static constexpr uint32_t kOffOth = kOffOwn + kStages * kOwnStageBytes;
-  static constexpr uint32_t kOffP = kOffOth + kStages * kOthStageBytes;
-  static constexpr uint32_t kOffCtrl = kOffP + kPBytes;
-  static constexpr int kBarOwnFull = 0;
-  static constexpr int kBarOwnEmpty = kBarOwnFull + kStages;
-  static constexpr int kBarOthFull = kBarOwnEmpty + kStages;
-  static constexpr int kBarOthEmpty = kBarOthFull + kStages;
-  static constexpr int kBarSFull = kBarOthEmpty + kStages;  // phase i: S of block i ready
-  static constexpr int kBarSFree = kBarSFull + 1;           // phase i: S of block i read
-  static constexpr int kBarPFull = kBarSFree + 1;           // phase i: P of block i written
-  static constexpr int kBarODone = kBarPFull + 1;           // phase i: P.V of block i done
-  static constexpr int kBarQFull = kBarODone + 1;
-  static constexpr int kBarQtFull = kBarQFull + 1;   // other half of Q stored in TMEM
-  static constexpr int kBarDrain = kBarQtFull + 1;
+  static constexpr uint32_t kOffKv = kOffQ + kQBytes;
+  static constexpr uint32_t kOffCtrl = kOffKv + kStages * kStageBytes;
+  static constexpr int kBarKvFull = 0;                       // [kStages]
+  static constexpr int kBarKvEmpty = kBarKvFull + kStages;   // [kStages]
+  static constexpr int kBarSFull = kBarKvEmpty + kStages;    // [kSBufs] scores of a block ready
+  static constexpr int kBarSFree = kBarSFull + kSBufs;       // [kSBufs] ... read by every reader
+  static constexpr int kBarRecvFull = kBarSFree + kSBufs;    // [kXBufs] peer's partial arrived
+  static constexpr int kBarPFull = kBarRecvFull + kXBufs;    // [2] P of block i in buffer i % 2
+  static constexpr int kBarODone = kBarPFull + 2;            // [2] P.V of block i done
+  static constexpr int kBarQFull = kBarODone + 2;
+  static constexpr int kBarDrain = kBarQFull + 1;
   static constexpr int kBarXmax = kBarDrain + 1;     // [2], by block parity
   static constexpr int kBarLsum = kBarXmax + 2;
   static constexpr int kNumBars = kBarLsum + 1;
@@ -76,41 +85,54 @@ struct FwdLayout {
   static constexpr uint32_t kOffLsum = kOffXmax + 2 * 2 * 128 * 4; // float [2][128]
   static constexpr uint32_t kOffTmemHolder = kOffLsum + 2 * 128 * 4;
   static constexpr uint32_t kOffAbort = kOffTmemHolder + 4;
-  static constexpr uint32_t kOffWarpLast = kOffAbort + 4;  // int [16]
+  static constexpr uint32_t kOffSlot = kOffAbort + 4;
+  static constexpr uint32_t kOffWarpLast = kOffSlot + 4;  // int [16]
+  static constexpr uint32_t kOffMask = kOffWarpLast + 64;  // uint32 [kStages][2]
   static constexpr uint32_t kCtrlBytes = 4096;
-  static_assert(kOffWarpLast + 64 - kOffCtrl <= kCtrlBytes, "control block overflow");
+  static_assert(kOffMask + 8 * kStages - kOffCtrl <= kCtrlBytes, "control block overflow");
   static constexpr uint32_t kSmemBytes = kOffCtrl + kCtrlBytes + 1024;  // +1024: realignment
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  // TMEM: O, the other half of Q (bf16 pairs), then the score tile as two
-  // partial sums: chain A over the own column half, chain B over the other.
+  // TMEM: O, the ring of score tiles, then two P buffers (bf16 pairs, 32
+  // columns each).
   static constexpr uint32_t kTmemO = 0;
-  static constexpr uint32_t kTmemQt = kDC;
-  static constexpr uint32_t kTmemSA = kDC + (D - kDC) / 2;
-  static constexpr uint32_t kTmemSB = kTmemSA + kBI;
-  static constexpr uint32_t kTmemUsed = kTmemSA + (kOthChunks > 0 ? 2 : 1) * kBI;
+  static constexpr uint32_t kTmemS = kDC;  // + (block % kSBufs) * kBI
+  static constexpr uint32_t kTmemP = kTmemS + kSBufs * kBI;  // + (block % 2) * kBI / 2
+  static constexpr uint32_t kTmemUsed = kTmemP + kBI;
   static constexpr uint32_t kTmemCols = kTmemUsed <= 256 ? 256 : 512;
   static_assert(kTmemUsed <= 512, "TMEM budget");
-  // warps 0-7: softmax; 8-9: gather own column half; 10-11: gather the other
-  // half; 12: TMEM owner + MMA issuer
+  // warps 0-7: softmax; 8-10: gather; 11: TMEM owner + MMA issuer; 12-15
+  // (D split across the pair only): send this CTA's partial scores.  (Three
+  // gather warps: the copies a warp keeps in flight bound its gather rate.)
   static constexpr int kSoftmaxThreads = 256;
-  static constexpr int kOwnWarp0 = 8;
-  static constexpr int kOthWarp0 = 10;
-  static constexpr int kMmaWarp = 12;
-  static constexpr int kThreads = 416;
+  static constexpr int kGatherWarp0 = 8;
+  static constexpr int kGatherWarps = 3;
+  static constexpr int kMmaWarp = kGatherWarp0 + kGatherWarps;
+  static constexpr int kSenderWarp0 = kMmaWarp + 1;
+  static constexpr int kThreads = NSPLIT == 2 ? 512 : 384;
+  // Readers of a score tile: the softmax threads and (D split) the senders;
+  // with the D split a softmax thread frees the tile only once it has also
+  // read the peer's partial of the block.
+  static constexpr int kSReaders = NSPLIT == 2 ? 384 : 256;
+  // Exchange buffer of one receiver and block: 16 pieces of 16 bytes per
+  // head (4 slots of fp32 each), piece-major, so a warp's 32 heads are 512
+  // contiguous bytes.
+  static constexpr int kPieces = 16;
+  static constexpr uint32_t kXchgBytes = kPieces * 16u * kHPad;
+  static_assert(2 * kXBufs * kXchgBytes == kFwdSlotBytes, "exchange slot size");
 };
 
-// Gathers one column half of a block's kv rows into a 128-byte-swizzled
-// K-major tile of `nchunks` 64-column chunks.  Warp w (0 or 1) of the pair
-// issues instructions w, w+2, ...; instruction k moves 16-byte pieces
-// q = 32k + lane, piece q being column piece q % (8 nchunks) of slot row
-// q / (8 nchunks).
-template <int NCHUNKS, int D>
-__device__ __forceinline__ void gather_half(uint32_t stage, const __nv_bfloat16* kv, int col0,
-                                            int row0, int row1, int w, int lane) {
+// Gathers this CTA's column half of a block's kv rows into a
+// 128-byte-swizzled K-major tile of NCHUNKS 64-column chunks.  Warp w of the
+// NW gather warps issues instructions w, w+NW, ...; instruction k moves
+// 16-byte pieces q = 32k + lane, piece q being column piece q % (8 NCHUNKS)
+// of slot row q / (8 NCHUNKS).
+template <int NCHUNKS, int D, int NW>
+__device__ __forceinline__ void gather_block(uint32_t stage, const __nv_bfloat16* kv, int col0,
+                                             int row0, int row1, int w, int lane) {
   constexpr int kRcpr = NCHUNKS * 8;
   constexpr int kInstr = 64 * kRcpr / 32;
 #pragma unroll 4
-  for (int k = w; k < kInstr; k += 2) {
+  for (int k = w; k < kInstr; k += NW) {
     const int q = 32 * k + lane;
     const int r = q / kRcpr;
     const int cc = q % kRcpr;
@@ -125,7 +147,7 @@ __device__ __forceinline__ void gather_half(uint32_t stage, const __nv_bfloat16*
 }
 
 template <int D, int NSPLIT>
-__global__ void __launch_bounds__(416, 1)
+__global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 384, 1)
     smqa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const FwdParams p) {
   using L = FwdLayout<D, NSPLIT>;
   constexpr int DC = L::kDC;
@@ -138,7 +160,7 @@ __global__ void __launch_bounds__(416, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x / NSPLIT;
-  const int rank = NSPLIT == 2 ? static_cast<int>(blockIdx.x % NSPLIT) : 0;
+  const uint32_t rank = NSPLIT == 2 ? cluster_ctarank() : 0u;
   const int b = t / p.S;
   const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
   auto bar = [&](int i) -> uint32_t { return base + L::kOffCtrl + 8u * static_cast<uint32_t>(i); };
@@ -146,51 +168,65 @@ __global__ void __launch_bounds__(416, 1)
   volatile float* lsum = reinterpret_cast<volatile float*>(smem + L::kOffLsum);
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(smem + L::kOffTmemHolder);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
+  volatile int* slot_smem = reinterpret_cast<volatile int*>(smem + L::kOffSlot);
+  volatile uint32_t* vmask = reinterpret_cast<volatile uint32_t*>(smem + L::kOffMask);
   const WaitCtl ctl{abort_flag, p.status, p.limit_ns};
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(bar(L::kBarOwnFull + s), 64);  // one cp.async arrival per gather thread
-      mbar_init(bar(L::kBarOwnEmpty + s), 1);
-      mbar_init(bar(L::kBarOthFull + s), 64);
-      mbar_init(bar(L::kBarOthEmpty + s), 1);
+      // One cp.async arrival per gather thread, plus the arrival that
+      // publishes the block's valid-slot mask.
+      mbar_init(bar(L::kBarKvFull + s), 32 * L::kGatherWarps + 1);
+      mbar_init(bar(L::kBarKvEmpty + s), 1);
     }
-    mbar_init(bar(L::kBarSFull), 1);
-    mbar_init(bar(L::kBarSFree), L::kSoftmaxThreads);
-    mbar_init(bar(L::kBarPFull), L::kSoftmaxThreads);
-    mbar_init(bar(L::kBarODone), 1);
+    for (int s = 0; s < L::kSBufs; ++s) {
+      mbar_init(bar(L::kBarSFull + s), 1);
+      mbar_init(bar(L::kBarSFree + s), L::kSReaders);
+    }
+    // Exchange: the peer's four sender warps each signal a filled buffer.
+    for (int s = 0; s < L::kXBufs; ++s) mbar_init(bar(L::kBarRecvFull + s), 4);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(L::kBarPFull + s), L::kSoftmaxThreads);
+      mbar_init(bar(L::kBarODone + s), 1);
+    }
     mbar_init(bar(L::kBarQFull), 1);
-    mbar_init(bar(L::kBarQtFull), L::kSoftmaxThreads);
     mbar_init(bar(L::kBarDrain), 1);
     mbar_init(bar(L::kBarXmax), L::kSoftmaxThreads);
     mbar_init(bar(L::kBarXmax + 1), L::kSoftmaxThreads);
     mbar_init(bar(L::kBarLsum), L::kSoftmaxThreads);
     *abort_flag = *reinterpret_cast<volatile int*>(p.status) != 0 ? 1 : 0;
+    *slot_smem = -1;
+    if (NSPLIT == 2 && rank == 0 && *abort_flag == 0) {
+      // Claim an exchange slot for the pair (bounded; released at exit).
+      const uint64_t t0 = globaltimer_ns();
+      int got = -1;
+      for (uint32_t it = 0; got < 0; ++it) {
+        const int s = static_cast<int>((static_cast<uint32_t>(t) + it) % static_cast<uint32_t>(p.nslots));
+        if (atomicCAS(p.slot_flags + s, 0, 1) == 0) {
+          got = s;
+        } else if ((it % static_cast<uint32_t>(p.nslots)) == static_cast<uint32_t>(p.nslots) - 1u &&
+                   globaltimer_ns() - t0 > p.limit_ns) {
+          *abort_flag = 1;
+          atomicOr(p.status, kStatusTimeout);
+          break;
+        }
+      }
+      *slot_smem = got;
+    }
     fence_mbar_init();
     // This CTA's column half of Q, issued before anything else waits on
-    // memory (the index scan below and the other half's loads overlap it).
-    mbar_arrive_expect_tx(bar(L::kBarQFull), static_cast<uint32_t>(p.H) * 128u * L::kOwnChunks);
-    for (int c = 0; c < L::kOwnChunks; ++c)
-      tma_load_2d(base + L::kOffQ + c * L::kQChunkBytes, &tm_q, rank * DC + c * 64, t * p.H,
-                  bar(L::kBarQFull));
+    // memory (the index scan below overlaps it).
+    mbar_arrive_expect_tx(bar(L::kBarQFull), static_cast<uint32_t>(p.H) * 128u * L::kChunks);
+    for (int c = 0; c < L::kChunks; ++c)
+      tma_load_2d(base + L::kOffQ + c * L::kQChunkBytes, &tm_q, static_cast<int>(rank) * DC + c * 64,
+                  t * p.H, bar(L::kBarQFull));
   }
   if (warp == L::kMmaWarp) tmem_alloc(base + L::kOffTmemHolder, L::kTmemCols);
-  // Softmax threads (h, g) start loading their part of the other column half
-  // of Q (stored into TMEM once it is allocated).
-  uint4 qt_pre[16];
-  if (NSPLIT == 2 && warp < L::kOwnWarp0) {
-    const int hq = threadIdx.x & 127;
-    const uint4* src = reinterpret_cast<const uint4*>(
-        p.q + (static_cast<size_t>(t) * p.H + (hq < p.H ? hq : 0)) * D + (1 - rank) * DC +
-        (warp >> 2) * 128);
-#pragma unroll
-    for (int k = 0; k < 16; ++k) qt_pre[k] = hq < p.H ? __ldg(src + k) : make_uint4(0u, 0u, 0u, 0u);
-  }
   // Heads beyond H are zero rows of the smem A operand (the TMA box covers H rows).
   if (threadIdx.x < L::kHPad && static_cast<int>(threadIdx.x) >= p.H) {
     const uint32_t h = threadIdx.x;
 #pragma unroll
-    for (int c = 0; c < L::kOwnChunks; ++c)
+    for (int c = 0; c < L::kChunks; ++c)
 #pragma unroll
       for (int k = 0; k < 8; ++k)
         st_shared_v4(base + L::kOffQ + c * L::kQChunkBytes + h * 128u + k * 16u, 0u, 0u, 0u, 0u);
@@ -200,54 +236,59 @@ __global__ void __launch_bounds__(416, 1)
   scan_last_valid(idx_row, p.topk, p.S_kv, warp_last);
   tc_fence_before();
   __syncthreads();
+  if (NSPLIT == 2) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  // Blocks up to the last one holding a valid slot (0: no valid slot).
+  // Blocks up to the last one holding a valid slot (0: no valid slot); both
+  // CTAs of a pair read the same index row, so they agree on it.
   const int nblk = live_blocks(warp_last, L::kBI);
+  // The pair's exchange slot (claimed by rank 0); without one, nothing runs.
+  int slot = -1;
+  if (NSPLIT == 2) {
+    slot = rank == 0 ? *slot_smem : ld_shared_cluster_s32(mapa_shared(base + L::kOffSlot, 0u));
+    if (slot < 0) *abort_flag = 1;
+  }
+  __syncwarp();
+  const bool run = *abort_flag == 0;
 
-  if (warp >= L::kOwnWarp0 && warp < L::kMmaWarp) {
+  if (warp >= L::kGatherWarp0 && warp < L::kMmaWarp) {
     // ------------------------------------------------------------ gather
-    // Warps 8-9 fill the own-column-half ring (needed until P.V), warps
-    // 10-11 the other-half ring (needed only by the scores), so the other
-    // half of block i+2 can land as soon as the scores of block i are done.
-    const bool own = warp < L::kOthWarp0;
-    const int w = (warp - L::kOwnWarp0) & 1;
-    if (own || L::kOthChunks > 0) {
-      auto load_idx = [&](int blk, int half) -> int {
-        const int j = blk * L::kBI + 32 * half + lane;
-        return j < p.topk ? __ldg(idx_row + j) : -1;
-      };
-      const int full0 = own ? L::kBarOwnFull : L::kBarOthFull;
-      const int empty0 = own ? L::kBarOwnEmpty : L::kBarOthEmpty;
-      const uint32_t ring = base + (own ? L::kOffOwn : L::kOffOth);
-      const uint32_t stage_bytes = own ? L::kOwnStageBytes : L::kOthStageBytes;
-      const int col0 = (own ? rank : 1 - rank) * DC;
-      int n0 = load_idx(0, 0), n1 = load_idx(0, 1);
-      for (int i = 0; i < nblk; ++i) {
-        const int s = i % L::kStages;
-        const int r0 = n0, r1 = n1;
-        if (i + 1 < nblk) {
-          n0 = load_idx(i + 1, 0);
-          n1 = load_idx(i + 1, 1);
-        }
-        const int row0 = b * p.S_kv + (static_cast<unsigned>(r0) < static_cast<unsigned>(p.S_kv) ? r0 : 0);
-        const int row1 = b * p.S_kv + (static_cast<unsigned>(r1) < static_cast<unsigned>(p.S_kv) ? r1 : 0);
-        if (i >= L::kStages) {
-          const bool ok = mbar_wait(bar(empty0 + s), ((i / L::kStages) - 1) & 1, ctl);
-          if (!__all_sync(0xffffffffu, ok)) break;
-        }
-        const uint32_t stage = ring + static_cast<uint32_t>(s) * stage_bytes;
-        if (own)
-          gather_half<L::kOwnChunks, D>(stage, p.kv, col0, row0, row1, w, lane);
-        else
-          gather_half<(L::kOthChunks > 0 ? L::kOthChunks : 1), D>(stage, p.kv, col0, row0, row1,
-                                                                  w, lane);
-        cp_async_arrive_noinc(bar(full0 + s));
+    const int w = warp - L::kGatherWarp0;
+    auto load_idx = [&](int blk, int half) -> int {
+      const int j = blk * L::kBI + 32 * half + lane;
+      return j < p.topk ? __ldg(idx_row + j) : -1;
+    };
+    const int col0 = static_cast<int>(rank) * DC;
+    int n0 = load_idx(0, 0), n1 = load_idx(0, 1);
+    for (int i = 0; run && i < nblk; ++i) {
+      const int s = i % L::kStages;
+      const int r0 = n0, r1 = n1;
+      if (i + 1 < nblk) {
+        n0 = load_idx(i + 1, 0);
+        n1 = load_idx(i + 1, 1);
       }
-      // Let every copy this warp started land before the CTA can exit.
-      cp_async_wait_all();
-      if (own && w == 0 && lane == 0) mbar_wait_drain(bar(L::kBarQFull), 0);
+      const int row0 = b * p.S_kv + (static_cast<unsigned>(r0) < static_cast<unsigned>(p.S_kv) ? r0 : 0);
+      const int row1 = b * p.S_kv + (static_cast<unsigned>(r1) < static_cast<unsigned>(p.S_kv) ? r1 : 0);
+      if (i >= L::kStages) {
+        const bool ok = mbar_wait(bar(L::kBarKvEmpty + s), ((i / L::kStages) - 1) & 1, ctl);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+      // The block's valid-slot mask (bit j of word h: slot 32h + j), read by
+      // the softmax once this stage's full barrier has completed.
+      const uint32_t m0 = __ballot_sync(0xffffffffu, static_cast<unsigned>(r0) < static_cast<unsigned>(p.S_kv));
+      const uint32_t m1 = __ballot_sync(0xffffffffu, static_cast<unsigned>(r1) < static_cast<unsigned>(p.S_kv));
+      gather_block<L::kChunks, D, L::kGatherWarps>(base + L::kOffKv + static_cast<uint32_t>(s) * L::kStageBytes,
+                                  p.kv, col0, row0, row1, w, lane);
+      cp_async_arrive_noinc(bar(L::kBarKvFull + s));
+      if (w == 0 && lane == 0) {
+        vmask[2 * s] = m0;
+        vmask[2 * s + 1] = m1;
+        mbar_arrive(bar(L::kBarKvFull + s));
+      }
     }
+    // Let every copy this warp started land before the CTA can exit.
+    cp_async_wait_all();
+    if (w == 0 && lane == 0) mbar_wait_drain(bar(L::kBarQFull), 0);
   } else if (warp == L::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -256,79 +297,57 @@ __global__ void __launch_bounds__(416, 1)
       // Descriptors are built once; per MMA only the start-address field
       // (bits 0-13, in 16-byte units) moves, by compile-time offsets.
       const uint64_t d_q = smem_desc(base + L::kOffQ, 16u, 1024u, kSwizzle128B);
-      const uint64_t d_p = smem_desc(base + L::kOffP, 16u, 1024u, kSwizzle128B);
-      const uint64_t d_own = smem_desc(base + L::kOffOwn, 16u, 1024u, kSwizzle128B);
-      const uint64_t d_oth = smem_desc(base + L::kOffOth, 16u, 1024u, kSwizzle128B);
-      const uint64_t d_v = smem_desc(base + L::kOffOwn, L::kKvChunkBytes, 1024u, kSwizzle128B);
-      // Chain A: own column half, Q from smem.  Chain B: the other half, Q
-      // from TMEM.  Chunk j of a half is chunk j of that half on both CTAs,
-      // so each chain sums the same products in the same order everywhere.
-      auto issue_a = [&](int i) {
-        const uint64_t dk = d_own + ((static_cast<uint32_t>(i % L::kStages) * L::kOwnStageBytes) >> 4);
+      const uint64_t d_k = smem_desc(base + L::kOffKv, 16u, 1024u, kSwizzle128B);
+      const uint64_t d_v = smem_desc(base + L::kOffKv, L::kKvChunkBytes, 1024u, kSwizzle128B);
+      // Scores of block i over this CTA's columns (M = 128 heads, N = 64
+      // slots, K = DC) into score tile i % kSBufs.
+      auto issue_s = [&](int i) {
+        const uint64_t dk = d_k + ((static_cast<uint32_t>(i % L::kStages) * L::kStageBytes) >> 4);
+        const uint32_t d_tm = tmem + L::kTmemS + static_cast<uint32_t>(i % L::kSBufs) * L::kBI;
 #pragma unroll
-        for (int c = 0; c < L::kOwnChunks; ++c)
+        for (int c = 0; c < L::kChunks; ++c)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + L::kTmemSA, d_q + ((c * L::kQChunkBytes + k * 32u) >> 4),
+            mma_ss(d_tm, d_q + ((c * L::kQChunkBytes + k * 32u) >> 4),
                    dk + ((c * L::kKvChunkBytes + k * 32u) >> 4), idesc_s, (c | k) ? 1u : 0u);
+        mma_commit(bar(L::kBarSFull + i % L::kSBufs));
       };
-      auto issue_b = [&](int i) {
-        const uint64_t dk = d_oth + ((static_cast<uint32_t>(i % L::kStages) * L::kOthStageBytes) >> 4);
-#pragma unroll
-        for (int c = 0; c < L::kOthChunks; ++c)
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + L::kTmemSB, tmem + L::kTmemQt + (c * 4 + k) * 8,
-                   dk + ((c * L::kKvChunkBytes + k * 32u) >> 4), idesc_s, (c | k) ? 1u : 0u);
-      };
-      // O += P.V for block j; V = the own column half, read MN-major.
+      // O += P.V for block j; P (A operand) from TMEM buffer j % 2, V = this
+      // CTA's columns of the block, MN-major.
       auto issue_pv = [&](int j) {
         const int sj = j % L::kStages;
-        const uint64_t dv = d_v + ((static_cast<uint32_t>(sj) * L::kOwnStageBytes) >> 4);
+        const uint64_t dv = d_v + ((static_cast<uint32_t>(sj) * L::kStageBytes) >> 4);
+        const uint32_t a_tm = tmem + L::kTmemP + static_cast<uint32_t>(j & 1) * (L::kBI / 2);
 #pragma unroll
         for (int k = 0; k < L::kBI / 16; ++k)
-          mma_ss(tmem + L::kTmemO, d_p + (k * 32u >> 4), dv + (k * 2048u >> 4), idesc_o,
+          mma_ts(tmem + L::kTmemO, a_tm + k * 8, dv + (k * 2048u >> 4), idesc_o,
                  (j > 0 || k > 0) ? 1u : 0u);
-        mma_commit(bar(L::kBarOwnEmpty + sj));
-        mma_commit(bar(L::kBarODone));
+        mma_commit(bar(L::kBarKvEmpty + sj));
+        mma_commit(bar(L::kBarODone + (j & 1)));
       };
-      bool ok = mbar_wait(bar(L::kBarQFull), 0, ctl);
-      if (ok && NSPLIT == 2) ok = mbar_wait(bar(L::kBarQtFull), 0, ctl);
-      // Event loop over three kinds of work, oldest first (polled with
-      // non-blocking tests, so that waiting on one never delays another): P.V of block npv
-      // once its P is written; chain A (+ completion of S) of block na once
-      // the own half has landed; chain B of block nb once the other half has
-      // landed.  Both score chains of a block need the previous block's
-      // scores to have been read (one score tile in TMEM), and a block's
-      // scores may complete at most one block ahead of P.V.
-      constexpr bool kHasB = L::kOthChunks > 0;
-      int nb = 0, na = 0, npv = 0;
+      // Event loop (non-blocking tests, so that waiting on one kind of work
+      // never delays the other), oldest work first: P.V of block npv once
+      // its P is written; scores of block ns once its kv rows have landed
+      // and its score tile has been read by every reader (block ns - kSBufs).
+      bool ok = run && mbar_wait(bar(L::kBarQFull), 0, ctl);
+      int ns = 0, npv = 0;
       PollState ps = poll_start();
       uint32_t spins = 0;
       while (ok && npv < nblk) {
-        if (npv < na && mbar_probe(bar(L::kBarPFull), npv & 1)) {
+        if (npv < ns && mbar_probe(bar(L::kBarPFull + (npv & 1)), (npv >> 1) & 1)) {
           tc_fence_after();
           issue_pv(npv);
           ++npv;
-        } else if (na < nblk && (!kHasB || nb > na) && na <= npv + 1 &&
-                   (na == 0 || mbar_probe(bar(L::kBarSFree), (na - 1) & 1)) &&
-                   mbar_probe(bar(L::kBarOwnFull + na % L::kStages), (na / L::kStages) & 1)) {
+        } else if (ns < nblk &&
+                   mbar_probe(bar(L::kBarKvFull + ns % L::kStages), (ns / L::kStages) & 1) &&
+                   (ns < L::kSBufs ||
+                    mbar_probe(bar(L::kBarSFree + ns % L::kSBufs), ((ns / L::kSBufs) - 1) & 1))) {
           // The kv tile was written by cp.async (generic proxy): order it
           // before the tensor core's (async proxy) reads.
           fence_proxy_async_smem();
           tc_fence_after();
-          issue_a(na);
-          mma_commit(bar(L::kBarSFull));
-          ++na;
-        } else if (kHasB && nb < nblk && nb <= na &&
-                   (nb == 0 || mbar_probe(bar(L::kBarSFree), (nb - 1) & 1)) &&
-                   mbar_probe(bar(L::kBarOthFull + nb % L::kStages), (nb / L::kStages) & 1)) {
-          fence_proxy_async_smem();
-          tc_fence_after();
-          issue_b(nb);
-          // Only chain B reads the other column half: free its stage.
-          mma_commit(bar(L::kBarOthEmpty + nb % L::kStages));
-          ++nb;
+          issue_s(ns);
+          ++ns;
         } else {
           if ((++spins & 63u) == 0u && !poll_check(ctl, ps)) {
             ok = false;
@@ -336,15 +355,62 @@ __global__ void __launch_bounds__(416, 1)
           }
           continue;
         }
-        // Progress: the limit counts from the last issued work.
-        ps.t0 = globaltimer_ns();
+        ps.t0 = globaltimer_ns();  // progress: the limit counts from the last issue
       }
       // No MMA may still be running when TMEM is released.
       mma_commit(bar(L::kBarDrain));
       mbar_wait_drain(bar(L::kBarDrain), 0);
     }
     __syncwarp();
-  } else {
+  } else if (NSPLIT == 2 && warp >= L::kSenderWarp0) {
+    // ------------------------------------------------------------ sender
+    // Thread = head row h: this CTA's partial scores of each block, scaled
+    // into the exp2 domain, into the peer's receive buffer of the block (L2),
+    // then one release-arrive per warp on the peer's barrier.
+    const int sq = warp & 3;  // TMEM lane quarter
+    const int h = sq * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(sq * 32) << 16;
+    const float s1 = p.ref_round ? p.scale : p.scale_log2;
+    const uint32_t peer_full = mapa_shared(bar(L::kBarRecvFull), rank ^ 1u);
+    uint4* dst0 = reinterpret_cast<uint4*>(
+                      p.exch + (static_cast<size_t>(slot) * 2 + (rank ^ 1u)) *
+                                   (L::kXBufs * L::kXchgBytes)) + h;
+    for (int i = 0; run && i < nblk; ++i) {
+      const int sb = i % L::kSBufs;
+      bool ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + sb), (i / L::kSBufs) & 1, ctl));
+      if (!ok) break;
+      tc_fence_after();
+      float x0[32], x1[32];
+      tmem_ld32x2(tmem + lane_base + L::kTmemS + sb * L::kBI,
+                  tmem + lane_base + L::kTmemS + sb * L::kBI + 32, x0, x1);
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarSFree + sb));
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        x0[j] *= s1;
+        x1[j] *= s1;
+      }
+      // The peer has read block i - kXBufs from this buffer once its block
+      // i - 1 has arrived here (it computed that block into the score tile
+      // it freed after reading block i - kXBufs).
+      const int xb = i % L::kXBufs;
+      if (i >= L::kXBufs) {
+        const int j = i - 1;
+        ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull + j % L::kXBufs),
+                                                     (j / L::kXBufs) & 1, ctl));
+        if (!ok) break;
+      }
+      float4* dst = reinterpret_cast<float4*>(dst0 + xb * (L::kXchgBytes / 16));
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        dst[j * L::kHPad] = make_float4(x0[4 * j], x0[4 * j + 1], x0[4 * j + 2], x0[4 * j + 3]);
+        dst[(8 + j) * L::kHPad] =
+            make_float4(x1[4 * j], x1[4 * j + 1], x1[4 * j + 2], x1[4 * j + 3]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(peer_full + 8u * static_cast<uint32_t>(xb));
+    }
+  } else if (warp < L::kGatherWarp0) {
     // ------------------------------------------------------------ softmax
     // Thread (h, g): head row h (TMEM lane), score columns [32g, 32g+32) of
     // every block, O columns [DC/2 g, DC/2 (g+1)) for rescaling and output.
@@ -356,62 +422,60 @@ __global__ void __launch_bounds__(416, 1)
     const float s1 = p.ref_round ? p.scale : p.scale_log2;
     const float s2 = p.ref_round ? 1.4426950408889634f : 1.f;
     constexpr int kOHalf = DC / 2;
-    if (NSPLIT == 2) {
-      // The other column half of this head's q row -> TMEM (A operand of
-      // score chain B), as bf16 pairs: this thread stores words [64g, 64g+64)
-      // (loaded into qt_pre during the prologue).
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float v[32];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint4 w = qt_pre[half * 8 + k];
-          v[4 * k] = __uint_as_float(w.x);
-          v[4 * k + 1] = __uint_as_float(w.y);
-          v[4 * k + 2] = __uint_as_float(w.z);
-          v[4 * k + 3] = __uint_as_float(w.w);
-        }
-        tmem_st32(tmem + lane_base + L::kTmemQt + 64 * g + 32 * half, v);
-      }
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarQtFull));
-    }
-    // Slot validity: lane j of each warp holds slot 32g + j of the block;
-    // the warp's ballot is this thread's 32-bit column mask (read one block
-    // ahead from L2).
-    auto slot_ok = [&](int blk) -> bool {
-      const int j = blk * L::kBI + 32 * g + lane;
-      if (j >= p.topk) return false;
-      const int r = __ldg(idx_row + j);
-      return static_cast<unsigned>(r) < static_cast<unsigned>(p.S_kv);
-    };
-    bool v_next = slot_ok(0);
+    const uint4* src0 = NSPLIT == 2
+                            ? reinterpret_cast<const uint4*>(
+                                  p.exch + (static_cast<size_t>(slot) * 2 + rank) *
+                                               (L::kXBufs * L::kXchgBytes)) + 8 * g * L::kHPad + h
+                            : nullptr;
     float m_run = -INFINITY;
     float l_part = 0.f;
-    bool ok = true;
-    for (int i = 0; i < nblk; ++i) {
+    bool ok = run;
+    for (int i = 0; ok && i < nblk; ++i) {
+      const int sb = i % L::kSBufs;
       const int bb = i & 1;
-      const uint32_t msk = __ballot_sync(0xffffffffu, v_next);
-      if (i + 1 < nblk) v_next = slot_ok(i + 1);
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull), i & 1, ctl));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + sb), (i / L::kSBufs) & 1, ctl));
       if (!ok) break;
       tc_fence_after();
+      // The scores imply that the block's kv stage (and its valid-slot mask)
+      // has landed; its full barrier is tested only to order the mask read.
+      // Column j of this thread is valid iff bit j of msk is set.
+      const int st = i % L::kStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarKvFull + st), (i / L::kStages) & 1, ctl));
+      if (!ok) break;
+      const uint32_t msk = vmask[2 * st + g];
       float x[32];
-      if constexpr (L::kOthChunks > 0) {
-        // Both partial tiles in one TMEM round trip.
-        float x2[32];
-        tmem_ld32x2(tmem + lane_base + L::kTmemSA + 32 * g, tmem + lane_base + L::kTmemSB + 32 * g,
-                    x, x2);
+      tmem_ld32(tmem + lane_base + L::kTmemS + sb * L::kBI + 32 * g, x);
+      if constexpr (NSPLIT == 2) {
+        // S = own partial + peer's partial, each scaled exactly as the
+        // sender scales this CTA's partial for the peer.
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] += x2[j];
+        for (int j = 0; j < 32; ++j) x[j] *= s1;
+        const int xb = i % L::kXBufs;
+        ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull + xb),
+                                                     (i / L::kXBufs) & 1, ctl));
+        if (!ok) break;
+        const float4* src = reinterpret_cast<const float4*>(src0 + xb * (L::kXchgBytes / 16));
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float4 y = __ldcg(src + c * L::kHPad);
+          x[4 * c] += y.x;
+          x[4 * c + 1] += y.y;
+          x[4 * c + 2] += y.z;
+          x[4 * c + 3] += y.w;
+        }
+        // The values are in registers: the score tile may be reused (which
+        // is what tells the peer that this buffer has been read).
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarSFree + sb));
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = ((msk >> j) & 1u) ? x[j] * s2 : -INFINITY;
       } else {
-        tmem_ld32(tmem + lane_base + L::kTmemSA + 32 * g, x);
-      }
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarSFree));
-      float mq[8];
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarSFree + sb));
 #pragma unroll
-      for (int j = 0; j < 32; ++j) x[j] = ((msk >> j) & 1u) ? (x[j] * s1) * s2 : -INFINITY;
+        for (int j = 0; j < 32; ++j) x[j] = ((msk >> j) & 1u) ? (x[j] * s1) * s2 : -INFINITY;
+      }
+      float mq[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         mq[j] = fmaxf(fmaxf(x[4 * j], x[4 * j + 1]), fmaxf(x[4 * j + 2], x[4 * j + 3]));
@@ -432,18 +496,15 @@ __global__ void __launch_bounds__(416, 1)
         l_part *= alpha;
         m_run = m_new;
       }
-      // The P buffer and the O accumulator are free once P.V of block i-1
-      // has completed.
-      if (i >= 1) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone), (i - 1) & 1, ctl));
-        if (!ok) break;
-        tc_fence_after();
-      }
-      // O was accumulated against the old max: rescale this thread's half of
-      // the row (whole warp, since TMEM accesses are warp-collective; rows
-      // without a bump use 1).
+      // O was accumulated against the old max: once P.V of block i-1 has
+      // completed, rescale this thread's half of the row (whole warp, since
+      // TMEM accesses are warp-collective; rows without a bump use 1).
       const bool need_rescale = bump && alpha != 0.f && i > 0;
       if (__any_sync(0xffffffffu, need_rescale)) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + ((i - 1) & 1)),
+                                               ((i - 1) >> 1) & 1, ctl));
+        if (!ok) break;
+        tc_fence_after();
         const float a = need_rescale ? alpha : 1.f;
 #pragma unroll 1
         for (int c = 0; c < kOHalf / 32; ++c) {
@@ -465,16 +526,21 @@ __global__ void __launch_bounds__(416, 1)
         rs[w & 3] += p0 + p1;  // fp32 probabilities: the LSE must not carry bf16 rounding
       }
       l_part += (rs[0] + rs[1]) + (rs[2] + rs[3]);
-      const uint32_t p_row = base + L::kOffP + static_cast<uint32_t>(h) * 128u;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        st_shared_v4(p_row + (((4 * g + c) ^ (h & 7)) << 4), pk[4 * c], pk[4 * c + 1],
-                     pk[4 * c + 2], pk[4 * c + 3]);
-      fence_proxy_async_smem();
+      // P buffer i % 2 was last read by P.V of block i-2.
+      if (i >= 2) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(bar(L::kBarODone + (i & 1)), ((i - 2) >> 1) & 1, ctl));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      tmem_st16u(tmem + lane_base + L::kTmemP + static_cast<uint32_t>(i & 1) * (L::kBI / 2) +
+                     16 * g, pk);
       tc_fence_before();
-      mbar_arrive(bar(L::kBarPFull));
+      mbar_arrive(bar(L::kBarPFull + (i & 1)));
     }
-    if (ok && nblk > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone), (nblk - 1) & 1, ctl));
+    if (ok && nblk > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + ((nblk - 1) & 1)),
+                                             ((nblk - 1) >> 1) & 1, ctl));
     // Row sums: the two halves of each row meet here.
     lsum[g * 128 + h] = l_part;
     mbar_arrive(bar(L::kBarLsum));
@@ -514,9 +580,15 @@ __global__ void __launch_bounds__(416, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (NSPLIT == 2) cluster_sync();
   if (warp == L::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
+  }
+  // Release the pair's exchange slot once both CTAs are done with it.
+  if (NSPLIT == 2 && rank == 0 && threadIdx.x == 0 && slot >= 0) {
+    __threadfence();
+    atomicExch(p.slot_flags + slot, 0);
   }
 }
 
@@ -528,8 +600,19 @@ static cudaError_t launch_fwd_impl(const CUtensorMap& tm_q, const FwdParams& p, 
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<static_cast<unsigned>(tokens) * NSPLIT, L::kThreads, L::kSmemBytes, stream>>>(tm_q, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(tokens) * NSPLIT, 1, 1);
+  cfg.blockDim = dim3(L::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = NSPLIT;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tm_q, p);
 }
 
 cudaError_t launch_fwd(const CUtensorMap& tm_q, const FwdParams& p, int tokens,

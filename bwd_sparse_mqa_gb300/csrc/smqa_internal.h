@@ -22,6 +22,12 @@ struct FwdParams {
   int ref_round;         // 1: exp2 argument as (score * scale) * log2(e)
   int* status;           // device status word
   uint64_t limit_ns;     // bounded-wait limit
+  // D split across a CTA pair: the pairs trade their partial scores through
+  // an L2-resident pool of nslots slots (kFwdSlotBytes each); slot_flags[s]
+  // is 1 while a pair holds slot s (all zero before the launch).
+  uint8_t* exch;
+  int* slot_flags;
+  int nslots;
 };
 
 struct BwdParams {
@@ -44,8 +50,11 @@ struct BwdParams {
   int nslots;
 };
 
-// One exchange slot: two receivers x two block parities x 32 KB (the fp16
-// partial S and dP of 128 heads x 64 slots).
+// One exchange slot of the forward: two receivers x four block buffers x
+// 32 KB (the fp32 partial scores of 128 heads x 64 slots).
+constexpr size_t kFwdSlotBytes = 2 * 4 * 32768;
+// One exchange slot of the backward: two receivers x two block parities x
+// 32 KB (the fp16 partial S and dP of 128 heads x 64 slots).
 constexpr size_t kBwdSlotBytes = 2 * 2 * 32768;
 
 // Records `msg` as the text smqa_last_error() returns on this thread.

@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define SMQA_ABI_VERSION 2
+#define SMQA_ABI_VERSION 3
 
 typedef enum {
     SMQA_OK = 0,
@@ -76,6 +76,17 @@ typedef struct {
 #define SMQA_FLAG_RETURN_DKV_FP32 1u
 
 /*
+ * Bytes of device workspace smqa_fwd needs for `shape`: 0 when D = 64; for
+ * D = 512 the exchange pool (4 KB of slot flags + 96 slots of 256 KB).  For
+ * D = 512 each token is handled by a pair of CTAs that own one half of D
+ * each; every 64-slot block they trade their fp32 partial scores through a
+ * slot of this pool (it stays in L2).  The contents need no initialisation:
+ * smqa_fwd clears the slot flags on its stream.  Returns 0 for an
+ * unsupported shape.
+ */
+size_t smqa_fwd_workspace_bytes(smqa_shape shape);
+
+/*
  * Forward (tilelang_sparse_mla_fwd: `sparse_mqa_fwd_interface`, the kernel
  * factory `sparse_mqa_fwd`).
  *   q         [B,S,H,D]    bf16  queries
@@ -85,12 +96,21 @@ typedef struct {
  *   sm_scale               score multiplier; <= 0 (or NaN) selects D^-1/2
  *   o         [B,S,H,D]    bf16  output (written)
  *   lse       [B,S,H]      fp32  log2(sum_valid exp(sm_scale*q.k) + exp(sink))
+ *   workspace, workspace_bytes  a 256-byte-aligned device buffer of at least
+ *                          smqa_fwd_workspace_bytes(shape) bytes (may be NULL
+ *                          with size 0 when that is 0); a smaller one is
+ *                          rejected with SMQA_ERR_UNSUPPORTED.  Calls whose
+ *                          kernels may overlap must not share it.
  *   flags                  0 or SMQA_FLAG_REFERENCE_ROUNDING
  * A token whose slots are all masked gets O = 0 and lse = sink/ln 2.
+ * For D = 512 a score is the fp32 sum of two half-D partial scores, each
+ * already multiplied by sm_scale*log2(e) (by sm_scale with
+ * SMQA_FLAG_REFERENCE_ROUNDING, the sum then by log2(e)).
  */
 smqa_status smqa_fwd(const void* q, const void* kv, const float* attn_sink,
                      const int32_t* topk_idxs, smqa_shape shape, float sm_scale,
-                     void* o, float* lse, unsigned flags, cudaStream_t stream);
+                     void* o, float* lse, void* workspace, size_t workspace_bytes,
+                     unsigned flags, cudaStream_t stream);
 
 /*
  * Bytes of device workspace smqa_bwd needs for `shape` and `flags`: the fp32
@@ -133,19 +153,21 @@ smqa_status smqa_bwd(const void* q, const void* kv, const float* attn_sink, cons
                      cudaStream_t stream);
 
 /*
- * Backward for callers that cannot allocate device memory.  (The sparse MQA
- * pages have no counterpart: this entry point exists for this library's
- * users, not for parity with the pages.)
+ * Forward and backward for callers that cannot allocate device memory.  (The
+ * sparse MQA pages have no counterpart: these entry points exist for this
+ * library's users, not for parity with the pages.)
  *
- * smqa_bwd needs a device workspace of smqa_bwd_workspace_bytes() bytes.  Some
- * callers cannot provide one: code running under a memory planner that has
- * already handed every byte of device memory to its own pool, plugins that
- * get only the tensors they are given, or hot paths that must not take the
- * device-wide synchronisation cudaMalloc/cudaFree may imply.  This entry
- * point computes exactly what smqa_bwd computes, with the same arguments
- * minus the workspace, and allocates nothing: its scratch is a static device
- * buffer of SMQA_STATIC_SCRATCH_BYTES inside the library, which every GPU that
- * loads the library holds until the process exits.
+ * smqa_fwd and smqa_bwd need a device workspace of smqa_fwd_workspace_bytes()
+ * and smqa_bwd_workspace_bytes() bytes.  Some callers cannot provide one:
+ * code running under a memory planner that has already handed every byte of
+ * device memory to its own pool, plugins that get only the tensors they are
+ * given, or hot paths that must not take the device-wide synchronisation
+ * cudaMalloc/cudaFree may imply.  These entry
+ * points compute exactly what smqa_fwd and smqa_bwd compute, with the same
+ * arguments minus the workspace, and allocate nothing: their scratch is a
+ * static device buffer of SMQA_STATIC_SCRATCH_BYTES inside the library, which
+ * every GPU that loads the library holds until the process exits.  The
+ * forward's scratch always fits.
  *   - Shapes whose smqa_bwd_workspace_bytes(shape, flags) exceeds
  *     SMQA_STATIC_SCRATCH_BYTES are rejected with SMQA_ERR_UNSUPPORTED before
  *     anything runs (smqa_last_error() gives both sizes).  With
@@ -154,13 +176,16 @@ smqa_status smqa_bwd(const void* q, const void* kv, const float* attn_sink, cons
  *   - The first call on a device looks up the buffer's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.
- *   - All calls share the one buffer per device, and it keeps the previous
- *     call's contents (each call re-zeroes what must start at zero).  Calls
- *     whose kernels may overlap on the GPU -- different streams without
+ *   - All calls (forward and backward) share the one buffer per device, and
+ *     it keeps the previous call's contents (each call re-zeroes what must
+ *     start at zero).  Calls whose kernels may overlap on the GPU -- different streams without
  *     ordering between them, or several host threads -- race on it and give
  *     wrong results; order them on one stream.
  */
 #define SMQA_STATIC_SCRATCH_BYTES (40u << 20)
+smqa_status smqa_fwd_static_scratch(const void* q, const void* kv, const float* attn_sink,
+                                    const int32_t* topk_idxs, smqa_shape shape, float sm_scale,
+                                    void* o, float* lse, unsigned flags, cudaStream_t stream);
 smqa_status smqa_bwd_static_scratch(const void* q, const void* kv, const float* attn_sink,
                                     const void* o, const void* dout, const int32_t* topk_idxs,
                                     const float* lse, smqa_shape shape, float sm_scale, void* dq,

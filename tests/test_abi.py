@@ -32,7 +32,7 @@ def test_exports_match_header(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.smqa_abi_version() == 2
+    assert lib.smqa_abi_version() == 3
     assert lib.smqa_status_string(0) == b"SMQA_OK"
     assert lib.smqa_status_string(4) == b"SMQA_ERR_DEVICE_TIMEOUT"
     assert lib.smqa_status_string(99) == b"SMQA_ERR_UNKNOWN"
@@ -50,16 +50,16 @@ def test_fwd_rejects_bad_shapes(lib):
            (_lib.Shape(1, 1, 1, 16, 128, 1), _lib.SMQA_ERR_UNSUPPORTED),
            (_lib.Shape(1, 1, 1 << 23, 16, 512, 1), _lib.SMQA_ERR_UNSUPPORTED)]
     for shp, want in bad:
-        assert lib.smqa_fwd(p, p, p, p, shp, 0.0, p, p, 0, None) == want
+        assert lib.smqa_fwd(p, p, p, p, shp, 0.0, p, p, None, 0, 0, None) == want
 
 
 def test_fwd_rejects_null_misaligned_and_flags(lib):
     shp = _lib.Shape(1, 4, 4, 16, 64, 4)
     p = _fake()
-    assert lib.smqa_fwd(None, p, p, p, shp, 0.0, p, p, 0, None) == _lib.SMQA_ERR_INVALID_ARG
-    assert lib.smqa_fwd(_fake(0x10008), p, p, p, shp, 0.0, p, p, 0, None) == \
+    assert lib.smqa_fwd(None, p, p, p, shp, 0.0, p, p, None, 0, 0, None) == _lib.SMQA_ERR_INVALID_ARG
+    assert lib.smqa_fwd(_fake(0x10008), p, p, p, shp, 0.0, p, p, None, 0, 0, None) == \
         _lib.SMQA_ERR_INVALID_ARG
-    assert lib.smqa_fwd(p, p, p, p, shp, 0.0, p, p, 8, None) == _lib.SMQA_ERR_INVALID_ARG
+    assert lib.smqa_fwd(p, p, p, p, shp, 0.0, p, p, None, 0, 8, None) == _lib.SMQA_ERR_INVALID_ARG
     assert b"misaligned" in lib.smqa_last_error()
 
 
@@ -99,6 +99,29 @@ def test_bwd_exchange_pool_size_and_checks(lib):
     assert b"exchange pool too small" in lib.smqa_last_error()
     assert lib.smqa_bwd_main(*args, None, ex, None) == _lib.SMQA_ERR_INVALID_ARG
     assert lib.smqa_bwd_main(*args, _fake(0x10010), ex, None) == _lib.SMQA_ERR_INVALID_ARG
+
+
+def test_fwd_exchange_pool_size_and_checks(lib):
+    """D = 512: the forward's CTA pairs trade fp32 partial scores through an
+    exchange pool (4 KB of slot flags + 96 slots of 256 KB); D = 64 needs
+    none.  smqa_fwd
+    rejects a pool that is too small, missing or misaligned before any GPU
+    work, and the static-scratch entry rejects bad shapes the same way."""
+    s512 = _lib.Shape(1, 8, 16, 16, 512, 4)
+    ex = lib.smqa_fwd_workspace_bytes(s512)
+    assert ex == 4096 + 96 * 256 * 1024
+    assert ex <= _lib.STATIC_SCRATCH_BYTES
+    assert lib.smqa_fwd_workspace_bytes(_lib.Shape(1, 8, 16, 16, 64, 4)) == 0
+    assert lib.smqa_fwd_workspace_bytes(_lib.Shape(1, 8, 16, 16, 100, 4)) == 0
+    p = _fake()
+    args = [p] * 4 + [s512, 0.0, p, p]
+    assert lib.smqa_fwd(*args, p, ex - 1, 0, None) == _lib.SMQA_ERR_UNSUPPORTED
+    assert b"workspace too small" in lib.smqa_last_error()
+    assert lib.smqa_fwd(*args, None, ex, 0, None) == _lib.SMQA_ERR_INVALID_ARG
+    assert lib.smqa_fwd(*args, _fake(0x10010), ex, 0, None) == _lib.SMQA_ERR_INVALID_ARG
+    bad = _lib.Shape(1, 8, 16, 129, 512, 4)
+    assert lib.smqa_fwd_static_scratch(p, p, p, p, bad, 0.0, p, p, 0, None) == \
+        _lib.SMQA_ERR_UNSUPPORTED
 
 
 def test_python_interface_rejects_cpu_tensors():

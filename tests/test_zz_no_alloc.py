@@ -1,10 +1,11 @@
-"""The backward entry point for callers that cannot allocate device memory
-(smqa_bwd_static_scratch): it must give what the ordinary smqa_bwd gives,
-call after call, using only the library's static scratch buffer.
+"""The entry points for callers that cannot allocate device memory
+(smqa_fwd_static_scratch, smqa_bwd_static_scratch): they must give what the
+ordinary smqa_fwd / smqa_bwd give, call after call, using only the library's
+static scratch buffer.
 
 Such callers -- code under a memory planner that owns all device memory,
 plugins handed only their tensors, hot paths that must not risk cudaMalloc's
-synchronisation -- cannot pass smqa_bwd a workspace.  This file is collected
+synchronisation -- cannot pass smqa_fwd / smqa_bwd a workspace.  This file is collected
 last so that a run stopping at the first failure has run everything else.
 """
 import ctypes
@@ -71,3 +72,29 @@ def test_static_scratch_matches_workspace_backward_twice(fp32_dkv):
         assert torch.equal(dq, dq_ref)  # dq has no atomics: identical
         e = P.rel_err(dkv, dkv_ref.double().cpu().numpy())
         assert e <= P.TOL["dkv"], f"dkv differs from the workspace backward: {e:.3e}"
+
+
+@pytest.mark.gpu
+def test_static_scratch_forward_matches_workspace_forward_twice():
+    lib = _lib.load()
+    x = inputs.custom(2, 96, 512, 128, 512, 200, recipe="causal_masked10", seed=22)
+    g = P.to_dev(x)
+    B, S, H, D = g["q"].shape
+    S_kv, K = g["kv"].shape[1], g["topk_idxs"].shape[2]
+    shp = _lib.Shape(B, S, S_kv, H, D, K)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    args = [_p(g["q"]), _p(g["kv"]), _p(g["attn_sink"]), _p(g["topk_idxs"])]
+    ws = torch.empty(lib.smqa_fwd_workspace_bytes(shp), dtype=torch.uint8, device="cuda")
+    o_ref = torch.empty_like(g["q"])
+    lse_ref = torch.empty((B, S, H), dtype=torch.float32, device="cuda")
+    _lib.check("smqa_fwd", lib.smqa_fwd(*args, shp, 0.0, _p(o_ref), _p(lse_ref), _p(ws),
+                                        ws.numel(), 0, stream))
+    torch.cuda.synchronize()
+    for _ in range(2):
+        o = torch.full_like(g["q"], float("nan"))
+        lse = torch.full((B, S, H), float("nan"), device="cuda")
+        _lib.check("smqa_fwd_static_scratch",
+                   lib.smqa_fwd_static_scratch(*args, shp, 0.0, _p(o), _p(lse), 0, stream))
+        torch.cuda.synchronize()
+        assert lib.smqa_device_status(1) == 0
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
