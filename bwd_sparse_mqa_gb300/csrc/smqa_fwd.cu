@@ -15,34 +15,39 @@
 //     [256r, 256r+256) of Q, of every gathered kv row and of O (its O
 //     accumulator, 128 x 256 fp32, is half of TMEM).  Per block it computes
 //     the partial scores over its half, S_r = Q_r.K_r^T, and the pair trades
-//     them: each CTA scales its fp32 partial into the exp2 domain and writes
-//     it into the peer's receive buffer in an L2-resident exchange slot, and
-//     both CTAs form S = S_0 + S_1 from the same two fp32 values (so the
-//     pair's probabilities and LSE are bit-identical).  fp16 partials would
-//     halve the exchange but put up to ~2^-8 of a score's magnitude into a
-//     single-slot LSE.  Each CTA then runs the same online softmax and
-//     accumulates O_r += P.V_r.  The exchange slot (two receivers x four
-//     block buffers x 32 KB) is claimed from a pool by the pair's rank 0 and
-//     released at exit.
+//     them through an L2-resident exchange slot: each CTA scales its partial
+//     into the exp2 domain and sends it in block floating point (per head
+//     and block one power-of-two scale and 64 int16 mantissas, so the
+//     rounding error is below 2^-15 of the head's largest partial in the
+//     block: 16.5 KB per block instead of 32 KB of fp32, where fp16 would put
+//     up to ~2^-8 of a score's magnitude into a single-slot LSE).  Both CTAs
+//     form S = own + peer's from the same two rounded values, so the pair's
+//     probabilities and LSE are bit-identical.  Each CTA then runs the same
+//     online softmax and accumulates O_r += P.V_r.  The exchange slot (two
+//     receivers x four block buffers) is claimed from a pool by the pair's
+//     rank 0 and released at exit.
 //   * Exchange flow control without a consumed-signal: a CTA frees score
-//     tile i % 3 only after its softmax has read the peer's partial of block
-//     i, and it computes (and sends) block i + 3 only into a freed tile, so
-//     the arrival of the peer's block j + 3 proves that the peer has read
-//     block j; a sender writes block j + 4 into the buffer of block j only
-//     after its own CTA has received block j + 3.
+//     tile i % 3 only after its softmax has read the full scores of block i
+//     (formed after the peer's partial of block i was read), and it computes
+//     (and sends) block i + 3 only into a freed tile, so the arrival of the
+//     peer's block j + 3 proves that the peer has read block j; block j + 4
+//     goes into the buffer of block j only after its own CTA has received
+//     block j + 3.
 //   * D = 64: one CTA per token, no exchange.
-//   * Warp roles: warps 8-10 gather this CTA's half of the kv rows with
+//   * Warp roles (D = 512; for D = 64 the combiner and sender warps are
+//     absent): warps 8-10 gather this CTA's half of the kv rows with
 //     16-byte cp.async (coalesced 512-byte row pieces written into the
 //     128-byte-swizzled K-major tile; completion signalled per block by
-//     cp.async mbarrier arrivals) into a four-stage ring; warp 11 owns TMEM
-//     and issues the MMAs from one thread (scores into a ring of three
-//     64-column TMEM tiles; P.V with P, bf16, from a two-buffer ring in TMEM
-//     as the A operand); warps 12-15 (D = 512) read each score
-//     tile and send it to the peer; warps 0-7 (two warpgroups; thread = head
-//     row = TMEM lane, 32 score columns each) add the peer's partial, run the
-//     masked online softmax in the exp2 domain, rescale O lazily (only when
-//     the running max grows by more than 2^8), write P as bf16 into TMEM for
-//     the P.V MMA and finish with the sink and the log2 LSE.
+//     cp.async mbarrier arrivals) into a four-stage ring, and publish each
+//     block's valid-slot mask; warp 11 owns TMEM and issues the MMAs from
+//     one thread (partial scores into a ring of three 64-column TMEM tiles;
+//     P.V with P, bf16, from a two-buffer ring in TMEM as the A operand);
+//     warps 12-15 send each partial tile to the peer; warps 4-7 write the
+//     full scores (own + peer's) back into the tile; warps 0-3 (thread =
+//     head row = TMEM lane) run the masked online softmax in the exp2
+//     domain, rescale O lazily (only when the running max grows by more than
+//     2^8), write P as bf16 into TMEM for the P.V MMA and finish with the
+//     sink and the log2 LSE.
 //   * Masked slots load a real (finite) row and get a -inf score, so their
 //     probability is exactly 0; blocks past a token's last valid slot are
 //     skipped.
@@ -68,22 +73,27 @@ struct FwdLayout {
   static constexpr uint32_t kStageBytes = kChunks * kKvChunkBytes;
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffKv = kOffQ + kQBytes;
+  // Exchange buffer of one receiver and block: each head's 64 partial scores
+  // as int16 with one power-of-two scale (block floating point), in 8 pieces
+  // of 16 bytes per head, piece-major (a warp's 32 heads are 512 contiguous
+  // bytes), then the 128 heads' dequantization factors (fp32).
+  static constexpr int kPieces = 8;
+  static constexpr uint32_t kXchgScaleOff = kPieces * 16u * kHPad;
+  static constexpr uint32_t kXchgBytes = kXchgScaleOff + 4u * kHPad;
   static constexpr uint32_t kOffCtrl = kOffKv + kStages * kStageBytes;
   static constexpr int kBarKvFull = 0;                       // [kStages]
   static constexpr int kBarKvEmpty = kBarKvFull + kStages;   // [kStages]
-  static constexpr int kBarSFull = kBarKvEmpty + kStages;    // [kSBufs] scores of a block ready
-  static constexpr int kBarSFree = kBarSFull + kSBufs;       // [kSBufs] ... read by every reader
+  static constexpr int kBarSFull = kBarKvEmpty + kStages;    // [kSBufs] partial scores ready
+  static constexpr int kBarSRead = kBarSFull + kSBufs;       // [kSBufs] ... read by the sender
+  static constexpr int kBarSSum = kBarSRead + kSBufs;        // [kSBufs] full scores in the tile
+  static constexpr int kBarSFree = kBarSSum + kSBufs;        // [kSBufs] tile read by the softmax
   static constexpr int kBarRecvFull = kBarSFree + kSBufs;    // [kXBufs] peer's partial arrived
   static constexpr int kBarPFull = kBarRecvFull + kXBufs;    // [2] P of block i in buffer i % 2
   static constexpr int kBarODone = kBarPFull + 2;            // [2] P.V of block i done
   static constexpr int kBarQFull = kBarODone + 2;
   static constexpr int kBarDrain = kBarQFull + 1;
-  static constexpr int kBarXmax = kBarDrain + 1;     // [2], by block parity
-  static constexpr int kBarLsum = kBarXmax + 2;
-  static constexpr int kNumBars = kBarLsum + 1;
-  static constexpr uint32_t kOffXmax = kOffCtrl + 8 * kNumBars;    // float [2][2][128]
-  static constexpr uint32_t kOffLsum = kOffXmax + 2 * 2 * 128 * 4; // float [2][128]
-  static constexpr uint32_t kOffTmemHolder = kOffLsum + 2 * 128 * 4;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr uint32_t kOffTmemHolder = kOffCtrl + 8 * kNumBars;
   static constexpr uint32_t kOffAbort = kOffTmemHolder + 4;
   static constexpr uint32_t kOffSlot = kOffAbort + 4;
   static constexpr uint32_t kOffWarpLast = kOffSlot + 4;  // int [16]
@@ -100,24 +110,18 @@ struct FwdLayout {
   static constexpr uint32_t kTmemUsed = kTmemP + kBI;
   static constexpr uint32_t kTmemCols = kTmemUsed <= 256 ? 256 : 512;
   static_assert(kTmemUsed <= 512, "TMEM budget");
-  // warps 0-7: softmax; 8-10: gather; 11: TMEM owner + MMA issuer; 12-15
-  // (D split across the pair only): send this CTA's partial scores.  (Three
-  // gather warps: the copies a warp keeps in flight bound its gather rate.)
-  static constexpr int kSoftmaxThreads = 256;
-  static constexpr int kGatherWarp0 = 8;
+  // warps 0-3: softmax; 4-7 (D split across the pair only): add the peer's
+  // partial scores; then three gather warps, the TMEM owner + MMA issuer and
+  // (D split only) four warps that send this CTA's partial scores.  (Three
+  // gather warps, since the copies a warp keeps in flight bound its gather
+  // rate.)
+  static constexpr int kSoftmaxThreads = 128;
+  static constexpr int kCombWarp0 = 4;
+  static constexpr int kGatherWarp0 = kCombWarp0 + (NSPLIT == 2 ? 4 : 0);
   static constexpr int kGatherWarps = 3;
   static constexpr int kMmaWarp = kGatherWarp0 + kGatherWarps;
-  static constexpr int kSenderWarp0 = kMmaWarp + 1;
-  static constexpr int kThreads = NSPLIT == 2 ? 512 : 384;
-  // Readers of a score tile: the softmax threads and (D split) the senders;
-  // with the D split a softmax thread frees the tile only once it has also
-  // read the peer's partial of the block.
-  static constexpr int kSReaders = NSPLIT == 2 ? 384 : 256;
-  // Exchange buffer of one receiver and block: 16 pieces of 16 bytes per
-  // head (4 slots of fp32 each), piece-major, so a warp's 32 heads are 512
-  // contiguous bytes.
-  static constexpr int kPieces = 16;
-  static constexpr uint32_t kXchgBytes = kPieces * 16u * kHPad;
+  static constexpr int kSendWarp0 = kMmaWarp + 1;
+  static constexpr int kThreads = (kSendWarp0 + (NSPLIT == 2 ? 4 : 0)) * 32;
   static_assert(2 * kXBufs * kXchgBytes == kFwdSlotBytes, "exchange slot size");
 };
 
@@ -146,8 +150,49 @@ __device__ __forceinline__ void gather_block(uint32_t stage, const __nv_bfloat16
   }
 }
 
+// Block floating point of one head's 64 partial scores of a block, in the
+// exp2 domain (v = s1 x, x the raw partial, s1 the softmax scale): exponent
+// e = floor(log2(s1 max|x|)) (clamped to [-100, 100]); each value becomes
+// the integer n = rint(x * (s1 2^(14-e))) in [-32768, 32767] and stands for
+// n 2^(e-14).  n is stored offset by 32768 as an unsigned 16-bit field.
+// One fused multiply-add rounds: x * f + kRoundBias, with
+// kRoundBias = 1.5 * 2^23 + 32768, is exactly rounded to an integer whose
+// low 16 bits are n + 32768; the field is unpacked by placing it under the
+// exponent of 2^23.  Every step is exact or one IEEE rounding (explicit _rn
+// intrinsics), so the sender and the peer get the same value.
+constexpr float kRoundBias = 12615680.f;        // 1.5 * 2^23 + 32768
+constexpr float kRoundMax = 12615680.f + 32767.f;
+constexpr float kUnpackBias = 8421376.f;         // 2^23 + 32768
+
+__device__ __forceinline__ int bfp16_exponent(float vmax_abs) {
+  const int e = static_cast<int>((__float_as_uint(vmax_abs) >> 23) & 0xffu) - 127;
+  return min(max(e, -100), 100);
+}
+// 2^k as a float (k within the normal range).
+__device__ __forceinline__ float pow2f(int k) {
+  return __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+}
+// kRoundBias + n for the raw partial x (f = s1 2^(14-e)).
+__device__ __forceinline__ float bfp16_round(float x, float f) {
+  return fminf(__fmaf_rn(x, f, kRoundBias), kRoundMax);
+}
+// The value n 2^(e-14) of a rounded kRoundBias + n (inv = 2^(e-14)).
+__device__ __forceinline__ float bfp16_value(float r, float inv) {
+  return __fmaf_rn(r, inv, -kRoundBias * inv);
+}
+// Two rounded values -> two 16-bit fields (the first in the low half).
+__device__ __forceinline__ uint32_t bfp16_pack(float r_lo, float r_hi) {
+  return __byte_perm(__float_as_uint(r_lo), __float_as_uint(r_hi), 0x5410);
+}
+// A packed pair -> the two values it stands for.
+__device__ __forceinline__ float2 bfp16_unpack(uint32_t w, float inv) {
+  const float lo = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7610));
+  const float hi = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7632));
+  return make_float2(__fmaf_rn(lo, inv, -kUnpackBias * inv), __fmaf_rn(hi, inv, -kUnpackBias * inv));
+}
+
 template <int D, int NSPLIT>
-__global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 384, 1)
+__global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
     smqa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const FwdParams p) {
   using L = FwdLayout<D, NSPLIT>;
   constexpr int DC = L::kDC;
@@ -164,8 +209,6 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 384, 1)
   const int b = t / p.S;
   const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
   auto bar = [&](int i) -> uint32_t { return base + L::kOffCtrl + 8u * static_cast<uint32_t>(i); };
-  volatile float* xmax = reinterpret_cast<volatile float*>(smem + L::kOffXmax);
-  volatile float* lsum = reinterpret_cast<volatile float*>(smem + L::kOffLsum);
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(smem + L::kOffTmemHolder);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
   volatile int* slot_smem = reinterpret_cast<volatile int*>(smem + L::kOffSlot);
@@ -181,7 +224,9 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 384, 1)
     }
     for (int s = 0; s < L::kSBufs; ++s) {
       mbar_init(bar(L::kBarSFull + s), 1);
-      mbar_init(bar(L::kBarSFree + s), L::kSReaders);
+      mbar_init(bar(L::kBarSRead + s), 128);
+      mbar_init(bar(L::kBarSSum + s), 128);
+      mbar_init(bar(L::kBarSFree + s), L::kSoftmaxThreads);
     }
     // Exchange: the peer's four sender warps each signal a filled buffer.
     for (int s = 0; s < L::kXBufs; ++s) mbar_init(bar(L::kBarRecvFull + s), 4);
@@ -191,9 +236,6 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 384, 1)
     }
     mbar_init(bar(L::kBarQFull), 1);
     mbar_init(bar(L::kBarDrain), 1);
-    mbar_init(bar(L::kBarXmax), L::kSoftmaxThreads);
-    mbar_init(bar(L::kBarXmax + 1), L::kSoftmaxThreads);
-    mbar_init(bar(L::kBarLsum), L::kSoftmaxThreads);
     *abort_flag = *reinterpret_cast<volatile int*>(p.status) != 0 ? 1 : 0;
     *slot_smem = -1;
     if (NSPLIT == 2 && rank == 0 && *abort_flag == 0) {
@@ -328,7 +370,7 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 384, 1)
       // Event loop (non-blocking tests, so that waiting on one kind of work
       // never delays the other), oldest work first: P.V of block npv once
       // its P is written; scores of block ns once its kv rows have landed
-      // and its score tile has been read by every reader (block ns - kSBufs).
+      // and its score tile has been read by the softmax (block ns - kSBufs).
       bool ok = run && mbar_wait(bar(L::kBarQFull), 0, ctl);
       int ns = 0, npv = 0;
       PollState ps = poll_start();
@@ -362,143 +404,196 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 384, 1)
       mbar_wait_drain(bar(L::kBarDrain), 0);
     }
     __syncwarp();
-  } else if (NSPLIT == 2 && warp >= L::kSenderWarp0) {
+  } else if (NSPLIT == 2 && warp >= L::kSendWarp0) {
     // ------------------------------------------------------------ sender
-    // Thread = head row h: this CTA's partial scores of each block, scaled
-    // into the exp2 domain, into the peer's receive buffer of the block (L2),
-    // then one release-arrive per warp on the peer's barrier.
+    // Thread = head row h: this CTA's partial scores of each block, in block
+    // floating point, into the peer's receive buffer of the block (L2), then
+    // one release-arrive per warp on the peer's barrier; the tile gets the
+    // values the peer will see, for the combiner.
     const int sq = warp & 3;  // TMEM lane quarter
     const int h = sq * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(sq * 32) << 16;
     const float s1 = p.ref_round ? p.scale : p.scale_log2;
     const uint32_t peer_full = mapa_shared(bar(L::kBarRecvFull), rank ^ 1u);
-    uint4* dst0 = reinterpret_cast<uint4*>(
-                      p.exch + (static_cast<size_t>(slot) * 2 + (rank ^ 1u)) *
-                                   (L::kXBufs * L::kXchgBytes)) + h;
+    uint8_t* peer0 = p.exch + (static_cast<size_t>(slot) * 2 + (rank ^ 1u)) *
+                                  (L::kXBufs * L::kXchgBytes);
     for (int i = 0; run && i < nblk; ++i) {
       const int sb = i % L::kSBufs;
+      const int xb = i % L::kXBufs;
       bool ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + sb), (i / L::kSBufs) & 1, ctl));
       if (!ok) break;
       tc_fence_after();
-      float x0[32], x1[32];
-      tmem_ld32x2(tmem + lane_base + L::kTmemS + sb * L::kBI,
-                  tmem + lane_base + L::kTmemS + sb * L::kBI + 32, x0, x1);
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarSFree + sb));
+      const uint32_t tile = tmem + lane_base + L::kTmemS + sb * L::kBI;
+      float x[64];
+      tmem_ld32x2(tile, tile + 32, *reinterpret_cast<float(*)[32]>(x),
+                  *reinterpret_cast<float(*)[32]>(x + 32));
+      float mx = 0.f;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        x0[j] *= s1;
-        x1[j] *= s1;
+      for (int j = 0; j < 64; ++j) mx = fmaxf(mx, fabsf(x[j]));
+      const int ex = bfp16_exponent(__fmul_rn(mx, s1));
+      const float f = __fmul_rn(s1, pow2f(14 - ex)), inv = pow2f(ex - 14);
+      uint32_t w[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float r0 = bfp16_round(x[2 * k], f), r1 = bfp16_round(x[2 * k + 1], f);
+        w[k] = bfp16_pack(r0, r1);
+        x[2 * k] = bfp16_value(r0, inv);
+        x[2 * k + 1] = bfp16_value(r1, inv);
       }
+      // The tile now holds this CTA's partial as the peer will see it.
+      tmem_st32(tile, *reinterpret_cast<float(*)[32]>(x));
+      tmem_st32(tile + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarSRead + sb));
       // The peer has read block i - kXBufs from this buffer once its block
       // i - 1 has arrived here (it computed that block into the score tile
       // it freed after reading block i - kXBufs).
-      const int xb = i % L::kXBufs;
       if (i >= L::kXBufs) {
         const int j = i - 1;
         ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull + j % L::kXBufs),
                                                      (j / L::kXBufs) & 1, ctl));
         if (!ok) break;
       }
-      float4* dst = reinterpret_cast<float4*>(dst0 + xb * (L::kXchgBytes / 16));
+      uint8_t* buf = peer0 + static_cast<size_t>(xb) * L::kXchgBytes;
+      uint4* dst = reinterpret_cast<uint4*>(buf) + h;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        dst[j * L::kHPad] = make_float4(x0[4 * j], x0[4 * j + 1], x0[4 * j + 2], x0[4 * j + 3]);
-        dst[(8 + j) * L::kHPad] =
-            make_float4(x1[4 * j], x1[4 * j + 1], x1[4 * j + 2], x1[4 * j + 3]);
-      }
+      for (int c = 0; c < L::kPieces; ++c)
+        dst[c * L::kHPad] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+      reinterpret_cast<int*>(buf + L::kXchgScaleOff)[h] = ex;
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(peer_full + 8u * static_cast<uint32_t>(xb));
     }
-  } else if (warp < L::kGatherWarp0) {
+  } else if (NSPLIT == 2 && warp >= L::kCombWarp0 && warp < L::kGatherWarp0) {
+    // ------------------------------------------------------------ combiner
+    // Thread = head row h: once the peer's partial of block i has arrived
+    // and the sender has rounded this CTA's partial in the tile, the tile
+    // gets the full scores S = own + peer's, both as the block-floating-point
+    // values that were exchanged, so both CTAs add the same two fp32 terms.
+    // The peer's row is loaded first so that its L2 latency overlaps the
+    // wait for the sender.
+    const int sq = warp & 3;  // TMEM lane quarter
+    const int h = sq * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(sq * 32) << 16;
+    const uint8_t* recv0 = p.exch + (static_cast<size_t>(slot) * 2 + rank) *
+                                        (L::kXBufs * L::kXchgBytes);
+    for (int i = 0; run && i < nblk; ++i) {
+      const int sb = i % L::kSBufs;
+      const int xb = i % L::kXBufs;
+      bool ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull + xb),
+                                                        (i / L::kXBufs) & 1, ctl));
+      if (!ok) break;
+      const uint8_t* buf = recv0 + static_cast<size_t>(xb) * L::kXchgBytes;
+      const uint4* src = reinterpret_cast<const uint4*>(buf) + h;
+      uint4 y[L::kPieces];
+#pragma unroll
+      for (int c = 0; c < L::kPieces; ++c) y[c] = __ldcg(src + c * L::kHPad);
+      const float pinv = pow2f(__ldcg(reinterpret_cast<const int*>(buf + L::kXchgScaleOff) + h) - 14);
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSRead + sb), (i / L::kSBufs) & 1, ctl));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tile = tmem + lane_base + L::kTmemS + sb * L::kBI;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float x[32];
+        tmem_ld32(tile + 32 * half, x);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 yc = y[4 * half + c];
+          const uint32_t ya[4] = {yc.x, yc.y, yc.z, yc.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 pv = bfp16_unpack(ya[k], pinv);
+            const int j = 8 * c + 2 * k;
+            x[j] = __fadd_rn(x[j], pv.x);
+            x[j + 1] = __fadd_rn(x[j + 1], pv.y);
+          }
+        }
+        tmem_st32(tile + 32 * half, x);
+      }
+      // The peer's values are consumed (see the flow-control note above).
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarSSum + sb));
+    }
+  } else if (warp < L::kSoftmaxThreads / 32) {
     // ------------------------------------------------------------ softmax
-    // Thread (h, g): head row h (TMEM lane), score columns [32g, 32g+32) of
-    // every block, O columns [DC/2 g, DC/2 (g+1)) for rescaling and output.
-    const int g = warp >> 2;
-    const int h = threadIdx.x & 127;
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    // Thread = head row h (TMEM lane): all 64 score columns of every block,
+    // the whole O row for rescaling and output.
+    const int h = threadIdx.x;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     // exp2 argument: score * (c log2 e), or (score * c) * log2 e with the
     // reference-rounding flag (x * s1 * 1 is exact when the flag is off).
-    const float s1 = p.ref_round ? p.scale : p.scale_log2;
+    // With the D split the tile already holds s1 * score.
+    const float s1 = NSPLIT == 2 ? 1.f : (p.ref_round ? p.scale : p.scale_log2);
     const float s2 = p.ref_round ? 1.4426950408889634f : 1.f;
-    constexpr int kOHalf = DC / 2;
-    const uint4* src0 = NSPLIT == 2
-                            ? reinterpret_cast<const uint4*>(
-                                  p.exch + (static_cast<size_t>(slot) * 2 + rank) *
-                                               (L::kXBufs * L::kXchgBytes)) + 8 * g * L::kHPad + h
-                            : nullptr;
     float m_run = -INFINITY;
-    float l_part = 0.f;
+    float l_run = 0.f;
     bool ok = run;
     for (int i = 0; ok && i < nblk; ++i) {
       const int sb = i % L::kSBufs;
-      const int bb = i & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + sb), (i / L::kSBufs) & 1, ctl));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar((NSPLIT == 2 ? L::kBarSSum : L::kBarSFull) + sb),
+                                             (i / L::kSBufs) & 1, ctl));
       if (!ok) break;
       tc_fence_after();
       // The scores imply that the block's kv stage (and its valid-slot mask)
       // has landed; its full barrier is tested only to order the mask read.
-      // Column j of this thread is valid iff bit j of msk is set.
       const int st = i % L::kStages;
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarKvFull + st), (i / L::kStages) & 1, ctl));
       if (!ok) break;
-      const uint32_t msk = vmask[2 * st + g];
-      float x[32];
-      tmem_ld32(tmem + lane_base + L::kTmemS + sb * L::kBI + 32 * g, x);
-      if constexpr (NSPLIT == 2) {
-        // S = own partial + peer's partial, each scaled exactly as the
-        // sender scales this CTA's partial for the peer.
+      const uint32_t msk0 = vmask[2 * st];
+      const uint32_t msk1 = vmask[2 * st + 1];
+      float x[64];
+      tmem_ld32x2(tmem + lane_base + L::kTmemS + sb * L::kBI,
+                  tmem + lane_base + L::kTmemS + sb * L::kBI + 32,
+                  *reinterpret_cast<float(*)[32]>(x), *reinterpret_cast<float(*)[32]>(x + 32));
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarSFree + sb));
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] *= s1;
-        const int xb = i % L::kXBufs;
-        ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull + xb),
-                                                     (i / L::kXBufs) & 1, ctl));
-        if (!ok) break;
-        const float4* src = reinterpret_cast<const float4*>(src0 + xb * (L::kXchgBytes / 16));
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float4 y = __ldcg(src + c * L::kHPad);
-          x[4 * c] += y.x;
-          x[4 * c + 1] += y.y;
-          x[4 * c + 2] += y.z;
-          x[4 * c + 3] += y.w;
-        }
-        // The values are in registers: the score tile may be reused (which
-        // is what tells the peer that this buffer has been read).
-        tc_fence_before();
-        mbar_arrive(bar(L::kBarSFree + sb));
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = ((msk >> j) & 1u) ? x[j] * s2 : -INFINITY;
-      } else {
-        tc_fence_before();
-        mbar_arrive(bar(L::kBarSFree + sb));
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = ((msk >> j) & 1u) ? (x[j] * s1) * s2 : -INFINITY;
+      for (int j = 0; j < 64; ++j) {
+        const uint32_t bit = ((j < 32 ? msk0 : msk1) >> (j & 31)) & 1u;
+        x[j] = bit ? (x[j] * s1) * s2 : -INFINITY;
       }
       float mq[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        mq[j] = fmaxf(fmaxf(x[4 * j], x[4 * j + 1]), fmaxf(x[4 * j + 2], x[4 * j + 3]));
+        mq[j] = fmaxf(fmaxf(fmaxf(x[8 * j], x[8 * j + 1]), fmaxf(x[8 * j + 2], x[8 * j + 3])),
+                      fmaxf(fmaxf(x[8 * j + 4], x[8 * j + 5]), fmaxf(x[8 * j + 6], x[8 * j + 7])));
       const float mloc = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])),
                                fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
-      // Combine with the other half of the row (the thread of the other
-      // warpgroup with the same h); buffers alternate by block parity.
-      xmax[(bb * 2 + g) * 128 + h] = mloc;
-      mbar_arrive(bar(L::kBarXmax + bb));
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarXmax + bb), (i >> 1) & 1, ctl));
-      if (!ok) break;
-      const float mx = fmaxf(mloc, xmax[(bb * 2 + (g ^ 1)) * 128 + h]);
-      const float m_new = fmaxf(m_run, mx);
+      const float m_new = fmaxf(m_run, mloc);
       const bool bump = (m_run == -INFINITY) ? (m_new != -INFINITY) : (m_new > m_run + 8.f);
       float alpha = 1.f;
       if (bump) {
         alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_new);
-        l_part *= alpha;
+        l_run *= alpha;
         m_run = m_new;
       }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      // P buffer i % 2 was last read by P.V of block i-2.
+      if (i >= 2) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(bar(L::kBarODone + (i & 1)), ((i - 2) >> 1) & 1, ctl));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int w = 0; w < 16; ++w) {
+          const float p0 = fast_exp2(x[32 * half + 2 * w] - m_use);
+          const float p1 = fast_exp2(x[32 * half + 2 * w + 1] - m_use);
+          pk[w] = pack_bf16x2(p0, p1);
+          rs[w & 3] += p0 + p1;  // fp32 probabilities: the LSE must not carry bf16 rounding
+        }
+        tmem_st16u(tmem + lane_base + L::kTmemP + static_cast<uint32_t>(i & 1) * (L::kBI / 2) +
+                       16 * half, pk);
+      }
+      l_run += (rs[0] + rs[1]) + (rs[2] + rs[3]);
       // O was accumulated against the old max: once P.V of block i-1 has
-      // completed, rescale this thread's half of the row (whole warp, since
-      // TMEM accesses are warp-collective; rows without a bump use 1).
+      // completed, rescale this row before P.V of block i may start (whole
+      // warp, since TMEM accesses are warp-collective; rows without a bump
+      // use 1).
       const bool need_rescale = bump && alpha != 0.f && i > 0;
       if (__any_sync(0xffffffffu, need_rescale)) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + ((i - 1) & 1)),
@@ -507,46 +602,21 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 384, 1)
         tc_fence_after();
         const float a = need_rescale ? alpha : 1.f;
 #pragma unroll 1
-        for (int c = 0; c < kOHalf / 32; ++c) {
+        for (int c = 0; c < DC / 32; ++c) {
           float v[32];
-          tmem_ld32(tmem + lane_base + L::kTmemO + g * kOHalf + c * 32, v);
+          tmem_ld32(tmem + lane_base + L::kTmemO + c * 32, v);
 #pragma unroll
           for (int k = 0; k < 32; ++k) v[k] *= a;
-          tmem_st32(tmem + lane_base + L::kTmemO + g * kOHalf + c * 32, v);
+          tmem_st32(tmem + lane_base + L::kTmemO + c * 32, v);
         }
       }
-      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      uint32_t pk[16];
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int w = 0; w < 16; ++w) {
-        const float p0 = fast_exp2(x[2 * w] - m_use);
-        const float p1 = fast_exp2(x[2 * w + 1] - m_use);
-        pk[w] = pack_bf16x2(p0, p1);
-        rs[w & 3] += p0 + p1;  // fp32 probabilities: the LSE must not carry bf16 rounding
-      }
-      l_part += (rs[0] + rs[1]) + (rs[2] + rs[3]);
-      // P buffer i % 2 was last read by P.V of block i-2.
-      if (i >= 2) {
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(bar(L::kBarODone + (i & 1)), ((i - 2) >> 1) & 1, ctl));
-        if (!ok) break;
-        tc_fence_after();
-      }
-      tmem_st16u(tmem + lane_base + L::kTmemP + static_cast<uint32_t>(i & 1) * (L::kBI / 2) +
-                     16 * g, pk);
       tc_fence_before();
       mbar_arrive(bar(L::kBarPFull + (i & 1)));
     }
     if (ok && nblk > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + ((nblk - 1) & 1)),
                                              ((nblk - 1) >> 1) & 1, ctl));
-    // Row sums: the two halves of each row meet here.
-    lsum[g * 128 + h] = l_part;
-    mbar_arrive(bar(L::kBarLsum));
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarLsum), 0, ctl));
     if (ok) {
-      const float l_run = lsum[h] + lsum[128 + h];
       tc_fence_after();
       const float sink2 = h < p.H ? __ldg(p.sink + h) * 1.4426950408889634f : 0.f;
       const float m_fin = fmaxf(m_run, sink2);
@@ -554,11 +624,11 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 384, 1)
       const float Z = l_run * so + fast_exp2(sink2 - m_fin);
       const float inv = so / Z;
       __nv_bfloat16* orow = p.o + (static_cast<size_t>(t) * p.H + h) * D +
-                            static_cast<size_t>(rank) * DC + g * kOHalf;
+                            static_cast<size_t>(rank) * DC;
 #pragma unroll 1
-      for (int c = 0; c < kOHalf / 32; ++c) {
+      for (int c = 0; c < DC / 32; ++c) {
         float v[32];
-        tmem_ld32(tmem + lane_base + L::kTmemO + g * kOHalf + c * 32, v);
+        tmem_ld32(tmem + lane_base + L::kTmemO + c * 32, v);
         if (nblk == 0) {  // no valid slot: O was never written, the output is 0
 #pragma unroll
           for (int k = 0; k < 32; ++k) v[k] = 0.f;
@@ -573,8 +643,7 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 384, 1)
             dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
         }
       }
-      if (rank == 0 && g == 0 && h < p.H)
-        p.lse[static_cast<size_t>(t) * p.H + h] = m_fin + log2f(Z);
+      if (rank == 0 && h < p.H) p.lse[static_cast<size_t>(t) * p.H + h] = m_fin + log2f(Z);
     }
   }
 

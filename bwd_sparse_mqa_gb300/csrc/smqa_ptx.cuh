@@ -84,6 +84,20 @@ __device__ __forceinline__ bool mbar_probe(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test with cluster-scope acquire (for phases completed by
+// arrivals from another CTA of the cluster that publish its writes).
+__device__ __forceinline__ bool mbar_probe_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -191,6 +205,12 @@ __device__ __forceinline__ int live_blocks(const volatile int* warp_last, int bl
 // Generic-proxy shared-memory writes -> later async-proxy reads (MMA / TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Orders this thread's view of global memory (generic proxy) before its
+// later async-proxy (bulk copy) accesses of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
@@ -311,6 +331,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(m), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// Contiguous bulk copy global -> shared (both 16-byte aligned, bytes a
+// multiple of 16), completing as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
 

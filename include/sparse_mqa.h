@@ -77,10 +77,10 @@ typedef struct {
 
 /*
  * Bytes of device workspace smqa_fwd needs for `shape`: 0 when D = 64; for
- * D = 512 the exchange pool (4 KB of slot flags + 96 slots of 256 KB).  For
+ * D = 512 the exchange pool (4 KB of slot flags + 96 slots of 132 KB).  For
  * D = 512 each token is handled by a pair of CTAs that own one half of D
- * each; every 64-slot block they trade their fp32 partial scores through a
- * slot of this pool (it stays in L2).  The contents need no initialisation:
+ * each; every 64-slot block they trade their partial scores through a slot
+ * of this pool (it stays in L2).  The contents need no initialisation:
  * smqa_fwd clears the slot flags on its stream.  Returns 0 for an
  * unsupported shape.
  */
@@ -105,7 +105,10 @@ size_t smqa_fwd_workspace_bytes(smqa_shape shape);
  * A token whose slots are all masked gets O = 0 and lse = sink/ln 2.
  * For D = 512 a score is the fp32 sum of two half-D partial scores, each
  * already multiplied by sm_scale*log2(e) (by sm_scale with
- * SMQA_FLAG_REFERENCE_ROUNDING, the sum then by log2(e)).
+ * SMQA_FLAG_REFERENCE_ROUNDING, the sum then by log2(e)) and rounded to
+ * block floating point: per head and 64-slot block, one power-of-two scale
+ * and int16 mantissas, so each partial carries an absolute error of at most
+ * 2^-15 of the largest partial magnitude of its head and block.
  */
 smqa_status smqa_fwd(const void* q, const void* kv, const float* attn_sink,
                      const int32_t* topk_idxs, smqa_shape shape, float sm_scale,
