@@ -54,10 +54,17 @@ def peaks():
 
 
 def kernel_source_hash() -> str:
-    h = hashlib.sha256()
-    for f in ("smqa_bwd.cu", "smqa_ptx.cuh"):
-        with open(os.path.join(ROOT, "bwd_sparse_mqa_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    """Hash of the backward main kernel's source: its layout and body in
+    smqa_bwd.cu (from `struct BwdLayout` to its launcher) and the PTX helpers
+    it includes.  Other kernels in the file do not change it."""
+    csrc = os.path.join(ROOT, "bwd_sparse_mqa_gb300", "csrc")
+    with open(os.path.join(csrc, "smqa_bwd.cu")) as fh:
+        text = fh.read()
+    start = text.index("struct BwdLayout")
+    end = text.index("static cudaError_t launch_bwd_impl", start)
+    h = hashlib.sha256(text[start:end].encode())
+    with open(os.path.join(csrc, "smqa_ptx.cuh"), "rb") as fh:
+        h.update(fh.read())
     return h.hexdigest()[:16]
 
 

@@ -3,12 +3,14 @@ sink: forward and backward as hand-written tcgen05/TMA CUDA kernels behind a
 C ABI (include/sparse_mqa.h).
 
     from bwd_sparse_mqa_gb300 import sparse_mqa_fwd_interface, sparse_mqa_bwd_interface
+    from bwd_sparse_mqa_gb300 import sparse_mqa   # autograd: grads for q, kv, attn_sink
 
 The library is loaded on first use; importing this package does not touch
 the GPU.
 """
-from .api import (bwd_workspace_bytes, device_status, sparse_mqa_bwd_interface,  # noqa: F401
+from .api import (SparseMQAFunction, bwd_workspace_bytes, device_status,  # noqa: F401
+                  fwd_workspace_bytes, sparse_mqa, sparse_mqa_bwd_interface,
                   sparse_mqa_fwd_interface)
 
-__all__ = ["sparse_mqa_fwd_interface", "sparse_mqa_bwd_interface", "bwd_workspace_bytes",
-           "device_status"]
+__all__ = ["sparse_mqa_fwd_interface", "sparse_mqa_bwd_interface", "sparse_mqa",
+           "SparseMQAFunction", "bwd_workspace_bytes", "fwd_workspace_bytes", "device_status"]

@@ -28,7 +28,7 @@ EXPORTS = [
     "smqa_fwd", "smqa_bwd_workspace_bytes", "smqa_bwd", "smqa_bwd_preprocess", "smqa_bwd_main",
     "smqa_bwd_postprocess", "smqa_device_status", "smqa_status_string", "smqa_last_error",
     "smqa_abi_version", "smqa_bwd_static_scratch", "smqa_bwd_exchange_bytes",
-    "smqa_fwd_workspace_bytes", "smqa_fwd_static_scratch",
+    "smqa_fwd_workspace_bytes", "smqa_fwd_static_scratch", "smqa_bwd_sink_grad",
 ]
 STATIC_SCRATCH_BYTES = 40 << 20
 
@@ -55,7 +55,7 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.smqa_fwd_static_scratch.restype = st
     lib.smqa_bwd_workspace_bytes.argtypes = [S, U]
     lib.smqa_bwd_workspace_bytes.restype = ctypes.c_size_t
-    lib.smqa_bwd.argtypes = [P, P, P, P, P, P, P, S, F, P, P, P, ctypes.c_size_t, U, P]
+    lib.smqa_bwd.argtypes = [P, P, P, P, P, P, P, S, F, P, P, P, P, ctypes.c_size_t, U, P]
     lib.smqa_bwd.restype = st
     lib.smqa_bwd_preprocess.argtypes = [P, P, S, P, P, P]
     lib.smqa_bwd_preprocess.restype = st
@@ -65,7 +65,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.smqa_bwd_main.restype = st
     lib.smqa_bwd_postprocess.argtypes = [P, S, P, P]
     lib.smqa_bwd_postprocess.restype = st
-    lib.smqa_bwd_static_scratch.argtypes = [P, P, P, P, P, P, P, S, F, P, P, U, P]
+    lib.smqa_bwd_static_scratch.argtypes = [P, P, P, P, P, P, P, S, F, P, P, P, U, P]
+    lib.smqa_bwd_sink_grad.argtypes = [P, P, P, S, P, P]
+    lib.smqa_bwd_sink_grad.restype = st
     lib.smqa_bwd_static_scratch.restype = st
     lib.smqa_device_status.argtypes = [ctypes.c_int]
     lib.smqa_device_status.restype = st

@@ -118,15 +118,16 @@ def sparse_mqa_bwd_interface(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch
                              o: torch.Tensor, do: torch.Tensor, topk_idxs: torch.Tensor,
                              lse: torch.Tensor, sm_scale: Optional[float] = None,
                              return_dkv_accum_dtype: bool = False,
-                             workspace: Optional[torch.Tensor] = None
-                             ) -> tuple[torch.Tensor, torch.Tensor]:
+                             workspace: Optional[torch.Tensor] = None,
+                             return_dsink: bool = False):
     """Top-k sparse MQA backward.
 
     Takes the forward's inputs, its output o, the gradient do [B,S,H,D] bf16
     and its log2 lse [B,S,H] fp32.  Returns freshly allocated dq [B,S,H,D]
-    bf16 and dkv [B,S_kv,D] (bf16, or fp32 with return_dkv_accum_dtype).
-    ``workspace`` (uint8 CUDA tensor) may be passed to reuse scratch memory
-    between calls; otherwise one is allocated.
+    bf16 and dkv [B,S_kv,D] (bf16, or fp32 with return_dkv_accum_dtype), and
+    with ``return_dsink`` also the gradient w.r.t. attn_sink (fp32 [H]; not
+    among the pages' outputs).  ``workspace`` (uint8 CUDA tensor) may be
+    passed to reuse scratch memory between calls; otherwise one is allocated.
     """
     shp = _shape(q, kv, attn_sink, topk_idxs)
     _need(o, "o", torch.bfloat16, 4)
@@ -150,15 +151,45 @@ def sparse_mqa_bwd_interface(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch
     dkv = torch.empty((shp.B, shp.S_kv, shp.D),
                       dtype=torch.float32 if return_dkv_accum_dtype else torch.bfloat16,
                       device=q.device)
+    dsink = torch.empty((shp.H,), dtype=torch.float32, device=q.device) if return_dsink else None
     with torch.cuda.device(q.device):
         _lib.check("smqa_bwd", lib.smqa_bwd(_ptr(q), _ptr(kv), _ptr(attn_sink), _ptr(o), _ptr(do),
                                             _ptr(topk_idxs), _ptr(lse), shp, scale, _ptr(dq),
-                                            _ptr(dkv), _ptr(workspace), workspace.numel(), flags,
-                                            _stream(q.device)))
-    return dq, dkv
+                                            _ptr(dkv), _ptr(dsink), _ptr(workspace),
+                                            workspace.numel(), flags, _stream(q.device)))
+    return (dq, dkv, dsink) if return_dsink else (dq, dkv)
 
 
 def device_status(clear: bool = True) -> int:
     """The device status word (0, or SMQA_ERR_DEVICE_TIMEOUT after a kernel's
     bounded wait ran out).  Synchronizes the device."""
     return int(_lib.load().smqa_device_status(1 if clear else 0))
+
+
+class SparseMQAFunction(torch.autograd.Function):
+    """Autograd around the forward and backward kernels: gradients flow from
+    O to q, kv and attn_sink (the LSE output is not differentiable)."""
+
+    @staticmethod
+    def forward(ctx, q, kv, attn_sink, topk_idxs, sm_scale=None):
+        o, lse = sparse_mqa_fwd_interface(q, kv, attn_sink, topk_idxs, sm_scale)
+        ctx.save_for_backward(q, kv, attn_sink, topk_idxs, o, lse)
+        ctx.sm_scale = sm_scale
+        ctx.mark_non_differentiable(lse)
+        return o, lse
+
+    @staticmethod
+    def backward(ctx, do, dlse):
+        q, kv, attn_sink, topk_idxs, o, lse = ctx.saved_tensors
+        dq, dkv, dsink = sparse_mqa_bwd_interface(
+            q, kv, attn_sink, o, do.to(torch.bfloat16).contiguous(), topk_idxs, lse,
+            ctx.sm_scale, return_dsink=True)
+        return dq, dkv, dsink.to(attn_sink.dtype), None, None
+
+
+def sparse_mqa(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor,
+               topk_idxs: torch.Tensor, sm_scale: Optional[float] = None
+               ) -> tuple[torch.Tensor, torch.Tensor]:
+    """Differentiable top-k sparse MQA: (O, LSE) as sparse_mqa_fwd_interface
+    returns them, with gradients w.r.t. q, kv and attn_sink through O."""
+    return SparseMQAFunction.apply(q, kv, attn_sink, topk_idxs, sm_scale)

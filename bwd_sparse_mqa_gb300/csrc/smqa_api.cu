@@ -326,6 +326,21 @@ smqa_status smqa_bwd_main(const void* q, const void* kv, const float* attn_sink,
                        effective_scale(sm_scale, shape.D), dq, dkv_accum, exchange, stream);
 }
 
+smqa_status smqa_bwd_sink_grad(const float* attn_sink, const float* lse, const float* delta,
+                               smqa_shape shape, float* dsink, cudaStream_t stream) {
+  const smqa_status sc = check_shape(shape);
+  if (sc != SMQA_OK) return sc;
+  if (!attn_sink || !lse || !delta || !dsink || !aligned(attn_sink, 4) || !aligned(lse, 4) ||
+      !aligned(delta, 4) || !aligned(dsink, 4)) {
+    std::snprintf(g_last_error, sizeof g_last_error, "null or misaligned pointer");
+    return SMQA_ERR_INVALID_ARG;
+  }
+  const cudaError_t e = smqa::launch_bwd_sink_grad(
+      attn_sink, lse, delta, dsink, static_cast<int64_t>(shape.B) * shape.S, shape.H, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "bwd sink gradient launch");
+  return SMQA_OK;
+}
+
 smqa_status smqa_bwd_postprocess(const float* dkv_accum, smqa_shape shape, void* dkv_bf16,
                                  cudaStream_t stream) {
   const smqa_status sc = check_shape(shape);
@@ -343,15 +358,16 @@ smqa_status smqa_bwd_postprocess(const float* dkv_accum, smqa_shape shape, void*
 
 smqa_status smqa_bwd(const void* q, const void* kv, const float* attn_sink, const void* o,
                      const void* dout, const int32_t* topk_idxs, const float* lse,
-                     smqa_shape shape, float sm_scale, void* dq, void* dkv, void* workspace,
-                     size_t workspace_bytes, unsigned flags, cudaStream_t stream) {
+                     smqa_shape shape, float sm_scale, void* dq, void* dkv, float* dsink,
+                     void* workspace, size_t workspace_bytes, unsigned flags,
+                     cudaStream_t stream) {
   const smqa_status sc = check_shape(shape);
   if (sc != SMQA_OK) return sc;
   if (!q || !kv || !attn_sink || !o || !dout || !topk_idxs || !lse || !dq || !dkv || !workspace ||
       (flags & ~SMQA_FLAG_RETURN_DKV_FP32) || !aligned(q, 16) || !aligned(kv, 16) ||
       !aligned(o, 16) || !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dkv, 16) ||
       !aligned(workspace, 16) || !aligned(attn_sink, 4) || !aligned(topk_idxs, 4) ||
-      !aligned(lse, 4)) {
+      !aligned(lse, 4) || !aligned(dsink, 4)) {
     std::snprintf(g_last_error, sizeof g_last_error, "null/misaligned pointer or bad flags");
     return SMQA_ERR_INVALID_ARG;
   }
@@ -369,6 +385,10 @@ smqa_status smqa_bwd(const void* q, const void* kv, const float* attn_sink, cons
                round256(static_cast<size_t>(shape.B) * shape.S * shape.H * sizeof(float));
   smqa_status r = smqa_bwd_preprocess(o, dout, shape, delta, acc, stream);
   if (r != SMQA_OK) return r;
+  if (dsink) {
+    r = smqa_bwd_sink_grad(attn_sink, lse, delta, shape, dsink, stream);
+    if (r != SMQA_OK) return r;
+  }
   r = bwd_main_impl(q, kv, dout, topk_idxs, lse, delta, shape, effective_scale(sm_scale, shape.D),
                     dq, acc, exch, stream);
   if (r != SMQA_OK) return r;

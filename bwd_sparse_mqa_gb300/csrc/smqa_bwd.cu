@@ -86,6 +86,38 @@ __global__ void __launch_bounds__(256)
 }
 
 // --------------------------------------------------------------------------
+// sink gradient: dsink[h] = -sum_t 2^(sink_h log2 e - lse2[t,h]) Delta[t,h]
+// --------------------------------------------------------------------------
+// The sink adds exp(sink_h) to row (t,h)'s denominator but no value, so
+// dO[t,h]/dsink_h = -p_sink O[t,h] with p_sink = exp(sink_h)/Z, and the loss
+// gradient is -p_sink (dO . O) = -p_sink Delta summed over tokens.  One CTA
+// per head; thread i sums tokens i, i + 256, ... and the partial sums meet
+// in a fixed order, so the result does not vary from run to run.
+__global__ void __launch_bounds__(256)
+    smqa_bwd_sink_kernel(const float* __restrict__ sink, const float* __restrict__ lse,
+                         const float* __restrict__ delta, float* __restrict__ dsink, int64_t tokens,
+                         int H) {
+  __shared__ float part[8];
+  const int h = blockIdx.x;
+  const float s2 = __ldg(sink + h) * 1.4426950408889634f;
+  float acc = 0.f;
+  for (int64_t t = threadIdx.x; t < tokens; t += 256) {
+    const int64_t r = t * H + h;
+    acc = fmaf(exp2f(s2 - __ldg(lse + r)), __ldg(delta + r), acc);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += part[w];
+    dsink[h] = -tot;
+  }
+}
+
+// --------------------------------------------------------------------------
 // main backward kernel
 // --------------------------------------------------------------------------
 template <int DC, int NC>
@@ -726,6 +758,12 @@ cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* d
   const int64_t work = rows * 32 > acc_vec4 ? rows * 32 : acc_vec4;
   smqa_bwd_pre_kernel<<<grid_for(work, 256), 256, 0, stream>>>(o, dout, delta, dkv_acc, rows, D,
                                                                acc_vec4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_sink_grad(const float* sink, const float* lse, const float* delta,
+                                float* dsink, int64_t tokens, int H, cudaStream_t stream) {
+  smqa_bwd_sink_kernel<<<H, 256, 0, stream>>>(sink, lse, delta, dsink, tokens, H);
   return cudaGetLastError();
 }
 

@@ -68,6 +68,8 @@ cudaError_t launch_bwd_main(const CUtensorMap& tm_q, const CUtensorMap& tm_do,
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* dout,
                                   float* delta, float* dkv_acc, int64_t rows, int D,
                                   int64_t acc_elems, cudaStream_t stream);
+cudaError_t launch_bwd_sink_grad(const float* sink, const float* lse, const float* delta,
+                                float* dsink, int64_t tokens, int H, cudaStream_t stream);
 cudaError_t launch_bwd_postprocess(const float* acc, __nv_bfloat16* out, int64_t elems,
                                    cudaStream_t stream);
 

@@ -53,7 +53,7 @@ extern "C" smqa_status smqa_bwd_static_scratch(const void* q, const void* kv,
                                                const float* attn_sink, const void* o,
                                                const void* dout, const int32_t* topk_idxs,
                                                const float* lse, smqa_shape shape, float sm_scale,
-                                               void* dq, void* dkv, unsigned flags,
+                                               void* dq, void* dkv, float* dsink, unsigned flags,
                                                cudaStream_t stream) {
   // Size check first: a rejected call touches no CUDA state.
   const size_t need = smqa_bwd_workspace_bytes(shape, flags);
@@ -74,8 +74,8 @@ extern "C" smqa_status smqa_bwd_static_scratch(const void* q, const void* kv,
   // The ordinary backward on that buffer; its first kernel zeroes the fp32
   // accumulator region and overwrites Delta, so no state carries over from
   // the previous call.
-  return smqa_bwd(q, kv, attn_sink, o, dout, topk_idxs, lse, shape, sm_scale, dq, dkv, scratch,
-                  static_cast<size_t>(SMQA_STATIC_SCRATCH_BYTES), flags, stream);
+  return smqa_bwd(q, kv, attn_sink, o, dout, topk_idxs, lse, shape, sm_scale, dq, dkv, dsink,
+                  scratch, static_cast<size_t>(SMQA_STATIC_SCRATCH_BYTES), flags, stream);
 }
 
 extern "C" smqa_status smqa_fwd_static_scratch(const void* q, const void* kv,

@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define SMQA_ABI_VERSION 3
+#define SMQA_ABI_VERSION 4
 
 typedef enum {
     SMQA_OK = 0,
@@ -145,13 +145,18 @@ size_t smqa_bwd_exchange_bytes(smqa_shape shape);
  *   dq        [B,S,H,D]  bf16  written
  *   dkv       [B,S_kv,D] bf16 written, or fp32 with SMQA_FLAG_RETURN_DKV_FP32;
  *                              rows no slot names are 0
+ *   dsink     [H]        fp32  gradient w.r.t. attn_sink, written; may be NULL
+ *                              (not among the pages' outputs: the sink adds
+ *                              exp(attn_sink[h]) to every row's denominator,
+ *                              so dsink[h] = -sum over tokens of
+ *                              exp(attn_sink[h] - LSE_e) * rowsum(o * dout))
  *   workspace, workspace_bytes  >= smqa_bwd_workspace_bytes(shape, flags)
  * dkv sums contributions with fp32 atomics, so its low bits may differ from
- * run to run; dq is deterministic.
+ * run to run; dq and dsink are deterministic.
  */
 smqa_status smqa_bwd(const void* q, const void* kv, const float* attn_sink, const void* o,
                      const void* dout, const int32_t* topk_idxs, const float* lse,
-                     smqa_shape shape, float sm_scale, void* dq, void* dkv,
+                     smqa_shape shape, float sm_scale, void* dq, void* dkv, float* dsink,
                      void* workspace, size_t workspace_bytes, unsigned flags,
                      cudaStream_t stream);
 
@@ -192,15 +197,17 @@ smqa_status smqa_fwd_static_scratch(const void* q, const void* kv, const float* 
 smqa_status smqa_bwd_static_scratch(const void* q, const void* kv, const float* attn_sink,
                                     const void* o, const void* dout, const int32_t* topk_idxs,
                                     const float* lse, smqa_shape shape, float sm_scale, void* dq,
-                                    void* dkv, unsigned flags, cudaStream_t stream);
+                                    void* dkv, float* dsink, unsigned flags, cudaStream_t stream);
 
 /*
- * The three backward stages one at a time (same arguments as smqa_bwd; used
+ * The backward stages one at a time (same arguments as smqa_bwd; used
  * to time and profile them separately).
  *   preprocess  : delta[B,S,H] = rowsum(o * dout) in fp32, and dkv_accum
  *                 [B,S_kv,D] fp32 set to zero
  *   main        : dq, and dkv_accum += every slot's dKV contribution
  *   postprocess : dkv_bf16 = round-to-nearest-even(dkv_accum)
+ *   sink_grad   : dsink[H] from attn_sink, the forward's lse and the
+ *                 preprocess's delta (the optional output of smqa_bwd)
  * smqa_bwd_main also takes the exchange pool: a 256-byte-aligned device
  * buffer of at least smqa_bwd_exchange_bytes(shape) bytes (may be NULL with
  * size 0 when that is 0); a smaller pool is rejected with
@@ -215,6 +222,8 @@ smqa_status smqa_bwd_main(const void* q, const void* kv, const float* attn_sink,
                           cudaStream_t stream);
 smqa_status smqa_bwd_postprocess(const float* dkv_accum, smqa_shape shape, void* dkv_bf16,
                                  cudaStream_t stream);
+smqa_status smqa_bwd_sink_grad(const float* attn_sink, const float* lse, const float* delta,
+                               smqa_shape shape, float* dsink, cudaStream_t stream);
 
 /*
  * Reads the device status word that kernels set when a bounded wait runs out

@@ -1,7 +1,7 @@
 """Shared helpers for the GPU-vs-oracle parity tests.
 
 Tolerances (stated for this op, applied per tensor): max |gpu - ref| <=
-2e-2 * max |ref| for O, dQ and dKV, and <= 1e-4 * max |ref| for the log2 LSE,
+2e-2 * max |ref| for O, dQ, dKV and dsink, and <= 1e-4 * max |ref| for the log2 LSE,
 where ref is the fp64 oracle on the same bf16 inputs.
 """
 from __future__ import annotations
@@ -13,7 +13,7 @@ import oracle
 from bwd_sparse_mqa_gb300 import sparse_mqa_bwd_interface, sparse_mqa_fwd_interface
 from bwd_sparse_mqa_gb300.api import device_status
 
-TOL = {"o": 2e-2, "dq": 2e-2, "dkv": 2e-2, "lse": 1e-4}
+TOL = {"o": 2e-2, "dq": 2e-2, "dkv": 2e-2, "dsink": 2e-2, "lse": 1e-4}
 
 
 def rel_err(gpu, ref) -> float:
@@ -57,11 +57,11 @@ def run_fwd(g: dict, sm_scale=None, **kw):
 
 
 def run_bwd(g: dict, o, lse, dout, sm_scale=None, **kw):
-    dq, dkv = sparse_mqa_bwd_interface(g["q"], g["kv"], g["attn_sink"], o, dout, g["topk_idxs"],
-                                       lse, sm_scale=sm_scale, **kw)
+    out = sparse_mqa_bwd_interface(g["q"], g["kv"], g["attn_sink"], o, dout, g["topk_idxs"],
+                                   lse, sm_scale=sm_scale, **kw)
     torch.cuda.synchronize()
     assert device_status() == 0
-    return dq, dkv
+    return out
 
 
 def check_full(x: dict, sm_scale=None, bwd=True):
@@ -71,17 +71,19 @@ def check_full(x: dict, sm_scale=None, bwd=True):
     o_ref, lse_ref = oracle.fwd(x["q"], x["kv"], x["attn_sink"], x["topk_idxs"], sm_scale)
     errs = {"o": assert_close("o", o, o_ref), "lse": assert_close("lse", lse, lse_ref)}
     if bwd:
-        dq, dkv = run_bwd(g, o, lse, g["do"], sm_scale)
-        dq_ref, dkv_ref, _, _ = oracle.bwd(x["q"], x["kv"], x["attn_sink"], x["topk_idxs"],
-                                           x["do"], sm_scale)
+        dq, dkv, dsink = run_bwd(g, o, lse, g["do"], sm_scale, return_dsink=True)
+        dq_ref, dkv_ref, dsink_ref, _ = oracle.bwd(x["q"], x["kv"], x["attn_sink"],
+                                                   x["topk_idxs"], x["do"], sm_scale)
         errs["dq"] = assert_close("dq", dq, dq_ref)
         errs["dkv"] = assert_close("dkv", dkv, dkv_ref)
+        errs["dsink"] = assert_close("dsink", dsink, dsink_ref)
     return errs
 
 
 def check_sampled(g: dict, tokens: np.ndarray, do_fwd=True, do_bwd=True):
-    """Full-size GPU run, oracle on a token sample.  dKV uses a second backward
-    whose dO is zero outside the sample, so the sample alone feeds dKV."""
+    """Full-size GPU run, oracle on a token sample.  dKV and dsink use a second
+    backward whose dO is zero outside the sample, so the sample alone feeds
+    them (Delta, and with it each token's dsink term, is 0 elsewhere)."""
     B, S = g["q"].shape[:2]
     q_cpu = g["q"].cpu()
     kv_cpu = g["kv"].cpu()
@@ -100,11 +102,12 @@ def check_sampled(g: dict, tokens: np.ndarray, do_fwd=True, do_bwd=True):
         keep = torch.zeros(B * S, dtype=torch.bool, device=dout.device)
         keep[torch.as_tensor(tokens, device=dout.device)] = True
         d_r = torch.where(keep.view(B, S, 1, 1), dout, torch.zeros_like(dout))
-        dq, dkv = run_bwd(g, o, lse, d_r)
+        dq, dkv, dsink = run_bwd(g, o, lse, d_r, return_dsink=True)
         do_cpu = dout.cpu()
-        dq_ref, dkv_ref, _, _ = oracle.bwd(q_cpu, kv_cpu, sink_cpu, idx_cpu, do_cpu,
-                                           tokens=tokens)
+        dq_ref, dkv_ref, dsink_ref, _ = oracle.bwd(q_cpu, kv_cpu, sink_cpu, idx_cpu, do_cpu,
+                                                   tokens=tokens)
         dq_s = dq.reshape(B * S, *dq.shape[2:])[torch.as_tensor(tokens, device=dq.device)]
         errs["dq"] = assert_close("dq", dq_s, dq_ref)
         errs["dkv"] = assert_close("dkv", dkv, dkv_ref)
+        errs["dsink"] = assert_close("dsink", dsink, dsink_ref)
     return errs

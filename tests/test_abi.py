@@ -32,7 +32,7 @@ def test_exports_match_header(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.smqa_abi_version() == 3
+    assert lib.smqa_abi_version() == 4
     assert lib.smqa_status_string(0) == b"SMQA_OK"
     assert lib.smqa_status_string(4) == b"SMQA_ERR_DEVICE_TIMEOUT"
     assert lib.smqa_status_string(99) == b"SMQA_ERR_UNKNOWN"
@@ -74,11 +74,17 @@ def test_bwd_workspace_and_checks(lib):
     assert ws32 == r(delta)
     assert lib.smqa_bwd_workspace_bytes(_lib.Shape(1, 1, 1, 1, 100, 1), 0) == 0
     p = _fake()
-    args = [p] * 7 + [shp, 0.0, p, p, p]
+    args = [p] * 7 + [shp, 0.0, p, p, None, p]
     assert lib.smqa_bwd(*args, ws - 1, 0, None) == _lib.SMQA_ERR_UNSUPPORTED
     assert lib.smqa_bwd(*args, ws, 4, None) == _lib.SMQA_ERR_INVALID_ARG
-    args_null = [p] * 6 + [None, shp, 0.0, p, p, p]
+    args_null = [p] * 6 + [None, shp, 0.0, p, p, None, p]
     assert lib.smqa_bwd(*args_null, ws, 0, None) == _lib.SMQA_ERR_INVALID_ARG
+    # dsink is optional but, when given, must be 4-byte aligned.
+    args_bad_dsink = [p] * 7 + [shp, 0.0, p, p, _fake(0x10002), p]
+    assert lib.smqa_bwd(*args_bad_dsink, ws, 0, None) == _lib.SMQA_ERR_INVALID_ARG
+    assert lib.smqa_bwd_sink_grad(p, p, None, shp, p, None) == _lib.SMQA_ERR_INVALID_ARG
+    assert lib.smqa_bwd_sink_grad(p, p, p, _lib.Shape(1, 1, 1, 129, 64, 1), p, None) == \
+        _lib.SMQA_ERR_UNSUPPORTED
 
 
 def test_bwd_exchange_pool_size_and_checks(lib):
@@ -133,6 +139,17 @@ def test_python_interface_rejects_cpu_tensors():
     idx = torch.zeros(1, 4, 4, dtype=torch.int32)
     with pytest.raises(ValueError, match="CUDA"):
         sparse_mqa_fwd_interface(q, kv, sink, idx)
+
+
+def test_autograd_wrapper_rejects_cpu_tensors():
+    import torch
+    from bwd_sparse_mqa_gb300 import sparse_mqa
+    q = torch.zeros(1, 4, 16, 64, dtype=torch.bfloat16, requires_grad=True)
+    kv = torch.zeros(1, 4, 64, dtype=torch.bfloat16, requires_grad=True)
+    sink = torch.zeros(16, requires_grad=True)
+    idx = torch.zeros(1, 4, 4, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        sparse_mqa(q, kv, sink, idx)
 
 
 def test_product_package_does_not_import_oracle():

@@ -30,7 +30,7 @@ def test_static_scratch_rejects_oversized_shape_without_gpu_work():
     need = lib.smqa_bwd_workspace_bytes(big, 0)
     assert need > _lib.STATIC_SCRATCH_BYTES
     fake = ctypes.c_void_p(0x10000)
-    rc = lib.smqa_bwd_static_scratch(*([fake] * 7), big, 0.0, fake, fake, 0, None)
+    rc = lib.smqa_bwd_static_scratch(*([fake] * 7), big, 0.0, fake, fake, None, 0, None)
     assert rc == _lib.SMQA_ERR_UNSUPPORTED
     assert b"static buffer" in lib.smqa_last_error()
 
@@ -56,7 +56,7 @@ def test_static_scratch_matches_workspace_backward_twice(fp32_dkv):
     ws = torch.empty(lib.smqa_bwd_workspace_bytes(shp, flags), dtype=torch.uint8, device="cuda")
     dq_ref = torch.empty_like(g["q"])
     dkv_ref = torch.empty((B, S_kv, D), dtype=dkv_dtype, device="cuda")
-    _lib.check("smqa_bwd", lib.smqa_bwd(*args, shp, 0.0, _p(dq_ref), _p(dkv_ref), _p(ws),
+    _lib.check("smqa_bwd", lib.smqa_bwd(*args, shp, 0.0, _p(dq_ref), _p(dkv_ref), None, _p(ws),
                                         ws.numel(), flags, stream))
     torch.cuda.synchronize()
 
@@ -66,7 +66,8 @@ def test_static_scratch_matches_workspace_backward_twice(fp32_dkv):
         dq = torch.full_like(g["q"], float("nan"))
         dkv = torch.full((B, S_kv, D), float("nan"), dtype=dkv_dtype, device="cuda")
         _lib.check("smqa_bwd_static_scratch",
-                   lib.smqa_bwd_static_scratch(*args, shp, 0.0, _p(dq), _p(dkv), flags, stream))
+                   lib.smqa_bwd_static_scratch(*args, shp, 0.0, _p(dq), _p(dkv), None, flags,
+                                               stream))
         torch.cuda.synchronize()
         assert lib.smqa_device_status(1) == 0
         assert torch.equal(dq, dq_ref)  # dq has no atomics: identical
