@@ -22,6 +22,7 @@ SMQA_ERR_CUDA = 3
 SMQA_ERR_DEVICE_TIMEOUT = 4
 FLAG_RETURN_DKV_FP32 = 1
 FLAG_REFERENCE_ROUNDING = 2
+FLAG_DETERMINISTIC_DKV = 4
 
 # Every symbol include/sparse_mqa.h declares (checked by the tests).
 EXPORTS = [
@@ -30,7 +31,7 @@ EXPORTS = [
     "smqa_abi_version", "smqa_bwd_static_scratch", "smqa_bwd_exchange_bytes",
     "smqa_fwd_workspace_bytes", "smqa_fwd_static_scratch", "smqa_bwd_sink_grad",
 ]
-STATIC_SCRATCH_BYTES = 40 << 20
+STATIC_SCRATCH_BYTES = 64 << 20
 
 
 class Shape(ctypes.Structure):

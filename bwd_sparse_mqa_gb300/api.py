@@ -119,14 +119,16 @@ def sparse_mqa_bwd_interface(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch
                              lse: torch.Tensor, sm_scale: Optional[float] = None,
                              return_dkv_accum_dtype: bool = False,
                              workspace: Optional[torch.Tensor] = None,
-                             return_dsink: bool = False):
+                             return_dsink: bool = False, deterministic: bool = False):
     """Top-k sparse MQA backward.
 
     Takes the forward's inputs, its output o, the gradient do [B,S,H,D] bf16
     and its log2 lse [B,S,H] fp32.  Returns freshly allocated dq [B,S,H,D]
     bf16 and dkv [B,S_kv,D] (bf16, or fp32 with return_dkv_accum_dtype), and
     with ``return_dsink`` also the gradient w.r.t. attn_sink (fp32 [H]; not
-    among the pages' outputs).  ``workspace`` (uint8 CUDA tensor) may be
+    among the pages' outputs).  ``deterministic`` accumulates dkv in 32.32
+    fixed point with integer atomics, so it is bit-identical from run to run
+    (not a switch of the pages).  ``workspace`` (uint8 CUDA tensor) may be
     passed to reuse scratch memory between calls; otherwise one is allocated.
     """
     shp = _shape(q, kv, attn_sink, topk_idxs)
@@ -139,6 +141,8 @@ def sparse_mqa_bwd_interface(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch
         raise ValueError("lse must be [B,S,H]")
     scale = _scale(sm_scale, shp.D)
     flags = _lib.FLAG_RETURN_DKV_FP32 if return_dkv_accum_dtype else 0
+    if deterministic:
+        flags |= _lib.FLAG_DETERMINISTIC_DKV
     lib = _lib.load()
     need = int(lib.smqa_bwd_workspace_bytes(shp, flags))
     if need == 0:

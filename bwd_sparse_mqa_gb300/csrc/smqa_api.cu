@@ -143,7 +143,8 @@ size_t fwd_exchange_bytes(const smqa_shape& s) {
 
 smqa_status bwd_main_impl(const void* q, const void* kv, const void* dout, const int32_t* idx,
                           const float* lse, const float* delta, const smqa_shape& s, float scale,
-                          void* dq, float* acc, void* exch, cudaStream_t stream) {
+                          void* dq, float* acc, void* exch, cudaStream_t stream,
+                          unsigned long long* acc_fixed = nullptr) {
   cudaError_t e;
   int* st = status_ptr(&e);
   if (!st) return cuda_fail(e, "status word");
@@ -164,6 +165,8 @@ smqa_status bwd_main_impl(const void* q, const void* kv, const void* dout, const
   p.delta = delta;
   p.dq = static_cast<__nv_bfloat16*>(dq);
   p.dkv_acc = acc;
+  p.dkv_fix = acc_fixed;
+  p.det = acc_fixed != nullptr ? 1 : 0;
   p.S = s.S;
   p.S_kv = s.S_kv;
   p.H = s.H;
@@ -273,8 +276,11 @@ size_t smqa_fwd_workspace_bytes(smqa_shape shape) {
 size_t smqa_bwd_workspace_bytes(smqa_shape shape, unsigned flags) {
   if (check_shape(shape) != SMQA_OK) return 0;
   size_t bytes = 0;
-  if (!(flags & SMQA_FLAG_RETURN_DKV_FP32))
-    bytes += round256(static_cast<size_t>(shape.B) * shape.S_kv * shape.D * sizeof(float));
+  const size_t elems = static_cast<size_t>(shape.B) * shape.S_kv * shape.D;
+  if (flags & SMQA_FLAG_DETERMINISTIC_DKV)
+    bytes += round256(elems * sizeof(unsigned long long));  // 32.32 fixed-point accumulator
+  else if (!(flags & SMQA_FLAG_RETURN_DKV_FP32))
+    bytes += round256(elems * sizeof(float));
   bytes += round256(static_cast<size_t>(shape.B) * shape.S * shape.H * sizeof(float));
   bytes += round256(exchange_bytes(shape));
   return bytes;
@@ -364,10 +370,10 @@ smqa_status smqa_bwd(const void* q, const void* kv, const float* attn_sink, cons
   const smqa_status sc = check_shape(shape);
   if (sc != SMQA_OK) return sc;
   if (!q || !kv || !attn_sink || !o || !dout || !topk_idxs || !lse || !dq || !dkv || !workspace ||
-      (flags & ~SMQA_FLAG_RETURN_DKV_FP32) || !aligned(q, 16) || !aligned(kv, 16) ||
-      !aligned(o, 16) || !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dkv, 16) ||
-      !aligned(workspace, 16) || !aligned(attn_sink, 4) || !aligned(topk_idxs, 4) ||
-      !aligned(lse, 4) || !aligned(dsink, 4)) {
+      (flags & ~(SMQA_FLAG_RETURN_DKV_FP32 | SMQA_FLAG_DETERMINISTIC_DKV)) || !aligned(q, 16) ||
+      !aligned(kv, 16) || !aligned(o, 16) || !aligned(dout, 16) || !aligned(dq, 16) ||
+      !aligned(dkv, 16) || !aligned(workspace, 16) || !aligned(attn_sink, 4) ||
+      !aligned(topk_idxs, 4) || !aligned(lse, 4) || !aligned(dsink, 4)) {
     std::snprintf(g_last_error, sizeof g_last_error, "null/misaligned pointer or bad flags");
     return SMQA_ERR_INVALID_ARG;
   }
@@ -376,22 +382,41 @@ smqa_status smqa_bwd(const void* q, const void* kv, const float* attn_sink, cons
     return SMQA_ERR_UNSUPPORTED;
   }
   const bool fp32_out = (flags & SMQA_FLAG_RETURN_DKV_FP32) != 0;
+  const bool det = (flags & SMQA_FLAG_DETERMINISTIC_DKV) != 0;
+  const int64_t elems = static_cast<int64_t>(shape.B) * shape.S_kv * shape.D;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* acc = fp32_out ? static_cast<float*>(dkv) : reinterpret_cast<float*>(ws);
+  float* acc = (fp32_out && !det) ? static_cast<float*>(dkv) : reinterpret_cast<float*>(ws);
+  unsigned long long* acc_fixed = det ? reinterpret_cast<unsigned long long*>(ws) : nullptr;
   const size_t acc_bytes =
-      fp32_out ? 0 : round256(static_cast<size_t>(shape.B) * shape.S_kv * shape.D * sizeof(float));
+      det ? round256(static_cast<size_t>(elems) * sizeof(unsigned long long))
+          : (fp32_out ? 0 : round256(static_cast<size_t>(elems) * sizeof(float)));
   float* delta = reinterpret_cast<float*>(ws + acc_bytes);
   void* exch = ws + acc_bytes +
                round256(static_cast<size_t>(shape.B) * shape.S * shape.H * sizeof(float));
-  smqa_status r = smqa_bwd_preprocess(o, dout, shape, delta, acc, stream);
-  if (r != SMQA_OK) return r;
+  smqa_status r;
+  if (det) {
+    // Delta, and the fixed-point accumulator zeroed (two floats' worth of
+    // zero bits per element).
+    const cudaError_t e = smqa::launch_bwd_preprocess(
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), delta,
+        acc, static_cast<int64_t>(shape.B) * shape.S * shape.H, shape.D, 2 * elems, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "bwd preprocess launch");
+  } else {
+    r = smqa_bwd_preprocess(o, dout, shape, delta, acc, stream);
+    if (r != SMQA_OK) return r;
+  }
   if (dsink) {
     r = smqa_bwd_sink_grad(attn_sink, lse, delta, shape, dsink, stream);
     if (r != SMQA_OK) return r;
   }
   r = bwd_main_impl(q, kv, dout, topk_idxs, lse, delta, shape, effective_scale(sm_scale, shape.D),
-                    dq, acc, exch, stream);
+                    dq, acc, exch, stream, acc_fixed);
   if (r != SMQA_OK) return r;
+  if (det) {
+    const cudaError_t e = smqa::launch_bwd_post_fixed(acc_fixed, dkv, fp32_out ? 1 : 0, elems, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "bwd postprocess launch");
+    return SMQA_OK;
+  }
   if (!fp32_out) return smqa_bwd_postprocess(acc, shape, dkv, stream);
   return SMQA_OK;
 }

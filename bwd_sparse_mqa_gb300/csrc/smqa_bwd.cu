@@ -86,6 +86,29 @@ __global__ void __launch_bounds__(256)
 }
 
 // --------------------------------------------------------------------------
+// postprocess of the deterministic mode: 32.32 fixed point -> bf16 or fp32
+// --------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+    smqa_bwd_post_fixed_kernel(const unsigned long long* __restrict__ acc, void* __restrict__ out,
+                               int fp32_out, int64_t vec4) {
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const ulonglong2* a2 = reinterpret_cast<const ulonglong2*>(acc);
+  constexpr float kInv = 1.f / 4294967296.f;  // 2^-32
+  for (int64_t i = tid; i < vec4; i += nthr) {
+    const ulonglong2 x = a2[2 * i], y = a2[2 * i + 1];
+    const float v0 = __ll2float_rn(static_cast<long long>(x.x)) * kInv;
+    const float v1 = __ll2float_rn(static_cast<long long>(x.y)) * kInv;
+    const float v2 = __ll2float_rn(static_cast<long long>(y.x)) * kInv;
+    const float v3 = __ll2float_rn(static_cast<long long>(y.y)) * kInv;
+    if (fp32_out)
+      reinterpret_cast<float4*>(out)[i] = make_float4(v0, v1, v2, v3);
+    else
+      reinterpret_cast<uint2*>(out)[i] = make_uint2(pack_bf16x2(v0, v1), pack_bf16x2(v2, v3));
+  }
+}
+
+// --------------------------------------------------------------------------
 // sink gradient: dsink[h] = -sum_t 2^(sink_h log2 e - lse2[t,h]) Delta[t,h]
 // --------------------------------------------------------------------------
 // The sink adds exp(sink_h) to row (t,h)'s denominator but no value, so
@@ -204,7 +227,7 @@ __device__ __forceinline__ void load_own_partials(uint32_t t_s, uint32_t t_dp, f
   }
 }
 
-template <int DC, int NC>
+template <int DC, int NC, bool DET>
 __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
     smqa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
@@ -498,7 +521,23 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
     const bool active = (wq * 32) < DC;  // DC = 64: rows 64..127 are padding
-    float* col = p.dkv_acc + static_cast<size_t>(rank) * DC + wq * 32 + lane;
+    const size_t col0 = static_cast<size_t>(rank) * DC + wq * 32 + lane;
+    float* col = p.dkv_acc + col0;
+    unsigned long long* colx = p.dkv_fix + col0;
+    // One contribution to element off of this lane's column: an fp32
+    // reduction, or in the deterministic mode the value as a 32.32
+    // fixed-point integer (rounded to nearest, saturating) added as an
+    // integer, so the sum does not depend on the order of the additions.
+    auto add = [&](size_t off, float v) {
+      if constexpr (DET) {
+        const long long n = __float2ll_rn(v * 4294967296.f);
+        asm volatile("red.global.add.u64 [%0], %1;" ::"l"(colx + off),
+                     "l"(static_cast<unsigned long long>(n))
+                     : "memory");
+      } else {
+        red_add_f32(col + off, v);
+      }
+    };
     for (int j = 0; j < nblk; ++j) {
       const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDkvFull), j & 1, ctl));
       if (!ok) break;
@@ -528,8 +567,8 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
             for (int k = 0; k < 32; ++k) {
               const int rk = __shfl_sync(0xffffffffu, row[half], k);
               if ((vm[half] >> k) & 1u) {
-                red_add_f32(col + static_cast<size_t>(rk) * p.D, x[0][k]);
-                red_add_f32(col + static_cast<size_t>(rk) * p.D + 128, x[1][k]);
+                add(static_cast<size_t>(rk) * p.D, x[0][k]);
+                add(static_cast<size_t>(rk) * p.D + 128, x[1][k]);
               }
             }
           }
@@ -545,7 +584,7 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
               const int rk = __shfl_sync(0xffffffffu, row[half], k);
-              if ((vm[half] >> k) & 1u) red_add_f32(col + static_cast<size_t>(rk) * p.D, x[half][k]);
+              if ((vm[half] >> k) & 1u) add(static_cast<size_t>(rk) * p.D, x[half][k]);
             }
         }
       }
@@ -714,11 +753,11 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
   }
 }
 
-template <int DC, int NC>
+template <int DC, int NC, bool DET>
 static cudaError_t launch_bwd_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_do,
                                    const BwdParams& p, int tokens, cudaStream_t stream) {
   using L = BwdLayout<DC, NC>;
-  auto kern = smqa_bwd_kernel<DC, NC>;
+  auto kern = smqa_bwd_kernel<DC, NC, DET>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -739,8 +778,14 @@ static cudaError_t launch_bwd_impl(const CUtensorMap& tm_q, const CUtensorMap& t
 
 cudaError_t launch_bwd_main(const CUtensorMap& tm_q, const CUtensorMap& tm_do,
                             const BwdParams& p, int tokens, cudaStream_t stream) {
-  if (p.D == 512) return launch_bwd_impl<256, 2>(tm_q, tm_do, p, tokens, stream);
-  if (p.D == 64) return launch_bwd_impl<64, 1>(tm_q, tm_do, p, tokens, stream);
+  // The deterministic mode is a separate instantiation, so the default
+  // kernel's reduction loop carries no branch for it.
+  if (p.D == 512)
+    return p.det ? launch_bwd_impl<256, 2, true>(tm_q, tm_do, p, tokens, stream)
+                 : launch_bwd_impl<256, 2, false>(tm_q, tm_do, p, tokens, stream);
+  if (p.D == 64)
+    return p.det ? launch_bwd_impl<64, 1, true>(tm_q, tm_do, p, tokens, stream)
+                 : launch_bwd_impl<64, 1, false>(tm_q, tm_do, p, tokens, stream);
   return cudaErrorInvalidValue;
 }
 
@@ -758,6 +803,13 @@ cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* d
   const int64_t work = rows * 32 > acc_vec4 ? rows * 32 : acc_vec4;
   smqa_bwd_pre_kernel<<<grid_for(work, 256), 256, 0, stream>>>(o, dout, delta, dkv_acc, rows, D,
                                                                acc_vec4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_post_fixed(const unsigned long long* acc, void* out, int fp32_out,
+                                 int64_t elems, cudaStream_t stream) {
+  const int64_t vec4 = elems / 4;
+  smqa_bwd_post_fixed_kernel<<<grid_for(vec4, 256), 256, 0, stream>>>(acc, out, fp32_out, vec4);
   return cudaGetLastError();
 }
 

@@ -37,6 +37,10 @@ struct BwdParams {
   const float* delta;    // [B,S,H]  rowsum(O * dO)
   __nv_bfloat16* dq;     // [B,S,H,D]
   float* dkv_acc;        // [B,S_kv,D] fp32 accumulator (zeroed beforehand)
+  // Deterministic mode (det != 0): the accumulator is dkv_fix instead, each
+  // element a signed 32.32 fixed-point integer (zeroed beforehand).
+  unsigned long long* dkv_fix;
+  int det;
   int S, S_kv, H, D, topk;
   float scale;           // sm_scale
   float scale_log2;      // sm_scale * log2(e)
@@ -70,6 +74,8 @@ cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* d
                                   int64_t acc_elems, cudaStream_t stream);
 cudaError_t launch_bwd_sink_grad(const float* sink, const float* lse, const float* delta,
                                 float* dsink, int64_t tokens, int H, cudaStream_t stream);
+cudaError_t launch_bwd_post_fixed(const unsigned long long* acc, void* out, int fp32_out,
+                                 int64_t elems, cudaStream_t stream);
 cudaError_t launch_bwd_postprocess(const float* acc, __nv_bfloat16* out, int64_t elems,
                                    cudaStream_t stream);
 

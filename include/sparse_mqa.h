@@ -75,6 +75,15 @@ typedef struct {
  * pages' backward interface has the same switch (`return_dkv_accum_dtype`). */
 #define SMQA_FLAG_RETURN_DKV_FP32 1u
 
+/* smqa_bwd: accumulate dkv deterministically.  Every contribution is added
+ * as a signed 32.32 fixed-point integer (the fp32 value times 2^32, rounded
+ * to nearest, saturating) with 64-bit integer atomics, whose sum does not
+ * depend on the order of the additions; the result is converted back to
+ * bf16 (or fp32 with SMQA_FLAG_RETURN_DKV_FP32).  Resolution 2^-32, range
+ * +-2^31 per element; the accumulator doubles (8 bytes per dkv element, in
+ * the workspace).  Not a flag of the pages. */
+#define SMQA_FLAG_DETERMINISTIC_DKV 4u
+
 /*
  * Bytes of device workspace smqa_fwd needs for `shape`: 0 when D = 64; for
  * D = 512 the exchange pool (4 KB of slot flags + 96 slots of 132 KB).  For
@@ -118,7 +127,8 @@ smqa_status smqa_fwd(const void* q, const void* kv, const float* attn_sink,
 /*
  * Bytes of device workspace smqa_bwd needs for `shape` and `flags`: the fp32
  * dKV accumulator [B,S_kv,D] (absent with SMQA_FLAG_RETURN_DKV_FP32, where
- * dkv itself accumulates), Delta [B,S,H] fp32, and for D = 512 the exchange
+ * dkv itself accumulates; with SMQA_FLAG_DETERMINISTIC_DKV always present and
+ * 8 bytes per element), Delta [B,S,H] fp32, and for D = 512 the exchange
  * pool of smqa_bwd_exchange_bytes(shape), each 256-byte aligned.
  * Returns 0 for an unsupported shape.
  */
@@ -152,7 +162,9 @@ size_t smqa_bwd_exchange_bytes(smqa_shape shape);
  *                              exp(attn_sink[h] - LSE_e) * rowsum(o * dout))
  *   workspace, workspace_bytes  >= smqa_bwd_workspace_bytes(shape, flags)
  * dkv sums contributions with fp32 atomics, so its low bits may differ from
- * run to run; dq and dsink are deterministic.
+ * run to run (bit-identical with SMQA_FLAG_DETERMINISTIC_DKV); dq and dsink
+ * are deterministic.  flags: any of SMQA_FLAG_RETURN_DKV_FP32,
+ * SMQA_FLAG_DETERMINISTIC_DKV.
  */
 smqa_status smqa_bwd(const void* q, const void* kv, const float* attn_sink, const void* o,
                      const void* dout, const int32_t* topk_idxs, const float* lse,
@@ -190,7 +202,7 @@ smqa_status smqa_bwd(const void* q, const void* kv, const float* attn_sink, cons
  *     ordering between them, or several host threads -- race on it and give
  *     wrong results; order them on one stream.
  */
-#define SMQA_STATIC_SCRATCH_BYTES (40u << 20)
+#define SMQA_STATIC_SCRATCH_BYTES (64u << 20)
 smqa_status smqa_fwd_static_scratch(const void* q, const void* kv, const float* attn_sink,
                                     const int32_t* topk_idxs, smqa_shape shape, float sm_scale,
                                     void* o, float* lse, unsigned flags, cudaStream_t stream);

@@ -76,7 +76,7 @@ def test_bwd_workspace_and_checks(lib):
     p = _fake()
     args = [p] * 7 + [shp, 0.0, p, p, None, p]
     assert lib.smqa_bwd(*args, ws - 1, 0, None) == _lib.SMQA_ERR_UNSUPPORTED
-    assert lib.smqa_bwd(*args, ws, 4, None) == _lib.SMQA_ERR_INVALID_ARG
+    assert lib.smqa_bwd(*args, ws, 8, None) == _lib.SMQA_ERR_INVALID_ARG
     args_null = [p] * 6 + [None, shp, 0.0, p, p, None, p]
     assert lib.smqa_bwd(*args_null, ws, 0, None) == _lib.SMQA_ERR_INVALID_ARG
     # dsink is optional but, when given, must be 4-byte aligned.
@@ -85,6 +85,23 @@ def test_bwd_workspace_and_checks(lib):
     assert lib.smqa_bwd_sink_grad(p, p, None, shp, p, None) == _lib.SMQA_ERR_INVALID_ARG
     assert lib.smqa_bwd_sink_grad(p, p, p, _lib.Shape(1, 1, 1, 129, 64, 1), p, None) == \
         _lib.SMQA_ERR_UNSUPPORTED
+
+
+def test_bwd_deterministic_flag_workspace_and_checks(lib):
+    """SMQA_FLAG_DETERMINISTIC_DKV: the accumulator is 8 bytes per dkv element
+    and always in the workspace (also with the fp32 output); unknown flags
+    are rejected."""
+    r = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    shp = _lib.Shape(2, 8, 16, 16, 64, 4)
+    acc8, delta = 2 * 16 * 64 * 8, 2 * 8 * 16 * 4
+    det = _lib.FLAG_DETERMINISTIC_DKV
+    assert lib.smqa_bwd_workspace_bytes(shp, det) == r(acc8) + r(delta)
+    assert lib.smqa_bwd_workspace_bytes(shp, det | _lib.FLAG_RETURN_DKV_FP32) == r(acc8) + r(delta)
+    p = _fake()
+    args = [p] * 7 + [shp, 0.0, p, p, None, p]
+    need = lib.smqa_bwd_workspace_bytes(shp, det)
+    assert lib.smqa_bwd(*args, need - 1, det, None) == _lib.SMQA_ERR_UNSUPPORTED
+    assert lib.smqa_bwd(*args, need, 8, None) == _lib.SMQA_ERR_INVALID_ARG
 
 
 def test_bwd_exchange_pool_size_and_checks(lib):

@@ -24,9 +24,11 @@ def _p(t):
 def test_static_scratch_rejects_oversized_shape_without_gpu_work():
     """Too large for the static buffer: rejected on the host, nothing runs."""
     lib = _lib.load()
-    big = _lib.Shape(1, 8192, 32768, 128, 512, 2048)   # 64 MiB accumulator alone
+    big = _lib.Shape(1, 8192, 65536, 128, 512, 2048)   # 128 MiB accumulator alone
     head = _lib.Shape(1, 8192, 8192, 128, 512, 2048)   # the H=128 D=512 benchmark shape
     assert lib.smqa_bwd_workspace_bytes(head, 0) <= _lib.STATIC_SCRATCH_BYTES
+    assert lib.smqa_bwd_workspace_bytes(head, _lib.FLAG_DETERMINISTIC_DKV) <= \
+        _lib.STATIC_SCRATCH_BYTES
     need = lib.smqa_bwd_workspace_bytes(big, 0)
     assert need > _lib.STATIC_SCRATCH_BYTES
     fake = ctypes.c_void_p(0x10000)
