@@ -73,6 +73,9 @@ struct FwdLayout {
   static constexpr uint32_t kStageBytes = kChunks * kKvChunkBytes;
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffKv = kOffQ + kQBytes;
+  // The epilogue stages O in the (then idle) kv ring: 64-column tiles of
+  // 128 rows x 128 bytes.
+  static constexpr uint32_t kOTileBytes = kHPad * 128;
   // Exchange buffer of one receiver and block: each head's 64 partial scores
   // as int16 with one power-of-two scale (block floating point), in 8 pieces
   // of 16 bytes per head, piece-major (a warp's 32 heads are 512 contiguous
@@ -92,7 +95,8 @@ struct FwdLayout {
   static constexpr int kBarODone = kBarPFull + 2;            // [2] P.V of block i done
   static constexpr int kBarQFull = kBarODone + 2;
   static constexpr int kBarDrain = kBarQFull + 1;
-  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kBarOStaged = kBarDrain + 1;          // O tile in shared memory
+  static constexpr int kNumBars = kBarOStaged + 1;
   static constexpr uint32_t kOffTmemHolder = kOffCtrl + 8 * kNumBars;
   static constexpr uint32_t kOffAbort = kOffTmemHolder + 4;
   static constexpr uint32_t kOffSlot = kOffAbort + 4;
@@ -102,6 +106,7 @@ struct FwdLayout {
   static_assert(kOffMask + 8 * kStages - kOffCtrl <= kCtrlBytes, "control block overflow");
   static constexpr uint32_t kSmemBytes = kOffCtrl + kCtrlBytes + 1024;  // +1024: realignment
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert((kDC / 64) * kOTileBytes <= kStages * kStageBytes, "O staging fits the kv ring");
   // TMEM: O, the ring of score tiles, then two P buffers (bf16 pairs, 32
   // columns each).
   static constexpr uint32_t kTmemO = 0;
@@ -124,6 +129,20 @@ struct FwdLayout {
   static constexpr int kThreads = (kSendWarp0 + (NSPLIT == 2 ? 4 : 0)) * 32;
   static_assert(2 * kXBufs * kXchgBytes == kFwdSlotBytes, "exchange slot size");
 };
+
+// 2-D tensor store of one shared-memory box (tracked by this thread's bulk
+// async-groups), and the group commit / wait for it.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(m),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_group0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 
 // Gathers this CTA's column half of a block's kv rows into a
 // 128-byte-swizzled K-major tile of NCHUNKS 64-column chunks.  Warp w of the
@@ -193,7 +212,8 @@ __device__ __forceinline__ float2 bfp16_unpack(uint32_t w, float inv) {
 
 template <int D, int NSPLIT>
 __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
-    smqa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const FwdParams p) {
+    smqa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
+                    const FwdParams p) {
   using L = FwdLayout<D, NSPLIT>;
   constexpr int DC = L::kDC;
   extern __shared__ uint8_t smem_raw[];
@@ -236,6 +256,7 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
     }
     mbar_init(bar(L::kBarQFull), 1);
     mbar_init(bar(L::kBarDrain), 1);
+    mbar_init(bar(L::kBarOStaged), L::kSoftmaxThreads);
     *abort_flag = *reinterpret_cast<volatile int*>(p.status) != 0 ? 1 : 0;
     *slot_smem = -1;
     if (NSPLIT == 2 && rank == 0 && *abort_flag == 0) {
@@ -623,27 +644,48 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
       const float so = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_fin);
       const float Z = l_run * so + fast_exp2(sink2 - m_fin);
       const float inv = so / Z;
-      __nv_bfloat16* orow = p.o + (static_cast<size_t>(t) * p.H + h) * D +
-                            static_cast<size_t>(rank) * DC;
+      // O, scaled, into shared memory as 64-column tiles in the
+      // 128-byte-swizzled layout of the output's tensor map (the kv ring is
+      // free: every MMA has completed); the TMA then writes whole rows.
 #pragma unroll 1
-      for (int c = 0; c < DC / 32; ++c) {
-        float v[32];
-        tmem_ld32(tmem + lane_base + L::kTmemO + c * 32, v);
-        if (nblk == 0) {  // no valid slot: O was never written, the output is 0
+      for (int cc = 0; cc < DC / 64; ++cc) {
+        float v[2][32];
+        if (nblk > 0) {
+          tmem_ld32x2(tmem + lane_base + L::kTmemO + cc * 64,
+                      tmem + lane_base + L::kTmemO + cc * 64 + 32, v[0], v[1]);
+        } else {  // no valid slot: O was never written, the output is 0
 #pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = 0.f;
+          for (int k = 0; k < 32; ++k) v[0][k] = v[1][k] = 0.f;
         }
-        if (h < p.H) {
+        const uint32_t row = base + L::kOffKv + static_cast<uint32_t>(cc) * L::kOTileBytes +
+                             static_cast<uint32_t>(h) * 128u;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
           uint32_t w[16];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(v[2 * k] * inv, v[2 * k + 1] * inv);
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(v[u][2 * k] * inv, v[u][2 * k + 1] * inv);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t piece = static_cast<uint32_t>(4 * u + k);
+            st_shared_v4(row + ((piece ^ (static_cast<uint32_t>(h) & 7u)) << 4), w[4 * k],
+                         w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+          }
         }
       }
       if (rank == 0 && h < p.H) p.lse[static_cast<size_t>(t) * p.H + h] = m_fin + log2f(Z);
+    }
+    // Every softmax thread arrives (also after a failed wait, so that the
+    // storing thread never waits in vain); one thread ships the tiles.
+    fence_proxy_async_smem();
+    mbar_arrive(bar(L::kBarOStaged));
+    if (threadIdx.x == 0) {
+      if (mbar_wait(bar(L::kBarOStaged), 0, ctl) && *abort_flag == 0) {
+        for (int cc = 0; cc < DC / 64; ++cc)
+          tma_store_2d(&tm_o, base + L::kOffKv + static_cast<uint32_t>(cc) * L::kOTileBytes,
+                       static_cast<int>(rank) * DC + cc * 64, t * p.H);
+        bulk_commit_group();
+        bulk_wait_group0();  // complete before the CTA (and its shared memory) goes away
+      }
     }
   }
 
@@ -662,8 +704,8 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
 }
 
 template <int D, int NSPLIT>
-static cudaError_t launch_fwd_impl(const CUtensorMap& tm_q, const FwdParams& p, int tokens,
-                                   cudaStream_t stream) {
+static cudaError_t launch_fwd_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_o,
+                                   const FwdParams& p, int tokens, cudaStream_t stream) {
   using L = FwdLayout<D, NSPLIT>;
   auto kern = smqa_fwd_kernel<D, NSPLIT>;
   cudaError_t e =
@@ -681,13 +723,13 @@ static cudaError_t launch_fwd_impl(const CUtensorMap& tm_q, const FwdParams& p, 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tm_q, p);
+  return cudaLaunchKernelEx(&cfg, kern, tm_q, tm_o, p);
 }
 
-cudaError_t launch_fwd(const CUtensorMap& tm_q, const FwdParams& p, int tokens,
-                       cudaStream_t stream) {
-  if (p.D == 512) return launch_fwd_impl<512, 2>(tm_q, p, tokens, stream);
-  if (p.D == 64) return launch_fwd_impl<64, 1>(tm_q, p, tokens, stream);
+cudaError_t launch_fwd(const CUtensorMap& tm_q, const CUtensorMap& tm_o, const FwdParams& p,
+                       int tokens, cudaStream_t stream) {
+  if (p.D == 512) return launch_fwd_impl<512, 2>(tm_q, tm_o, p, tokens, stream);
+  if (p.D == 64) return launch_fwd_impl<64, 1>(tm_q, tm_o, p, tokens, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -65,8 +65,8 @@ constexpr size_t kBwdSlotBytes = 2 * 2 * 32768;
 // Records `msg` as the text smqa_last_error() returns on this thread.
 void set_last_error(const char* msg);
 
-cudaError_t launch_fwd(const CUtensorMap& tm_q, const FwdParams& p, int tokens,
-                       cudaStream_t stream);
+cudaError_t launch_fwd(const CUtensorMap& tm_q, const CUtensorMap& tm_o, const FwdParams& p,
+                       int tokens, cudaStream_t stream);
 cudaError_t launch_bwd_main(const CUtensorMap& tm_q, const CUtensorMap& tm_do,
                             const BwdParams& p, int tokens, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* dout,
