@@ -153,10 +153,11 @@ smqa_status bwd_main_impl(const void* q, const void* kv, const void* dout, const
     e = cudaMemsetAsync(exch, 0, kExchSlots * sizeof(int), stream);
     if (e != cudaSuccess) return cuda_fail(e, "exchange flags clear");
   }
-  CUtensorMap tq, tdo;
+  CUtensorMap tq, tdo, tdq;
   const uint64_t T = static_cast<uint64_t>(s.B) * s.S;
   if (!encode_bf16_2d(&tq, q, s.D, T * s.H, 64, static_cast<uint32_t>(s.H)) ||
-      !encode_bf16_2d(&tdo, dout, s.D, T * s.H, 64, static_cast<uint32_t>(s.H)))
+      !encode_bf16_2d(&tdo, dout, s.D, T * s.H, 64, static_cast<uint32_t>(s.H)) ||
+      !encode_bf16_2d(&tdq, dq, s.D, T * s.H, 64, static_cast<uint32_t>(s.H)))
     return SMQA_ERR_CUDA;
   smqa::BwdParams p{};
   p.kv = static_cast<const __nv_bfloat16*>(kv);
@@ -181,7 +182,7 @@ smqa_status bwd_main_impl(const void* q, const void* kv, const void* dout, const
     p.exch = static_cast<uint8_t*>(exch) + kExchFlagBytes;
     p.nslots = kExchSlots;
   }
-  e = smqa::launch_bwd_main(tq, tdo, p, static_cast<int>(T), stream);
+  e = smqa::launch_bwd_main(tq, tdo, tdq, p, static_cast<int>(T), stream);
   if (e != cudaSuccess) return cuda_fail(e, "bwd main launch");
   return SMQA_OK;
 }

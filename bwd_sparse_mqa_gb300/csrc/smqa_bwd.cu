@@ -176,7 +176,8 @@ struct BwdLayout {
   static constexpr int kBarQdoFull = kBarSendOk + 2;
   static constexpr int kBarDqDone = kBarQdoFull + 1;
   static constexpr int kBarDrain = kBarDqDone + 1;
-  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kBarDqStaged = kBarDrain + 1;  // dQ tile in shared memory
+  static constexpr int kNumBars = kBarDqStaged + 1;
   static constexpr uint32_t kOffTmemHolder = kOffCtrl + 8 * kNumBars;
   static constexpr uint32_t kOffAbort = kOffTmemHolder + 4;
   static constexpr uint32_t kOffSlot = kOffAbort + 4;
@@ -185,6 +186,7 @@ struct BwdLayout {
   static_assert(kOffWarpLast + 64 - kOffCtrl <= kCtrlBytes, "control block overflow");
   static constexpr uint32_t kSmemBytes = kOffCtrl + kCtrlBytes + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert((DC / 64) * kQChunkBytes <= kStages * kKvStageBytes, "dQ staging fits the kv ring");
   // TMEM: dQ, S, dP, dKV^T (one tile each).
   static constexpr uint32_t kTmemDq = 0;
   static constexpr uint32_t kTmemS = DC;
@@ -230,7 +232,8 @@ __device__ __forceinline__ void load_own_partials(uint32_t t_s, uint32_t t_dp, f
 template <int DC, int NC, bool DET>
 __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
     smqa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
-                    const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using L = BwdLayout<DC, NC>;
   extern __shared__ uint8_t smem_raw[];
   uint32_t base = smem_u32(smem_raw);
@@ -269,6 +272,7 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
     mbar_init(bar(L::kBarQdoFull), 1);
     mbar_init(bar(L::kBarDqDone), 1);
     mbar_init(bar(L::kBarDrain), 1);
+    mbar_init(bar(L::kBarDqStaged), 128);
     *abort_flag = *reinterpret_cast<volatile int*>(p.status) != 0 ? 1 : 0;
     *slot_smem = -1;
     if (NC == 2 && rank == 0 && *abort_flag == 0) {
@@ -716,25 +720,46 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDqDone), 0, ctl));
     if (ok) {
       tc_fence_after();
-      __nv_bfloat16* qrow = p.dq + (static_cast<size_t>(t) * p.H + h) * p.D +
-                            static_cast<size_t>(rank) * DC;
+      // dQ into shared memory as 64-column tiles in the 128-byte-swizzled
+      // layout of dq's tensor map (the kv ring is free: every MMA has
+      // completed); the TMA then writes whole rows.
 #pragma unroll 1
-      for (int c = 0; c < DC / 32; ++c) {
-        float v[32];
-        tmem_ld32(tmem + lane_base + L::kTmemDq + c * 32, v);
-        if (nblk == 0) {  // no valid slot: dQ was never written, the gradient is 0
+      for (int cc = 0; cc < DC / 64; ++cc) {
+        float v[2][32];
+        if (nblk > 0) {
+          tmem_ld32x2(tmem + lane_base + L::kTmemDq + cc * 64,
+                      tmem + lane_base + L::kTmemDq + cc * 64 + 32, v[0], v[1]);
+        } else {  // no valid slot: dQ was never written, the gradient is 0
 #pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = 0.f;
+          for (int k = 0; k < 32; ++k) v[0][k] = v[1][k] = 0.f;
         }
-        if (h < p.H) {
+        const uint32_t row = base + L::kOffKv + static_cast<uint32_t>(cc) * L::kQChunkBytes +
+                             static_cast<uint32_t>(h) * 128u;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
           uint32_t w[16];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
-          uint4* dst = reinterpret_cast<uint4*>(qrow + c * 32);
+          for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(v[u][2 * k], v[u][2 * k + 1]);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t piece = static_cast<uint32_t>(4 * u + k);
+            st_shared_v4(row + ((piece ^ (static_cast<uint32_t>(h) & 7u)) << 4), w[4 * k],
+                         w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+          }
         }
+      }
+    }
+    // Every P / dS thread arrives (also after a failed wait, so that the
+    // storing thread never waits in vain); one thread ships the tiles.
+    fence_proxy_async_smem();
+    mbar_arrive(bar(L::kBarDqStaged));
+    if (threadIdx.x == 0) {
+      if (mbar_wait(bar(L::kBarDqStaged), 0, ctl) && *abort_flag == 0) {
+        for (int cc = 0; cc < DC / 64; ++cc)
+          tma_store_2d(&tm_dq, base + L::kOffKv + static_cast<uint32_t>(cc) * L::kQChunkBytes,
+                       static_cast<int>(rank) * DC + cc * 64, t * p.H);
+        bulk_commit_group();
+        bulk_wait_group0();  // complete before the CTA (and its shared memory) goes away
       }
     }
   }
@@ -755,7 +780,8 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
 
 template <int DC, int NC, bool DET>
 static cudaError_t launch_bwd_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_do,
-                                   const BwdParams& p, int tokens, cudaStream_t stream) {
+                                   const CUtensorMap& tm_dq, const BwdParams& p, int tokens,
+                                   cudaStream_t stream) {
   using L = BwdLayout<DC, NC>;
   auto kern = smqa_bwd_kernel<DC, NC, DET>;
   cudaError_t e =
@@ -773,19 +799,20 @@ static cudaError_t launch_bwd_impl(const CUtensorMap& tm_q, const CUtensorMap& t
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tm_q, tm_do, p);
+  return cudaLaunchKernelEx(&cfg, kern, tm_q, tm_do, tm_dq, p);
 }
 
 cudaError_t launch_bwd_main(const CUtensorMap& tm_q, const CUtensorMap& tm_do,
-                            const BwdParams& p, int tokens, cudaStream_t stream) {
+                            const CUtensorMap& tm_dq, const BwdParams& p, int tokens,
+                            cudaStream_t stream) {
   // The deterministic mode is a separate instantiation, so the default
   // kernel's reduction loop carries no branch for it.
   if (p.D == 512)
-    return p.det ? launch_bwd_impl<256, 2, true>(tm_q, tm_do, p, tokens, stream)
-                 : launch_bwd_impl<256, 2, false>(tm_q, tm_do, p, tokens, stream);
+    return p.det ? launch_bwd_impl<256, 2, true>(tm_q, tm_do, tm_dq, p, tokens, stream)
+                 : launch_bwd_impl<256, 2, false>(tm_q, tm_do, tm_dq, p, tokens, stream);
   if (p.D == 64)
-    return p.det ? launch_bwd_impl<64, 1, true>(tm_q, tm_do, p, tokens, stream)
-                 : launch_bwd_impl<64, 1, false>(tm_q, tm_do, p, tokens, stream);
+    return p.det ? launch_bwd_impl<64, 1, true>(tm_q, tm_do, tm_dq, p, tokens, stream)
+                 : launch_bwd_impl<64, 1, false>(tm_q, tm_do, tm_dq, p, tokens, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -130,20 +130,6 @@ struct FwdLayout {
   static_assert(2 * kXBufs * kXchgBytes == kFwdSlotBytes, "exchange slot size");
 };
 
-// 2-D tensor store of one shared-memory box (tracked by this thread's bulk
-// async-groups), and the group commit / wait for it.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int x, int y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(m),
-               "r"(src), "r"(x), "r"(y)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_group0() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // Gathers this CTA's column half of a block's kv rows into a
 // 128-byte-swizzled K-major tile of NCHUNKS 64-column chunks.  Warp w of the
 // NW gather warps issues instructions w, w+NW, ...; instruction k moves

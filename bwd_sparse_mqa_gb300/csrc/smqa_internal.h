@@ -68,7 +68,8 @@ void set_last_error(const char* msg);
 cudaError_t launch_fwd(const CUtensorMap& tm_q, const CUtensorMap& tm_o, const FwdParams& p,
                        int tokens, cudaStream_t stream);
 cudaError_t launch_bwd_main(const CUtensorMap& tm_q, const CUtensorMap& tm_do,
-                            const BwdParams& p, int tokens, cudaStream_t stream);
+                            const CUtensorMap& tm_dq, const BwdParams& p, int tokens,
+                            cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* dout,
                                   float* delta, float* dkv_acc, int64_t rows, int D,
                                   int64_t acc_elems, cudaStream_t stream);

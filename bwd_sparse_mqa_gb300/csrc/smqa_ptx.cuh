@@ -345,6 +345,20 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// 2-D tensor store of one shared-memory box (tracked by this thread's bulk
+// async-groups), and the group commit / wait for it.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(m),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_group0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Gathers four rows (y0..y3) of a 2-D tensor, each one box row of width
 // box_x starting at column x, into four consecutive box rows at dst.
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, int x, int y0,
