@@ -222,6 +222,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the timings of the optional paths outside the step "
+                         "(deterministic-dKV backward, sink gradient)")
     ap.add_argument("--seq", type=int, default=None,
                     help="profiling only: override S = S_kv (the bench line then names the "
                          "smaller workload)")
@@ -325,42 +328,54 @@ def main():
     ms_step = elapsed_ms / args.steps
     value = world * (f_fwd + f_bwd) * args.steps / (elapsed_ms * 1e-3) / 1e12
 
-    # The sink gradient (an optional backward output the pages do not return,
-    # so not part of the step): its own kernel, timed alone on the step's
-    # Delta and LSE.
-    dsink = torch.empty((H,), dtype=torch.float32, device=dev)
-    for _ in range(3):
-        _lib.check("sink", lib.smqa_bwd_sink_grad(P(sink), P(lse), P(delta), shp, P(dsink), sp))
-    s0 = torch.cuda.Event(enable_timing=True)
-    s1 = torch.cuda.Event(enable_timing=True)
-    s0.record(stream)
-    for _ in range(20):
-        _lib.check("sink", lib.smqa_bwd_sink_grad(P(sink), P(lse), P(delta), shp, P(dsink), sp))
-    s1.record(stream)
-    torch.cuda.synchronize(dev)
-    t_sink = s0.elapsed_time(s1) / 20
+    def time_extras():
+        """The optional paths outside the step, each timed alone."""
+        # The sink gradient (an optional backward output the pages do not return,
+        # so not part of the step): its own kernel, timed alone on the step's
+        # Delta and LSE.
+        dsink = torch.empty((H,), dtype=torch.float32, device=dev)
 
-    # The deterministic-dKV backward (fixed-point integer accumulation; an
-    # option, not part of the step): the whole smqa_bwd call, timed alone.
-    det = _lib.FLAG_DETERMINISTIC_DKV
-    det_ws = torch.empty((int(lib.smqa_bwd_workspace_bytes(shp, det)),), dtype=torch.uint8,
-                         device=dev)
+        def sink_grad():
+            _lib.check("sink", lib.smqa_bwd_sink_grad(P(sink), P(lse), P(delta), shp, P(dsink),
+                                                      sp))
 
-    def det_bwd():
-        _lib.check("det", lib.smqa_bwd(P(q), P(kv), P(sink), P(o), P(dout), P(idx), P(lse), shp,
-                                       scale, P(dq), P(dkv), None, P(det_ws), det_ws.numel(), det,
-                                       sp))
+        for _ in range(3):
+            sink_grad()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(20):
+            sink_grad()
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        t_sink = s0.elapsed_time(s1) / 20
 
-    for _ in range(2):
-        det_bwd()
-    s0.record(stream)
-    for _ in range(5):
-        det_bwd()
-    s1.record(stream)
-    torch.cuda.synchronize(dev)
-    t_det = s0.elapsed_time(s1) / 5
-    if lib.smqa_device_status(1) != 0:
-        raise RuntimeError("device timeout in the deterministic backward")
+        # The deterministic-dKV backward (fixed-point integer accumulation; an
+        # option, not part of the step): the whole smqa_bwd call, timed alone.
+        det = _lib.FLAG_DETERMINISTIC_DKV
+        det_ws = torch.empty((int(lib.smqa_bwd_workspace_bytes(shp, det)),), dtype=torch.uint8,
+                             device=dev)
+
+        def det_bwd():
+            _lib.check("det", lib.smqa_bwd(P(q), P(kv), P(sink), P(o), P(dout), P(idx), P(lse),
+                                           shp, scale, P(dq), P(dkv), None, P(det_ws),
+                                           det_ws.numel(), det, sp))
+
+        for _ in range(2):
+            det_bwd()
+        s0.record(stream)
+        for _ in range(5):
+            det_bwd()
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        t_det = s0.elapsed_time(s1) / 5
+        if lib.smqa_device_status(1) != 0:
+            raise RuntimeError("device timeout in the deterministic backward")
+        return t_sink, t_det
+
+    t_sink = t_det = None
+    if not args.no_extras:
+        t_sink, t_det = time_extras()
 
     # end to end through the public API: pinned host inputs -> device, fwd,
     # bwd, results -> pinned host, every step
@@ -445,12 +460,14 @@ def main():
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
             "gpu_launches": 4 * args.steps,
-            "bwd_deterministic": {"ms": t_det, "vs_atomic_bwd": t_det / bwd_ms,
-                                  "note": "smqa_bwd with SMQA_FLAG_DETERMINISTIC_DKV, timed "
-                                          "alone (5 calls), not in the step"},
-            "sink_grad": {"ms": t_sink, "bytes": 8 * T * H + 8 * H,
-                          "gbs": (8 * T * H + 8 * H) / (t_sink * 1e-3) / 1e9,
-                          "note": "dsink kernel timed alone (20 launches), not in the step"},
+            "bwd_deterministic": None if t_det is None else {
+                "ms": t_det, "vs_atomic_bwd": t_det / bwd_ms,
+                "note": "smqa_bwd with SMQA_FLAG_DETERMINISTIC_DKV, timed alone (5 calls), "
+                        "not in the step"},
+            "sink_grad": None if t_sink is None else {
+                "ms": t_sink, "bytes": 8 * T * H + 8 * H,
+                "gbs": (8 * T * H + 8 * H) / (t_sink * 1e-3) / 1e9,
+                "note": "dsink kernel timed alone (20 launches), not in the step"},
             "clocks": clk.summary(),
         }
         if not args.no_cpu_baseline:

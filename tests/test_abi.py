@@ -56,7 +56,8 @@ def test_fwd_rejects_bad_shapes(lib):
 def test_fwd_rejects_null_misaligned_and_flags(lib):
     shp = _lib.Shape(1, 4, 4, 16, 64, 4)
     p = _fake()
-    assert lib.smqa_fwd(None, p, p, p, shp, 0.0, p, p, None, 0, 0, None) == _lib.SMQA_ERR_INVALID_ARG
+    assert lib.smqa_fwd(None, p, p, p, shp, 0.0, p, p, None, 0, 0, None) == \
+        _lib.SMQA_ERR_INVALID_ARG
     assert lib.smqa_fwd(_fake(0x10008), p, p, p, shp, 0.0, p, p, None, 0, 0, None) == \
         _lib.SMQA_ERR_INVALID_ARG
     assert lib.smqa_fwd(p, p, p, p, shp, 0.0, p, p, None, 0, 8, None) == _lib.SMQA_ERR_INVALID_ARG
