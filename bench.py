@@ -10,7 +10,10 @@ synthetic and seeded; q, o, dO and dq are 1 GiB each (larger than L2), kv
 (8 MiB) stays L2-resident as it would in the real workload.
 
 Metric: TFLOP/s of the step, FLOPs counted on valid slots only
-(4*H*D per valid slot forward, 10*H*D backward).
+(4*H*D per valid slot forward, 10*H*D backward).  `value` times the kernels
+on device-resident inputs; `e2e` times the host-buffer entry point
+(smqa_fwd_bwd_host: page-locked inputs in, results out, copies overlapped
+with the kernels in token chunks).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -36,7 +39,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from bwd_sparse_mqa_gb300 import _lib, inputs  # noqa: E402
-from bwd_sparse_mqa_gb300 import sparse_mqa_bwd_interface, sparse_mqa_fwd_interface  # noqa: E402
+from bwd_sparse_mqa_gb300 import sparse_mqa_fwd_bwd_host  # noqa: E402
 
 WORKLOAD = "h128_d512_k2048_s8192"
 METRIC = "sparse MQA fwd/bwd TFLOP/s + % BF16 roofline, 1×GB300, H=128 D=512 topk=2048"
@@ -387,19 +390,14 @@ def main():
             "dkv": torch.empty((B, S_kv, D), dtype=torch.bfloat16).pin_memory()}
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = sum(v.numel() * v.element_size() for v in outs.values())
-    ws = torch.empty((int(lib.smqa_bwd_workspace_bytes(shp, 0)),), dtype=torch.uint8, device=dev)
-    fws = torch.empty((max(int(lib.smqa_fwd_workspace_bytes(shp)), 1),), dtype=torch.uint8,
-                      device=dev)
+    ws = torch.empty((int(lib.smqa_fwd_bwd_host_workspace_bytes(shp, 0)),), dtype=torch.uint8,
+                     device=dev)
 
     def e2e_step():
-        g = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
-        oo, ll = sparse_mqa_fwd_interface(g["q"], g["kv"], g["sink"], g["idx"], workspace=fws)
-        gq, gkv = sparse_mqa_bwd_interface(g["q"], g["kv"], g["sink"], oo, g["do"], g["idx"], ll,
-                                           workspace=ws)
-        outs["o"].copy_(oo, non_blocking=True)
-        outs["lse"].copy_(ll, non_blocking=True)
-        outs["dq"].copy_(gq, non_blocking=True)
-        outs["dkv"].copy_(gkv, non_blocking=True)
+        # one call: chunked host->device copies, forward, backward and
+        # device->host copies, overlapped on the library's streams
+        sparse_mqa_fwd_bwd_host(host["q"], host["kv"], host["sink"], host["idx"], host["do"],
+                                device=dev, workspace=ws, out=outs, synchronize=False)
 
     e2e_value = None
     if args.e2e_steps > 0:

@@ -30,6 +30,8 @@ EXPORTS = [
     "smqa_bwd_postprocess", "smqa_device_status", "smqa_status_string", "smqa_last_error",
     "smqa_abi_version", "smqa_bwd_static_scratch", "smqa_bwd_exchange_bytes",
     "smqa_fwd_workspace_bytes", "smqa_fwd_static_scratch", "smqa_bwd_sink_grad",
+    "smqa_fwd_host_workspace_bytes", "smqa_fwd_bwd_host_workspace_bytes", "smqa_fwd_host",
+    "smqa_fwd_bwd_host",
 ]
 STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -70,6 +72,15 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.smqa_bwd_sink_grad.argtypes = [P, P, P, S, P, P]
     lib.smqa_bwd_sink_grad.restype = st
     lib.smqa_bwd_static_scratch.restype = st
+    lib.smqa_fwd_host_workspace_bytes.argtypes = [S]
+    lib.smqa_fwd_host_workspace_bytes.restype = ctypes.c_size_t
+    lib.smqa_fwd_bwd_host_workspace_bytes.argtypes = [S, U]
+    lib.smqa_fwd_bwd_host_workspace_bytes.restype = ctypes.c_size_t
+    lib.smqa_fwd_host.argtypes = [P, P, P, P, S, F, P, P, P, ctypes.c_size_t, U, P]
+    lib.smqa_fwd_host.restype = st
+    lib.smqa_fwd_bwd_host.argtypes = [P, P, P, P, P, S, F, P, P, P, P, P, P, ctypes.c_size_t, U,
+                                      P]
+    lib.smqa_fwd_bwd_host.restype = st
     lib.smqa_device_status.argtypes = [ctypes.c_int]
     lib.smqa_device_status.restype = st
     lib.smqa_status_string.argtypes = [st]

@@ -164,6 +164,140 @@ def sparse_mqa_bwd_interface(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch
     return (dq, dkv, dsink) if return_dsink else (dq, dkv)
 
 
+def _need_host(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cpu":
+        raise ValueError(f"{name} must be a CPU tensor (host buffer), got {t.device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _host_shape(q, kv, attn_sink, topk_idxs) -> _lib.Shape:
+    for t, name in ((q, "q"), (kv, "kv"), (topk_idxs, "topk_idxs")):
+        if not isinstance(t, torch.Tensor) or t.dim() != 3 + (name == "q"):
+            raise ValueError(f"{name} has the wrong rank")
+    B, S, H, D = q.shape
+    shp = _lib.Shape(B, S, kv.shape[1], H, D, topk_idxs.shape[2])
+    _need_host(q, "q", torch.bfloat16, (B, S, H, D))
+    _need_host(kv, "kv", torch.bfloat16, (B, shp.S_kv, D))
+    _need_host(attn_sink, "attn_sink", torch.float32, (H,))
+    _need_host(topk_idxs, "topk_idxs", torch.int32, (B, S, shp.topk))
+    return shp
+
+
+def _host_out(out: Optional[dict], name: str, dtype: torch.dtype, shape: tuple) -> torch.Tensor:
+    t = None if out is None else out.get(name)
+    if t is None:
+        return torch.empty(shape, dtype=dtype, pin_memory=True)
+    _need_host(t, f"out[{name!r}]", dtype, shape)
+    return t
+
+
+def _host_workspace(workspace: Optional[torch.Tensor], need: int,
+                    device: torch.device) -> torch.Tensor:
+    if need == 0:
+        raise ValueError("unsupported shape")
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8, 1)
+        if workspace.device != device:
+            raise ValueError(f"workspace must be on {device}")
+        if workspace.numel() >= need:
+            return workspace
+    return torch.empty((need,), dtype=torch.uint8, device=device)
+
+
+def fwd_host_workspace_bytes(shape: _lib.Shape) -> int:
+    return int(_lib.load().smqa_fwd_host_workspace_bytes(shape))
+
+
+def fwd_bwd_host_workspace_bytes(shape: _lib.Shape, return_dkv_accum_dtype: bool = False,
+                                 deterministic: bool = False) -> int:
+    flags = (_lib.FLAG_RETURN_DKV_FP32 if return_dkv_accum_dtype else 0) | \
+        (_lib.FLAG_DETERMINISTIC_DKV if deterministic else 0)
+    return int(_lib.load().smqa_fwd_bwd_host_workspace_bytes(shape, flags))
+
+
+def sparse_mqa_fwd_host(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor,
+                        topk_idxs: torch.Tensor, sm_scale: Optional[float] = None, *,
+                        device: Optional[torch.device] = None,
+                        workspace: Optional[torch.Tensor] = None,
+                        out: Optional[dict] = None, reference_rounding: bool = False,
+                        synchronize: bool = True) -> tuple[torch.Tensor, torch.Tensor]:
+    """The forward on HOST (CPU) tensors: copies in, kernels and copies out
+    run in token chunks that overlap (C ABI ``smqa_fwd_host``).
+
+    Inputs as for sparse_mqa_fwd_interface but CPU tensors (page-locked ones
+    let the copies overlap the kernels).  Returns CPU tensors O and LSE, taken
+    from ``out`` ({"o", "lse"}) when given, else freshly allocated page-locked.
+    ``device`` (default: the current CUDA device) runs the kernels;
+    ``workspace`` (uint8 CUDA tensor there) is reused when large enough.  The
+    work is queued on that device's current stream; with ``synchronize`` the
+    call waits for it, otherwise the results are complete once that stream is.
+    """
+    shp = _host_shape(q, kv, attn_sink, topk_idxs)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else \
+        torch.device(device)
+    lib = _lib.load()
+    ws = _host_workspace(workspace, int(lib.smqa_fwd_host_workspace_bytes(shp)), dev)
+    o = _host_out(out, "o", torch.bfloat16, tuple(q.shape))
+    lse = _host_out(out, "lse", torch.float32, (shp.B, shp.S, shp.H))
+    flags = _lib.FLAG_REFERENCE_ROUNDING if reference_rounding else 0
+    with torch.cuda.device(dev):
+        _lib.check("smqa_fwd_host", lib.smqa_fwd_host(
+            _ptr(q), _ptr(kv), _ptr(attn_sink), _ptr(topk_idxs), shp, _scale(sm_scale, shp.D),
+            _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), flags, _stream(dev)))
+        if synchronize:
+            torch.cuda.current_stream(dev).synchronize()
+    return o, lse
+
+
+def sparse_mqa_fwd_bwd_host(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor,
+                            topk_idxs: torch.Tensor, do: torch.Tensor,
+                            sm_scale: Optional[float] = None, *,
+                            device: Optional[torch.device] = None,
+                            workspace: Optional[torch.Tensor] = None,
+                            out: Optional[dict] = None, return_dsink: bool = False,
+                            return_dkv_accum_dtype: bool = False, deterministic: bool = False,
+                            reference_rounding: bool = False, synchronize: bool = True):
+    """Forward and backward on HOST (CPU) tensors with a known gradient ``do``
+    of O (C ABI ``smqa_fwd_bwd_host``): copies in, kernels and copies out run
+    in overlapping token chunks.
+
+    Returns CPU tensors (o, lse, dq, dkv) and, with ``return_dsink``, dsink,
+    taken from ``out`` ({"o", "lse", "dq", "dkv", "dsink"}) when given, else
+    freshly allocated page-locked.  Other arguments as in
+    sparse_mqa_fwd_host and sparse_mqa_bwd_interface.
+    """
+    shp = _host_shape(q, kv, attn_sink, topk_idxs)
+    _need_host(do, "do", torch.bfloat16, tuple(q.shape))
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else \
+        torch.device(device)
+    flags = (_lib.FLAG_RETURN_DKV_FP32 if return_dkv_accum_dtype else 0) | \
+        (_lib.FLAG_DETERMINISTIC_DKV if deterministic else 0) | \
+        (_lib.FLAG_REFERENCE_ROUNDING if reference_rounding else 0)
+    lib = _lib.load()
+    ws = _host_workspace(workspace, int(lib.smqa_fwd_bwd_host_workspace_bytes(shp, flags)), dev)
+    o = _host_out(out, "o", torch.bfloat16, tuple(q.shape))
+    lse = _host_out(out, "lse", torch.float32, (shp.B, shp.S, shp.H))
+    dq = _host_out(out, "dq", torch.bfloat16, tuple(q.shape))
+    dkv = _host_out(out, "dkv", torch.float32 if return_dkv_accum_dtype else torch.bfloat16,
+                    (shp.B, shp.S_kv, shp.D))
+    dsink = _host_out(out, "dsink", torch.float32, (shp.H,)) if return_dsink else None
+    with torch.cuda.device(dev):
+        _lib.check("smqa_fwd_bwd_host", lib.smqa_fwd_bwd_host(
+            _ptr(q), _ptr(kv), _ptr(attn_sink), _ptr(topk_idxs), _ptr(do), shp,
+            _scale(sm_scale, shp.D), _ptr(o), _ptr(lse), _ptr(dq), _ptr(dkv), _ptr(dsink),
+            _ptr(ws), ws.numel(), flags, _stream(dev)))
+        if synchronize:
+            torch.cuda.current_stream(dev).synchronize()
+    return (o, lse, dq, dkv, dsink) if return_dsink else (o, lse, dq, dkv)
+
+
 def device_status(clear: bool = True) -> int:
     """The device status word (0, or SMQA_ERR_DEVICE_TIMEOUT after a kernel's
     bounded wait ran out).  Synchronizes the device."""

@@ -121,11 +121,6 @@ smqa_status check_shape(const smqa_shape& s) {
   return SMQA_OK;
 }
 
-float effective_scale(float sm_scale, int D) {
-  if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return 1.0f / std::sqrt(static_cast<float>(D));
-  return sm_scale;
-}
-
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Exchange pool of the D = 512 forward and backward: slot flags, then the
@@ -191,7 +186,23 @@ smqa_status bwd_main_impl(const void* q, const void* kv, const void* dout, const
 
 namespace smqa {
 void set_last_error(const char* msg) { std::snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+
+smqa_status validate_shape(const smqa_shape& s) { return check_shape(s); }
+
+float effective_scale(float sm_scale, int D) {
+  if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return 1.0f / std::sqrt(static_cast<float>(D));
+  return sm_scale;
+}
+
+smqa_status bwd_main_launch(const void* q, const void* kv, const void* dout, const int32_t* idx,
+                            const float* lse, const float* delta, const smqa_shape& s,
+                            float scale, void* dq, float* acc, unsigned long long* acc_fixed,
+                            void* exch, cudaStream_t stream) {
+  return bwd_main_impl(q, kv, dout, idx, lse, delta, s, scale, dq, acc, exch, stream, acc_fixed);
+}
 }  // namespace smqa
+
+using smqa::effective_scale;
 
 extern "C" {
 

@@ -7,6 +7,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "sparse_mqa.h"
+
 namespace smqa {
 
 struct FwdParams {
@@ -79,5 +81,19 @@ cudaError_t launch_bwd_post_fixed(const unsigned long long* acc, void* out, int 
                                  int64_t elems, cudaStream_t stream);
 cudaError_t launch_bwd_postprocess(const float* acc, __nv_bfloat16* out, int64_t elems,
                                    cudaStream_t stream);
+
+// The backward's main kernel over the tokens of `s` (a whole call or a chunk
+// of one): writes dq and adds every slot's dKV contribution into `acc`
+// (fp32), or into `acc_fixed` (32.32 fixed point) when that is non-null.
+// `exch` is the exchange pool of smqa_bwd_exchange_bytes(s) bytes (D = 512).
+// The caller has checked shapes and pointers.
+smqa_status bwd_main_launch(const void* q, const void* kv, const void* dout, const int32_t* idx,
+                            const float* lse, const float* delta, const smqa_shape& s,
+                            float scale, void* dq, float* acc, unsigned long long* acc_fixed,
+                            void* exch, cudaStream_t stream);
+// The entry points' shape check (records the reason on failure).
+smqa_status validate_shape(const smqa_shape& s);
+// sm_scale as the entry points interpret it (<= 0 or NaN selects D^-1/2).
+float effective_scale(float sm_scale, int D);
 
 }  // namespace smqa

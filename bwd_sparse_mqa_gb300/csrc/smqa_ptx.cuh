@@ -1,6 +1,7 @@
 // smqa_ptx.cuh -- sm_103a building blocks written as inline PTX: mbarriers with
-// bounded waits, TMA tile / gather4 loads, tcgen05 (TMEM alloc, MMA, commit,
-// ld/st), shared-memory matrix descriptors and cluster (DSMEM) stores.
+// bounded waits, cp.async, TMA tile loads and stores, tcgen05 (TMEM alloc,
+// MMA, commit, ld/st), shared-memory matrix descriptors and cluster (DSMEM)
+// addressing.
 #pragma once
 
 #include <cstdint>
@@ -77,20 +78,6 @@ __device__ __forceinline__ bool mbar_probe(uint32_t bar, uint32_t parity) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Non-blocking test with cluster-scope acquire (for phases completed by
-// arrivals from another CTA of the cluster that publish its writes).
-__device__ __forceinline__ bool mbar_probe_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -207,16 +194,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Orders this thread's view of global memory (generic proxy) before its
-// later async-proxy (bulk copy) accesses of global memory.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // Cluster helpers
 // ---------------------------------------------------------------------------
@@ -233,16 +210,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t local, uint32_t rank) {
   return r;
 }
 
-// 16-byte global load cached in L2 only (never a stale L1 line), kept in
-// program order so that callers control how many are in flight.
-__device__ __forceinline__ uint4 ld_global_cg_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 // 32-bit load from another CTA's shared memory (`remote` from mapa).
 __device__ __forceinline__ int ld_shared_cluster_s32(uint32_t remote) {
   int v;
@@ -255,53 +222,11 @@ __device__ __forceinline__ void cluster_sync() {
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// 16-byte store into another CTA's shared memory that counts its bytes on
-// that CTA's barrier (`remote_bar`) when it lands.
-// 16-byte store into another CTA's shared memory that counts its bytes
-// toward that CTA's barrier `remote_bar` (complete_tx); the receiver posts the
-// expected byte count.
-__device__ __forceinline__ void st_async_v4u(uint32_t remote_addr, uint32_t a, uint32_t b,
-                                             uint32_t c, uint32_t d, uint32_t remote_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
-      "[%5];" ::"r"(remote_addr),
-      "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float a, float b, float c,
-                                            float d, uint32_t remote_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
-      "[%5];" ::"r"(remote_addr),
-      "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
-      : "memory");
-}
-
-// Plain 16-byte store into another CTA's shared memory (ordered for the peer
-// by a later release-arrive of the same thread).
-__device__ __forceinline__ void st_cluster_v4(uint32_t remote_addr, float a, float b, float c,
-                                              float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote_addr), "f"(a),
-               "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_v4u(uint32_t remote_addr, uint32_t a, uint32_t b,
-                                               uint32_t c, uint32_t d) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(remote_addr), "r"(a),
-               "r"(b), "r"(c), "r"(d)
-               : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // cp.async (16-byte global -> shared copies, L1 bypassed)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
 }
 // Arrive on `bar` once every cp.async this thread has issued so far has
 // landed (the arrival is counted in the barrier's expected count).
@@ -311,10 +236,6 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
 // Waits for every cp.async this thread started (committed or not).
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -334,17 +255,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
-// Contiguous bulk copy global -> shared (both 16-byte aligned, bytes a
-// multiple of 16), completing as transaction bytes on `bar`.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 // 2-D tensor store of one shared-memory box (tracked by this thread's bulk
 // async-groups), and the group commit / wait for it.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int x, int y) {
@@ -357,17 +267,6 @@ __device__ __forceinline__ void bulk_commit_group() {
 }
 __device__ __forceinline__ void bulk_wait_group0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-// Gathers four rows (y0..y3) of a 2-D tensor, each one box row of width
-// box_x starting at column x, into four consecutive box rows at dst.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, int x, int y0,
-                                            int y1, int y2, int y3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(m), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
-      : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -496,34 +395,6 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t taddr0, uint32_t taddr1, fl
   }
 }
 
-// 32 lanes x 16 / 8 consecutive fp32 columns (same mapping as tmem_ld32).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
-  uint32_t r[8];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 // 16 consecutive 32-bit columns from this thread's lane (warp-collective),
 // waiting until the stores have completed.
 __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
@@ -603,26 +474,10 @@ __device__ __forceinline__ float2 add_f16x2_f32(uint32_t a, uint32_t b) {
   return r;
 }
 
-__device__ __forceinline__ void ld_shared_v4u(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c,
-                                              uint32_t& d) {
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
-               : "r"(addr)
-               : "memory");
-}
-
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                "r"(d)
-               : "memory");
-}
-
-__device__ __forceinline__ void ld_shared_v4f(uint32_t addr, float& a, float& b, float& c,
-                                              float& d) {
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(a), "=f"(b), "=f"(c), "=f"(d)
-               : "r"(addr)
                : "memory");
 }
 

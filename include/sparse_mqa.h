@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define SMQA_ABI_VERSION 4
+#define SMQA_ABI_VERSION 5
 
 typedef enum {
     SMQA_OK = 0,
@@ -210,6 +210,64 @@ smqa_status smqa_bwd_static_scratch(const void* q, const void* kv, const float* 
                                     const void* o, const void* dout, const int32_t* topk_idxs,
                                     const float* lse, smqa_shape shape, float sm_scale, void* dq,
                                     void* dkv, float* dsink, unsigned flags, cudaStream_t stream);
+
+/*
+ * Forward, and forward + backward, on HOST buffers.  (The sparse MQA pages
+ * have no counterpart: the pages' interfaces take device tensors.)
+ *
+ * Every tensor argument below is HOST memory with the shape and dtype of
+ * smqa_fwd / smqa_bwd (page-locked memory lets the copies run asynchronously
+ * and overlap the kernels; pageable memory works but each copy then blocks
+ * the calling thread).  The call copies the inputs into `workspace` (DEVICE
+ * memory of the current device, 256-byte aligned, at least the size the
+ * matching *_workspace_bytes function returns), runs the kernels of smqa_fwd
+ * and smqa_bwd and copies the results back.  It works in token chunks (about
+ * eight per call, at least 256 tokens each, a chunk never splitting a token's
+ * rows) so that the copies of one chunk overlap the kernels of others: a
+ * host->device stream, the caller's `stream` for the forward, a backward
+ * stream and a device->host stream, ordered by events.  Every token's
+ * arithmetic is that of smqa_fwd / smqa_bwd, so o, lse, dq and dsink are
+ * bit-identical to theirs (dkv too with SMQA_FLAG_DETERMINISTIC_DKV).
+ *
+ * Ordering: the work starts after what is already queued on `stream`, and
+ * `stream` continues only after all of it (the host outputs are complete once
+ * `stream` is synchronized).  The three helper streams and their events are
+ * created by the first call on a device and shared by all calls on it (calls
+ * from several threads are serialised while they enqueue).  Inputs must stay
+ * unchanged and outputs untouched until `stream` has reached the call's end.
+ * A workspace must not be shared by calls that may overlap.
+ *
+ * Errors: arguments are checked before anything is queued (null or device
+ * pointers for host tensors, a workspace that is not device memory of the
+ * current device, a small workspace, bad flags, unsupported shapes); a
+ * failing CUDA call part-way returns SMQA_ERR_CUDA with the work queued so
+ * far left in place and `stream` still ordered after it.
+ *
+ * smqa_fwd_host      : q, kv, attn_sink, topk_idxs -> o, lse.
+ *                      flags: 0 or SMQA_FLAG_REFERENCE_ROUNDING.
+ * smqa_fwd_bwd_host  : the forward, then the backward with the given dout
+ *                      (the gradient of the loss w.r.t. o, known to the
+ *                      caller in advance: a fixed upstream gradient, a
+ *                      gradient check, a benchmark) -> o, lse, dq, dkv and,
+ *                      if dsink is non-NULL, dsink.  flags: any of
+ *                      SMQA_FLAG_REFERENCE_ROUNDING, SMQA_FLAG_RETURN_DKV_FP32,
+ *                      SMQA_FLAG_DETERMINISTIC_DKV.
+ * The *_workspace_bytes functions return 0 for an unsupported shape.  The
+ * workspace holds a device copy of every input and output plus the scratch
+ * of smqa_fwd and smqa_bwd (q, o: 2*B*S*H*D bytes each; forward + backward
+ * adds dout and dq of the same size and the dkv accumulator).
+ */
+size_t smqa_fwd_host_workspace_bytes(smqa_shape shape);
+size_t smqa_fwd_bwd_host_workspace_bytes(smqa_shape shape, unsigned flags);
+smqa_status smqa_fwd_host(const void* q, const void* kv, const float* attn_sink,
+                          const int32_t* topk_idxs, smqa_shape shape, float sm_scale, void* o,
+                          float* lse, void* workspace, size_t workspace_bytes, unsigned flags,
+                          cudaStream_t stream);
+smqa_status smqa_fwd_bwd_host(const void* q, const void* kv, const float* attn_sink,
+                              const int32_t* topk_idxs, const void* dout, smqa_shape shape,
+                              float sm_scale, void* o, float* lse, void* dq, void* dkv,
+                              float* dsink, void* workspace, size_t workspace_bytes,
+                              unsigned flags, cudaStream_t stream);
 
 /*
  * The backward stages one at a time (same arguments as smqa_bwd; used

@@ -32,7 +32,7 @@ def test_exports_match_header(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.smqa_abi_version() == 4
+    assert lib.smqa_abi_version() == 5
     assert lib.smqa_status_string(0) == b"SMQA_OK"
     assert lib.smqa_status_string(4) == b"SMQA_ERR_DEVICE_TIMEOUT"
     assert lib.smqa_status_string(99) == b"SMQA_ERR_UNKNOWN"
@@ -146,6 +146,71 @@ def test_fwd_exchange_pool_size_and_checks(lib):
     bad = _lib.Shape(1, 8, 16, 129, 512, 4)
     assert lib.smqa_fwd_static_scratch(p, p, p, p, bad, 0.0, p, p, 0, None) == \
         _lib.SMQA_ERR_UNSUPPORTED
+
+
+def _r256(x):
+    return (x + 255) // 256 * 256
+
+
+def test_host_entry_workspace_sizes_and_checks(lib):
+    """smqa_fwd_host / smqa_fwd_bwd_host: the workspace holds a device copy of
+    every input and output (each region 256-byte aligned) plus the exchange
+    pools; bad arguments are rejected before any CUDA call."""
+    B, S, S_kv, H, D, K = 2, 300, 200, 16, 512, 64
+    shp = _lib.Shape(B, S, S_kv, H, D, K)
+    rows, kvel = B * S * H, B * S_kv * D
+    fwd = (_r256(kvel * 2) + _r256(H * 4) + 2 * _r256(rows * D * 2) + _r256(B * S * K * 4) +
+           _r256(rows * 4) + _r256(lib.smqa_fwd_workspace_bytes(shp)))
+    assert lib.smqa_fwd_host_workspace_bytes(shp) == fwd
+    bwd_tail = (2 * _r256(rows * D * 2) + _r256(rows * 4) + _r256(H * 4) +
+                _r256(lib.smqa_bwd_exchange_bytes(shp)))
+    assert lib.smqa_fwd_bwd_host_workspace_bytes(shp, 0) == \
+        fwd + bwd_tail + _r256(kvel * 4) + _r256(kvel * 2)
+    # fp32 dkv: the accumulator is the result; deterministic: 8-byte accumulator
+    assert lib.smqa_fwd_bwd_host_workspace_bytes(shp, _lib.FLAG_RETURN_DKV_FP32) == \
+        fwd + bwd_tail + _r256(kvel * 4)
+    assert lib.smqa_fwd_bwd_host_workspace_bytes(shp, _lib.FLAG_DETERMINISTIC_DKV) == \
+        fwd + bwd_tail + _r256(kvel * 8) + _r256(kvel * 2)
+    assert lib.smqa_fwd_host_workspace_bytes(_lib.Shape(1, 8, 16, 129, 512, 4)) == 0
+    assert lib.smqa_fwd_bwd_host_workspace_bytes(_lib.Shape(1, 8, 16, 16, 100, 4), 0) == 0
+
+    p = _fake()
+    need = lib.smqa_fwd_bwd_host_workspace_bytes(shp, 0)
+    args = [p] * 5 + [shp, 0.0] + [p] * 5
+    assert lib.smqa_fwd_bwd_host(*args, p, need - 1, 0, None) == _lib.SMQA_ERR_UNSUPPORTED
+    assert b"workspace too small" in lib.smqa_last_error()
+    assert lib.smqa_fwd_bwd_host(*args, _fake(0x10010), need, 0, None) == \
+        _lib.SMQA_ERR_INVALID_ARG
+    assert lib.smqa_fwd_bwd_host(*args, p, need, 8, None) == _lib.SMQA_ERR_INVALID_ARG
+    no_dout = [p] * 4 + [None, shp, 0.0] + [p] * 5
+    assert lib.smqa_fwd_bwd_host(*no_dout, p, need, 0, None) == _lib.SMQA_ERR_INVALID_ARG
+    no_dkv = [p] * 5 + [shp, 0.0] + [p] * 3 + [None, p]
+    assert lib.smqa_fwd_bwd_host(*no_dkv, p, need, 0, None) == _lib.SMQA_ERR_INVALID_ARG
+    fneed = lib.smqa_fwd_host_workspace_bytes(shp)
+    fargs = [p] * 4 + [shp, 0.0, p, p]
+    assert lib.smqa_fwd_host(*fargs, p, fneed - 1, 0, None) == _lib.SMQA_ERR_UNSUPPORTED
+    assert lib.smqa_fwd_host(*fargs, None, fneed, 0, None) == _lib.SMQA_ERR_INVALID_ARG
+    # the backward's flags are not forward flags
+    assert lib.smqa_fwd_host(*fargs, p, fneed, _lib.FLAG_RETURN_DKV_FP32, None) == \
+        _lib.SMQA_ERR_INVALID_ARG
+    bad = _lib.Shape(1, 8, 16, 16, 100, 4)
+    assert lib.smqa_fwd_host(p, p, p, p, bad, 0.0, p, p, p, fneed, 0, None) == \
+        _lib.SMQA_ERR_UNSUPPORTED
+
+
+def test_host_interface_rejects_device_tensors():
+    import torch
+    from bwd_sparse_mqa_gb300 import sparse_mqa_fwd_bwd_host, sparse_mqa_fwd_host
+    q = torch.zeros(1, 4, 16, 64, dtype=torch.bfloat16)
+    kv = torch.zeros(1, 4, 64, dtype=torch.bfloat16)
+    sink = torch.zeros(16)
+    idx = torch.zeros(1, 4, 4, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CPU tensor"):
+        sparse_mqa_fwd_host(q.to("meta"), kv, sink, idx)
+    with pytest.raises(TypeError, match="int32"):
+        sparse_mqa_fwd_host(q, kv, sink, idx.long())
+    with pytest.raises(ValueError, match="shape"):
+        sparse_mqa_fwd_bwd_host(q, kv, sink, idx, q[:, :2].contiguous())
 
 
 def test_python_interface_rejects_cpu_tensors():
