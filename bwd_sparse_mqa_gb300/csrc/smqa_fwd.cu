@@ -155,19 +155,46 @@ __device__ __forceinline__ void gather_block(uint32_t stage, const __nv_bfloat16
   }
 }
 
+// max(a, b, c) in one instruction (the three-input form of sm_100 and later).
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// The largest of 64 values (ABS: of their magnitudes), as a tree of
+// three-input maxima (32 instructions instead of 63).
+template <bool ABS>
+__device__ __forceinline__ float max64(const float* x) {
+  float a[22];
+#pragma unroll
+  for (int j = 0; j < 21; ++j)
+    a[j] = ABS ? fmax3f(fabsf(x[3 * j]), fabsf(x[3 * j + 1]), fabsf(x[3 * j + 2]))
+               : fmax3f(x[3 * j], x[3 * j + 1], x[3 * j + 2]);
+  a[21] = ABS ? fabsf(x[63]) : x[63];
+  float b[8];
+#pragma unroll
+  for (int j = 0; j < 7; ++j) b[j] = fmax3f(a[3 * j], a[3 * j + 1], a[3 * j + 2]);
+  b[7] = a[21];
+  return fmax3f(fmax3f(b[0], b[1], b[2]), fmax3f(b[3], b[4], b[5]), fmaxf(b[6], b[7]));
+}
+
 // Block floating point of one head's 64 partial scores of a block, in the
 // exp2 domain (v = s1 x, x the raw partial, s1 the softmax scale): exponent
-// e = floor(log2(s1 max|x|)) (clamped to [-100, 100]); each value becomes
-// the integer n = rint(x * (s1 2^(14-e))) in [-32768, 32767] and stands for
-// n 2^(e-14).  n is stored offset by 32768 as an unsigned 16-bit field.
-// One fused multiply-add rounds: x * f + kRoundBias, with
-// kRoundBias = 1.5 * 2^23 + 32768, is exactly rounded to an integer whose
-// low 16 bits are n + 32768; the field is unpacked by placing it under the
-// exponent of 2^23.  Every step is exact or one IEEE rounding (explicit _rn
-// intrinsics), so the sender and the peer get the same value.
+// e = floor(log2(v_max (1 + 2^-15))) with v_max = s1 max|x| (clamped to
+// [-100, 100]); each value becomes the integer n = rint(x * (s1 2^(14-e)))
+// and stands for n 2^(e-14).  The factor 1 + 2^-15 keeps |x s1 2^(14-e)|
+// below 32767.5 (with every fp32 rounding of v_max counted), so |n| <= 32767
+// without a clamp; for 2^-100 <= v_max < 2^101 the absolute error of a value
+// is at most 2^-15 (1 + 2^-14) v_max.  n is stored offset by 32768 as an
+// unsigned 16-bit field.  One fused multiply-add rounds: x * f + kRoundBias,
+// with kRoundBias = 1.5 * 2^23 + 32768, is exactly rounded to an integer
+// whose low 16 bits are n + 32768; the field is unpacked by placing it under
+// the exponent of 2^23.  Every step is exact or one IEEE rounding (explicit
+// _rn intrinsics), so the sender and the peer get the same value.
 constexpr float kRoundBias = 12615680.f;        // 1.5 * 2^23 + 32768
-constexpr float kRoundMax = 12615680.f + 32767.f;
 constexpr float kUnpackBias = 8421376.f;         // 2^23 + 32768
+constexpr float kExpMargin = 1.000030517578125f;  // 1 + 2^-15
 
 __device__ __forceinline__ int bfp16_exponent(float vmax_abs) {
   const int e = static_cast<int>((__float_as_uint(vmax_abs) >> 23) & 0xffu) - 127;
@@ -179,7 +206,7 @@ __device__ __forceinline__ float pow2f(int k) {
 }
 // kRoundBias + n for the raw partial x (f = s1 2^(14-e)).
 __device__ __forceinline__ float bfp16_round(float x, float f) {
-  return fminf(__fmaf_rn(x, f, kRoundBias), kRoundMax);
+  return __fmaf_rn(x, f, kRoundBias);
 }
 // The value n 2^(e-14) of a rounded kRoundBias + n (inv = 2^(e-14)).
 __device__ __forceinline__ float bfp16_value(float r, float inv) {
@@ -434,10 +461,7 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
       float x[64];
       tmem_ld32x2(tile, tile + 32, *reinterpret_cast<float(*)[32]>(x),
                   *reinterpret_cast<float(*)[32]>(x + 32));
-      float mx = 0.f;
-#pragma unroll
-      for (int j = 0; j < 64; ++j) mx = fmaxf(mx, fabsf(x[j]));
-      const int ex = bfp16_exponent(__fmul_rn(mx, s1));
+      const int ex = bfp16_exponent(__fmul_rn(__fmul_rn(max64<true>(x), s1), kExpMargin));
       const float f = __fmul_rn(s1, pow2f(14 - ex)), inv = pow2f(ex - 14);
       uint32_t w[32];
 #pragma unroll
@@ -447,11 +471,6 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
         x[2 * k] = bfp16_value(r0, inv);
         x[2 * k + 1] = bfp16_value(r1, inv);
       }
-      // The tile now holds this CTA's partial as the peer will see it.
-      tmem_st32(tile, *reinterpret_cast<float(*)[32]>(x));
-      tmem_st32(tile + 32, *reinterpret_cast<float(*)[32]>(x + 32));
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarSRead + sb));
       // The peer has read block i - kXBufs from this buffer once its block
       // i - 1 has arrived here (it computed that block into the score tile
       // it freed after reading block i - kXBufs).
@@ -461,12 +480,18 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
                                                      (j / L::kXBufs) & 1, ctl));
         if (!ok) break;
       }
+      // The stores first, so that their way to L2 overlaps the write-back.
       uint8_t* buf = peer0 + static_cast<size_t>(xb) * L::kXchgBytes;
       uint4* dst = reinterpret_cast<uint4*>(buf) + h;
 #pragma unroll
       for (int c = 0; c < L::kPieces; ++c)
         dst[c * L::kHPad] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
       reinterpret_cast<int*>(buf + L::kXchgScaleOff)[h] = ex;
+      // The tile now gets this CTA's partial as the peer will see it.
+      tmem_st32(tile, *reinterpret_cast<float(*)[32]>(x));
+      tmem_st32(tile + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarSRead + sb));
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(peer_full + 8u * static_cast<uint32_t>(xb));
     }
@@ -554,18 +579,20 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
                   *reinterpret_cast<float(*)[32]>(x), *reinterpret_cast<float(*)[32]>(x + 32));
       tc_fence_before();
       mbar_arrive(bar(L::kBarSFree + sb));
+      // Scale (unless the tile already holds the exp2 argument), then mask
+      // (a block whose 64 slots are all valid has nothing to mask).
+      if (NSPLIT == 1 || p.ref_round) {
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const uint32_t bit = ((j < 32 ? msk0 : msk1) >> (j & 31)) & 1u;
-        x[j] = bit ? (x[j] * s1) * s2 : -INFINITY;
+        for (int j = 0; j < 64; ++j) x[j] = (x[j] * s1) * s2;
       }
-      float mq[8];
+      if ((msk0 & msk1) != 0xffffffffu) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        mq[j] = fmaxf(fmaxf(fmaxf(x[8 * j], x[8 * j + 1]), fmaxf(x[8 * j + 2], x[8 * j + 3])),
-                      fmaxf(fmaxf(x[8 * j + 4], x[8 * j + 5]), fmaxf(x[8 * j + 6], x[8 * j + 7])));
-      const float mloc = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])),
-                               fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
+        for (int j = 0; j < 64; ++j) {
+          const uint32_t bit = ((j < 32 ? msk0 : msk1) >> (j & 31)) & 1u;
+          x[j] = bit ? x[j] : -INFINITY;
+        }
+      }
+      const float mloc = max64<false>(x);
       const float m_new = fmaxf(m_run, mloc);
       const bool bump = (m_run == -INFINITY) ? (m_new != -INFINITY) : (m_new > m_run + 8.f);
       float alpha = 1.f;

@@ -117,7 +117,7 @@ size_t smqa_fwd_workspace_bytes(smqa_shape shape);
  * SMQA_FLAG_REFERENCE_ROUNDING, the sum then by log2(e)) and rounded to
  * block floating point: per head and 64-slot block, one power-of-two scale
  * and int16 mantissas, so each partial carries an absolute error of at most
- * 2^-15 of the largest partial magnitude of its head and block.
+ * 2^-15 (1 + 2^-14) of the largest partial magnitude of its head and block.
  */
 smqa_status smqa_fwd(const void* q, const void* kv, const float* attn_sink,
                      const int32_t* topk_idxs, smqa_shape shape, float sm_scale,
