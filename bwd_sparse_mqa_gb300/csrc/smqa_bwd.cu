@@ -223,8 +223,11 @@ __device__ __forceinline__ void load_own_partials(uint32_t t_s, uint32_t t_dp, f
     tmem_ld32x2(t_s + 32 * half, t_dp + 32 * half, xs, xp);
 #pragma unroll
     for (int w = 0; w < 16; ++w) {
-      hs[16 * half + w] = pack_f16x2_sat(xs[2 * w] * scale_log2, xs[2 * w + 1] * scale_log2);
-      hp[16 * half + w] = pack_f16x2_sat(xp[2 * w] * scale, xp[2 * w + 1] * scale);
+      const float2 a =
+          mul2(make_float2(xs[2 * w], xs[2 * w + 1]), make_float2(scale_log2, scale_log2));
+      const float2 d = mul2(make_float2(xp[2 * w], xp[2 * w + 1]), make_float2(scale, scale));
+      hs[16 * half + w] = pack_f16x2_sat(a.x, a.y);
+      hp[16 * half + w] = pack_f16x2_sat(d.x, d.y);
     }
   }
 }
@@ -621,16 +624,14 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
       uint32_t pp[4], pd[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        float pv[2], dv[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int jj = (8 * c + 2 * k + u) & 31;
-          const float pr = ((msk >> jj) & 1u) ? fast_exp2(zs[2 * k + u] - lse2) : 0.f;
-          pv[u] = pr;
-          dv[u] = pr * (zp[2 * k + u] - dlt_s);
-        }
-        pp[k] = pack_bf16x2(pv[0], pv[1]);
-        pd[k] = pack_bf16x2(dv[0], dv[1]);
+        const float2 e = add2(make_float2(zs[2 * k], zs[2 * k + 1]), make_float2(-lse2, -lse2));
+        const float2 g = add2(make_float2(zp[2 * k], zp[2 * k + 1]), make_float2(-dlt_s, -dlt_s));
+        const int jj = (8 * c + 2 * k) & 31;
+        const float2 pv = make_float2(((msk >> jj) & 1u) ? fast_exp2(e.x) : 0.f,
+                                      ((msk >> (jj + 1)) & 1u) ? fast_exp2(e.y) : 0.f);
+        const float2 dv = mul2(pv, g);
+        pp[k] = pack_bf16x2(pv.x, pv.y);
+        pd[k] = pack_bf16x2(dv.x, dv.y);
       }
       const uint32_t off = row128 + ((static_cast<uint32_t>(c) ^ static_cast<uint32_t>(h & 7)) << 4);
       st_shared_v4(base + L::kOffP + off, pp[0], pp[1], pp[2], pp[3]);

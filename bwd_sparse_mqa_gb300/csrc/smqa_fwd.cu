@@ -191,7 +191,7 @@ __device__ __forceinline__ float max64(const float* x) {
 // with kRoundBias = 1.5 * 2^23 + 32768, is exactly rounded to an integer
 // whose low 16 bits are n + 32768; the field is unpacked by placing it under
 // the exponent of 2^23.  Every step is exact or one IEEE rounding (explicit
-// _rn intrinsics), so the sender and the peer get the same value.
+// round-to-nearest operations), so the sender and the peer get the same value.
 constexpr float kRoundBias = 12615680.f;        // 1.5 * 2^23 + 32768
 constexpr float kUnpackBias = 8421376.f;         // 2^23 + 32768
 constexpr float kExpMargin = 1.000030517578125f;  // 1 + 2^-15
@@ -204,13 +204,13 @@ __device__ __forceinline__ int bfp16_exponent(float vmax_abs) {
 __device__ __forceinline__ float pow2f(int k) {
   return __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
 }
-// kRoundBias + n for the raw partial x (f = s1 2^(14-e)).
-__device__ __forceinline__ float bfp16_round(float x, float f) {
-  return __fmaf_rn(x, f, kRoundBias);
+// kRoundBias + n for two raw partials x (f = s1 2^(14-e)).
+__device__ __forceinline__ float2 bfp16_round2(float2 x, float f) {
+  return fma2(x, make_float2(f, f), make_float2(kRoundBias, kRoundBias));
 }
-// The value n 2^(e-14) of a rounded kRoundBias + n (inv = 2^(e-14)).
-__device__ __forceinline__ float bfp16_value(float r, float inv) {
-  return __fmaf_rn(r, inv, -kRoundBias * inv);
+// The values n 2^(e-14) of two rounded kRoundBias + n (inv = 2^(e-14)).
+__device__ __forceinline__ float2 bfp16_value2(float2 r, float inv) {
+  return fma2(r, make_float2(inv, inv), make_float2(-kRoundBias * inv, -kRoundBias * inv));
 }
 // Two rounded values -> two 16-bit fields (the first in the low half).
 __device__ __forceinline__ uint32_t bfp16_pack(float r_lo, float r_hi) {
@@ -220,7 +220,8 @@ __device__ __forceinline__ uint32_t bfp16_pack(float r_lo, float r_hi) {
 __device__ __forceinline__ float2 bfp16_unpack(uint32_t w, float inv) {
   const float lo = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7610));
   const float hi = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7632));
-  return make_float2(__fmaf_rn(lo, inv, -kUnpackBias * inv), __fmaf_rn(hi, inv, -kUnpackBias * inv));
+  return fma2(make_float2(lo, hi), make_float2(inv, inv),
+              make_float2(-kUnpackBias * inv, -kUnpackBias * inv));
 }
 
 template <int D, int NSPLIT>
@@ -466,10 +467,11 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
       uint32_t w[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
-        const float r0 = bfp16_round(x[2 * k], f), r1 = bfp16_round(x[2 * k + 1], f);
-        w[k] = bfp16_pack(r0, r1);
-        x[2 * k] = bfp16_value(r0, inv);
-        x[2 * k + 1] = bfp16_value(r1, inv);
+        const float2 r = bfp16_round2(make_float2(x[2 * k], x[2 * k + 1]), f);
+        w[k] = bfp16_pack(r.x, r.y);
+        const float2 v = bfp16_value2(r, inv);
+        x[2 * k] = v.x;
+        x[2 * k + 1] = v.y;
       }
       // The peer has read block i - kXBufs from this buffer once its block
       // i - 1 has arrived here (it computed that block into the score tile
@@ -536,8 +538,9 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
           for (int k = 0; k < 4; ++k) {
             const float2 pv = bfp16_unpack(ya[k], pinv);
             const int j = 8 * c + 2 * k;
-            x[j] = __fadd_rn(x[j], pv.x);
-            x[j + 1] = __fadd_rn(x[j + 1], pv.y);
+            const float2 sum = add2(make_float2(x[j], x[j + 1]), pv);
+            x[j] = sum.x;
+            x[j + 1] = sum.y;
           }
         }
         tmem_st32(tile + 32 * half, x);
@@ -602,6 +605,7 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
         m_run = m_new;
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      const float2 nm2 = make_float2(-m_use, -m_use);
       // P buffer i % 2 was last read by P.V of block i-2.
       if (i >= 2) {
         ok = __all_sync(0xffffffffu,
@@ -615,8 +619,9 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int w = 0; w < 16; ++w) {
-          const float p0 = fast_exp2(x[32 * half + 2 * w] - m_use);
-          const float p1 = fast_exp2(x[32 * half + 2 * w + 1] - m_use);
+          const float2 d = add2(make_float2(x[32 * half + 2 * w], x[32 * half + 2 * w + 1]), nm2);
+          const float p0 = fast_exp2(d.x);
+          const float p1 = fast_exp2(d.y);
           pk[w] = pack_bf16x2(p0, p1);
           rs[w & 3] += p0 + p1;  // fp32 probabilities: the LSE must not carry bf16 rounding
         }
@@ -676,7 +681,10 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
         for (int u = 0; u < 2; ++u) {
           uint32_t w[16];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(v[u][2 * k] * inv, v[u][2 * k + 1] * inv);
+          for (int k = 0; k < 16; ++k) {
+            const float2 y = mul2(make_float2(v[u][2 * k], v[u][2 * k + 1]), make_float2(inv, inv));
+            w[k] = pack_bf16x2(y.x, y.y);
+          }
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint32_t piece = static_cast<uint32_t>(4 * u + k);
