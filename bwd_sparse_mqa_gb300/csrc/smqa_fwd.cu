@@ -24,15 +24,16 @@
 //     form S = own + peer's from the same two rounded values, so the pair's
 //     probabilities and LSE are bit-identical.  Each CTA then runs the same
 //     online softmax and accumulates O_r += P.V_r.  The exchange slot (two
-//     receivers x four block buffers) is claimed from a pool by the pair's
+//     receivers x six block buffers) is claimed from a pool by the pair's
 //     rank 0 and released at exit.
 //   * Exchange flow control without a consumed-signal: a CTA frees score
 //     tile i % 3 only after its softmax has read the full scores of block i
 //     (formed after the peer's partial of block i was read), and it computes
 //     (and sends) block i + 3 only into a freed tile, so the arrival of the
-//     peer's block j + 3 proves that the peer has read block j; block j + 4
+//     peer's block j + 3 proves that the peer has read block j; block j + 6
 //     goes into the buffer of block j only after its own CTA has received
-//     block j + 3.
+//     block j + 3 (six buffers rather than the four this needs at least, so
+//     that a sender waits for the peer's block i - 3 rather than i - 1).
 //   * D = 64: one CTA per token, no exchange.
 //   * Warp roles (D = 512; for D = 64 the combiner and sender warps are
 //     absent): warps 8-10 gather this CTA's half of the kv rows with
@@ -66,7 +67,7 @@ struct FwdLayout {
   static constexpr int kChunks = kDC / 64;    // 64-column (128-byte) swizzle chunks per row
   static constexpr int kStages = 4;           // kv ring
   static constexpr int kSBufs = 3;            // score tiles in TMEM
-  static constexpr int kXBufs = kSBufs + 1;   // exchange buffers per receiver
+  static constexpr int kXBufs = kSBufs + 3;   // exchange buffers per receiver
   static constexpr uint32_t kQChunkBytes = kHPad * 128;
   static constexpr uint32_t kQBytes = kChunks * kQChunkBytes;
   static constexpr uint32_t kKvChunkBytes = kBI * 128;   // kBI rows x 128 B
@@ -474,10 +475,10 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
         x[2 * k + 1] = v.y;
       }
       // The peer has read block i - kXBufs from this buffer once its block
-      // i - 1 has arrived here (it computed that block into the score tile
-      // it freed after reading block i - kXBufs).
+      // i - kXBufs + kSBufs has arrived here (it computed that block into
+      // the score tile it freed after reading block i - kXBufs).
       if (i >= L::kXBufs) {
-        const int j = i - 1;
+        const int j = i - L::kXBufs + L::kSBufs;
         ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull + j % L::kXBufs),
                                                      (j / L::kXBufs) & 1, ctl));
         if (!ok) break;

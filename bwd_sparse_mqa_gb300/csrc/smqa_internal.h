@@ -56,10 +56,10 @@ struct BwdParams {
   int nslots;
 };
 
-// One exchange slot of the forward: two receivers x four block buffers x
+// One exchange slot of the forward: two receivers x six block buffers x
 // 16.5 KB (the partial scores of 128 heads x 64 slots as int16 mantissas
 // with one int32 power-of-two exponent per head).
-constexpr size_t kFwdSlotBytes = 2 * 4 * (16384 + 512);
+constexpr size_t kFwdSlotBytes = 2 * 6 * (16384 + 512);
 // One exchange slot of the backward: two receivers x two block parities x
 // 32 KB (the fp16 partial S and dP of 128 heads x 64 slots).
 constexpr size_t kBwdSlotBytes = 2 * 2 * 32768;

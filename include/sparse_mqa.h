@@ -86,7 +86,7 @@ typedef struct {
 
 /*
  * Bytes of device workspace smqa_fwd needs for `shape`: 0 when D = 64; for
- * D = 512 the exchange pool (4 KB of slot flags + 96 slots of 132 KB).  For
+ * D = 512 the exchange pool (4 KB of slot flags + 96 slots of 198 KB).  For
  * D = 512 each token is handled by a pair of CTAs that own one half of D
  * each; every 64-slot block they trade their partial scores through a slot
  * of this pool (it stays in L2).  The contents need no initialisation:

@@ -128,12 +128,12 @@ def test_bwd_exchange_pool_size_and_checks(lib):
 def test_fwd_exchange_pool_size_and_checks(lib):
     """D = 512: the forward's CTA pairs trade block-floating-point partial
     scores through an exchange pool (4 KB of slot flags + 96 slots of two
-    receivers x four buffers x 16.5 KB); D = 64 needs none.  smqa_fwd
+    receivers x six buffers x 16.5 KB); D = 64 needs none.  smqa_fwd
     rejects a pool that is too small, missing or misaligned before any GPU
     work, and the static-scratch entry rejects bad shapes the same way."""
     s512 = _lib.Shape(1, 8, 16, 16, 512, 4)
     ex = lib.smqa_fwd_workspace_bytes(s512)
-    assert ex == 4096 + 96 * 2 * 4 * (16384 + 512)
+    assert ex == 4096 + 96 * 2 * 6 * (16384 + 512)
     assert ex <= _lib.STATIC_SCRATCH_BYTES
     assert lib.smqa_fwd_workspace_bytes(_lib.Shape(1, 8, 16, 16, 64, 4)) == 0
     assert lib.smqa_fwd_workspace_bytes(_lib.Shape(1, 8, 16, 16, 100, 4)) == 0
