@@ -24,8 +24,11 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 // Chunking: about this many chunks per call, none below kMinChunkTokens
-// tokens (a chunk's kernels then still fill every SM several times).
-constexpr int64_t kTargetChunks = 8;
+// tokens (a chunk's kernels then still fill every SM).  More chunks shorten
+// the copies before the first kernel and after the last one; on the
+// H=128 D=512 topk=2048 S=8192 workload 8, 16 and 24 chunks measured 20.8,
+// 20.1 and 19.8 ms per forward + backward.
+constexpr int64_t kTargetChunks = 24;
 constexpr int64_t kMinChunkTokens = 256;
 
 size_t r256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }

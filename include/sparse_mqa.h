@@ -222,7 +222,7 @@ smqa_status smqa_bwd_static_scratch(const void* q, const void* kv, const float* 
  * memory of the current device, 256-byte aligned, at least the size the
  * matching *_workspace_bytes function returns), runs the kernels of smqa_fwd
  * and smqa_bwd and copies the results back.  It works in token chunks (about
- * eight per call, at least 256 tokens each, a chunk never splitting a token's
+ * 24 per call, at least 256 tokens each, a chunk never splitting a token's
  * rows) so that the copies of one chunk overlap the kernels of others: a
  * host->device stream, the caller's `stream` for the forward, a backward
  * stream and a device->host stream, ordered by events.  Every token's

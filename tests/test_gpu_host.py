@@ -11,8 +11,8 @@ import oracle
 from bwd_sparse_mqa_gb300 import (_lib, inputs, sparse_mqa_fwd_bwd_host, sparse_mqa_fwd_host)
 from tests import _parity as P
 
-# (B, S, S_kv, H, D, topk, recipe): chunk plans of about eight chunks of at
-# least 256 tokens --
+# (B, S, S_kv, H, D, topk, recipe): chunk plans of about 24 chunks of at
+# least 256 tokens (the minimum decides at these sizes) --
 #   1 x 1100 -> five pieces of S (220 tokens each);
 #   2 x 600  -> three pieces per batch element (kv and dKV offsets per b);
 #   3 x 100  -> whole batch elements, two per chunk and a remainder of one.
