@@ -31,7 +31,7 @@ EXPORTS = [
     "smqa_abi_version", "smqa_bwd_static_scratch", "smqa_bwd_exchange_bytes",
     "smqa_fwd_workspace_bytes", "smqa_fwd_static_scratch", "smqa_bwd_sink_grad",
     "smqa_fwd_host_workspace_bytes", "smqa_fwd_bwd_host_workspace_bytes", "smqa_fwd_host",
-    "smqa_fwd_bwd_host",
+    "smqa_fwd_bwd_host", "smqa_host_chunk_plan",
 ]
 STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -76,6 +76,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.smqa_fwd_host_workspace_bytes.restype = ctypes.c_size_t
     lib.smqa_fwd_bwd_host_workspace_bytes.argtypes = [S, U]
     lib.smqa_fwd_bwd_host_workspace_bytes.restype = ctypes.c_size_t
+    lib.smqa_host_chunk_plan.argtypes = [S, P, ctypes.c_int]
+    lib.smqa_host_chunk_plan.restype = ctypes.c_int
     lib.smqa_fwd_host.argtypes = [P, P, P, P, S, F, P, P, P, ctypes.c_size_t, U, P]
     lib.smqa_fwd_host.restype = st
     lib.smqa_fwd_bwd_host.argtypes = [P, P, P, P, P, S, F, P, P, P, P, P, P, ctypes.c_size_t, U,

@@ -23,8 +23,9 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-// Chunking: about this many chunks per call, none below kMinChunkTokens
-// tokens (a chunk's kernels then still fill every SM).  More chunks shorten
+// Chunking: at most about this many chunks per call, none below
+// kMinChunkTokens tokens except a last group of whole batch elements (a
+// chunk's kernels then still fill every SM).  More chunks shorten
 // the copies before the first kernel and after the last one; on the
 // H=128 D=512 topk=2048 S=8192 workload 8, 16 and 24 chunks measured 20.8,
 // 20.1 and 19.8 ms per forward + backward.
@@ -57,7 +58,7 @@ std::vector<Chunk> plan_chunks(const smqa_shape& s) {
   const int64_t t = std::max((total + kTargetChunks - 1) / kTargetChunks, kMinChunkTokens);
   std::vector<Chunk> out;
   if (s.S >= t) {
-    const int per = static_cast<int>((s.S + t - 1) / t);  // near-equal pieces of each S
+    const int per = static_cast<int>(s.S / t);  // near-equal pieces of each S, each >= t
     for (int b = 0; b < s.B; ++b)
       for (int i = 0; i < per; ++i) {
         const int a = static_cast<int>(static_cast<int64_t>(s.S) * i / per);
@@ -65,7 +66,9 @@ std::vector<Chunk> plan_chunks(const smqa_shape& s) {
         out.push_back({b, 1, a, e - a});
       }
   } else {
-    const int k = static_cast<int>(t / s.S);  // >= 1 whole batch elements per chunk
+    // Whole batch elements, k * S >= t tokens per chunk (the last chunk may
+    // hold fewer elements).
+    const int k = static_cast<int>((t + s.S - 1) / s.S);
     for (int b = 0; b < s.B; b += k) out.push_back({b, std::min(k, s.B - b), 0, s.S});
   }
   return out;
@@ -399,6 +402,19 @@ smqa_status run(const HostArgs& a, void* workspace, size_t workspace_bytes, cuda
 }  // namespace
 
 extern "C" {
+
+int smqa_host_chunk_plan(smqa_shape shape, int32_t* out, int max_chunks) {
+  if (smqa::validate_shape(shape) != SMQA_OK) return 0;
+  const std::vector<Chunk> ch = plan_chunks(shape);
+  const int n = static_cast<int>(ch.size());
+  for (int c = 0; out && c < n && c < max_chunks; ++c) {
+    out[4 * c] = ch[c].b0;
+    out[4 * c + 1] = ch[c].nb;
+    out[4 * c + 2] = ch[c].s0;
+    out[4 * c + 3] = ch[c].ns;
+  }
+  return n;
+}
 
 size_t smqa_fwd_host_workspace_bytes(smqa_shape shape) {
   if (smqa::validate_shape(shape) != SMQA_OK) return 0;

@@ -221,9 +221,10 @@ smqa_status smqa_bwd_static_scratch(const void* q, const void* kv, const float* 
  * the calling thread).  The call copies the inputs into `workspace` (DEVICE
  * memory of the current device, 256-byte aligned, at least the size the
  * matching *_workspace_bytes function returns), runs the kernels of smqa_fwd
- * and smqa_bwd and copies the results back.  It works in token chunks (about
- * 24 per call, at least 256 tokens each, a chunk never splitting a token's
- * rows) so that the copies of one chunk overlap the kernels of others: a
+ * and smqa_bwd and copies the results back.  It works in token chunks (at
+ * most about 24 per call, at least 256 tokens each except a last group of
+ * whole batch elements; see smqa_host_chunk_plan) so that the copies of one
+ * chunk overlap the kernels of others: a
  * host->device stream, the caller's `stream` for the forward, a backward
  * stream and a device->host stream, ordered by events.  Every token's
  * arithmetic is that of smqa_fwd / smqa_bwd, so o, lse, dq and dsink are
@@ -258,6 +259,14 @@ smqa_status smqa_bwd_static_scratch(const void* q, const void* kv, const float* 
  * adds dout and dq of the same size and the dkv accumulator).
  */
 size_t smqa_fwd_host_workspace_bytes(smqa_shape shape);
+
+/* The token chunks of smqa_fwd_host / smqa_fwd_bwd_host for `shape`, in the
+ * order they are processed: writes min(count, max_chunks) quadruples
+ * (b0, nb, s0, ns) -- batch elements [b0, b0 + nb) x positions [s0, s0 + ns),
+ * nb > 1 only with s0 = 0 and ns = S -- into `out` (4 int32 per chunk; may be
+ * NULL) and returns the number of chunks, or 0 for an unsupported shape.
+ * Host only: no CUDA call. */
+int smqa_host_chunk_plan(smqa_shape shape, int32_t* out, int max_chunks);
 size_t smqa_fwd_bwd_host_workspace_bytes(smqa_shape shape, unsigned flags);
 smqa_status smqa_fwd_host(const void* q, const void* kv, const float* attn_sink,
                           const int32_t* topk_idxs, smqa_shape shape, float sm_scale, void* o,

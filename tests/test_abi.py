@@ -243,3 +243,29 @@ def test_product_package_does_not_import_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "smqa_oracle" not in text, f
+
+
+@pytest.mark.parametrize("B,S", [(1, 1), (1, 255), (1, 256), (1, 1100), (1, 8192), (2, 600),
+                                 (3, 100), (7, 300), (64, 128), (1000, 3), (4, 32768),
+                                 (5, 257)])
+def test_host_chunk_plan_partitions_the_tokens(lib, B, S):
+    """The host entry's chunk plan covers every (b, s) exactly once, in
+    order, with contiguous tokens per chunk, at least 256 tokens per chunk
+    (except a last group of whole batch elements, or a smaller problem),
+    and at most about 24 chunks."""
+    shp = _lib.Shape(B, S, 64, 16, 64, 8)
+    n = lib.smqa_host_chunk_plan(shp, None, 0)
+    assert n >= 1
+    buf = (ctypes.c_int32 * (4 * n))()
+    assert lib.smqa_host_chunk_plan(shp, buf, n) == n
+    plan = [tuple(buf[4 * c:4 * c + 4]) for c in range(n)]
+    flat = []
+    for b0, nb, s0, ns in plan:
+        assert nb >= 1 and ns >= 1 and b0 + nb <= B and s0 + ns <= S
+        if nb > 1:
+            assert s0 == 0 and ns == S
+        flat.extend(range(b0 * S + s0, b0 * S + s0 + nb * ns))
+        assert nb * ns >= min(256, B * S) or (b0 + nb == B and s0 == 0 and ns == S)
+    assert flat == list(range(B * S))
+    assert n <= 25
+    assert lib.smqa_host_chunk_plan(_lib.Shape(B, S, 64, 16, 100, 8), None, 0) == 0

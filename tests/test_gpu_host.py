@@ -11,24 +11,34 @@ import oracle
 from bwd_sparse_mqa_gb300 import (_lib, inputs, sparse_mqa_fwd_bwd_host, sparse_mqa_fwd_host)
 from tests import _parity as P
 
-# (B, S, S_kv, H, D, topk, recipe): chunk plans of about 24 chunks of at
-# least 256 tokens (the minimum decides at these sizes) --
-#   1 x 1100 -> five pieces of S (220 tokens each);
-#   2 x 600  -> three pieces per batch element (kv and dKV offsets per b);
-#   3 x 100  -> whole batch elements, two per chunk and a remainder of one.
+# (B, S, S_kv, H, D, topk, recipe): chunks of at least 256 tokens (the
+# minimum decides at these sizes; smqa_host_chunk_plan gives the plan) --
+#   1 x 1100 -> four pieces of S (275 tokens each);
+#   2 x 600  -> two pieces per batch element (kv and dKV offsets per b);
+#   5 x 100  -> whole batch elements, three in a chunk and a last chunk of two.
 CASES = [(1, 1100, 500, 32, 512, 96, "causal_masked10"),
          (2, 600, 300, 128, 512, 64, "hot4096_masked10"),
-         (3, 100, 120, 32, 64, 64, "causal_uniform")]
+         (5, 100, 120, 32, 64, 64, "causal_uniform")]
 
 
 def _pinned(x: dict) -> dict:
     return {k: v.pin_memory() for k, v in x.items()}
 
 
+def _plan(shape) -> list:
+    lib = _lib.load()
+    n = lib.smqa_host_chunk_plan(shape, None, 0)
+    buf = (ctypes.c_int32 * (4 * n))()
+    lib.smqa_host_chunk_plan(shape, buf, n)
+    return [tuple(buf[4 * c:4 * c + 4]) for c in range(n)]
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c[:6])))
 def test_fwd_bwd_host_matches_device_path_and_oracle(case):
     B, S, S_kv, H, D, K, recipe = case
+    plan = _plan(_lib.Shape(B, S, S_kv, H, D, K))
+    assert len(plan) >= 2  # the case spans several chunks
     x = inputs.custom(B, S, S_kv, H, D, K, recipe=recipe, seed=21)
     h = _pinned(x)
     o, lse, dq, dkv, dsink = sparse_mqa_fwd_bwd_host(
