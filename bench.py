@@ -171,6 +171,22 @@ def cpu_baseline(x: dict, cfg, target_s: float = 15.0, max_tokens: int = 512):
                       f"{dt:.1f} s"}
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest of every rank's x (x itself without a process group); the
+    tensor lives on `device` (the GPU for NCCL, the CPU for gloo)."""
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, units_per_rank_step: float, steps: int, max_ms: float) -> float:
+    """Weak scaling: every rank processes the same units each step, so the
+    job's rate is all ranks' units over the slowest rank's time (per second)."""
+    return world * units_per_rank_step * steps / (max_ms * 1e-3)
+
+
 def reference_arm(args, rank: int):
     """--impl reference: the fp64 oracle timed on the host cores, each step a
     bounded token sample of the same workload."""
@@ -180,6 +196,11 @@ def reference_arm(args, rank: int):
 
     import oracle
     cfg = inputs.by_name(WORKLOAD)
+    workload = WORKLOAD
+    if args.seq:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, S=args.seq, S_kv=args.seq)
+        workload = f"{WORKLOAD} with S=S_kv={args.seq} (profiling size)"
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     x = inputs.make_inputs(cfg, device=dev)
     q, kv, sink, idx, dout = (x["q"].cpu(), x["kv"].cpu(), x["attn_sink"].cpu(),
@@ -206,7 +227,7 @@ def reference_arm(args, rank: int):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": WORKLOAD, "B": cfg.B, "S": cfg.S, "S_kv": cfg.S_kv,
+            "config": {"workload": workload, "B": cfg.B, "S": cfg.S, "S_kv": cfg.S_kv,
                        "H": cfg.H, "D": cfg.D, "topk": cfg.topk,
                        "sample_tokens_per_step": per_step},
             "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": oracle.num_threads(),
@@ -324,12 +345,9 @@ def main():
     t_pre = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     t_main = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
     t_post = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
     ms_step = elapsed_ms / args.steps
-    value = world * (f_fwd + f_bwd) * args.steps / (elapsed_ms * 1e-3) / 1e12
+    value = whole_job_rate(world, f_fwd + f_bwd, args.steps, elapsed_ms) / 1e12
 
     def time_extras():
         """The optional paths outside the step, each timed alone."""
@@ -417,14 +435,9 @@ def main():
                 e2e_step()
             e1.record(stream)
             torch.cuda.synchronize(dev)
-            w_ms = e0.elapsed_time(e1)
-            if dist is not None:
-                t = torch.tensor([w_ms], device=dev)
-                dist.all_reduce(t, op=dist.ReduceOp.MAX)
-                w_ms = float(t.item())
-            e2e_windows.append(w_ms)
+            e2e_windows.append(max_over_ranks(e0.elapsed_time(e1), dist, dev))
         e2e_ms = min(e2e_windows)
-        e2e_value = world * (f_fwd + f_bwd) * args.e2e_steps / (e2e_ms * 1e-3) / 1e12
+        e2e_value = whole_job_rate(world, f_fwd + f_bwd, args.e2e_steps, e2e_ms) / 1e12
 
     if rank == 0:
         pk, src = peaks()
@@ -461,7 +474,7 @@ def main():
                     "frac_tensor": f_bwd / (bwd_ms * 1e-3) / 1e12 / peak_tf,
                     "frac_roofline_slower_of":
                         max(f_bwd / (peak_tf * 1e12), bwd_bytes / (hbm * 1e9)) / (bwd_ms * 1e-3)},
-            "tokens_per_s": world * T * args.steps / (elapsed_ms * 1e-3),
+            "tokens_per_s": whole_job_rate(world, T, args.steps, elapsed_ms),
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                     "windows_ms": [round(w, 3) for w in e2e_windows],
