@@ -18,7 +18,7 @@
 //     them through an L2-resident exchange slot: each CTA scales its partial
 //     into the exp2 domain and sends it in block floating point (per head
 //     and block one power-of-two scale and 64 int16 mantissas, so the
-//     rounding error is below 2^-15 of the head's largest partial in the
+//     rounding error is about 2^-15 of the head's largest partial in the
 //     block: 16.5 KB per block instead of 32 KB of fp32, where fp16 would put
 //     up to ~2^-8 of a score's magnitude into a single-slot LSE).  Both CTAs
 //     form S = own + peer's from the same two rounded values, so the pair's
@@ -43,12 +43,18 @@
 //     block's valid-slot mask; warp 11 owns TMEM and issues the MMAs from
 //     one thread (partial scores into a ring of three 64-column TMEM tiles;
 //     P.V with P, bf16, from a two-buffer ring in TMEM as the A operand);
-//     warps 12-15 send each partial tile to the peer; warps 4-7 write the
-//     full scores (own + peer's) back into the tile; warps 0-3 (thread =
-//     head row = TMEM lane) run the masked online softmax in the exp2
-//     domain, rescale O lazily (only when the running max grows by more than
-//     2^8), write P as bf16 into TMEM for the P.V MMA and finish with the
-//     sink and the log2 LSE.
+//     warps 12-15 round each partial tile, store it to the peer's buffer
+//     and then write the rounded values back into the tile (the stores'
+//     way to L2 overlaps the write-back); warps 4-7 write the full scores
+//     (own + peer's) back into the tile; warps 0-3 (thread = head row =
+//     TMEM lane) run the masked online softmax in the exp2 domain (the mask
+//     only on blocks holding an invalid slot), rescale O lazily (only when
+//     the running max grows by more than 2^8), write P as bf16 into TMEM
+//     for the P.V MMA and finish with the sink and the log2 LSE.
+//   * Per-element arithmetic of these roles uses the packed two-lane fp32
+//     instructions (add/mul/fma.rn.f32x2) and three-input maxima, which
+//     halve their instruction counts; the roles' chain of latencies, not
+//     the tensor core, bounds a block's time.
 //   * Masked slots load a real (finite) row and get a -inf score, so their
 //     probability is exactly 0; blocks past a token's last valid slot are
 //     skipped.
