@@ -1,0 +1,107 @@
+"""A model check of the forward's exchange flow control (the D = 512 CTA pair
+in smqa_fwd.cu), run on the CPU.
+
+Two CTAs, each with three score tiles, a four-stage kv ring and X exchange
+buffers per receiver.  Per block i each CTA:
+  gather(i)   needs kv stage i % 4 free (P.V of block i - 4 done);
+  scores(i)   needs gather(i) and score tile i % 3 free (softmax read i - 3);
+  send(i)     needs scores(i) and, for i >= X, the peer's block i - X + 3 to
+              have arrived here; it writes block i into the peer's buffer
+              i % X, and the block arrives there some time later;
+  combine(i)  needs the peer's block i in buffer i % X (then consumes it)
+              and this CTA's send(i) (the rounded own partial);
+  softmax(i)  needs combine(i); frees score tile i % 3;
+  pv(i)       needs softmax(i); frees kv stage i % 4.
+Each role runs its blocks in order.  A random scheduler picks among the
+enabled steps (message deliveries included) until both CTAs finish.
+
+Checked: a send never overwrites a buffer block the peer has not consumed;
+every wait on a receive barrier (phase i // X of barrier i % X, tested by
+parity as mbarriers are) is never two or more phases behind the barrier,
+where a parity test would misread it; and the run never deadlocks.  X = 3
+must deadlock (each sender would wait for the peer's same block), which
+shows that the model can fail."""
+import random
+
+import pytest
+
+ROLES = ("gather", "scores", "send", "combine", "softmax", "pv")
+
+
+def run_model(X: int, nblk: int, seed: int, tiles: int = 3, stages: int = 4):
+    rng = random.Random(seed)
+    nxt = [{r: 0 for r in ROLES} for _ in range(2)]  # next block of each role
+    arrived = [set(), set()]        # blocks that have arrived in CTA c's buffers
+    in_flight = []                  # (dest CTA, block) messages not yet delivered
+    consumed = [set(), set()]       # blocks CTA c's combiner has consumed
+    phases = [[0] * X for _ in range(2)]  # completed phases of CTA c's receive barriers
+
+    def done(c, role, i):
+        return i < nxt[c][role]
+
+    def check_wait(c, blk):
+        # waiting for phase blk // X of barrier blk % X: the barrier must not
+        # have completed phase blk // X + 1 already
+        assert phases[c][blk % X] <= blk // X + 1, ("phase aliasing", c, blk)
+
+    def enabled(c):
+        out = []
+        i = nxt[c]["gather"]
+        if i < nblk and (i < stages or done(c, "pv", i - stages)):
+            out.append("gather")
+        i = nxt[c]["scores"]
+        if i < nblk and done(c, "gather", i) and (i < tiles or done(c, "softmax", i - tiles)):
+            out.append("scores")
+        i = nxt[c]["send"]
+        if i < nblk and done(c, "scores", i):
+            if i >= X:
+                j = i - X + tiles
+                check_wait(c, j)
+                if j in arrived[c]:
+                    out.append("send")
+            else:
+                out.append("send")
+        i = nxt[c]["combine"]
+        if i < nblk and done(c, "send", i):
+            check_wait(c, i)
+            if i in arrived[c]:
+                out.append("combine")
+        i = nxt[c]["softmax"]
+        if i < nblk and done(c, "combine", i):
+            out.append("softmax")
+        i = nxt[c]["pv"]
+        if i < nblk and done(c, "softmax", i):
+            out.append("pv")
+        return out
+
+    while any(nxt[c][r] < nblk for c in range(2) for r in ROLES):
+        choices = [(c, r) for c in range(2) for r in enabled(c)]
+        choices += [("deliver", k) for k in range(len(in_flight))]
+        if not choices:
+            return "deadlock"
+        c, r = rng.choice(choices)
+        if c == "deliver":
+            dest, blk = in_flight.pop(r)
+            arrived[dest].add(blk)
+            phases[dest][blk % X] += 1
+            continue
+        i = nxt[c][r]
+        if r == "send":
+            peer = 1 - c
+            if i >= X:  # the buffer's previous block must have been consumed
+                assert (i - X) in consumed[peer], ("overwrite", c, i)
+            in_flight.append((peer, i))
+        elif r == "combine":
+            consumed[c].add(i)
+        nxt[c][r] += 1
+    return "ok"
+
+
+@pytest.mark.parametrize("X", [4, 5, 6])
+@pytest.mark.parametrize("seed", range(40))
+def test_exchange_protocol_is_safe_and_live(X, seed):
+    assert run_model(X, nblk=24, seed=seed) == "ok"
+
+
+def test_three_buffers_deadlock():
+    assert all(run_model(3, nblk=12, seed=s) == "deadlock" for s in range(5))
