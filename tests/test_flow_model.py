@@ -1,5 +1,5 @@
-"""A model check of the forward's exchange flow control (the D = 512 CTA pair
-in smqa_fwd.cu), run on the CPU.
+"""Model checks of the exchange flow control of the D = 512 CTA pairs (the
+forward's in smqa_fwd.cu, the backward's in smqa_bwd.cu), run on the CPU.
 
 Two CTAs, each with three score tiles, a four-stage kv ring and X exchange
 buffers per receiver.  Per block i each CTA:
@@ -105,3 +105,106 @@ def test_exchange_protocol_is_safe_and_live(X, seed):
 
 def test_three_buffers_deadlock():
     assert all(run_model(3, nblk=12, seed=s) == "deadlock" for s in range(5))
+
+
+# ---------------------------------------------------------------------------
+# The backward pair (smqa_bwd.cu): one S/dP tile, a two-stage kv ring and
+# NB exchange buffers with an explicit consumed-signal (SendOk).
+#   gather(i)    needs kv stage i % 2 free (the gradient MMAs of i - 2 done);
+#   sdp(i)       needs gather(i) and the S/dP tile read by send_read(i - 1)
+#                and pds_read(i - 1);
+#   send_read(i) needs sdp(i);
+#   send(i)      needs send_read(i) and, for i >= NB, the peer's SendOk for
+#                block i - NB; writes buffer i % NB of the peer (in flight);
+#   pds_read(i)  needs sdp(i);
+#   pds(i)       needs pds_read(i), grad(i - 1) (single P/dS buffers) and the
+#                peer's block i; consumes it and, if i + NB < nblk, sends
+#                SendOk for buffer i % NB to the peer (in flight);
+#   grad(i)      needs pds(i) and drain(i - 1) (single dKV tile);
+#   drain(i)     needs grad(i).
+BWD_ROLES = ("gather", "sdp", "send_read", "send", "pds_read", "pds", "grad", "drain")
+
+
+def run_bwd_model(NB: int, nblk: int, seed: int):
+    rng = random.Random(seed)
+    nxt = [{r: 0 for r in BWD_ROLES} for _ in range(2)]
+    arrived = [set(), set()]
+    sendok = [set(), set()]        # consumed-signals received by CTA c (block numbers)
+    consumed = [set(), set()]
+    recv_ph = [[0] * NB for _ in range(2)]
+    ok_ph = [[0] * NB for _ in range(2)]
+    in_flight = []                 # (kind, dest, block)
+
+    def done(c, role, i):
+        return i < nxt[c][role]
+
+    def enabled(c):
+        out = []
+        n = nxt[c]
+        i = n["gather"]
+        if i < nblk and (i < 2 or done(c, "grad", i - 2)):
+            out.append("gather")
+        i = n["sdp"]
+        if i < nblk and done(c, "gather", i) and (
+                i == 0 or (done(c, "send_read", i - 1) and done(c, "pds_read", i - 1))):
+            out.append("sdp")
+        i = n["send_read"]
+        if i < nblk and done(c, "sdp", i):
+            out.append("send_read")
+        i = n["send"]
+        if i < nblk and done(c, "send_read", i):
+            if i >= NB:
+                assert ok_ph[c][i % NB] <= (i // NB - 1) + 1, ("sendok aliasing", c, i)
+                if (i - NB) in sendok[c]:
+                    out.append("send")
+            else:
+                out.append("send")
+        i = n["pds_read"]
+        if i < nblk and done(c, "sdp", i):
+            out.append("pds_read")
+        i = n["pds"]
+        if i < nblk and done(c, "pds_read", i) and (i == 0 or done(c, "grad", i - 1)):
+            assert recv_ph[c][i % NB] <= i // NB + 1, ("recv aliasing", c, i)
+            if i in arrived[c]:
+                out.append("pds")
+        i = n["grad"]
+        if i < nblk and done(c, "pds", i) and (i == 0 or done(c, "drain", i - 1)):
+            out.append("grad")
+        i = n["drain"]
+        if i < nblk and done(c, "grad", i):
+            out.append("drain")
+        return out
+
+    while any(nxt[c][r] < nblk for c in range(2) for r in BWD_ROLES):
+        choices = [(c, r) for c in range(2) for r in enabled(c)]
+        choices += [("deliver", k) for k in range(len(in_flight))]
+        if not choices:
+            return "deadlock"
+        c, r = rng.choice(choices)
+        if c == "deliver":
+            kind, dest, blk = in_flight.pop(r)
+            if kind == "data":
+                arrived[dest].add(blk)
+                recv_ph[dest][blk % NB] += 1
+            else:
+                sendok[dest].add(blk)
+                ok_ph[dest][blk % NB] += 1
+            continue
+        i = nxt[c][r]
+        peer = 1 - c
+        if r == "send":
+            if i >= NB:
+                assert (i - NB) in consumed[peer], ("overwrite", c, i)
+            in_flight.append(("data", peer, i))
+        elif r == "pds":
+            consumed[c].add(i)
+            if i + NB < nblk:
+                in_flight.append(("ok", peer, i))
+        nxt[c][r] += 1
+    return "ok"
+
+
+@pytest.mark.parametrize("NB", [2, 3, 4])
+@pytest.mark.parametrize("seed", range(40))
+def test_backward_exchange_protocol_is_safe_and_live(NB, seed):
+    assert run_bwd_model(NB, nblk=24, seed=seed) == "ok"
