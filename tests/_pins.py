@@ -316,6 +316,47 @@ def pin_bf16_entry_matches_f64(lib):
         assert np.allclose(a, b, rtol=1e-14, atol=1e-15), "bf16 bwd entry differs from fp64"
 
 
+def pin_linear_in_dout(lib):
+    """The backward is linear in dO: scaling dO by a power of two scales dQ,
+    dKV, dsink and Delta by that power (fp64 rounding commutes with it), so
+    the oracle has no absolute floor or offset at small or large gradient
+    magnitudes."""
+    rng = np.random.default_rng(23)
+    q, kv, sink, idx, dout = _tiny(rng, B=2, S=3, S_kv=6, H=3, D=5, topk=4)
+    base = oracle.bwd_f64(q, kv, sink, idx, dout, lib=lib)
+    for alpha in (2.0 ** -30, 2.0 ** -20, 2.0 ** 10):
+        got = oracle.bwd_f64(q, kv, sink, idx, dout * alpha, lib=lib)
+        # dQ and Delta are per-token sums in a fixed order: exact.  dKV and
+        # dsink are summed over tokens with OpenMP atomics in a varying order,
+        # so they agree to a few fp64 roundings.
+        for name, a, b in zip(("dq", "delta"), (got[0], got[3]), (base[0], base[3])):
+            assert np.array_equal(a, b * alpha), f"{name} not linear in dO at {alpha}"
+        for name, a, b in zip(("dkv", "dsink"), got[1:3], base[1:3]):
+            _close(a / alpha, b, rtol=1e-12, atol=1e-14 * float(np.max(np.abs(b))),
+                   what=f"{name} linear in dO at {alpha}")
+    # And it is really a function of dO: a different dO changes dQ.
+    other = oracle.bwd_f64(q, kv, sink, idx, dout[::-1].copy(), lib=lib)
+    assert not np.allclose(other[0], base[0]), "dQ does not depend on dO"
+
+
+def pin_query_scale_equals_sm_scale(lib):
+    """Scaling q by a power of two is the same as scaling sm_scale by it:
+    the logits c*q.k are equal, so O and LSE agree exactly, dKV agrees
+    exactly (c*g*(a q) = (a c)*g*q), and dQ(q, a c) = a dQ(a q, c)."""
+    rng = np.random.default_rng(24)
+    q, kv, sink, idx, dout = _tiny(rng, B=1, S=4, S_kv=6, H=2, D=4, topk=5)
+    c, a = 0.37, 8.0
+    o1, l1 = oracle.fwd_f64(q * a, kv, sink, idx, c, lib=lib)
+    o2, l2 = oracle.fwd_f64(q, kv, sink, idx, c * a, lib=lib)
+    _close(o1, o2, rtol=1e-13, atol=1e-15, what="O under q scaling")
+    _close(l1, l2, rtol=1e-13, atol=1e-15, what="LSE under q scaling")
+    dq1, dkv1, ds1, _ = oracle.bwd_f64(q * a, kv, sink, idx, dout, c, lib=lib)
+    dq2, dkv2, ds2, _ = oracle.bwd_f64(q, kv, sink, idx, dout, c * a, lib=lib)
+    _close(dq2, a * dq1, rtol=1e-12, atol=1e-14, what="dQ under q scaling")
+    _close(dkv1, dkv2, rtol=1e-12, atol=1e-14, what="dKV under q scaling")
+    _close(ds1, ds2, rtol=1e-12, atol=1e-14, what="dsink under q scaling")
+
+
 ALL_PINS = [
     pin_dense_sdpa_fwd,
     pin_dense_autograd_bwd,
@@ -329,4 +370,6 @@ ALL_PINS = [
     pin_token_subset_linearity,
     pin_duplicate_slot,
     pin_bf16_entry_matches_f64,
+    pin_linear_in_dout,
+    pin_query_scale_equals_sm_scale,
 ]

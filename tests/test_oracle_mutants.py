@@ -33,6 +33,8 @@ MUTANTS = [
      "dkv + ((size_t)b * S_kv + (size_t)idx_row[j]) * D",
      "dkv + ((size_t)b * S_kv + (size_t)j) * D"),
     ("dsink sign flipped", "dsink[h] += -psink * Delta;", "dsink[h] += psink * Delta;"),
+    ("absolute floor on dP - Delta", "g[j] = p[j] * (dP - Delta);",
+     "g[j] = fabs(dP - Delta) < 1e-7 ? 0.0 : p[j] * (dP - Delta);"),
 ]
 
 
