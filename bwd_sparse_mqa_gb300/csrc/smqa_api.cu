@@ -139,7 +139,8 @@ size_t fwd_exchange_bytes(const smqa_shape& s) {
 smqa_status bwd_main_impl(const void* q, const void* kv, const void* dout, const int32_t* idx,
                           const float* lse, const float* delta, const smqa_shape& s, float scale,
                           void* dq, float* acc, void* exch, cudaStream_t stream,
-                          unsigned long long* acc_fixed = nullptr) {
+                          unsigned long long* acc_fixed = nullptr,
+                          const int* fix_shift = nullptr) {
   cudaError_t e;
   int* st = status_ptr(&e);
   if (!st) return cuda_fail(e, "status word");
@@ -162,6 +163,7 @@ smqa_status bwd_main_impl(const void* q, const void* kv, const void* dout, const
   p.dq = static_cast<__nv_bfloat16*>(dq);
   p.dkv_acc = acc;
   p.dkv_fix = acc_fixed;
+  p.fix_shift = fix_shift;
   p.det = acc_fixed != nullptr ? 1 : 0;
   p.S = s.S;
   p.S_kv = s.S_kv;
@@ -197,8 +199,9 @@ float effective_scale(float sm_scale, int D) {
 smqa_status bwd_main_launch(const void* q, const void* kv, const void* dout, const int32_t* idx,
                             const float* lse, const float* delta, const smqa_shape& s,
                             float scale, void* dq, float* acc, unsigned long long* acc_fixed,
-                            void* exch, cudaStream_t stream) {
-  return bwd_main_impl(q, kv, dout, idx, lse, delta, s, scale, dq, acc, exch, stream, acc_fixed);
+                            const int* fix_shift, void* exch, cudaStream_t stream) {
+  return bwd_main_impl(q, kv, dout, idx, lse, delta, s, scale, dq, acc, exch, stream, acc_fixed,
+                       fix_shift);
 }
 }  // namespace smqa
 
@@ -291,7 +294,7 @@ size_t smqa_bwd_workspace_bytes(smqa_shape shape, unsigned flags) {
   size_t bytes = 0;
   const size_t elems = static_cast<size_t>(shape.B) * shape.S_kv * shape.D;
   if (flags & SMQA_FLAG_DETERMINISTIC_DKV)
-    bytes += round256(elems * sizeof(unsigned long long));  // 32.32 fixed-point accumulator
+    bytes += smqa::det_region_bytes(shape);  // fixed-point accumulator, statistics, row counts
   else if (!(flags & SMQA_FLAG_RETURN_DKV_FP32))
     bytes += round256(elems * sizeof(float));
   bytes += round256(static_cast<size_t>(shape.B) * shape.S * shape.H * sizeof(float));
@@ -401,19 +404,31 @@ smqa_status smqa_bwd(const void* q, const void* kv, const float* attn_sink, cons
   float* acc = (fp32_out && !det) ? static_cast<float*>(dkv) : reinterpret_cast<float*>(ws);
   unsigned long long* acc_fixed = det ? reinterpret_cast<unsigned long long*>(ws) : nullptr;
   const size_t acc_bytes =
-      det ? round256(static_cast<size_t>(elems) * sizeof(unsigned long long))
+      det ? smqa::det_region_bytes(shape)
           : (fp32_out ? 0 : round256(static_cast<size_t>(elems) * sizeof(float)));
   float* delta = reinterpret_cast<float*>(ws + acc_bytes);
   void* exch = ws + acc_bytes +
                round256(static_cast<size_t>(shape.B) * shape.S * shape.H * sizeof(float));
+  const float scale = effective_scale(sm_scale, shape.D);
   smqa_status r;
+  uint32_t* stats = nullptr;
   if (det) {
-    // Delta, and the fixed-point accumulator zeroed (two floats' worth of
-    // zero bits per element).
-    const cudaError_t e = smqa::launch_bwd_preprocess(
+    // Delta, and the whole fixed-point region zeroed (accumulator,
+    // statistics and row counts); then the statistics and the binary point.
+    stats = reinterpret_cast<uint32_t*>(ws + smqa::det_stats_offset(shape));
+    uint32_t* counts = stats + smqa::kDetStatsBytes / sizeof(uint32_t);
+    cudaError_t e = smqa::launch_bwd_preprocess(
         static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), delta,
-        acc, static_cast<int64_t>(shape.B) * shape.S * shape.H, shape.D, 2 * elems, stream);
+        acc, static_cast<int64_t>(shape.B) * shape.S * shape.H, shape.D,
+        static_cast<int64_t>(acc_bytes / sizeof(float)), stream);
     if (e != cudaSuccess) return cuda_fail(e, "bwd preprocess launch");
+    e = smqa::launch_bwd_det_stats(static_cast<const __nv_bfloat16*>(q),
+                                   static_cast<const __nv_bfloat16*>(kv),
+                                   static_cast<const __nv_bfloat16*>(dout), delta, topk_idxs,
+                                   shape, stats, counts, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "bwd statistics launch");
+    e = smqa::launch_bwd_det_scale(shape, scale, stats, counts, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "bwd scale launch");
   } else {
     r = smqa_bwd_preprocess(o, dout, shape, delta, acc, stream);
     if (r != SMQA_OK) return r;
@@ -422,11 +437,13 @@ smqa_status smqa_bwd(const void* q, const void* kv, const float* attn_sink, cons
     r = smqa_bwd_sink_grad(attn_sink, lse, delta, shape, dsink, stream);
     if (r != SMQA_OK) return r;
   }
-  r = bwd_main_impl(q, kv, dout, topk_idxs, lse, delta, shape, effective_scale(sm_scale, shape.D),
-                    dq, acc, exch, stream, acc_fixed);
+  const int* shift = det ? reinterpret_cast<const int*>(stats + smqa::kDetShift) : nullptr;
+  r = bwd_main_impl(q, kv, dout, topk_idxs, lse, delta, shape, scale, dq, acc, exch, stream,
+                    acc_fixed, shift);
   if (r != SMQA_OK) return r;
   if (det) {
-    const cudaError_t e = smqa::launch_bwd_post_fixed(acc_fixed, dkv, fp32_out ? 1 : 0, elems, stream);
+    const cudaError_t e =
+        smqa::launch_bwd_post_fixed(acc_fixed, dkv, fp32_out ? 1 : 0, elems, shift, stream);
     if (e != cudaSuccess) return cuda_fail(e, "bwd postprocess launch");
     return SMQA_OK;
   }

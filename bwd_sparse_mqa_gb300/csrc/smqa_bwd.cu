@@ -14,15 +14,19 @@
 //   preprocess   Delta[t,h] in fp32 (one warp per row) and zeroing of the
 //                fp32 dKV accumulator, fused into one launch;
 //   main         per token (a CTA pair for D = 512, each CTA owning half of
-//                D): S = Q.K^T and dP = dO.V^T on the tensor core, partial
-//                sums exchanged with the peer CTA through DSMEM, P and dS on
-//                CUDA cores, then dQ += dS.K accumulated in TMEM over all
+//                D): S = Q.K^T and dP = dO.V^T on the tensor core over 64-slot
+//                blocks, the pair's half-D partial sums traded in block
+//                floating point through an L2-resident exchange slot (two
+//                buffers per receiver, freed by a consumed-signal), P and dS
+//                on CUDA cores, then dQ += dS.K accumulated in TMEM over all
 //                blocks and dKV^T = Q^T.dS + dO^T.P per block, which a drain
 //                warpgroup reads from TMEM and scatters with fp32
 //                red.global.add into the accumulator;
 //   postprocess  fp32 accumulator -> bf16 (round to nearest even).
-// dKV^T (lanes = head-dim rows, columns = slots) keeps M = 128 for 32-slot
-// blocks and lets each warp's 32 lanes add to 32 consecutive floats of a row.
+// dKV^T (lanes = head-dim rows, columns = slots) keeps M = 128 for the
+// 64-slot blocks and lets each warp's 32 lanes add to 32 consecutive floats
+// of a kv row.  A deterministic mode replaces the fp32 reductions by 64-bit
+// fixed-point integer ones with a per-call binary point (below).
 #include <cuda_runtime.h>
 
 #include "smqa_internal.h"
@@ -86,21 +90,163 @@ __global__ void __launch_bounds__(256)
 }
 
 // --------------------------------------------------------------------------
-// postprocess of the deterministic mode: 32.32 fixed point -> bf16 or fp32
+// deterministic mode: statistics, binary point, postprocess
 // --------------------------------------------------------------------------
+// Every dKV contribution is added as a signed 64-bit fixed-point integer
+// (value * 2^k rounded to nearest), and integer addition is associative, so
+// the sum does not depend on the order of the atomics.  The binary point k
+// is chosen per call from a bound on the contributions: one slot's
+// contribution to dKV[r, d] (the sum over the H heads of the MMA) is
+//   sum_h dS'_h q_h[d] + P_h dO_h[d],   dS'_h = P_h c (dP_h - Delta_h),
+// with P_h <= 1, |dP_h| <= |dO_h| |kv_r| (Cauchy-Schwarz), so its magnitude
+// is at most X = H (max|dO| + c (max|dO_h| max|kv_r| + max|Delta|) max|q|),
+// and an element's sum is at most n X, n the most slots naming one kv row.
+// k = 61 - ceil(log2(n X)) keeps every contribution and every sum below
+// 2^61 (room for the fp32 roundings of the MMA and of the statistics); the
+// resolution 2^-k is then at most n X 2^-60, relative to the bound, at any
+// input scale.  All statistics are maxima or integer counts, so k itself is
+// the same from run to run.
+__device__ __forceinline__ void atomic_max_nonneg(uint32_t* w, float v) {
+  // Non-negative floats order as their bit patterns.
+  atomicMax(w, __float_as_uint(v));
+}
+
+__global__ void __launch_bounds__(256)
+    smqa_bwd_det_stats_kernel(const __nv_bfloat16* __restrict__ q,
+                              const __nv_bfloat16* __restrict__ kv,
+                              const __nv_bfloat16* __restrict__ dout,
+                              const float* __restrict__ delta, const int32_t* __restrict__ idx,
+                              int64_t rows, int64_t kv_rows, int D, int S, int S_kv, int topk,
+                              uint32_t* __restrict__ stats, uint32_t* __restrict__ counts) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  float m_do = 0.f, m_dosq = 0.f, m_kvsq = 0.f, m_q = 0.f, m_dl = 0.f;
+  // Squared norm (warp-wide, in a fixed order) and largest magnitude of row r.
+  auto row_stats = [&](const __nv_bfloat16* base, int64_t r, float& sq, float& mx) {
+    const uint4* pr = reinterpret_cast<const uint4*>(base + r * D);
+    float s = 0.f, m = 0.f;
+    for (int v = lane; v < D / 8; v += 32) {
+      const uint4 a = __ldg(pr + v);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __bfloat1622float2(a2[k]);
+        s = fmaf(f.x, f.x, s);
+        s = fmaf(f.y, f.y, s);
+        m = fmax3f(m, fabsf(f.x), fabsf(f.y));
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    sq = s;
+    mx = m;
+  };
+  for (int64_t r = warp_id; r < rows; r += nwarps) {
+    float sq, mx;
+    row_stats(dout, r, sq, mx);
+    m_dosq = fmaxf(m_dosq, sq);
+    m_do = fmaxf(m_do, mx);
+    row_stats(q, r, sq, mx);
+    m_q = fmaxf(m_q, mx);
+  }
+  for (int64_t r = warp_id; r < kv_rows; r += nwarps) {
+    float sq, mx;
+    row_stats(kv, r, sq, mx);
+    m_kvsq = fmaxf(m_kvsq, sq);
+  }
+  for (int64_t i = tid; i < rows; i += nthr) m_dl = fmaxf(m_dl, fabsf(__ldg(delta + i)));
+  // Reference counts: slot i of token t = i / topk names row idx[i] of batch
+  // element t / S.
+  const int64_t per_b = static_cast<int64_t>(S) * topk;
+  const int64_t total = kv_rows / S_kv * per_b;
+  for (int64_t i = tid; i < total; i += nthr) {
+    const int r = __ldg(idx + i);
+    if (static_cast<unsigned>(r) < static_cast<unsigned>(S_kv))
+      atomicAdd(counts + (i / per_b) * S_kv + r, 1u);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    m_do = fmaxf(m_do, __shfl_xor_sync(0xffffffffu, m_do, off));
+    m_dosq = fmaxf(m_dosq, __shfl_xor_sync(0xffffffffu, m_dosq, off));
+    m_kvsq = fmaxf(m_kvsq, __shfl_xor_sync(0xffffffffu, m_kvsq, off));
+    m_q = fmaxf(m_q, __shfl_xor_sync(0xffffffffu, m_q, off));
+    m_dl = fmaxf(m_dl, __shfl_xor_sync(0xffffffffu, m_dl, off));
+  }
+  if (lane == 0) {
+    atomic_max_nonneg(stats + kDetMaxAbsDout, m_do);
+    atomic_max_nonneg(stats + kDetMaxDoutSq, m_dosq);
+    atomic_max_nonneg(stats + kDetMaxKvSq, m_kvsq);
+    atomic_max_nonneg(stats + kDetMaxAbsQ, m_q);
+    atomic_max_nonneg(stats + kDetMaxAbsDelta, m_dl);
+  }
+}
+
+// The most slots naming one kv row (block maxima, then atomicMax), and in
+// the last block to finish the binary point k from the statistics.
+__global__ void __launch_bounds__(256)
+    smqa_bwd_det_scale_kernel(uint32_t* __restrict__ stats, const uint32_t* __restrict__ counts,
+                              int64_t n, int H, float scale) {
+  __shared__ uint32_t part[8];
+  __shared__ bool last;
+  uint32_t m = 0;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    m = max(m, __ldg(counts + i));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t bm = 0;
+    for (int w = 0; w < 8; ++w) bm = max(bm, part[w]);
+    atomicMax(stats + kDetMaxCount, bm);
+    __threadfence();
+    last = atomicAdd(stats + kDetTicket, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!last || threadIdx.x != 0) return;
+  __threadfence();
+  volatile uint32_t* vs = stats;
+  const double a_do = __uint_as_float(vs[kDetMaxAbsDout]);
+  const double n_do = sqrt(static_cast<double>(__uint_as_float(vs[kDetMaxDoutSq])));
+  const double n_kv = sqrt(static_cast<double>(__uint_as_float(vs[kDetMaxKvSq])));
+  const double a_q = __uint_as_float(vs[kDetMaxAbsQ]);
+  const double a_dl = __uint_as_float(vs[kDetMaxAbsDelta]);
+  const double cnt = static_cast<double>(vs[kDetMaxCount]);
+  // X with a margin of 1 + 2^-8 for the fp32 roundings of the statistics.
+  const double x = static_cast<double>(H) * (a_do + scale * (n_do * n_kv + a_dl) * a_q) *
+                   (1.0 + 1.0 / 256.0);
+  const double bound = cnt * x;
+  int k;
+  if (!(bound > 0.0)) {
+    k = 100;  // every contribution is zero
+  } else if (!(bound < 1e300)) {
+    k = -100;  // non-finite inputs: the result is undefined
+  } else {
+    int e;
+    frexp(bound, &e);  // bound <= 2^e
+    k = min(max(61 - e, -100), 100);
+  }
+  vs[kDetShift] = static_cast<uint32_t>(k);
+}
+
+// Fixed point -> bf16 or fp32: value = integer * 2^-k.
 __global__ void __launch_bounds__(256)
     smqa_bwd_post_fixed_kernel(const unsigned long long* __restrict__ acc, void* __restrict__ out,
-                               int fp32_out, int64_t vec4) {
+                               int fp32_out, int64_t vec4, const int* __restrict__ shift) {
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const ulonglong2* a2 = reinterpret_cast<const ulonglong2*>(acc);
-  constexpr float kInv = 1.f / 4294967296.f;  // 2^-32
+  const float inv = pow2f(-__ldg(shift));
   for (int64_t i = tid; i < vec4; i += nthr) {
     const ulonglong2 x = a2[2 * i], y = a2[2 * i + 1];
-    const float v0 = __ll2float_rn(static_cast<long long>(x.x)) * kInv;
-    const float v1 = __ll2float_rn(static_cast<long long>(x.y)) * kInv;
-    const float v2 = __ll2float_rn(static_cast<long long>(y.x)) * kInv;
-    const float v3 = __ll2float_rn(static_cast<long long>(y.y)) * kInv;
+    const float v0 = __ll2float_rn(static_cast<long long>(x.x)) * inv;
+    const float v1 = __ll2float_rn(static_cast<long long>(x.y)) * inv;
+    const float v2 = __ll2float_rn(static_cast<long long>(y.x)) * inv;
+    const float v3 = __ll2float_rn(static_cast<long long>(y.y)) * inv;
     if (fp32_out)
       reinterpret_cast<float4*>(out)[i] = make_float4(v0, v1, v2, v3);
     else
@@ -195,45 +341,59 @@ struct BwdLayout {
   static constexpr uint32_t kTmemUsed = kTmemDkv + kNE * kBI;
   static constexpr uint32_t kTmemCols = kTmemUsed <= 256 ? 256 : 512;
   static_assert(kTmemUsed <= 512, "TMEM budget");
-  // warps 0-3: P / dS (thread = head row); 4-7: dKV drain (thread = head-dim
-  // row); 8-9: gather; 10: TMEM owner + MMA issuer; 11-14 (D split across
-  // the pair only): send this CTA's partial S / dP to the peer.
-  static constexpr int kProducerWarp0 = 8;
-  static constexpr int kMmaWarp = 10;
-  static constexpr int kSenderWarp0 = 11;
-  static constexpr int kThreads = NC == 2 ? 480 : 352;
-  // Readers of the S / dP tile: the P / dS warps and the senders.
-  static constexpr int kSdpReaders = NC == 2 ? 256 : 128;
+  // warps 0-7: P / dS (thread = head row 32 (warp % 4) + lane and slot half
+  // warp / 4 of each block; for D split across the pair they also send this
+  // CTA's partial S / dP of their slots to the peer); 8-11: dKV drain
+  // (thread = head-dim row); 12-13: gather; 14: TMEM owner + MMA issuer.
+  static constexpr int kPdsThreads = 256;
+  static constexpr int kDrainWarp0 = 8;
+  static constexpr int kProducerWarp0 = 12;
+  static constexpr int kMmaWarp = 14;
+  static constexpr int kThreads = 480;
   // Exchange buffer of one receiver and block parity: 16 pieces of 16 bytes
-  // per head (8 of S, 8 of dP, each 8 slots of fp16), piece-major.
-  static constexpr uint32_t kXchgBytes = 16u * 16u * kHPad;
+  // per head (8 of S, 8 of dP, each the 16-bit block-floating-point fields
+  // of 8 slots), piece-major, then per slot half and head one packed pair of
+  // exponents.
+  static constexpr uint32_t kXchgScaleOff = 16u * 16u * kHPad;
+  static constexpr uint32_t kXchgBytes = kXchgScaleOff + 2u * 4u * kHPad;
   static_assert(2 * 2 * kXchgBytes == kBwdSlotBytes, "exchange slot size");
 };
 
-// Partial S (exp2 domain) and sm_scale dP of one head row over the block's
-// 64 slots, rounded to fp16 pairs: hs[w] / hp[w] hold slots 2w, 2w+1.  The
-// sender and the P / dS warps round the same TMEM values the same way.
-template <int DC, int NC>
-__device__ __forceinline__ void load_own_partials(uint32_t t_s, uint32_t t_dp, float scale_log2,
-                                                  float scale, uint32_t (&hs)[32],
-                                                  uint32_t (&hp)[32]) {
+// This CTA's partial S (exp2 domain) and sm_scale dP of one head row over
+// 32 slots of the block (one slot half), each in block floating point (one
+// exponent per head, block and half, see bfp16_exponent): hs[w] / hp[w] hold
+// the 16-bit fields of slots 2w, 2w+1; the returned word packs the two
+// exponents (S in the low half, dP in the high half, each offset by 128).
+// Both CTAs add the same two rounded values, so they agree bit for bit.
+__device__ __forceinline__ uint32_t own_partials_bfp(uint32_t t_s, uint32_t t_dp,
+                                                     float scale_log2, float scale,
+                                                     uint32_t (&hs)[16], uint32_t (&hp)[16]) {
+  float xs[32], xp[32];
+  tmem_ld32x2(t_s, t_dp, xs, xp);
+  const int es = bfp16_exponent(__fmul_rn(__fmul_rn(absmax_n<32>(xs), scale_log2), kExpMargin));
+  const int ep = bfp16_exponent(__fmul_rn(__fmul_rn(absmax_n<32>(xp), scale), kExpMargin));
+  const float fs = __fmul_rn(scale_log2, pow2f(14 - es));
+  const float fp = __fmul_rn(scale, pow2f(14 - ep));
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    float xs[32], xp[32];
-    tmem_ld32x2(t_s + 32 * half, t_dp + 32 * half, xs, xp);
-#pragma unroll
-    for (int w = 0; w < 16; ++w) {
-      const float2 a =
-          mul2(make_float2(xs[2 * w], xs[2 * w + 1]), make_float2(scale_log2, scale_log2));
-      const float2 d = mul2(make_float2(xp[2 * w], xp[2 * w + 1]), make_float2(scale, scale));
-      hs[16 * half + w] = pack_f16x2_sat(a.x, a.y);
-      hp[16 * half + w] = pack_f16x2_sat(d.x, d.y);
-    }
+  for (int w = 0; w < 16; ++w) {
+    const float2 rs = bfp16_round2(make_float2(xs[2 * w], xs[2 * w + 1]), fs);
+    hs[w] = bfp16_pack(rs.x, rs.y);
+    const float2 rp = bfp16_round2(make_float2(xp[2 * w], xp[2 * w + 1]), fp);
+    hp[w] = bfp16_pack(rp.x, rp.y);
   }
+  return static_cast<uint32_t>(es + 128) | (static_cast<uint32_t>(ep + 128) << 16);
+}
+
+// 2^(e - 14) for the exponent in the low (HI = false) or high half of a
+// packed exponent word: the weight of one unit of that half's fields.
+template <bool HI>
+__device__ __forceinline__ float bfp16_unit(uint32_t exps) {
+  const int e = static_cast<int>(HI ? (exps >> 16) : (exps & 0xffffu)) - 128;
+  return pow2f(e - 14);
 }
 
 template <int DC, int NC, bool DET>
-__global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
+__global__ void __launch_bounds__(480, 1)
     smqa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
@@ -261,21 +421,21 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
       mbar_init(bar(L::kBarKvEmpty + s), 1);
     }
     mbar_init(bar(L::kBarSdpFull), 1);
-    mbar_init(bar(L::kBarSdpFree), L::kSdpReaders);
-    mbar_init(bar(L::kBarPdsFull), 128);
+    mbar_init(bar(L::kBarSdpFree), L::kPdsThreads);
+    mbar_init(bar(L::kBarPdsFull), L::kPdsThreads);
     mbar_init(bar(L::kBarPdsFree), 1);
     mbar_init(bar(L::kBarDkvFull), 1);
     mbar_init(bar(L::kBarDkvFree), 128);
-    // Exchange: the peer's four sender warps each signal a filled buffer,
-    // the peer's four P / dS warps each signal a consumed one.
+    // Exchange: the peer's eight P / dS warps each signal a filled buffer
+    // and, later, a consumed one.
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(L::kBarRecvFull + i), 4);
-      mbar_init(bar(L::kBarSendOk + i), 4);
+      mbar_init(bar(L::kBarRecvFull + i), L::kPdsThreads / 32);
+      mbar_init(bar(L::kBarSendOk + i), L::kPdsThreads / 32);
     }
     mbar_init(bar(L::kBarQdoFull), 1);
     mbar_init(bar(L::kBarDqDone), 1);
     mbar_init(bar(L::kBarDrain), 1);
-    mbar_init(bar(L::kBarDqStaged), 128);
+    mbar_init(bar(L::kBarDqStaged), L::kPdsThreads);
     *abort_flag = *reinterpret_cast<volatile int*>(p.status) != 0 ? 1 : 0;
     *slot_smem = -1;
     if (NC == 2 && rank == 0 && *abort_flag == 0) {
@@ -484,47 +644,11 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
       mbar_wait_drain(bar(L::kBarDrain), 0);
     }
     __syncwarp();
-  } else if (NC == 2 && warp >= L::kSenderWarp0) {
-    // ------------------------------------------------------------ sender
-    // Thread = head row h: this CTA's fp16 partial S / dP of each block into
-    // the peer's exchange buffer of the block's parity (L2), then one
-    // release-arrive per warp on the peer's barrier.
-    const int sq = warp & 3;  // TMEM lane quarter
-    const int h = sq * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(sq * 32) << 16;
-    const uint32_t peer_full = mapa_shared(bar(L::kBarRecvFull), rank ^ 1u);
-    uint8_t* dst0 = p.exch + (static_cast<size_t>(slot) * 2 + (rank ^ 1u)) * (2 * L::kXchgBytes);
-    for (int i = 0; i < nblk; ++i) {
-      const int sb = i & 1;
-      bool ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSdpFull), i & 1, ctl));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t hs[32], hp[32];
-      load_own_partials<DC, NC>(tmem + lane_base + L::kTmemS, tmem + lane_base + L::kTmemDp,
-                                p.scale_log2, p.scale, hs, hp);
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarSdpFree));
-      // The peer has consumed block i-2 from this buffer.
-      if (i >= 2) {
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait<true>(bar(L::kBarSendOk + sb), ((i >> 1) - 1) & 1, ctl));
-        if (!ok) break;
-      }
-      uint4* dst = reinterpret_cast<uint4*>(dst0 + sb * L::kXchgBytes) + h;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        dst[j * L::kHPad] = make_uint4(hs[4 * j], hs[4 * j + 1], hs[4 * j + 2], hs[4 * j + 3]);
-        dst[(8 + j) * L::kHPad] =
-            make_uint4(hp[4 * j], hp[4 * j + 1], hp[4 * j + 2], hp[4 * j + 3]);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(peer_full + 8u * static_cast<uint32_t>(sb));
-    }
-  } else if (warp >= 4) {
+  } else if (warp >= L::kDrainWarp0) {
     // ------------------------------------------------------------ dKV drain
     // Thread = head-dim row of one lane quarter; per block 64 slots, read as
     // two 32-slot halves (both 128-row halves of the tile per TMEM trip).
-    const int wq = warp - 4;  // TMEM lane quarter
+    const int wq = warp - L::kDrainWarp0;  // TMEM lane quarter
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
     const bool active = (wq * 32) < DC;  // DC = 64: rows 64..127 are padding
@@ -532,12 +656,13 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
     float* col = p.dkv_acc + col0;
     unsigned long long* colx = p.dkv_fix + col0;
     // One contribution to element off of this lane's column: an fp32
-    // reduction, or in the deterministic mode the value as a 32.32
-    // fixed-point integer (rounded to nearest, saturating) added as an
+    // reduction, or in the deterministic mode the value times 2^k (the
+    // call's binary point) rounded to a 64-bit integer and added as an
     // integer, so the sum does not depend on the order of the additions.
+    const float fix_scale = DET ? pow2f(__ldg(p.fix_shift)) : 0.f;
     auto add = [&](size_t off, float v) {
       if constexpr (DET) {
-        const long long n = __float2ll_rn(v * 4294967296.f);
+        const long long n = __float2ll_rn(v * fix_scale);
         asm volatile("red.global.add.u64 [%0], %1;" ::"l"(colx + off),
                      "l"(static_cast<unsigned long long>(n))
                      : "memory");
@@ -598,65 +723,92 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
     }
   } else {
     // ------------------------------------------------------------ P / dS
-    // Thread = head row h.  Per block: the full S and dP of the row (own
-    // partial + the peer's, both fp16-rounded, for D = 512), then
+    // Thread = head row h and slot half hh: per block the full S and dP of
+    // the row's 32 slots (for D = 512 this CTA's partial plus the peer's,
+    // both in block floating point), then
     //   P = 2^(S - lse2),  dS' = P (sm_scale dP - sm_scale Delta),
-    // written bf16 for the gradient MMAs, 8 slots at a time.
-    const int h = threadIdx.x;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // written bf16 for the gradient MMAs, 8 slots at a time.  For D = 512 the
+    // same thread first rounds its partial and writes it into the peer's
+    // exchange buffer, so each partial is rounded once and read from TMEM
+    // once.
+    const int h = (warp & 3) * 32 + lane;
+    const int hh = warp >> 2;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + L::kTmemS + 32 * hh;
+    const uint32_t t_dp = tmem + lane_base + L::kTmemDp + 32 * hh;
     const float lse2 = h < p.H ? __ldg(p.lse + static_cast<size_t>(t) * p.H + h) : INFINITY;
     const float dlt_s =
         h < p.H ? __ldg(p.delta + static_cast<size_t>(t) * p.H + h) * p.scale : 0.f;
+    const uint32_t peer_full = NC == 2 ? mapa_shared(bar(L::kBarRecvFull), rank ^ 1u) : 0u;
     const uint32_t peer_sendok = NC == 2 ? mapa_shared(bar(L::kBarSendOk), rank ^ 1u) : 0u;
-    const uint4* src0 = NC == 2 ? reinterpret_cast<const uint4*>(
-                                      p.exch + (static_cast<size_t>(slot) * 2 + rank) *
-                                                   (2 * L::kXchgBytes)) + h
-                                : nullptr;
+    // This CTA's receive buffers, and the peer's (which this thread fills).
+    const uint8_t* recv0 =
+        NC == 2 ? p.exch + (static_cast<size_t>(slot) * 2 + rank) * (2 * L::kXchgBytes) : nullptr;
+    uint8_t* send0 = NC == 2 ? p.exch + (static_cast<size_t>(slot) * 2 + (rank ^ 1u)) *
+                                            (2 * L::kXchgBytes)
+                             : nullptr;
     const uint32_t row128 = static_cast<uint32_t>(h) * 128u;
     const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
-    auto load_idx = [&](int blk, int half) -> int {
-      const int j = blk * L::kBI + 32 * half + lane;
+    auto load_idx = [&](int blk) -> int {
+      const int j = blk * L::kBI + 32 * hh + lane;
       return j < p.topk ? __ldg(idx_row + j) : -1;
     };
-    // P and dS' of slots 8c .. 8c+7 from their scores zs and scaled dP zp
-    // (slot validity: bit (8c + k) % 32 of msk).
+    // P and dS' of the half's slots 8c .. 8c+7 (c = 0..3) from their scores
+    // zs and scaled dP zp (slot validity: bit 8c + k of msk).
     auto emit = [&](int c, uint32_t msk, const float* zs, const float* zp) {
       uint32_t pp[4], pd[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const float2 e = add2(make_float2(zs[2 * k], zs[2 * k + 1]), make_float2(-lse2, -lse2));
         const float2 g = add2(make_float2(zp[2 * k], zp[2 * k + 1]), make_float2(-dlt_s, -dlt_s));
-        const int jj = (8 * c + 2 * k) & 31;
+        const int jj = 8 * c + 2 * k;
         const float2 pv = make_float2(((msk >> jj) & 1u) ? fast_exp2(e.x) : 0.f,
                                       ((msk >> (jj + 1)) & 1u) ? fast_exp2(e.y) : 0.f);
         const float2 dv = mul2(pv, g);
         pp[k] = pack_bf16x2(pv.x, pv.y);
         pd[k] = pack_bf16x2(dv.x, dv.y);
       }
-      const uint32_t off = row128 + ((static_cast<uint32_t>(c) ^ static_cast<uint32_t>(h & 7)) << 4);
+      const uint32_t chunk = static_cast<uint32_t>(4 * hh + c);
+      const uint32_t off = row128 + ((chunk ^ static_cast<uint32_t>(h & 7)) << 4);
       st_shared_v4(base + L::kOffP + off, pp[0], pp[1], pp[2], pp[3]);
       st_shared_v4(base + L::kOffDs + off, pd[0], pd[1], pd[2], pd[3]);
     };
-    int r0 = load_idx(0, 0), r1 = load_idx(0, 1);
+    int r_next = load_idx(0);
     bool ok = *abort_flag == 0;
     for (int i = 0; ok && i < nblk; ++i) {
       const int sb = i & 1;
-      // Valid-slot masks of the block's two 32-slot halves (prefetched).
-      const uint32_t m0 = __ballot_sync(0xffffffffu, static_cast<unsigned>(r0) < static_cast<unsigned>(p.S_kv));
-      const uint32_t m1 = __ballot_sync(0xffffffffu, static_cast<unsigned>(r1) < static_cast<unsigned>(p.S_kv));
-      if (i + 1 < nblk) {
-        r0 = load_idx(i + 1, 0);
-        r1 = load_idx(i + 1, 1);
-      }
+      // Valid-slot mask of this half of the block (prefetched index).
+      const uint32_t msk =
+          __ballot_sync(0xffffffffu, static_cast<unsigned>(r_next) < static_cast<unsigned>(p.S_kv));
+      if (i + 1 < nblk) r_next = load_idx(i + 1);
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSdpFull), i & 1, ctl));
       if (!ok) break;
       tc_fence_after();
       if constexpr (NC == 2) {
-        uint32_t hs[32], hp[32];
-        load_own_partials<DC, NC>(tmem + lane_base + L::kTmemS, tmem + lane_base + L::kTmemDp,
-                                  p.scale_log2, p.scale, hs, hp);
+        uint32_t hs[16], hp[16];
+        const uint32_t own_exps = own_partials_bfp(t_s, t_dp, p.scale_log2, p.scale, hs, hp);
         tc_fence_before();
         mbar_arrive(bar(L::kBarSdpFree));
+        // Send: the peer has consumed block i-2 from this buffer.
+        if (i >= 2) {
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait<true>(bar(L::kBarSendOk + sb), ((i >> 1) - 1) & 1, ctl));
+          if (!ok) break;
+        }
+        {
+          uint8_t* buf = send0 + sb * L::kXchgBytes;
+          uint4* dst = reinterpret_cast<uint4*>(buf) + h;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            dst[(4 * hh + c) * L::kHPad] =
+                make_uint4(hs[4 * c], hs[4 * c + 1], hs[4 * c + 2], hs[4 * c + 3]);
+            dst[(8 + 4 * hh + c) * L::kHPad] =
+                make_uint4(hp[4 * c], hp[4 * c + 1], hp[4 * c + 2], hp[4 * c + 3]);
+          }
+          reinterpret_cast<uint32_t*>(buf + L::kXchgScaleOff)[hh * L::kHPad + h] = own_exps;
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(peer_full + 8u * static_cast<uint32_t>(sb));
+        }
         // P / dS buffers were last read by the gradient MMAs of block i-1.
         if (i >= 1) {
           ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarPdsFree), (i - 1) & 1, ctl));
@@ -664,24 +816,31 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
         }
         ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull + sb), (i >> 1) & 1, ctl));
         if (!ok) break;
-        const uint4* src = src0 + sb * (L::kXchgBytes / 16);
+        const uint8_t* buf = recv0 + sb * L::kXchgBytes;
+        const uint4* src = reinterpret_cast<const uint4*>(buf) + h;
+        const uint32_t peer_exps =
+            __ldcg(reinterpret_cast<const unsigned int*>(buf + L::kXchgScaleOff) + hh * L::kHPad + h);
+        const float us = bfp16_unit<false>(own_exps), up = bfp16_unit<true>(own_exps);
+        const float vs = bfp16_unit<false>(peer_exps), vp = bfp16_unit<true>(peer_exps);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 ys = __ldcg(src + c * L::kHPad);
-          const uint4 yp = __ldcg(src + (8 + c) * L::kHPad);
+        for (int c = 0; c < 4; ++c) {
+          const uint4 ys = __ldcg(src + (4 * hh + c) * L::kHPad);
+          const uint4 yp = __ldcg(src + (8 + 4 * hh + c) * L::kHPad);
           const uint32_t ysa[4] = {ys.x, ys.y, ys.z, ys.w};
           const uint32_t ypa[4] = {yp.x, yp.y, yp.z, yp.w};
           float zs[8], zp[8];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const float2 a = add_f16x2_f32(hs[4 * c + k], ysa[k]);
-            const float2 d = add_f16x2_f32(hp[4 * c + k], ypa[k]);
+            // Both decodings are exact; the sum is one rounding and commutes,
+            // so the two CTAs get the same full S and dP.
+            const float2 a = add2(bfp16_unpack(hs[4 * c + k], us), bfp16_unpack(ysa[k], vs));
+            const float2 d = add2(bfp16_unpack(hp[4 * c + k], up), bfp16_unpack(ypa[k], vp));
             zs[2 * k] = a.x;
             zs[2 * k + 1] = a.y;
             zp[2 * k] = d.x;
             zp[2 * k + 1] = d.y;
           }
-          emit(c, c < 4 ? m0 : m1, zs, zp);
+          emit(c, msk, zs, zp);
         }
         fence_proxy_async_smem();
         mbar_arrive(bar(L::kBarPdsFull));
@@ -690,42 +849,38 @@ __global__ void __launch_bounds__(NC == 2 ? 480 : 352, 1)
         __syncwarp();
         if (lane == 0 && i + 2 < nblk)
           mbar_arrive_remote(peer_sendok + 8u * static_cast<uint32_t>(sb));
-        continue;
       } else {
+        float xs[32], xp[32];
+        tmem_ld32x2(t_s, t_dp, xs, xp);
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarSdpFree));
         if (i >= 1) {
           ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarPdsFree), (i - 1) & 1, ctl));
           if (!ok) break;
         }
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          float xs[32], xp[32];
-          tmem_ld32x2(tmem + lane_base + L::kTmemS + 32 * half,
-                      tmem + lane_base + L::kTmemDp + 32 * half, xs, xp);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float zs[8], zp[8];
+        for (int c = 0; c < 4; ++c) {
+          float zs[8], zp[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              zs[k] = xs[8 * c + k] * p.scale_log2;
-              zp[k] = xp[8 * c + k] * p.scale;
-            }
-            emit(4 * half + c, half == 0 ? m0 : m1, zs, zp);
+          for (int k = 0; k < 8; ++k) {
+            zs[k] = xs[8 * c + k] * p.scale_log2;
+            zp[k] = xp[8 * c + k] * p.scale;
           }
+          emit(c, msk, zs, zp);
         }
-        tc_fence_before();
-        mbar_arrive(bar(L::kBarSdpFree));
+        fence_proxy_async_smem();
+        mbar_arrive(bar(L::kBarPdsFull));
       }
-      fence_proxy_async_smem();
-      mbar_arrive(bar(L::kBarPdsFull));
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDqDone), 0, ctl));
     if (ok) {
       tc_fence_after();
       // dQ into shared memory as 64-column tiles in the 128-byte-swizzled
       // layout of dq's tensor map (the kv ring is free: every MMA has
-      // completed); the TMA then writes whole rows.
+      // completed); the TMA then writes whole rows.  Slot half hh stages
+      // the tiles cc = hh, hh + 2, ...
 #pragma unroll 1
-      for (int cc = 0; cc < DC / 64; ++cc) {
+      for (int cc = hh; cc < DC / 64; cc += 2) {
         float v[2][32];
         if (nblk > 0) {
           tmem_ld32x2(tmem + lane_base + L::kTmemDq + cc * 64,
@@ -835,9 +990,33 @@ cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* d
 }
 
 cudaError_t launch_bwd_post_fixed(const unsigned long long* acc, void* out, int fp32_out,
-                                 int64_t elems, cudaStream_t stream) {
+                                 int64_t elems, const int* shift, cudaStream_t stream) {
   const int64_t vec4 = elems / 4;
-  smqa_bwd_post_fixed_kernel<<<grid_for(vec4, 256), 256, 0, stream>>>(acc, out, fp32_out, vec4);
+  smqa_bwd_post_fixed_kernel<<<grid_for(vec4, 256), 256, 0, stream>>>(acc, out, fp32_out, vec4,
+                                                                      shift);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_det_stats(const __nv_bfloat16* q, const __nv_bfloat16* kv,
+                                 const __nv_bfloat16* dout, const float* delta,
+                                 const int32_t* idx, const smqa_shape& s, uint32_t* stats,
+                                 uint32_t* counts, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(s.B) * s.S * s.H;
+  const int64_t kv_rows = static_cast<int64_t>(s.B) * s.S_kv;
+  const int64_t slots = static_cast<int64_t>(s.B) * s.S * s.topk;
+  const int64_t work = rows * 32 > slots ? rows * 32 : slots;
+  smqa_bwd_det_stats_kernel<<<grid_for(work, 256), 256, 0, stream>>>(
+      q, kv, dout, delta, idx, rows, kv_rows, s.D, s.S, s.S_kv, s.topk, stats, counts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_det_scale(const smqa_shape& s, float scale, uint32_t* stats,
+                                 const uint32_t* counts, cudaStream_t stream) {
+  const int64_t n = static_cast<int64_t>(s.B) * s.S_kv;
+  int g = static_cast<int>((n + 256 * 16 - 1) / (256 * 16));
+  if (g < 1) g = 1;
+  if (g > 152) g = 152;
+  smqa_bwd_det_scale_kernel<<<g, 256, 0, stream>>>(stats, counts, n, s.H, scale);
   return cudaGetLastError();
 }
 

@@ -162,75 +162,6 @@ __device__ __forceinline__ void gather_block(uint32_t stage, const __nv_bfloat16
   }
 }
 
-// max(a, b, c) in one instruction (the three-input form of sm_100 and later).
-__device__ __forceinline__ float fmax3f(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
-// The largest of 64 values (ABS: of their magnitudes), as a tree of
-// three-input maxima (32 instructions instead of 63).
-template <bool ABS>
-__device__ __forceinline__ float max64(const float* x) {
-  float a[22];
-#pragma unroll
-  for (int j = 0; j < 21; ++j)
-    a[j] = ABS ? fmax3f(fabsf(x[3 * j]), fabsf(x[3 * j + 1]), fabsf(x[3 * j + 2]))
-               : fmax3f(x[3 * j], x[3 * j + 1], x[3 * j + 2]);
-  a[21] = ABS ? fabsf(x[63]) : x[63];
-  float b[8];
-#pragma unroll
-  for (int j = 0; j < 7; ++j) b[j] = fmax3f(a[3 * j], a[3 * j + 1], a[3 * j + 2]);
-  b[7] = a[21];
-  return fmax3f(fmax3f(b[0], b[1], b[2]), fmax3f(b[3], b[4], b[5]), fmaxf(b[6], b[7]));
-}
-
-// Block floating point of one head's 64 partial scores of a block, in the
-// exp2 domain (v = s1 x, x the raw partial, s1 the softmax scale): exponent
-// e = floor(log2(v_max (1 + 2^-15))) with v_max = s1 max|x| (clamped to
-// [-100, 100]); each value becomes the integer n = rint(x * (s1 2^(14-e)))
-// and stands for n 2^(e-14).  The factor 1 + 2^-15 keeps |x s1 2^(14-e)|
-// below 32767.5 (with every fp32 rounding of v_max counted), so |n| <= 32767
-// without a clamp; for 2^-100 <= v_max < 2^101 the absolute error of a value
-// is at most 2^-15 (1 + 2^-14) v_max.  n is stored offset by 32768 as an
-// unsigned 16-bit field.  One fused multiply-add rounds: x * f + kRoundBias,
-// with kRoundBias = 1.5 * 2^23 + 32768, is exactly rounded to an integer
-// whose low 16 bits are n + 32768; the field is unpacked by placing it under
-// the exponent of 2^23.  Every step is exact or one IEEE rounding (explicit
-// round-to-nearest operations), so the sender and the peer get the same value.
-constexpr float kRoundBias = 12615680.f;        // 1.5 * 2^23 + 32768
-constexpr float kUnpackBias = 8421376.f;         // 2^23 + 32768
-constexpr float kExpMargin = 1.000030517578125f;  // 1 + 2^-15
-
-__device__ __forceinline__ int bfp16_exponent(float vmax_abs) {
-  const int e = static_cast<int>((__float_as_uint(vmax_abs) >> 23) & 0xffu) - 127;
-  return min(max(e, -100), 100);
-}
-// 2^k as a float (k within the normal range).
-__device__ __forceinline__ float pow2f(int k) {
-  return __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
-}
-// kRoundBias + n for two raw partials x (f = s1 2^(14-e)).
-__device__ __forceinline__ float2 bfp16_round2(float2 x, float f) {
-  return fma2(x, make_float2(f, f), make_float2(kRoundBias, kRoundBias));
-}
-// The values n 2^(e-14) of two rounded kRoundBias + n (inv = 2^(e-14)).
-__device__ __forceinline__ float2 bfp16_value2(float2 r, float inv) {
-  return fma2(r, make_float2(inv, inv), make_float2(-kRoundBias * inv, -kRoundBias * inv));
-}
-// Two rounded values -> two 16-bit fields (the first in the low half).
-__device__ __forceinline__ uint32_t bfp16_pack(float r_lo, float r_hi) {
-  return __byte_perm(__float_as_uint(r_lo), __float_as_uint(r_hi), 0x5410);
-}
-// A packed pair -> the two values it stands for.
-__device__ __forceinline__ float2 bfp16_unpack(uint32_t w, float inv) {
-  const float lo = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7610));
-  const float hi = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7632));
-  return fma2(make_float2(lo, hi), make_float2(inv, inv),
-              make_float2(-kUnpackBias * inv, -kUnpackBias * inv));
-}
-
 template <int D, int NSPLIT>
 __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
     smqa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
@@ -469,7 +400,7 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
       float x[64];
       tmem_ld32x2(tile, tile + 32, *reinterpret_cast<float(*)[32]>(x),
                   *reinterpret_cast<float(*)[32]>(x + 32));
-      const int ex = bfp16_exponent(__fmul_rn(__fmul_rn(max64<true>(x), s1), kExpMargin));
+      const int ex = bfp16_exponent(__fmul_rn(__fmul_rn(absmax_fold_n<64>(x), s1), kExpMargin));
       const float f = __fmul_rn(s1, pow2f(14 - ex)), inv = pow2f(ex - 14);
       uint32_t w[32];
 #pragma unroll
@@ -602,7 +533,7 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
           x[j] = bit ? x[j] : -INFINITY;
         }
       }
-      const float mloc = max64<false>(x);
+      const float mloc = max_n<64>(x);
       const float m_new = fmaxf(m_run, mloc);
       const bool bump = (m_run == -INFINITY) ? (m_new != -INFINITY) : (m_new > m_run + 8.f);
       float alpha = 1.f;

@@ -106,7 +106,7 @@ Layout layout(const smqa_shape& s, unsigned flags, bool bwd) {
     L.dout = take(rows * s.D * 2);
     L.dq = take(rows * s.D * 2);
     L.delta = take(rows * 4);
-    L.acc = take(kvel * (det ? 8 : 4));
+    L.acc = take(det ? smqa::det_region_bytes(s) : kvel * 4);
     // Without the deterministic mode an fp32 result is the accumulator itself.
     L.dkv = (det || !f32) ? take(kvel * (f32 ? 4 : 2)) : L.acc;
     L.dsink = take(static_cast<size_t>(s.H) * 4);
@@ -263,13 +263,16 @@ smqa_status enqueue(const HostArgs& a, const Layout& L, uint8_t* ws,
     float* acc = reinterpret_cast<float*>(dev(L.acc, 0));
     unsigned long long* acc_fixed = det ? reinterpret_cast<unsigned long long*>(acc) : nullptr;
     float* delta = reinterpret_cast<float*>(dev(L.delta, 0));
-    // The accumulator starts at zero (two floats' worth of zero bits per
-    // element in the fixed-point mode).
+    // The accumulator starts at zero (in the deterministic mode the whole
+    // fixed-point region: accumulator, statistics and row counts).
+    const size_t acc_bytes = det ? smqa::det_region_bytes(s) : kvel * 4;
     SMQA_TRY(smqa::launch_bwd_preprocess(nullptr, nullptr, nullptr, acc, 0, s.D,
-                                         static_cast<int64_t>(det ? 2 * kvel : kvel), sd.bwd),
+                                         static_cast<int64_t>(acc_bytes / 4), sd.bwd),
              "accumulator clear");
-    for (size_t c = 0; c < n; ++c) {
-      const smqa_shape cs{ch[c].nb, ch[c].ns, s.S_kv, s.H, s.D, s.topk};
+    uint32_t* stats = det ? reinterpret_cast<uint32_t*>(dev(L.acc, smqa::det_stats_offset(s)))
+                          : nullptr;
+    const int* shift = det ? reinterpret_cast<const int*>(stats + smqa::kDetShift) : nullptr;
+    auto delta_chunk = [&](size_t c) -> smqa_status {
       const size_t t0 = tok0(c);
       SMQA_TRY(cudaStreamWaitEvent(sd.bwd, sd.ev[ev_fwd(c)], 0), "stream wait");
       SMQA_TRY(cudaStreamWaitEvent(sd.bwd, sd.ev[ev_do(c)], 0), "stream wait");
@@ -278,6 +281,34 @@ smqa_status enqueue(const HostArgs& a, const Layout& L, uint8_t* ws,
       SMQA_TRY(smqa::launch_bwd_preprocess(o, g, delta + t0 * s.H, nullptr,
                                            static_cast<int64_t>(ntok(c)) * s.H, s.D, 0, sd.bwd),
                "bwd preprocess launch");
+      return SMQA_OK;
+    };
+    if (det) {
+      // The binary point depends on the whole call's inputs: every chunk's
+      // Delta first, then the statistics, then the main kernels.
+      for (size_t c = 0; c < n; ++c) {
+        const smqa_status r = delta_chunk(c);
+        if (r != SMQA_OK) return r;
+      }
+      SMQA_TRY(smqa::launch_bwd_det_stats(
+                   reinterpret_cast<const __nv_bfloat16*>(dev(L.q, 0)),
+                   reinterpret_cast<const __nv_bfloat16*>(dev(L.kv, 0)),
+                   reinterpret_cast<const __nv_bfloat16*>(dev(L.dout, 0)), delta,
+                   reinterpret_cast<const int32_t*>(dev(L.idx, 0)), s, stats,
+                   stats + smqa::kDetStatsBytes / 4, sd.bwd),
+               "bwd statistics launch");
+      SMQA_TRY(smqa::launch_bwd_det_scale(s, scale, stats, stats + smqa::kDetStatsBytes / 4,
+                                          sd.bwd),
+               "bwd scale launch");
+    }
+    for (size_t c = 0; c < n; ++c) {
+      const smqa_shape cs{ch[c].nb, ch[c].ns, s.S_kv, s.H, s.D, s.topk};
+      const size_t t0 = tok0(c);
+      if (!det) {
+        const smqa_status r = delta_chunk(c);
+        if (r != SMQA_OK) return r;
+      }
+      const auto* g = reinterpret_cast<const __nv_bfloat16*>(dev(L.dout, t0 * row_bytes));
       const size_t kv_off = static_cast<size_t>(ch[c].b0) * kv_per_b;
       const smqa_status r = smqa::bwd_main_launch(
           dev(L.q, t0 * row_bytes), dev(L.kv, kv_off * 2), g,
@@ -285,7 +316,7 @@ smqa_status enqueue(const HostArgs& a, const Layout& L, uint8_t* ws,
           reinterpret_cast<const float*>(dev(L.lse, t0 * lse_bytes)), delta + t0 * s.H, cs,
           scale, dev(L.dq, t0 * row_bytes),
           det ? reinterpret_cast<float*>(acc_fixed + kv_off) : acc + kv_off,
-          det ? acc_fixed + kv_off : nullptr, dev(L.bexch, 0), sd.bwd);
+          det ? acc_fixed + kv_off : nullptr, shift, dev(L.bexch, 0), sd.bwd);
       if (r != SMQA_OK) return r;
       SMQA_TRY(cudaEventRecord(sd.ev[ev_bwd(c)], sd.bwd), "event record");
     }
@@ -297,7 +328,7 @@ smqa_status enqueue(const HostArgs& a, const Layout& L, uint8_t* ws,
                "bwd sink gradient launch");
     if (det)
       SMQA_TRY(smqa::launch_bwd_post_fixed(acc_fixed, dev(L.dkv, 0), f32 ? 1 : 0,
-                                           static_cast<int64_t>(kvel), sd.bwd),
+                                           static_cast<int64_t>(kvel), shift, sd.bwd),
                "bwd postprocess launch");
     else if (!f32)
       SMQA_TRY(smqa::launch_bwd_postprocess(acc, reinterpret_cast<__nv_bfloat16*>(dev(L.dkv, 0)),

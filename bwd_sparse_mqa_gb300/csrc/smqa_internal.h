@@ -40,8 +40,10 @@ struct BwdParams {
   __nv_bfloat16* dq;     // [B,S,H,D]
   float* dkv_acc;        // [B,S_kv,D] fp32 accumulator (zeroed beforehand)
   // Deterministic mode (det != 0): the accumulator is dkv_fix instead, each
-  // element a signed 32.32 fixed-point integer (zeroed beforehand).
+  // element a signed fixed-point integer with the per-call binary point
+  // *fix_shift (value = integer * 2^-shift; zeroed beforehand).
   unsigned long long* dkv_fix;
+  const int* fix_shift;
   int det;
   int S, S_kv, H, D, topk;
   float scale;           // sm_scale
@@ -61,8 +63,35 @@ struct BwdParams {
 // with one int32 power-of-two exponent per head).
 constexpr size_t kFwdSlotBytes = 2 * 6 * (16384 + 512);
 // One exchange slot of the backward: two receivers x two block parities x
-// 32 KB (the fp16 partial S and dP of 128 heads x 64 slots).
-constexpr size_t kBwdSlotBytes = 2 * 2 * 32768;
+// 33 KB (the partial S and dP of 128 heads x 64 slots as int16 mantissas
+// with one packed pair of power-of-two exponents per head and 32-slot half).
+constexpr size_t kBwdSlotBytes = 2 * 2 * (32768 + 1024);
+
+// The deterministic mode's accumulator region: the fixed-point accumulator
+// (8 bytes per element), a block of per-call statistics (kDet* words, 32-bit
+// each) and a reference count per kv row ([B, S_kv] uint32).  The whole
+// region is zeroed before use, as a multiple of 16 bytes.
+constexpr size_t kDetStatsBytes = 256;
+enum : int {
+  kDetMaxAbsDout = 0,   // max |dO| (fp32 bits)
+  kDetMaxDoutSq = 1,    // max over (token, head) rows of |dO row|^2 (fp32 bits)
+  kDetMaxKvSq = 2,      // max over kv rows of |kv row|^2 (fp32 bits)
+  kDetMaxAbsQ = 3,      // max |q| (fp32 bits)
+  kDetMaxAbsDelta = 4,  // max |Delta| (fp32 bits)
+  kDetMaxCount = 5,     // most slots naming one kv row
+  kDetShift = 6,        // the binary point k: value = integer * 2^-k
+  kDetTicket = 7,       // blocks of the scale kernel done
+};
+inline size_t det_region_bytes(const smqa_shape& s) {
+  const size_t elems = static_cast<size_t>(s.B) * s.S_kv * s.D;
+  const size_t rows = static_cast<size_t>(s.B) * s.S_kv;
+  auto r256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  return r256(elems * 8) + kDetStatsBytes + r256(rows * 4);
+}
+inline size_t det_stats_offset(const smqa_shape& s) {
+  const size_t elems = static_cast<size_t>(s.B) * s.S_kv * s.D;
+  return (elems * 8 + 255) & ~static_cast<size_t>(255);
+}
 
 // Records `msg` as the text smqa_last_error() returns on this thread.
 void set_last_error(const char* msg);
@@ -78,19 +107,29 @@ cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* d
 cudaError_t launch_bwd_sink_grad(const float* sink, const float* lse, const float* delta,
                                 float* dsink, int64_t tokens, int H, cudaStream_t stream);
 cudaError_t launch_bwd_post_fixed(const unsigned long long* acc, void* out, int fp32_out,
-                                 int64_t elems, cudaStream_t stream);
+                                 int64_t elems, const int* shift, cudaStream_t stream);
+// Deterministic mode, before the main kernel: the statistics of the call's
+// inputs (q, kv, dO, Delta, topk_idxs over all of `s`) into stats / counts
+// (zeroed beforehand), then the binary point stats[kDetShift].
+cudaError_t launch_bwd_det_stats(const __nv_bfloat16* q, const __nv_bfloat16* kv,
+                                 const __nv_bfloat16* dout, const float* delta,
+                                 const int32_t* idx, const smqa_shape& s, uint32_t* stats,
+                                 uint32_t* counts, cudaStream_t stream);
+cudaError_t launch_bwd_det_scale(const smqa_shape& s, float scale, uint32_t* stats,
+                                 const uint32_t* counts, cudaStream_t stream);
 cudaError_t launch_bwd_postprocess(const float* acc, __nv_bfloat16* out, int64_t elems,
                                    cudaStream_t stream);
 
 // The backward's main kernel over the tokens of `s` (a whole call or a chunk
 // of one): writes dq and adds every slot's dKV contribution into `acc`
-// (fp32), or into `acc_fixed` (32.32 fixed point) when that is non-null.
+// (fp32), or into `acc_fixed` (fixed point with the binary point *fix_shift)
+// when that is non-null.
 // `exch` is the exchange pool of smqa_bwd_exchange_bytes(s) bytes (D = 512).
 // The caller has checked shapes and pointers.
 smqa_status bwd_main_launch(const void* q, const void* kv, const void* dout, const int32_t* idx,
                             const float* lse, const float* delta, const smqa_shape& s,
                             float scale, void* dq, float* acc, unsigned long long* acc_fixed,
-                            void* exch, cudaStream_t stream);
+                            const int* fix_shift, void* exch, cudaStream_t stream);
 // The entry points' shape check (records the reason on failure).
 smqa_status validate_shape(const smqa_shape& s);
 // sm_scale as the entry points interpret it (<= 0 or NaN selects D^-1/2).

@@ -467,35 +467,151 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Two floats -> packed fp16x2 (round to nearest even, saturating to the
-// largest finite fp16), `lo` in the low half.
-__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
+// max(a, b, c) / min(a, b, c) in one instruction (the three-input forms of
+// sm_100 and later).
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fmin3f(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
-// Packed fp16x2 -> the two floats (exact).
-// Sum of two fp16 pairs in fp32 with one rounding per element:
-// {float(a.lo) + float(b.lo), float(a.hi) + float(b.hi)}.  Uses the sm_100
-// mixed-precision add (fp16 operand, fp32 operand and result), which runs on
-// the FMA pipe instead of the conversion unit.  The result does not depend on
-// the order of a and b (both conversions are exact, the addition commutes).
-__device__ __forceinline__ float2 add_f16x2_f32(uint32_t a, uint32_t b) {
-  float2 r;
-  asm("{\n"
-      ".reg .b16 alo, ahi, blo, bhi;\n"
-      ".reg .f32 t0, t1;\n"
-      "mov.b32 {alo, ahi}, %2;\n"
-      "mov.b32 {blo, bhi}, %3;\n"
-      "add.rn.f32.f16 t0, alo, 0f00000000;\n"
-      "add.rn.f32.f16 t1, ahi, 0f00000000;\n"
-      "add.rn.f32.f16 %0, blo, t0;\n"
-      "add.rn.f32.f16 %1, bhi, t1;\n"
-      "}"
-      : "=f"(r.x), "=f"(r.y)
-      : "r"(a), "r"(b));
-  return r;
+// The largest and the smallest of N values (N = 32 or 64), as trees of
+// three-input maxima and minima.
+template <int N>
+__device__ __forceinline__ float2 maxmin_n(const float* x) {
+  static_assert(N == 32 || N == 64, "maxmin_n: 32 or 64 values");
+  constexpr int G = N / 3;  // full groups of three; N % 3 values are left over
+  float a[G + 1], b[G + 1];
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    a[j] = fmax3f(x[3 * j], x[3 * j + 1], x[3 * j + 2]);
+    b[j] = fmin3f(x[3 * j], x[3 * j + 1], x[3 * j + 2]);
+  }
+  if constexpr (N % 3 == 2) {
+    a[G] = fmaxf(x[N - 2], x[N - 1]);
+    b[G] = fminf(x[N - 2], x[N - 1]);
+  } else {
+    a[G] = x[N - 1];
+    b[G] = x[N - 1];
+  }
+  // Reduce the G + 1 partial results three at a time.
+  int n = G + 1;
+#pragma unroll
+  for (int round = 0; round < 4; ++round) {
+    if (n <= 1) break;
+    int m = 0;
+#pragma unroll
+    for (int j = 0; j + 2 < n; j += 3, ++m) {
+      a[m] = fmax3f(a[j], a[j + 1], a[j + 2]);
+      b[m] = fmin3f(b[j], b[j + 1], b[j + 2]);
+    }
+    const int rest = n % 3;
+    if (rest == 1) {
+      a[m] = a[n - 1];
+      b[m] = b[n - 1];
+      ++m;
+    } else if (rest == 2) {
+      a[m] = fmaxf(a[n - 2], a[n - 1]);
+      b[m] = fminf(b[n - 2], b[n - 1]);
+      ++m;
+    }
+    n = m;
+  }
+  return make_float2(a[0], b[0]);
+}
+
+// The largest of N values; and the largest of their magnitudes, taken as
+// max(max x, -min x) (no absolute-value instruction per element).
+template <int N>
+__device__ __forceinline__ float max_n(const float* x) {
+  static_assert(N >= 2, "max_n: at least two values");
+  float a[N / 3 + 1];
+  constexpr int G = N / 3;
+#pragma unroll
+  for (int j = 0; j < G; ++j) a[j] = fmax3f(x[3 * j], x[3 * j + 1], x[3 * j + 2]);
+  a[G] = N % 3 == 2 ? fmaxf(x[N - 2], x[N - 1]) : x[N - 1];
+  int n = G + 1;
+#pragma unroll
+  for (int round = 0; round < 4; ++round) {
+    if (n <= 1) break;
+    int m = 0;
+#pragma unroll
+    for (int j = 0; j + 2 < n; j += 3, ++m) a[m] = fmax3f(a[j], a[j + 1], a[j + 2]);
+    const int rest = n % 3;
+    if (rest == 1) a[m++] = a[n - 1];
+    else if (rest == 2) { a[m] = fmaxf(a[n - 2], a[n - 1]); ++m; }
+    n = m;
+  }
+  return a[0];
+}
+template <int N>
+__device__ __forceinline__ float absmax_n(const float* x) {
+  const float2 mm = maxmin_n<N>(x);
+  return fmaxf(mm.x, -mm.y);
+}
+// The same magnitude maximum with the absolute values taken in the first
+// level of the tree (the form the forward's sender runs faster with; the
+// backward's runs faster with absmax_n).
+template <int N>
+__device__ __forceinline__ float absmax_fold_n(const float* x) {
+  float y[N / 3 + 1];
+  constexpr int G = N / 3;
+#pragma unroll
+  for (int j = 0; j < G; ++j) y[j] = fmax3f(fabsf(x[3 * j]), fabsf(x[3 * j + 1]), fabsf(x[3 * j + 2]));
+  y[G] = N % 3 == 2 ? fmaxf(fabsf(x[N - 2]), fabsf(x[N - 1])) : fabsf(x[N - 1]);
+  return max_n<G + 1>(y);
+}
+
+// Block floating point of one head's partial sums of a block (the forward's
+// partial scores and the backward's partial S and dP), v = s1 x with x the
+// raw partial and s1 its scale (the softmax scale in the exp2 domain, or
+// sm_scale for dP): exponent
+// e = floor(log2(v_max (1 + 2^-15))) with v_max = s1 max|x| (clamped to
+// [-100, 100]); each value becomes the integer n = rint(x * (s1 2^(14-e)))
+// and stands for n 2^(e-14).  The factor 1 + 2^-15 keeps |x s1 2^(14-e)|
+// below 32767.5 (with every fp32 rounding of v_max counted), so |n| <= 32767
+// without a clamp; for 2^-100 <= v_max < 2^101 the absolute error of a value
+// is at most 2^-15 (1 + 2^-14) v_max.  n is stored offset by 32768 as an
+// unsigned 16-bit field.  One fused multiply-add rounds: x * f + kRoundBias,
+// with kRoundBias = 1.5 * 2^23 + 32768, is exactly rounded to an integer
+// whose low 16 bits are n + 32768; the field is unpacked by placing it under
+// the exponent of 2^23.  Every step is exact or one IEEE rounding (explicit
+// round-to-nearest operations), so the sender and the peer get the same value.
+constexpr float kRoundBias = 12615680.f;        // 1.5 * 2^23 + 32768
+constexpr float kUnpackBias = 8421376.f;         // 2^23 + 32768
+constexpr float kExpMargin = 1.000030517578125f;  // 1 + 2^-15
+
+__device__ __forceinline__ int bfp16_exponent(float vmax_abs) {
+  const int e = static_cast<int>((__float_as_uint(vmax_abs) >> 23) & 0xffu) - 127;
+  return min(max(e, -100), 100);
+}
+// 2^k as a float (k within the normal range).
+__device__ __forceinline__ float pow2f(int k) {
+  return __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+}
+// kRoundBias + n for two raw partials x (f = s1 2^(14-e)).
+__device__ __forceinline__ float2 bfp16_round2(float2 x, float f) {
+  return fma2(x, make_float2(f, f), make_float2(kRoundBias, kRoundBias));
+}
+// The values n 2^(e-14) of two rounded kRoundBias + n (inv = 2^(e-14)).
+__device__ __forceinline__ float2 bfp16_value2(float2 r, float inv) {
+  return fma2(r, make_float2(inv, inv), make_float2(-kRoundBias * inv, -kRoundBias * inv));
+}
+// Two rounded values -> two 16-bit fields (the first in the low half).
+__device__ __forceinline__ uint32_t bfp16_pack(float r_lo, float r_hi) {
+  return __byte_perm(__float_as_uint(r_lo), __float_as_uint(r_hi), 0x5410);
+}
+// A packed pair -> the two values it stands for.
+__device__ __forceinline__ float2 bfp16_unpack(uint32_t w, float inv) {
+  const float lo = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7610));
+  const float hi = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7632));
+  return fma2(make_float2(lo, hi), make_float2(inv, inv),
+              make_float2(-kUnpackBias * inv, -kUnpackBias * inv));
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,

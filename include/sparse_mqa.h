@@ -76,12 +76,18 @@ typedef struct {
 #define SMQA_FLAG_RETURN_DKV_FP32 1u
 
 /* smqa_bwd: accumulate dkv deterministically.  Every contribution is added
- * as a signed 32.32 fixed-point integer (the fp32 value times 2^32, rounded
- * to nearest, saturating) with 64-bit integer atomics, whose sum does not
- * depend on the order of the additions; the result is converted back to
- * bf16 (or fp32 with SMQA_FLAG_RETURN_DKV_FP32).  Resolution 2^-32, range
- * +-2^31 per element; the accumulator doubles (8 bytes per dkv element, in
- * the workspace).  Not a flag of the pages. */
+ * as a signed 64-bit fixed-point integer (the fp32 value times 2^k, rounded
+ * to nearest) with 64-bit integer atomics, whose sum does not depend on the
+ * order of the additions; the result is converted back to bf16 (or fp32 with
+ * SMQA_FLAG_RETURN_DKV_FP32).  The binary point k is chosen per call on the
+ * GPU (no host synchronisation) from maxima of the inputs (|q|, |dO|, the
+ * row norms of dO and kv, |Delta|) and the largest number of slots naming
+ * one kv row, so that no contribution or sum can exceed 2^61: the resolution
+ * follows the magnitude of the gradients (a dO scaled by 2^-30 gives the
+ * same relative accuracy as one of order 1), and the result is bit-identical
+ * from run to run for the same inputs.  The workspace holds the 8-byte
+ * accumulator, 256 bytes of statistics and a 4-byte count per kv row.  Not a
+ * flag of the pages. */
 #define SMQA_FLAG_DETERMINISTIC_DKV 4u
 
 /*
@@ -127,8 +133,9 @@ smqa_status smqa_fwd(const void* q, const void* kv, const float* attn_sink,
 /*
  * Bytes of device workspace smqa_bwd needs for `shape` and `flags`: the fp32
  * dKV accumulator [B,S_kv,D] (absent with SMQA_FLAG_RETURN_DKV_FP32, where
- * dkv itself accumulates; with SMQA_FLAG_DETERMINISTIC_DKV always present and
- * 8 bytes per element), Delta [B,S,H] fp32, and for D = 512 the exchange
+ * dkv itself accumulates; with SMQA_FLAG_DETERMINISTIC_DKV always present,
+ * 8 bytes per element, followed by 256 bytes of per-call statistics and a
+ * uint32 count per kv row), Delta [B,S,H] fp32, and for D = 512 the exchange
  * pool of smqa_bwd_exchange_bytes(shape), each 256-byte aligned.
  * Returns 0 for an unsupported shape.
  */
@@ -136,10 +143,12 @@ size_t smqa_bwd_workspace_bytes(smqa_shape shape, unsigned flags);
 
 /*
  * Bytes of the exchange pool the main backward kernel uses for `shape`
- * (0 when D = 64; 4 KB of slot flags + 96 slots of 128 KB when D = 512).
+ * (0 when D = 64; 4 KB of slot flags + 96 slots of 132 KB when D = 512).
  * For D = 512 each token is handled by a pair of CTAs that own one half of D
- * each; every 64-slot block they trade their fp16 partial scores and dP
- * through a slot of this pool (it stays in L2).  The pool's contents need no
+ * each; every 64-slot block they trade their partial scores and dP, in block
+ * floating point (16-bit mantissas with one power-of-two exponent per head
+ * and block, so the precision is relative to the block's largest value at any
+ * magnitude), through a slot of this pool (it stays in L2).  The pool's contents need no
  * initialisation: smqa_bwd_main clears the slot flags on its stream.
  * Returns 0 for an unsupported shape.
  */

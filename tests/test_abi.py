@@ -89,15 +89,17 @@ def test_bwd_workspace_and_checks(lib):
 
 
 def test_bwd_deterministic_flag_workspace_and_checks(lib):
-    """SMQA_FLAG_DETERMINISTIC_DKV: the accumulator is 8 bytes per dkv element
-    and always in the workspace (also with the fp32 output); unknown flags
-    are rejected."""
+    """SMQA_FLAG_DETERMINISTIC_DKV: the fixed-point accumulator (8 bytes per
+    dkv element), a 256-byte block of per-call statistics and a 4-byte
+    reference count per kv row, always in the workspace (also with the fp32
+    output); unknown flags are rejected."""
     r = lambda x: (x + 255) // 256 * 256  # noqa: E731
     shp = _lib.Shape(2, 8, 16, 16, 64, 4)
-    acc8, delta = 2 * 16 * 64 * 8, 2 * 8 * 16 * 4
+    acc8, stats, counts, delta = 2 * 16 * 64 * 8, 256, 2 * 16 * 4, 2 * 8 * 16 * 4
     det = _lib.FLAG_DETERMINISTIC_DKV
-    assert lib.smqa_bwd_workspace_bytes(shp, det) == r(acc8) + r(delta)
-    assert lib.smqa_bwd_workspace_bytes(shp, det | _lib.FLAG_RETURN_DKV_FP32) == r(acc8) + r(delta)
+    want = r(acc8) + stats + r(counts) + r(delta)
+    assert lib.smqa_bwd_workspace_bytes(shp, det) == want
+    assert lib.smqa_bwd_workspace_bytes(shp, det | _lib.FLAG_RETURN_DKV_FP32) == want
     p = _fake()
     args = [p] * 7 + [shp, 0.0, p, p, None, p]
     need = lib.smqa_bwd_workspace_bytes(shp, det)
@@ -107,12 +109,13 @@ def test_bwd_deterministic_flag_workspace_and_checks(lib):
 
 def test_bwd_exchange_pool_size_and_checks(lib):
     """D = 512: the workspace carries the CTA-pair exchange pool (4 KB of slot
-    flags + 96 slots of 128 KB); D = 64 needs none.  smqa_bwd_main rejects a
+    flags + 96 slots of two receivers x two block parities x 33 KB of
+    block-floating-point partial S and dP); D = 64 needs none.  smqa_bwd_main rejects a
     pool that is too small, or missing, before any GPU work."""
     r = lambda x: (x + 255) // 256 * 256  # noqa: E731
     s512 = _lib.Shape(1, 8, 16, 16, 512, 4)
     ex = lib.smqa_bwd_exchange_bytes(s512)
-    assert ex == 4096 + 96 * 128 * 1024
+    assert ex == 4096 + 96 * 2 * 2 * (32768 + 1024)
     acc, delta = 16 * 512 * 4, 8 * 16 * 4
     assert lib.smqa_bwd_workspace_bytes(s512, 0) == r(acc) + r(delta) + r(ex)
     assert lib.smqa_bwd_exchange_bytes(_lib.Shape(1, 8, 16, 16, 64, 4)) == 0
@@ -166,11 +169,12 @@ def test_host_entry_workspace_sizes_and_checks(lib):
                 _r256(lib.smqa_bwd_exchange_bytes(shp)))
     assert lib.smqa_fwd_bwd_host_workspace_bytes(shp, 0) == \
         fwd + bwd_tail + _r256(kvel * 4) + _r256(kvel * 2)
-    # fp32 dkv: the accumulator is the result; deterministic: 8-byte accumulator
+    # fp32 dkv: the accumulator is the result; deterministic: 8-byte
+    # accumulator, 256 bytes of statistics and a count per kv row
     assert lib.smqa_fwd_bwd_host_workspace_bytes(shp, _lib.FLAG_RETURN_DKV_FP32) == \
         fwd + bwd_tail + _r256(kvel * 4)
     assert lib.smqa_fwd_bwd_host_workspace_bytes(shp, _lib.FLAG_DETERMINISTIC_DKV) == \
-        fwd + bwd_tail + _r256(kvel * 8) + _r256(kvel * 2)
+        fwd + bwd_tail + _r256(kvel * 8) + 256 + _r256(B * S_kv * 4) + _r256(kvel * 2)
     assert lib.smqa_fwd_host_workspace_bytes(_lib.Shape(1, 8, 16, 129, 512, 4)) == 0
     assert lib.smqa_fwd_bwd_host_workspace_bytes(_lib.Shape(1, 8, 16, 16, 100, 4), 0) == 0
 

@@ -109,20 +109,20 @@ def test_three_buffers_deadlock():
 
 # ---------------------------------------------------------------------------
 # The backward pair (smqa_bwd.cu): one S/dP tile, a two-stage kv ring and
-# NB exchange buffers with an explicit consumed-signal (SendOk).
+# NB exchange buffers with an explicit consumed-signal (SendOk).  The P/dS
+# threads both send this CTA's partials and consume the peer's, in this order
+# per block:
 #   gather(i)    needs kv stage i % 2 free (the gradient MMAs of i - 2 done);
-#   sdp(i)       needs gather(i) and the S/dP tile read by send_read(i - 1)
-#                and pds_read(i - 1);
-#   send_read(i) needs sdp(i);
-#   send(i)      needs send_read(i) and, for i >= NB, the peer's SendOk for
-#                block i - NB; writes buffer i % NB of the peer (in flight);
-#   pds_read(i)  needs sdp(i);
-#   pds(i)       needs pds_read(i), grad(i - 1) (single P/dS buffers) and the
+#   sdp(i)       needs gather(i) and the S/dP tile read by read(i - 1);
+#   read(i)      needs sdp(i) and pds(i - 1) (the same threads, in order);
+#   send(i)      needs read(i) and, for i >= NB, the peer's SendOk for block
+#                i - NB; writes buffer i % NB of the peer (in flight);
+#   pds(i)       needs send(i), grad(i - 1) (single P/dS buffers) and the
 #                peer's block i; consumes it and, if i + NB < nblk, sends
 #                SendOk for buffer i % NB to the peer (in flight);
 #   grad(i)      needs pds(i) and drain(i - 1) (single dKV tile);
 #   drain(i)     needs grad(i).
-BWD_ROLES = ("gather", "sdp", "send_read", "send", "pds_read", "pds", "grad", "drain")
+BWD_ROLES = ("gather", "sdp", "read", "send", "pds", "grad", "drain")
 
 
 def run_bwd_model(NB: int, nblk: int, seed: int):
@@ -145,25 +145,21 @@ def run_bwd_model(NB: int, nblk: int, seed: int):
         if i < nblk and (i < 2 or done(c, "grad", i - 2)):
             out.append("gather")
         i = n["sdp"]
-        if i < nblk and done(c, "gather", i) and (
-                i == 0 or (done(c, "send_read", i - 1) and done(c, "pds_read", i - 1))):
+        if i < nblk and done(c, "gather", i) and (i == 0 or done(c, "read", i - 1)):
             out.append("sdp")
-        i = n["send_read"]
-        if i < nblk and done(c, "sdp", i):
-            out.append("send_read")
+        i = n["read"]
+        if i < nblk and done(c, "sdp", i) and (i == 0 or done(c, "pds", i - 1)):
+            out.append("read")
         i = n["send"]
-        if i < nblk and done(c, "send_read", i):
+        if i < nblk and done(c, "read", i):
             if i >= NB:
                 assert ok_ph[c][i % NB] <= (i // NB - 1) + 1, ("sendok aliasing", c, i)
                 if (i - NB) in sendok[c]:
                     out.append("send")
             else:
                 out.append("send")
-        i = n["pds_read"]
-        if i < nblk and done(c, "sdp", i):
-            out.append("pds_read")
         i = n["pds"]
-        if i < nblk and done(c, "pds_read", i) and (i == 0 or done(c, "grad", i - 1)):
+        if i < nblk and done(c, "send", i) and (i == 0 or done(c, "grad", i - 1)):
             assert recv_ph[c][i % NB] <= i // NB + 1, ("recv aliasing", c, i)
             if i in arrived[c]:
                 out.append("pds")

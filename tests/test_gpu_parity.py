@@ -93,14 +93,33 @@ def test_return_dkv_fp32_and_reference_rounding():
     assert P.rel_err(dkv, dkv32.double().cpu().numpy()) < 8e-3
 
 
+@pytest.mark.parametrize("D", [64, 512])
+@pytest.mark.parametrize("H", [1, 48, 100])
+def test_head_counts_off_the_tile(H, D):
+    """Head counts that are not a multiple of 16 (the MMA tile is 128 head
+    rows; rows H..127 are zero-filled and never stored), every token."""
+    x = inputs.custom(2, 40, 200, H, D, 150, recipe="causal_masked10", seed=40 + H)
+    print(P.check_full(x))
+
+
+@pytest.mark.parametrize("D", [64, 512])
+def test_topk_4096(D):
+    """topk = 4096 (64 slot blocks per token, twice the largest workload's),
+    each row a permutation of the same 4096 rows of S_kv = 5000 with 10% of
+    the slots masked, every token."""
+    x = inputs.custom(1, 12, 5000, 64, D, 4096, recipe="hot4096_masked10", seed=50)
+    print(P.check_full(x))
+
+
 @pytest.mark.parametrize("ci", [1, 2, 3, 4])
 def test_full_size_workloads_sampled(ci):
     """The full-size workloads (fwd h64/d512/k512; h128/d512/k2048 recent;
     hot-4096 scatter stress; 32k long context), run whole on the GPU in the
-    benchmark's launch configuration and checked on a seeded token sample."""
+    benchmark's launch configuration and checked on a seeded sample of 256
+    tokens (plus s = 0, topk-1, topk and S-1 of every batch element)."""
     cfg = inputs.CONFIGS[ci]
     x = inputs.make_inputs(cfg, device="cuda")
-    tokens = P.sample_tokens(cfg.B, cfg.S, cfg.topk, 24, seed=100 + ci)
+    tokens = P.sample_tokens(cfg.B, cfg.S, cfg.topk, 256, seed=100 + ci)
     errs = P.check_sampled(x, tokens, do_fwd=cfg.passes != "bwd",
                            do_bwd=cfg.passes != "fwd")
     print(cfg.name, errs)
