@@ -12,9 +12,9 @@ the GPU.
 from .api import (SparseMQAFunction, bwd_workspace_bytes, device_status,  # noqa: F401
                   fwd_bwd_host_workspace_bytes, fwd_host_workspace_bytes, fwd_workspace_bytes,
                   sparse_mqa, sparse_mqa_bwd_interface, sparse_mqa_fwd_bwd_host,
-                  sparse_mqa_fwd_host, sparse_mqa_fwd_interface)
+                  set_wait_limit_ns, sparse_mqa_fwd_host, sparse_mqa_fwd_interface)
 
 __all__ = ["sparse_mqa_fwd_interface", "sparse_mqa_bwd_interface", "sparse_mqa",
            "SparseMQAFunction", "bwd_workspace_bytes", "fwd_workspace_bytes", "device_status",
            "sparse_mqa_fwd_host", "sparse_mqa_fwd_bwd_host", "fwd_host_workspace_bytes",
-           "fwd_bwd_host_workspace_bytes"]
+           "fwd_bwd_host_workspace_bytes", "set_wait_limit_ns"]

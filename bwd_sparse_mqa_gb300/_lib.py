@@ -31,7 +31,7 @@ EXPORTS = [
     "smqa_abi_version", "smqa_bwd_static_scratch", "smqa_bwd_exchange_bytes",
     "smqa_fwd_workspace_bytes", "smqa_fwd_static_scratch", "smqa_bwd_sink_grad",
     "smqa_fwd_host_workspace_bytes", "smqa_fwd_bwd_host_workspace_bytes", "smqa_fwd_host",
-    "smqa_fwd_bwd_host", "smqa_host_chunk_plan",
+    "smqa_fwd_bwd_host", "smqa_host_chunk_plan", "smqa_set_wait_limit_ns", "smqa_debug_stall",
 ]
 STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -83,6 +83,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.smqa_fwd_bwd_host.argtypes = [P, P, P, P, P, S, F, P, P, P, P, P, P, ctypes.c_size_t, U,
                                       P]
     lib.smqa_fwd_bwd_host.restype = st
+    lib.smqa_debug_stall.argtypes = [ctypes.c_int]
+    lib.smqa_debug_stall.restype = None
+    lib.smqa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.smqa_set_wait_limit_ns.restype = ctypes.c_uint64
     lib.smqa_device_status.argtypes = [ctypes.c_int]
     lib.smqa_device_status.restype = st
     lib.smqa_status_string.argtypes = [st]

@@ -59,6 +59,17 @@ def _shape(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor,
     return _lib.Shape(B, S, kv.shape[1], H, D, topk_idxs.shape[2])
 
 
+def _check_device(device: torch.device, what: str) -> None:
+    """Synchronizes ``device`` and raises SMQAError if a kernel's bounded
+    wait ran out (the status word stays set; device_status(clear=True)
+    resets it)."""
+    with torch.cuda.device(device):
+        st = int(_lib.load().smqa_device_status(0))
+    if st != _lib.SMQA_OK:
+        raise _lib.SMQAError(what, st, "a kernel's bounded wait ran out; its outputs are "
+                             "undefined (device_status(clear=True) resets the status)")
+
+
 def _scale(sm_scale: Optional[float], D: int) -> float:
     """None selects D^-1/2 (the pages' default); a value is used as given."""
     if sm_scale is None:
@@ -73,7 +84,8 @@ def sparse_mqa_fwd_interface(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch
                              topk_idxs: torch.Tensor, sm_scale: Optional[float] = None,
                              block_I: int = 64, num_stages: int = 2, threads: int = 256,
                              reference_rounding: bool = False,
-                             workspace: Optional[torch.Tensor] = None
+                             workspace: Optional[torch.Tensor] = None,
+                             check_status: bool = False
                              ) -> tuple[torch.Tensor, torch.Tensor]:
     """Top-k sparse MQA forward.
 
@@ -82,7 +94,9 @@ def sparse_mqa_fwd_interface(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch
     [0,S_kv) are masked).  Returns freshly allocated O [B,S,H,D] bf16 and
     LSE [B,S,H] fp32 = log2(sum_valid exp(sm_scale q.k) + exp(sink)).
     ``workspace`` (uint8 CUDA tensor, D = 512 only) may be passed to reuse
-    the exchange pool between calls; otherwise one is allocated.
+    the exchange pool between calls; otherwise one is allocated.  With
+    ``check_status`` the call synchronizes and raises SMQAError
+    (SMQA_ERR_DEVICE_TIMEOUT) if a kernel's bounded wait ran out.
     """
     shp = _shape(q, kv, attn_sink, topk_idxs)
     scale = _scale(sm_scale, shp.D)
@@ -102,6 +116,8 @@ def sparse_mqa_fwd_interface(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch
                                             shp, scale, _ptr(o), _ptr(lse), _ptr(workspace),
                                             0 if workspace is None else workspace.numel(), flags,
                                             _stream(q.device)))
+    if check_status:
+        _check_device(q.device, "smqa_fwd")
     return o, lse
 
 
@@ -119,17 +135,21 @@ def sparse_mqa_bwd_interface(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch
                              lse: torch.Tensor, sm_scale: Optional[float] = None,
                              return_dkv_accum_dtype: bool = False,
                              workspace: Optional[torch.Tensor] = None,
-                             return_dsink: bool = False, deterministic: bool = False):
+                             return_dsink: bool = False, deterministic: bool = False,
+                             check_status: bool = False):
     """Top-k sparse MQA backward.
 
     Takes the forward's inputs, its output o, the gradient do [B,S,H,D] bf16
     and its log2 lse [B,S,H] fp32.  Returns freshly allocated dq [B,S,H,D]
     bf16 and dkv [B,S_kv,D] (bf16, or fp32 with return_dkv_accum_dtype), and
     with ``return_dsink`` also the gradient w.r.t. attn_sink (fp32 [H]; not
-    among the pages' outputs).  ``deterministic`` accumulates dkv in 32.32
-    fixed point with integer atomics, so it is bit-identical from run to run
-    (not a switch of the pages).  ``workspace`` (uint8 CUDA tensor) may be
-    passed to reuse scratch memory between calls; otherwise one is allocated.
+    among the pages' outputs).  ``deterministic`` accumulates dkv in 64-bit
+    fixed point (binary point chosen per call from the inputs' magnitudes)
+    with integer atomics, so it is bit-identical from run to run (not a
+    switch of the pages).  ``workspace`` (uint8 CUDA tensor) may be passed to
+    reuse scratch memory between calls; otherwise one is allocated.  With
+    ``check_status`` the call synchronizes and raises SMQAError
+    (SMQA_ERR_DEVICE_TIMEOUT) if a kernel's bounded wait ran out.
     """
     shp = _shape(q, kv, attn_sink, topk_idxs)
     _need(o, "o", torch.bfloat16, 4)
@@ -161,6 +181,8 @@ def sparse_mqa_bwd_interface(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch
                                             _ptr(topk_idxs), _ptr(lse), shp, scale, _ptr(dq),
                                             _ptr(dkv), _ptr(dsink), _ptr(workspace),
                                             workspace.numel(), flags, _stream(q.device)))
+    if check_status:
+        _check_device(q.device, "smqa_bwd")
     return (dq, dkv, dsink) if return_dsink else (dq, dkv)
 
 
@@ -304,15 +326,23 @@ def device_status(clear: bool = True) -> int:
     return int(_lib.load().smqa_device_status(1 if clear else 0))
 
 
+def set_wait_limit_ns(ns: int) -> int:
+    """Limit of every bounded wait in kernels launched from now on (0: the
+    default, SMQA_WAIT_LIMIT_NS or 4 s); returns the previous limit."""
+    return int(_lib.load().smqa_set_wait_limit_ns(int(ns)))
+
+
 class SparseMQAFunction(torch.autograd.Function):
     """Autograd around the forward and backward kernels: gradients flow from
     O to q, kv and attn_sink (the LSE output is not differentiable)."""
 
     @staticmethod
-    def forward(ctx, q, kv, attn_sink, topk_idxs, sm_scale=None):
-        o, lse = sparse_mqa_fwd_interface(q, kv, attn_sink, topk_idxs, sm_scale)
+    def forward(ctx, q, kv, attn_sink, topk_idxs, sm_scale=None, check_status=False):
+        o, lse = sparse_mqa_fwd_interface(q, kv, attn_sink, topk_idxs, sm_scale,
+                                          check_status=check_status)
         ctx.save_for_backward(q, kv, attn_sink, topk_idxs, o, lse)
         ctx.sm_scale = sm_scale
+        ctx.check_status = check_status
         ctx.mark_non_differentiable(lse)
         return o, lse
 
@@ -321,13 +351,15 @@ class SparseMQAFunction(torch.autograd.Function):
         q, kv, attn_sink, topk_idxs, o, lse = ctx.saved_tensors
         dq, dkv, dsink = sparse_mqa_bwd_interface(
             q, kv, attn_sink, o, do.to(torch.bfloat16).contiguous(), topk_idxs, lse,
-            ctx.sm_scale, return_dsink=True)
-        return dq, dkv, dsink.to(attn_sink.dtype), None, None
+            ctx.sm_scale, return_dsink=True, check_status=ctx.check_status)
+        return dq, dkv, dsink.to(attn_sink.dtype), None, None, None
 
 
 def sparse_mqa(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor,
-               topk_idxs: torch.Tensor, sm_scale: Optional[float] = None
-               ) -> tuple[torch.Tensor, torch.Tensor]:
+               topk_idxs: torch.Tensor, sm_scale: Optional[float] = None,
+               check_status: bool = False) -> tuple[torch.Tensor, torch.Tensor]:
     """Differentiable top-k sparse MQA: (O, LSE) as sparse_mqa_fwd_interface
-    returns them, with gradients w.r.t. q, kv and attn_sink through O."""
-    return SparseMQAFunction.apply(q, kv, attn_sink, topk_idxs, sm_scale)
+    returns them, with gradients w.r.t. q, kv and attn_sink through O.  With
+    ``check_status`` the forward and the backward each synchronize and raise
+    SMQAError if a kernel's bounded wait ran out."""
+    return SparseMQAFunction.apply(q, kv, attn_sink, topk_idxs, sm_scale, check_status)

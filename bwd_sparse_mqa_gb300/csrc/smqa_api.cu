@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -52,7 +53,7 @@ int* status_ptr(cudaError_t* err) {
   return g_status_ptr[dev];
 }
 
-uint64_t wait_limit_ns() {
+uint64_t default_wait_limit_ns() {
   static uint64_t v = [] {
     const char* s = std::getenv("SMQA_WAIT_LIMIT_NS");
     if (s && *s) {
@@ -62,6 +63,16 @@ uint64_t wait_limit_ns() {
     return static_cast<uint64_t>(4000000000ull);
   }();
   return v;
+}
+
+// A limit set through smqa_set_wait_limit_ns (0: none, use the default).
+std::atomic<uint64_t> g_wait_limit_override{0};
+// The CTA set through smqa_debug_stall (-1: none).
+std::atomic<int> g_stall_cta{-1};
+
+uint64_t wait_limit_ns() {
+  const uint64_t o = g_wait_limit_override.load(std::memory_order_relaxed);
+  return o != 0 ? o : default_wait_limit_ns();
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -174,6 +185,7 @@ smqa_status bwd_main_impl(const void* q, const void* kv, const void* dout, const
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = st;
   p.limit_ns = wait_limit_ns();
+  p.stall_cta = g_stall_cta.load(std::memory_order_relaxed);
   if (exchange_bytes(s) != 0) {
     p.slot_flags = static_cast<int*>(exch);
     p.exch = static_cast<uint8_t*>(exch) + kExchFlagBytes;
@@ -274,6 +286,7 @@ smqa_status smqa_fwd(const void* q, const void* kv, const float* attn_sink,
   p.ref_round = (flags & SMQA_FLAG_REFERENCE_ROUNDING) ? 1 : 0;
   p.status = st;
   p.limit_ns = wait_limit_ns();
+  p.stall_cta = g_stall_cta.load(std::memory_order_relaxed);
   if (need != 0) {
     p.slot_flags = static_cast<int*>(workspace);
     p.exch = static_cast<uint8_t*>(workspace) + kExchFlagBytes;
@@ -450,6 +463,14 @@ smqa_status smqa_bwd(const void* q, const void* kv, const float* attn_sink, cons
   if (!fp32_out) return smqa_bwd_postprocess(acc, shape, dkv, stream);
   return SMQA_OK;
 }
+
+uint64_t smqa_set_wait_limit_ns(uint64_t ns) {
+  const uint64_t before = wait_limit_ns();
+  g_wait_limit_override.store(ns, std::memory_order_relaxed);
+  return before;
+}
+
+void smqa_debug_stall(int cta) { g_stall_cta.store(cta < 0 ? -1 : cta, std::memory_order_relaxed); }
 
 smqa_status smqa_device_status(int clear) {
   cudaError_t e;

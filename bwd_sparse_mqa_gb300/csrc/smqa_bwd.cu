@@ -630,6 +630,10 @@ __global__ void __launch_bounds__(480, 1)
           tc_fence_after();
           issue_sdp(ns);
           ++ns;
+          if (static_cast<int>(blockIdx.x) == p.stall_cta) {  // test hook only
+            ok = stall_until_limit(ctl);
+            break;
+          }
         } else {
           if ((++spins & 63u) == 0u && !poll_check(ctl, ps)) {
             ok = false;

@@ -24,6 +24,7 @@ struct FwdParams {
   int ref_round;         // 1: exp2 argument as (score * scale) * log2(e)
   int* status;           // device status word
   uint64_t limit_ns;     // bounded-wait limit
+  int stall_cta;         // test hook: this CTA stalls after its first MMA (-1: none)
   // D split across a CTA pair: the pairs trade their partial scores through
   // an L2-resident pool of nslots slots (kFwdSlotBytes each); slot_flags[s]
   // is 1 while a pair holds slot s (all zero before the launch).
@@ -50,6 +51,7 @@ struct BwdParams {
   float scale_log2;      // sm_scale * log2(e)
   int* status;
   uint64_t limit_ns;
+  int stall_cta;         // test hook: this CTA stalls after its first MMA (-1: none)
   // D split across a CTA pair: the pairs trade their partial S / dP through
   // an L2-resident pool of nslots slots (kBwdSlotBytes each); slot_flags[s]
   // is 1 while a pair holds slot s (all zero before the launch).

@@ -137,6 +137,16 @@ __device__ __forceinline__ bool poll_check(const WaitCtl& c, PollState& ps) {
   return true;
 }
 
+// Test hook (the library's smqa_debug_stall): waits for a condition that
+// never comes true, bounded like every wait, until the limit runs out and
+// the CTA aborts.  Returns false.
+__device__ __forceinline__ bool stall_until_limit(const WaitCtl& c) {
+  PollState ps = poll_start();
+  while (poll_check(c, ps)) {
+  }
+  return false;
+}
+
 // Waits until the phase with parity `parity` of `bar` has completed.
 // Returns false (and aborts the CTA) if the limit runs out or the CTA has
 // already aborted.

@@ -25,7 +25,8 @@
  *     Argument checks happen on the host before anything is launched; a
  *     rejected call launches nothing and leaves every output untouched.
  *   - A kernel that waits longer than its bounded limit (4 s per wait, or
- *     SMQA_WAIT_LIMIT_NS nanoseconds from the environment) records
+ *     SMQA_WAIT_LIMIT_NS nanoseconds from the environment, or the value set by
+ *     smqa_set_wait_limit_ns) records
  *     SMQA_ERR_DEVICE_TIMEOUT in a per-device status word and exits cleanly;
  *     read it with smqa_device_status().  The word is sticky: while it is set,
  *     the forward and backward-main kernels skip their work (their outputs
@@ -45,7 +46,7 @@
 extern "C" {
 #endif
 
-#define SMQA_ABI_VERSION 5
+#define SMQA_ABI_VERSION 6
 
 typedef enum {
     SMQA_OK = 0,
@@ -319,6 +320,31 @@ smqa_status smqa_bwd_sink_grad(const float* attn_sink, const float* lse, const f
  * `clear` resets the word afterwards.
  */
 smqa_status smqa_device_status(int clear);
+
+/*
+ * Sets the limit, in nanoseconds, of every bounded wait in the kernels
+ * launched after this call (all devices, all threads); 0 restores the
+ * default (SMQA_WAIT_LIMIT_NS from the environment, else 4 s).  Returns the
+ * limit in force before the call.  A wait that runs out makes its kernel
+ * record SMQA_ERR_DEVICE_TIMEOUT and exit without finishing its work (the
+ * outputs of that call are undefined); the GPU context stays usable.  This
+ * is how a watchdog can be tightened, and how the failure path is tested
+ * without hanging a GPU.  Not a function of the pages.
+ */
+uint64_t smqa_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Test hook for the failure path.  In every forward and backward-main launch
+ * after this call, CTA `cta` (a block index of the launch; -1 turns the hook
+ * off) stops after issuing its first tensor-core instruction and waits for a
+ * condition that never comes true.  The wait is bounded like every other, so
+ * after the wait limit the CTA records SMQA_ERR_DEVICE_TIMEOUT, drains its
+ * copies and MMAs, frees TMEM and exits, and the other CTAs stop at their
+ * next check of the status word: the same path a real stall would take, with
+ * no fault, trap or endless loop.  Outputs of those launches are undefined.
+ * Not for production use.  Not a function of the pages.
+ */
+void smqa_debug_stall(int cta);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* smqa_status_string(smqa_status status);

@@ -32,10 +32,21 @@ def test_exports_match_header(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.smqa_abi_version() == 5
+    assert lib.smqa_abi_version() == 6
     assert lib.smqa_status_string(0) == b"SMQA_OK"
     assert lib.smqa_status_string(4) == b"SMQA_ERR_DEVICE_TIMEOUT"
     assert lib.smqa_status_string(99) == b"SMQA_ERR_UNKNOWN"
+
+
+def test_wait_limit_setter(lib):
+    """smqa_set_wait_limit_ns returns the limit in force before the call and
+    0 restores the default (4 s unless SMQA_WAIT_LIMIT_NS is set).  Host
+    state only: nothing is launched."""
+    default = lib.smqa_set_wait_limit_ns(0)
+    assert default > 0
+    assert lib.smqa_set_wait_limit_ns(12345) == default
+    assert lib.smqa_set_wait_limit_ns(0) == 12345
+    assert lib.smqa_set_wait_limit_ns(0) == default
 
 
 def _fake(addr=0x10000):
