@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for top-k sparse MQA with an attention sink.
+"""fp64 CPU oracle for top-k sparse MQA with an attention sink, and for the
+lightning-indexer backward.
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg may import this package; the product package
@@ -47,6 +48,13 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.smqa_oracle_fwd_f64.restype = ctypes.c_int
     lib.smqa_oracle_bwd_f64.argtypes = lib.smqa_oracle_bwd.argtypes
     lib.smqa_oracle_bwd_f64.restype = ctypes.c_int
+    lib.smqa_oracle_indexer_bwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, P, i64, f64,
+                                            P, P]
+    lib.smqa_oracle_indexer_bwd.restype = ctypes.c_int
+    lib.smqa_oracle_indexer_bwd_f64.argtypes = lib.smqa_oracle_indexer_bwd.argtypes
+    lib.smqa_oracle_indexer_bwd_f64.restype = ctypes.c_int
+    lib.smqa_oracle_indexer_scores_f64.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P, i64, P]
+    lib.smqa_oracle_indexer_scores_f64.restype = ctypes.c_int
     lib.smqa_oracle_num_threads.argtypes = []
     lib.smqa_oracle_num_threads.restype = ctypes.c_int
     return lib
@@ -186,3 +194,92 @@ def bwd_f64(q, kv, attn_sink, topk_idxs, dout, sm_scale: float | None = None, to
     if rc != 0:
         raise ValueError("oracle bwd rejected its arguments")
     return dq, dkv, dsink, delta
+
+
+# ---------------------------------------------------------------------------
+# Lightning-indexer backward (tilelang_indexer_bwd page; reading in the C
+# source: score[t,j] = sum_h w[t,h] ReLU(<q[t,h], k[idx[t,j]]>), dq only).
+# ---------------------------------------------------------------------------
+def _tok(tokens, n_all):
+    tok = None if tokens is None else np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
+    return tok, (n_all if tok is None else len(tok))
+
+
+def indexer_bwd(index_q, weights, index_k, topk_indices, grad_scores, tokens=None,
+                amb: float = 0.0, lib=None):
+    """dq (fp64 [n,H,D]) and its slack (fp64 [n,H,D], see the C source) for
+    one batch element: index_q [S,H,D] bf16, weights [S,H] fp32, index_k
+    [S_kv,D] bf16, topk_indices [S,topk] int32, grad_scores [S,topk] fp32."""
+    q16, k16 = _u16(index_q), _u16(index_k)
+    w = _np(weights, np.float32)
+    idx = _np(topk_indices, np.int32)
+    g = _np(grad_scores, np.float32)
+    S, H, D = q16.shape
+    S_kv = k16.shape[0]
+    topk = idx.shape[1]
+    tok, n = _tok(tokens, S)
+    dq = np.empty((n, H, D), np.float64)
+    slack = np.empty((n, H, D), np.float64)
+    rc = (lib or load()).smqa_oracle_indexer_bwd(_ptr(q16), _ptr(w), _ptr(k16), _ptr(idx),
+                                                 _ptr(g), S, S_kv, H, D, topk, _ptr(tok), n,
+                                                 float(amb), _ptr(dq), _ptr(slack))
+    if rc != 0:
+        raise ValueError("oracle indexer bwd rejected its arguments")
+    return dq, slack
+
+
+def indexer_bwd_f64(index_q, weights, index_k, topk_indices, grad_scores, tokens=None,
+                    amb: float = 0.0, lib=None):
+    """The indexer backward on fp64 numpy inputs; returns (dq, slack)."""
+    q, w, k = _np(index_q, np.float64), _np(weights, np.float64), _np(index_k, np.float64)
+    idx, g = _np(topk_indices, np.int32), _np(grad_scores, np.float64)
+    S, H, D = q.shape
+    S_kv, topk = k.shape[0], idx.shape[1]
+    tok, n = _tok(tokens, S)
+    dq = np.empty((n, H, D), np.float64)
+    slack = np.empty((n, H, D), np.float64)
+    rc = (lib or load()).smqa_oracle_indexer_bwd_f64(_ptr(q), _ptr(w), _ptr(k), _ptr(idx),
+                                                     _ptr(g), S, S_kv, H, D, topk, _ptr(tok), n,
+                                                     float(amb), _ptr(dq), _ptr(slack))
+    if rc != 0:
+        raise ValueError("oracle indexer bwd rejected its arguments")
+    return dq, slack
+
+
+def indexer_scores_f64(index_q, weights, index_k, topk_indices, tokens=None, lib=None):
+    """score[t,j] (fp64 [n,topk]) of the reading, on fp64 numpy inputs."""
+    q, w, k = _np(index_q, np.float64), _np(weights, np.float64), _np(index_k, np.float64)
+    idx = _np(topk_indices, np.int32)
+    S, H, D = q.shape
+    S_kv, topk = k.shape[0], idx.shape[1]
+    tok, n = _tok(tokens, S)
+    out = np.empty((n, topk), np.float64)
+    rc = (lib or load()).smqa_oracle_indexer_scores_f64(_ptr(q), _ptr(w), _ptr(k), _ptr(idx),
+                                                        S, S_kv, H, D, topk, _ptr(tok), n,
+                                                        _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle indexer scores rejected its arguments")
+    return out
+
+
+def indexer_bwd_batched(index_q, weights, index_k, topk_indices, grad_scores, tokens=None,
+                        amb: float = 0.0, lib=None):
+    """The batched layouts of `batched_indexer_bwd`: index_q [S,B,H,D],
+    weights [S,B,H], index_k [S_kv,B,D], topk_indices [B,S,topk],
+    grad_scores [B,S,topk].  Runs the single-element oracle on each batch
+    element (the page's function loops over the batch the same way) and
+    returns dq and slack as fp64 [S,B,H,D] (tokens: per-element positions s,
+    then [n,B,H,D])."""
+    q = index_q.detach().cpu()
+    S, B, H, D = q.shape
+    n = S if tokens is None else len(tokens)
+    dq = np.empty((n, B, H, D), np.float64)
+    slack = np.empty((n, B, H, D), np.float64)
+    for b in range(B):
+        d1, s1 = indexer_bwd(q[:, b].contiguous(), weights.detach().cpu()[:, b].contiguous(),
+                             index_k.detach().cpu()[:, b].contiguous(),
+                             topk_indices.detach().cpu()[b].contiguous(),
+                             grad_scores.detach().cpu()[b].contiguous(), tokens=tokens, amb=amb,
+                             lib=lib)
+        dq[:, b], slack[:, b] = d1, s1
+    return dq, slack

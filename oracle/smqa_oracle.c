@@ -1,6 +1,7 @@
 /*
  * smqa_oracle.c -- plain fp64 CPU oracle for top-k sparse multi-query
- * attention with a per-head attention sink, forward and backward.
+ * attention with a per-head attention sink, forward and backward, and for
+ * the lightning-indexer backward (at the end of this file).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call, link or
  * load this file: only the tests, the smoke check and the benchmark's
@@ -325,4 +326,183 @@ int smqa_oracle_bwd_f64(const double* q, const double* kv, const double* sink, c
     tref tq = {q, 1}, tkv = {kv, 1}, tdo = {dout, 1};
     return bwd_impl(tq, tkv, sink, idx, tdo, B, S, S_kv, H, D, topk, sm_scale, tokens, n_tok,
                     dq, dkv, dsink, delta);
+}
+
+/* ==========================================================================
+ * Lightning-indexer backward (DeepSeek-V4 kernel API pages of NeMo
+ * AutoModel, tilelang_indexer_bwd: `indexer_bwd_interface` for one batch
+ * element and `batched_indexer_bwd`).  The pages give the tensors only:
+ * index_q [S,H,D] bf16, weights [S,H] fp32, index_k [S_kv,D] bf16,
+ * topk_indices [S,topk] int32, grad_scores [S,topk] fp32, and one returned
+ * tensor [S,H,D] bf16, the gradient with respect to index_q.  They print no
+ * scoring formula.  Reading (reading-dependent: not pinned by the pages):
+ * the lightning indexer's score of slot j of token t is
+ *
+ *   score[t,j] = sum_h w[t,h] * ReLU(<q[t,h,:], k[idx[t,j],:]>)
+ *
+ * with masked slots (index outside [0,S_kv)) scoring 0, so
+ *
+ *   dq[t,h,:] = w[t,h] * sum_{valid j} g[t,j] * [<q[t,h,:], k_j> > 0] * k_j
+ *
+ * (the ReLU's derivative taken as 0 at 0).  A slot listed twice counts twice.
+ *
+ * The gate [<q,k_j> > 0] is a decision taken in floating point: a GPU that
+ * forms <q,k_j> in fp32 can decide differently where the exact value lies
+ * within its rounding of 0.  With amb > 0 every (token, head, slot) whose
+ * fp64 logit has |<q,k_j>| <= amb * sum_d |q_d k_jd| is left out of dq and
+ * the magnitude of its term |w g k_j| is added to slack[t,h,:], so a result
+ * that takes either decision there lies within slack of dq.  amb = 0 gives
+ * the plain definition (slack stays 0).
+ * ========================================================================== */
+
+/* score[i,j] for the selected tokens (scores: double [n_tok, topk]). */
+static int indexer_scores_impl(tref q, const double* w, tref k, const int32_t* idx, int S,
+                               int S_kv, int H, int D, int topk, const int64_t* tokens,
+                               int64_t n_tok, double* scores)
+{
+    if (S <= 0 || S_kv <= 0 || H <= 0 || D <= 0 || topk <= 0 || n_tok < 0) return -1;
+    if (!tokens && n_tok != (int64_t)S) return -1;
+    int err = 0;
+#pragma omp parallel
+    {
+        double* qh = (double*)malloc(sizeof(double) * (size_t)D);
+        double* kj = (double*)malloc(sizeof(double) * (size_t)D);
+        if (!qh || !kj) {
+#pragma omp atomic write
+            err = 1;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t i = 0; i < n_tok; ++i) {
+                int64_t t = tokens ? tokens[i] : i;
+                if (t < 0 || t >= (int64_t)S) {
+#pragma omp atomic write
+                    err = 1;
+                    continue;
+                }
+                const int32_t* idx_row = idx + (size_t)t * topk;
+                for (int j = 0; j < topk; ++j) {
+                    double sc = 0.0;
+                    if (slot_is_valid(idx_row[j], S_kv)) {
+                        load_row(k, (size_t)idx_row[j] * D, D, kj);
+                        for (int h = 0; h < H; ++h) {
+                            load_row(q, ((size_t)t * H + h) * D, D, qh);
+                            double l = 0.0;
+                            for (int d = 0; d < D; ++d) l += qh[d] * kj[d];
+                            if (l > 0.0) sc += w[(size_t)t * H + h] * l;
+                        }
+                    }
+                    scores[(size_t)i * topk + j] = sc;
+                }
+            }
+        }
+        free(qh); free(kj);
+    }
+    return err ? -1 : 0;
+}
+
+/* dq (and slack) for the selected tokens: double [n_tok, H, D] each. */
+static int indexer_bwd_impl(tref q, const double* w, tref k, const int32_t* idx,
+                            const double* g, int S, int S_kv, int H, int D, int topk,
+                            const int64_t* tokens, int64_t n_tok, double amb, double* dq,
+                            double* slack)
+{
+    if (S <= 0 || S_kv <= 0 || H <= 0 || D <= 0 || topk <= 0 || n_tok < 0 || amb < 0.0) return -1;
+    if (!tokens && n_tok != (int64_t)S) return -1;
+    int err = 0;
+#pragma omp parallel
+    {
+        double* qh = (double*)malloc(sizeof(double) * (size_t)D);
+        double* rows = (double*)malloc(sizeof(double) * (size_t)topk * D);
+        unsigned char* valid = (unsigned char*)malloc((size_t)topk);
+        if (!qh || !rows || !valid) {
+#pragma omp atomic write
+            err = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t i = 0; i < n_tok; ++i) {
+                int64_t t = tokens ? tokens[i] : i;
+                if (t < 0 || t >= (int64_t)S) {
+#pragma omp atomic write
+                    err = 1;
+                    continue;
+                }
+                const int32_t* idx_row = idx + (size_t)t * topk;
+                for (int j = 0; j < topk; ++j) {
+                    valid[j] = (unsigned char)slot_is_valid(idx_row[j], S_kv);
+                    if (valid[j]) load_row(k, (size_t)idx_row[j] * D, D, rows + (size_t)j * D);
+                }
+                for (int h = 0; h < H; ++h) {
+                    load_row(q, ((size_t)t * H + h) * D, D, qh);
+                    const double wh = w[(size_t)t * H + h];
+                    double* dqrow = dq + ((size_t)i * H + h) * D;
+                    double* slrow = slack ? slack + ((size_t)i * H + h) * D : NULL;
+                    for (int d = 0; d < D; ++d) dqrow[d] = 0.0;
+                    if (slrow)
+                        for (int d = 0; d < D; ++d) slrow[d] = 0.0;
+                    for (int j = 0; j < topk; ++j) {
+                        if (!valid[j]) continue;
+                        const double* kj = rows + (size_t)j * D;
+                        double l = 0.0, mag = 0.0;
+                        for (int d = 0; d < D; ++d) {
+                            l += qh[d] * kj[d];
+                            mag += fabs(qh[d] * kj[d]);
+                        }
+                        const double gj = g[(size_t)t * topk + j];
+                        if (amb > 0.0 && fabs(l) <= amb * mag) {
+                            if (slrow)
+                                for (int d = 0; d < D; ++d) slrow[d] += fabs(wh * gj * kj[d]);
+                            continue;
+                        }
+                        if (l > 0.0)
+                            for (int d = 0; d < D; ++d) dqrow[d] += wh * gj * kj[d];
+                    }
+                }
+            }
+        }
+        free(qh); free(rows); free(valid);
+    }
+    return err ? -1 : 0;
+}
+
+static double* f32_to_f64(const float* s, size_t n)
+{
+    double* out = (double*)malloc(sizeof(double) * (n > 0 ? n : 1));
+    if (out)
+        for (size_t i = 0; i < n; ++i) out[i] = (double)s[i];
+    return out;
+}
+
+int smqa_oracle_indexer_bwd(const uint16_t* q, const float* w, const uint16_t* k,
+                            const int32_t* idx, const float* g, int S, int S_kv, int H, int D,
+                            int topk, const int64_t* tokens, int64_t n_tok, double amb,
+                            double* dq, double* slack)
+{
+    double* w64 = f32_to_f64(w, (size_t)S * (size_t)H);
+    double* g64 = f32_to_f64(g, (size_t)S * (size_t)topk);
+    int rc = -1;
+    if (w64 && g64) {
+        tref tq = {q, 0}, tk = {k, 0};
+        rc = indexer_bwd_impl(tq, w64, tk, idx, g64, S, S_kv, H, D, topk, tokens, n_tok, amb, dq,
+                              slack);
+    }
+    free(w64); free(g64);
+    return rc;
+}
+
+int smqa_oracle_indexer_bwd_f64(const double* q, const double* w, const double* k,
+                                const int32_t* idx, const double* g, int S, int S_kv, int H,
+                                int D, int topk, const int64_t* tokens, int64_t n_tok,
+                                double amb, double* dq, double* slack)
+{
+    tref tq = {q, 1}, tk = {k, 1};
+    return indexer_bwd_impl(tq, w, tk, idx, g, S, S_kv, H, D, topk, tokens, n_tok, amb, dq,
+                            slack);
+}
+
+int smqa_oracle_indexer_scores_f64(const double* q, const double* w, const double* k,
+                                   const int32_t* idx, int S, int S_kv, int H, int D, int topk,
+                                   const int64_t* tokens, int64_t n_tok, double* scores)
+{
+    tref tq = {q, 1}, tk = {k, 1};
+    return indexer_scores_impl(tq, w, tk, idx, S, S_kv, H, D, topk, tokens, n_tok, scores);
 }

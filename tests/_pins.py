@@ -357,6 +357,135 @@ def pin_query_scale_equals_sm_scale(lib):
     _close(ds1, ds2, rtol=1e-12, atol=1e-14, what="dsink under q scaling")
 
 
+# ---------------------------------------------------------------------------
+# Lightning-indexer backward (tilelang_indexer_bwd page; the reading
+# score[t,j] = sum_h w[t,h] ReLU(<q[t,h], k[idx[t,j]]>) is not given by the
+# page, so these pins tie the oracle to that reading, not to the page).
+# ---------------------------------------------------------------------------
+def _tiny_indexer(rng, S=3, H=3, D=5, S_kv=6, topk=4):
+    q = _rand((S, H, D), rng)
+    w = _rand((S, H), rng)
+    k = _rand((S_kv, D), rng)
+    g = _rand((S, topk), rng)
+    idx = np.stack([_perm_rows(S_kv, topk, rng) for _ in range(S)]).astype(np.int32)
+    idx[0, 1] = -1          # masked by -1
+    idx[S - 1, 0] = S_kv    # masked by S_kv
+    idx[1, 2] = idx[1, 0]   # a row listed twice
+    return q, w, k, idx, g
+
+
+def pin_indexer_dense_autograd(lib):
+    """dq equals torch autograd (fp64) of sum_{t,j} g[t,j] score[t,j], the
+    score built from torch's matmul and relu over the listed rows."""
+    rng = np.random.default_rng(30)
+    q, w, k, idx, g = _tiny_indexer(rng)
+    S, H, D = q.shape
+    qt = torch.tensor(q, dtype=torch.float64, requires_grad=True)
+    kt = torch.tensor(k, dtype=torch.float64)
+    loss = qt.new_zeros(())
+    for t in range(S):
+        js = [j for j in range(idx.shape[1]) if 0 <= idx[t, j] < k.shape[0]]
+        rows = kt[[int(idx[t, j]) for j in js]]
+        logits = qt[t] @ rows.T                                     # [H, n]
+        score = (torch.tensor(w[t])[:, None] * torch.relu(logits)).sum(0)
+        loss = loss + (torch.tensor(g[t, js]) * score).sum()
+    (gq,) = torch.autograd.grad(loss, [qt])
+    dq, slack = oracle.indexer_bwd_f64(q, w, k, idx, g, lib=lib)
+    _close(dq, gq.numpy(), what="indexer dq vs autograd")
+    assert np.all(slack == 0.0), "slack without an ambiguity band"
+
+
+def pin_indexer_finite_differences(lib):
+    """Central differences of F(q) = sum g * score(q), with the oracle's own
+    score function, match dq (no logit near the ReLU kink)."""
+    rng = np.random.default_rng(31)
+    q, w, k, idx, g = _tiny_indexer(rng, S=2, H=2, D=4, S_kv=5, topk=3)
+    dq, _ = oracle.indexer_bwd_f64(q, w, k, idx, g, lib=lib)
+
+    def F(qq):
+        return float(np.sum(g * oracle.indexer_scores_f64(qq, w, k, idx, lib=lib)))
+
+    logits = np.einsum("thd,rd->thr", q, k)
+    assert np.min(np.abs(logits)) > 1e-4, "a logit sits on the kink; pick another seed"
+    eps = 1e-6
+    fd = np.zeros_like(q)
+    for pos in np.ndindex(*q.shape):
+        qp, qm = q.copy(), q.copy()
+        qp[pos] += eps
+        qm[pos] -= eps
+        fd[pos] = (F(qp) - F(qm)) / (2 * eps)
+    _close(dq, fd, rtol=1e-6, atol=1e-8, what="indexer dq vs finite differences")
+
+
+def pin_indexer_closed_forms(lib):
+    """All gates closed (every logit negative) gives dq = 0; all gates open
+    (every logit positive) gives the plain weighted sum
+    w[t,h] * sum_{valid j} g[t,j] k_j."""
+    rng = np.random.default_rng(32)
+    q, w, k, idx, g = _tiny_indexer(rng)
+    qn, kp = -np.abs(q), np.abs(k)
+    dq, _ = oracle.indexer_bwd_f64(qn, w, kp, idx, g, lib=lib)
+    assert np.all(dq == 0.0), "closed gates must give dq = 0"
+    qp = np.abs(q)
+    dq, _ = oracle.indexer_bwd_f64(qp, w, kp, idx, g, lib=lib)
+    want = np.zeros_like(q)
+    for t in range(q.shape[0]):
+        for j in range(idx.shape[1]):
+            if 0 <= idx[t, j] < k.shape[0]:
+                want[t] += np.outer(w[t], g[t, j] * kp[idx[t, j]])
+    _close(dq, want, what="indexer all-open closed form")
+
+
+def pin_indexer_invariants(lib):
+    """Masked slots equal dropped slots; permuting the slots together with
+    grad_scores changes nothing; dq is linear in grad_scores and in the
+    weights (power-of-two scalings are exact)."""
+    rng = np.random.default_rng(33)
+    q, w, k, idx, g = _tiny_indexer(rng, S=2, H=2, D=3, S_kv=7, topk=5)
+    idx[0] = [3, -1, 6, 7, 1]
+    idx[1] = [2, 4, -5, 0, 5]
+    base, _ = oracle.indexer_bwd_f64(q, w, k, idx, g, lib=lib)
+    keep = [[0, 2, 4], [0, 1, 3, 4]]
+    for t in range(2):
+        sub_idx = idx[t:t + 1, keep[t]].copy()
+        sub_g = g[t:t + 1, keep[t]].copy()
+        d1, _ = oracle.indexer_bwd_f64(q[t:t + 1], w[t:t + 1], k, sub_idx, sub_g, lib=lib)
+        _close(d1[0], base[t], what="indexer masked == dropped")
+    perm = rng.permutation(idx.shape[1])
+    d2, _ = oracle.indexer_bwd_f64(q, w, k, idx[:, perm].copy(), g[:, perm].copy(), lib=lib)
+    _close(d2, base, what="indexer slot permutation")
+    for a in (2.0 ** -20, 2.0 ** 7):
+        d3, _ = oracle.indexer_bwd_f64(q, w, k, idx, g * a, lib=lib)
+        assert np.array_equal(d3, base * a), "indexer dq not linear in grad_scores"
+        d4, _ = oracle.indexer_bwd_f64(q, w * a, k, idx, g, lib=lib)
+        assert np.array_equal(d4, base * a), "indexer dq not linear in weights"
+
+
+def pin_indexer_ambiguity_slack(lib):
+    """With an ambiguity band, every pair left out is accounted for: the
+    plain dq lies within slack of the banded one, and some slack is used."""
+    rng = np.random.default_rng(34)
+    q, w, k, idx, g = _tiny_indexer(rng, S=4, H=3, D=6, S_kv=8, topk=6)
+    plain, s0 = oracle.indexer_bwd_f64(q, w, k, idx, g, lib=lib)
+    banded, s1 = oracle.indexer_bwd_f64(q, w, k, idx, g, amb=0.3, lib=lib)
+    assert np.all(s0 == 0.0) and np.max(s1) > 0.0
+    assert np.all(np.abs(plain - banded) <= s1 + 1e-12), "slack does not cover the band"
+
+
+def pin_indexer_bf16_entry(lib):
+    """The bf16 entry point reads the same values as the fp64 one."""
+    rng = np.random.default_rng(35)
+    q, w, k, idx, g = _tiny_indexer(rng)
+    tq = torch.tensor(q).to(torch.bfloat16)
+    tk = torch.tensor(k).to(torch.bfloat16)
+    tw = torch.tensor(w, dtype=torch.float32)
+    tg = torch.tensor(g, dtype=torch.float32)
+    a, _ = oracle.indexer_bwd(tq, tw, tk, torch.tensor(idx), tg, lib=lib)
+    b, _ = oracle.indexer_bwd_f64(tq.double().numpy(), tw.double().numpy(), tk.double().numpy(),
+                                  idx, tg.double().numpy(), lib=lib)
+    assert np.array_equal(a, b), "indexer bf16 entry differs from fp64"
+
+
 ALL_PINS = [
     pin_dense_sdpa_fwd,
     pin_dense_autograd_bwd,
@@ -372,4 +501,10 @@ ALL_PINS = [
     pin_bf16_entry_matches_f64,
     pin_linear_in_dout,
     pin_query_scale_equals_sm_scale,
+    pin_indexer_dense_autograd,
+    pin_indexer_finite_differences,
+    pin_indexer_closed_forms,
+    pin_indexer_invariants,
+    pin_indexer_ambiguity_slack,
+    pin_indexer_bf16_entry,
 ]

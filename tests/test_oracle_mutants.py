@@ -35,6 +35,16 @@ MUTANTS = [
     ("dsink sign flipped", "dsink[h] += -psink * Delta;", "dsink[h] += psink * Delta;"),
     ("absolute floor on dP - Delta", "g[j] = p[j] * (dP - Delta);",
      "g[j] = fabs(dP - Delta) < 1e-7 ? 0.0 : p[j] * (dP - Delta);"),
+    ("indexer weight dropped", "dqrow[d] += wh * gj * kj[d];", "dqrow[d] += gj * kj[d];"),
+    ("indexer gate inverted", "if (l > 0.0)\n                            for (int d = 0; d < D; ++d) dqrow",
+     "if (l < 0.0)\n                            for (int d = 0; d < D; ++d) dqrow"),
+    ("indexer ReLU value instead of its slope", "dqrow[d] += wh * gj * kj[d];",
+     "dqrow[d] += wh * gj * l * kj[d];"),
+    ("indexer key row by slot number",
+     "if (valid[j]) load_row(k, (size_t)idx_row[j] * D, D, rows + (size_t)j * D);",
+     "if (valid[j]) load_row(k, (size_t)j * D, D, rows + (size_t)j * D);"),
+    ("indexer grad_scores of the mirrored slot", "const double gj = g[(size_t)t * topk + j];",
+     "const double gj = g[(size_t)t * topk + (topk - 1 - j)];"),
 ]
 
 
