@@ -517,6 +517,135 @@ def run_workload(args, name, dist, world, rank, local, dev):
     return line
 
 
+def run_indexer_workload(args, name, dist, world, rank, local, dev):
+    """The lightning-indexer backward (its own kernel; not part of the
+    attention step): one launch per step over the whole workload."""
+    cfg = inputs.indexer_by_name(name)
+    x = inputs.make_indexer_inputs(cfg, device=str(dev))
+    q, w, k, idx, g = (x["index_q"][0], x["weights"][0], x["index_k"][0], x["topk_indices"][0],
+                       x["grad_scores"][0])
+    S, S_kv, H, D, K = cfg.S, cfg.S_kv, cfg.H, cfg.D, cfg.topk
+    n_valid = int(((idx >= 0) & (idx < S_kv)).sum().item())
+    flops = 4.0 * H * D * n_valid          # L = q.k^T and dq += G.k, valid slots
+    nbytes = 2 * D * n_valid + 4 * H * D * S + 8 * K * S + 4 * H * S
+    lib = _lib.load()
+    shp = _lib.Shape(1, S, S_kv, H, D, K)
+    dq = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+
+    def launch():
+        _lib.check("indexer", lib.smqa_indexer_bwd(P(q), P(w), P(k), P(idx), P(g), shp, P(dq), sp))
+
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier(device_ids=[local])
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            evs[i][0].record(stream)
+            launch()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier(device_ids=[local])
+    if lib.smqa_device_status(1) != 0:
+        raise RuntimeError("device timeout in the indexer backward")
+    elapsed_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in evs), dist, dev)
+    t = elapsed_ms / args.steps
+    value = whole_job_rate(world, flops, args.steps, elapsed_ms) / 1e12
+
+    # End to end: page-locked host inputs -> device, the call, dq -> host.
+    host = {kk: v.cpu().pin_memory() for kk, v in (("q", q), ("w", w), ("k", k), ("idx", idx),
+                                                   ("g", g))}
+    dev_in = {kk: torch.empty_like(v, device=dev) for kk, v in host.items()}
+    out = torch.empty_like(host["q"]).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out.numel() * out.element_size()
+
+    def e2e_step():
+        for kk in host:
+            dev_in[kk].copy_(host[kk], non_blocking=True)
+        dd = dev_in
+        _lib.check("indexer", lib.smqa_indexer_bwd(P(dd["q"]), P(dd["w"]), P(dd["k"]),
+                                                   P(dd["idx"]), P(dd["g"]), shp, P(dq), sp))
+        out.copy_(dq, non_blocking=True)
+
+    e2e_windows = []
+    if args.e2e_steps > 0:
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        for _ in range(args.e2e_windows):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.e2e_steps):
+                e2e_step()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            e2e_windows.append(max_over_ranks(e0.elapsed_time(e1), dist, dev))
+    e2e_value = (whole_job_rate(world, flops, args.e2e_steps, statistics.median(e2e_windows))
+                 / 1e12 if e2e_windows else None)
+    if rank != 0:
+        return None
+    pk, src = peaks()
+    peak_tf = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
+    hbm = float(pk.get("hbm_gbs"))
+    ach = flops / (t * 1e-3) / 1e12
+    line = {
+        "metric": "lightning-indexer backward TFLOP/s + % BF16 roofline, 1\u00d7GB300",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": name, "B": 1, "S": S, "S_kv": S_kv, "H": H, "D": D, "topk": K,
+                   "index_recipe": cfg.recipe, "valid_slots": n_valid,
+                   "l2": "inputs larger than L2 (index_q, dq 128 MiB each, the index rows and "
+                         "grad_scores 64 MiB each); index_k 2 MiB stays L2-resident",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "kernel": "smqa_indexer_bwd_kernel", "achieved": ach,
+                     "peak": peak_tf, "unit": "TFLOP/s", "frac": ach / peak_tf,
+                     "peak_source": f"{src} bf16 sustained",
+                     "note": "H=64 fills half of the 128-row MMA tile; FLOPs count the 64 "
+                             "heads only", "traffic": None,
+                     "frac_slower_of_measured_hbm":
+                         max(flops / (peak_tf * 1e12), nbytes / (hbm * 1e9)) / (t * 1e-3)},
+        "kernels_ms": {"indexer_bwd": t},
+        "tokens_per_s": whole_job_rate(world, S, args.steps, elapsed_ms),
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                "windows_ms": [round(v, 3) for v in e2e_windows],
+                "window": f"median of {len(e2e_windows)} windows of `steps` steps",
+                "entry": "smqa_indexer_bwd with torch copies from / to page-locked memory"},
+        "gpu_launches": args.steps, "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        import numpy as np
+
+        import oracle
+        rng = np.random.default_rng(4321)
+        xc = {kk: v.cpu() for kk, v in (("q", q), ("w", w), ("k", k), ("idx", idx), ("g", g))}
+
+        def run(n):
+            toks = np.sort(rng.choice(S, size=n, replace=False))
+            nv = int(((xc["idx"][torch.as_tensor(toks)] >= 0) &
+                      (xc["idx"][torch.as_tensor(toks)] < S_kv)).sum())
+            t0 = time.perf_counter()
+            oracle.indexer_bwd(xc["q"], xc["w"], xc["k"], xc["idx"], xc["g"], tokens=toks)
+            return time.perf_counter() - t0, nv
+
+        dt, _ = run(8)
+        n = int(max(8, min(2048, 8 * 15.0 / max(dt, 1e-3))))
+        dt, nv = run(n)
+        line["cpu_baseline"] = {"value": 4.0 * H * D * nv / dt / 1e12, "unit": "TFLOP/s",
+                                "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": f"{n} seeded tokens of {name} (fp64), {dt:.1f} s"}
+    return line
+
+
 def time_extras(lib, shp, q, kv, sink, o, dout, idx, lse, delta, dq, dkv, scale, stream, sp,
                 dev):
     """The optional backward paths outside the step, each timed alone: the
@@ -567,7 +696,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=[c.name for c in inputs.CONFIGS] + ["all"],
+                    choices=[c.name for c in inputs.CONFIGS] +
+                    [c.name for c in inputs.INDEXER_CONFIGS] + ["all"],
                     help="the workload to time (default: the H=128 D=512 topk=2048 one); "
                          "'all' prints one line per workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -603,9 +733,12 @@ def main():
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    names = [c.name for c in inputs.CONFIGS] if args.workload == "all" else [args.workload]
+    names = ([c.name for c in inputs.CONFIGS] + [c.name for c in inputs.INDEXER_CONFIGS]
+             if args.workload == "all" else [args.workload])
+    indexer_names = {c.name for c in inputs.INDEXER_CONFIGS}
     for name in names:
-        line = run_workload(args, name, dist, world, rank, local, dev)
+        run = run_indexer_workload if name in indexer_names else run_workload
+        line = run(args, name, dist, world, rank, local, dev)
         if line is not None:
             print(json.dumps(line), flush=True)
         torch.cuda.empty_cache()

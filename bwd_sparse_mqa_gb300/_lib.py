@@ -32,6 +32,7 @@ EXPORTS = [
     "smqa_fwd_workspace_bytes", "smqa_fwd_static_scratch", "smqa_bwd_sink_grad",
     "smqa_fwd_host_workspace_bytes", "smqa_fwd_bwd_host_workspace_bytes", "smqa_fwd_host",
     "smqa_fwd_bwd_host", "smqa_host_chunk_plan", "smqa_set_wait_limit_ns", "smqa_debug_stall",
+    "smqa_indexer_bwd", "smqa_batched_indexer_bwd",
 ]
 STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -83,6 +84,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.smqa_fwd_bwd_host.argtypes = [P, P, P, P, P, S, F, P, P, P, P, P, P, ctypes.c_size_t, U,
                                       P]
     lib.smqa_fwd_bwd_host.restype = st
+    lib.smqa_indexer_bwd.argtypes = [P, P, P, P, P, S, P, P]
+    lib.smqa_indexer_bwd.restype = st
+    lib.smqa_batched_indexer_bwd.argtypes = [P, P, P, P, P, S, P, P]
+    lib.smqa_batched_indexer_bwd.restype = st
     lib.smqa_debug_stall.argtypes = [ctypes.c_int]
     lib.smqa_debug_stall.restype = None
     lib.smqa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]

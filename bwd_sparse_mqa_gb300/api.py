@@ -332,6 +332,59 @@ def set_wait_limit_ns(ns: int) -> int:
     return int(_lib.load().smqa_set_wait_limit_ns(int(ns)))
 
 
+def indexer_bwd_interface(index_q: torch.Tensor, weights: torch.Tensor, index_k: torch.Tensor,
+                          topk_indices: torch.Tensor, grad_scores: torch.Tensor) -> torch.Tensor:
+    """Lightning-indexer backward for one batch element (tilelang_indexer_bwd
+    page, `indexer_bwd_interface`): index_q [S,H,D] bf16, weights [S,H] fp32,
+    index_k [S_kv,D] bf16, topk_indices [S,topk] int32, grad_scores [S,topk]
+    fp32.  Returns a freshly allocated dq [S,H,D] bf16, the gradient of the
+    scores sum_h w[t,h] ReLU(q[t,h] . k[idx[t,j]]) with respect to index_q."""
+    _need(index_q, "index_q", torch.bfloat16, 3)
+    _need(weights, "weights", torch.float32, 2)
+    _need(index_k, "index_k", torch.bfloat16, 2)
+    _need(topk_indices, "topk_indices", torch.int32, 2)
+    _need(grad_scores, "grad_scores", torch.float32, 2)
+    S, H, D = index_q.shape
+    topk = topk_indices.shape[1]
+    if tuple(weights.shape) != (S, H) or index_k.shape[1] != D or \
+            tuple(topk_indices.shape) != (S, topk) or tuple(grad_scores.shape) != (S, topk):
+        raise ValueError("indexer tensors do not have matching shapes")
+    shp = _lib.Shape(1, S, index_k.shape[0], H, D, topk)
+    dq = torch.empty_like(index_q)
+    lib = _lib.load()
+    with torch.cuda.device(index_q.device):
+        _lib.check("smqa_indexer_bwd", lib.smqa_indexer_bwd(
+            _ptr(index_q), _ptr(weights), _ptr(index_k), _ptr(topk_indices), _ptr(grad_scores),
+            shp, _ptr(dq), _stream(index_q.device)))
+    return dq
+
+
+def batched_indexer_bwd(index_q: torch.Tensor, weights: torch.Tensor, index_k: torch.Tensor,
+                        topk_indices: torch.Tensor, grad_scores: torch.Tensor) -> torch.Tensor:
+    """The indexer backward in the page's batched layouts (`batched_indexer_bwd`):
+    index_q [S,B,H,D] bf16, weights [S,B,H] fp32, index_k [S_kv,B,D] bf16,
+    topk_indices [B,S,topk] int32, grad_scores [B,S,topk] fp32; returns dq
+    [S,B,H,D] bf16.  One launch covers every batch element."""
+    _need(index_q, "index_q", torch.bfloat16, 4)
+    _need(weights, "weights", torch.float32, 3)
+    _need(index_k, "index_k", torch.bfloat16, 3)
+    _need(topk_indices, "topk_indices", torch.int32, 3)
+    _need(grad_scores, "grad_scores", torch.float32, 3)
+    S, B, H, D = index_q.shape
+    topk = topk_indices.shape[2]
+    if tuple(weights.shape) != (S, B, H) or index_k.shape[1] != B or index_k.shape[2] != D or \
+            tuple(topk_indices.shape) != (B, S, topk) or tuple(grad_scores.shape) != (B, S, topk):
+        raise ValueError("indexer tensors do not have matching shapes")
+    shp = _lib.Shape(B, S, index_k.shape[0], H, D, topk)
+    dq = torch.empty_like(index_q)
+    lib = _lib.load()
+    with torch.cuda.device(index_q.device):
+        _lib.check("smqa_batched_indexer_bwd", lib.smqa_batched_indexer_bwd(
+            _ptr(index_q), _ptr(weights), _ptr(index_k), _ptr(topk_indices), _ptr(grad_scores),
+            shp, _ptr(dq), _stream(index_q.device)))
+    return dq
+
+
 class SparseMQAFunction(torch.autograd.Function):
     """Autograd around the forward and backward kernels: gradients flow from
     O to q, kv and attn_sink (the LSE output is not differentiable)."""

@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libsparse_mqa.so")
-SOURCES = ["smqa_api.cu", "smqa_fwd.cu", "smqa_bwd.cu", "smqa_noalloc.cu", "smqa_host.cu"]
+SOURCES = ["smqa_api.cu", "smqa_fwd.cu", "smqa_bwd.cu", "smqa_noalloc.cu", "smqa_host.cu",
+           "smqa_indexer.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,
                      "-I", CSRC]

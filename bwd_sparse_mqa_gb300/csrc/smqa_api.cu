@@ -470,6 +470,86 @@ uint64_t smqa_set_wait_limit_ns(uint64_t ns) {
   return before;
 }
 
+}  // extern "C"
+
+namespace {
+
+// The indexer backward's argument checks and launch, for both layouts.
+smqa_status indexer_impl(const void* q, const float* w, const void* k, const int32_t* idx,
+                         const float* g, const smqa_shape& s, bool batched, void* dq,
+                         cudaStream_t stream) {
+  if (s.B <= 0 || s.S <= 0 || s.S_kv <= 0 || s.H <= 0 || s.D <= 0 || s.topk <= 0) {
+    std::snprintf(g_last_error, sizeof g_last_error, "non-positive size in shape");
+    return SMQA_ERR_INVALID_ARG;
+  }
+  const int64_t lim = int64_t{1} << 31;
+  if (s.H > 128 || (s.D != 64 && s.D != 128) ||
+      static_cast<int64_t>(s.B) * s.S_kv * s.D >= lim ||
+      static_cast<int64_t>(s.B) * s.S * s.H * s.D >= lim ||
+      static_cast<int64_t>(s.B) * s.S * s.topk >= lim) {
+    std::snprintf(g_last_error, sizeof g_last_error,
+                  "unsupported indexer shape (need 1<=H<=128, D in {64,128}, sizes < 2^31)");
+    return SMQA_ERR_UNSUPPORTED;
+  }
+  if (!batched && s.B != 1) {
+    std::snprintf(g_last_error, sizeof g_last_error,
+                  "smqa_indexer_bwd takes one batch element (B = 1)");
+    return SMQA_ERR_INVALID_ARG;
+  }
+  if (!q || !w || !k || !idx || !g || !dq || !aligned(q, 16) || !aligned(k, 16) ||
+      !aligned(dq, 16) || !aligned(w, 4) || !aligned(idx, 4) || !aligned(g, 4)) {
+    std::snprintf(g_last_error, sizeof g_last_error, "null or misaligned pointer");
+    return SMQA_ERR_INVALID_ARG;
+  }
+  cudaError_t e;
+  int* st = status_ptr(&e);
+  if (!st) return cuda_fail(e, "status word");
+  const uint64_t rows = static_cast<uint64_t>(s.B) * s.S * s.H;
+  CUtensorMap tq, tdq;
+  if (!encode_bf16_2d(&tq, q, s.D, rows, 64, static_cast<uint32_t>(s.H)) ||
+      !encode_bf16_2d(&tdq, dq, s.D, rows, 64, static_cast<uint32_t>(s.H)))
+    return SMQA_ERR_CUDA;
+  smqa::IdxParams p{};
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.idx = idx;
+  p.g = g;
+  p.w = w;
+  p.B = s.B;
+  p.S = s.S;
+  p.S_kv = s.S_kv;
+  p.H = s.H;
+  p.D = s.D;
+  p.topk = s.topk;
+  p.q_tok_rows = batched ? static_cast<int64_t>(s.B) * s.H : s.H;
+  p.q_b_rows = batched ? s.H : 0;
+  p.k_row_stride = batched ? static_cast<int64_t>(s.B) * s.D : s.D;
+  p.k_b_stride = batched ? s.D : 0;
+  p.status = st;
+  p.limit_ns = wait_limit_ns();
+  e = smqa::launch_indexer_bwd(tq, tdq, p, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "indexer bwd launch");
+  return SMQA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+smqa_status smqa_indexer_bwd(const void* index_q, const float* weights, const void* index_k,
+                             const int32_t* topk_indices, const float* grad_scores,
+                             smqa_shape shape, void* dq, cudaStream_t stream) {
+  return indexer_impl(index_q, weights, index_k, topk_indices, grad_scores, shape, false, dq,
+                      stream);
+}
+
+smqa_status smqa_batched_indexer_bwd(const void* index_q, const float* weights,
+                                     const void* index_k, const int32_t* topk_indices,
+                                     const float* grad_scores, smqa_shape shape, void* dq,
+                                     cudaStream_t stream) {
+  return indexer_impl(index_q, weights, index_k, topk_indices, grad_scores, shape, true, dq,
+                      stream);
+}
+
 void smqa_debug_stall(int cta) { g_stall_cta.store(cta < 0 ? -1 : cta, std::memory_order_relaxed); }
 
 smqa_status smqa_device_status(int clear) {

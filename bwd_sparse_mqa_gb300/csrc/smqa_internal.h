@@ -60,6 +60,23 @@ struct BwdParams {
   int nslots;
 };
 
+// Lightning-indexer backward: dq[t,h] = w[t,h] sum_j g[t,j] [q.k_j > 0] k_j.
+// Token (s, b) has its H rows of q, weights and dq at row
+// s * q_tok_rows + b * q_b_rows ([S,H,D] per element: H, 0; the batched
+// [S,B,H,D]: B*H, H); key row r of element b starts at element
+// r * k_row_stride + b * k_b_stride; indices and grad_scores are [B,S,topk].
+struct IdxParams {
+  const __nv_bfloat16* k;
+  const int32_t* idx;
+  const float* g;
+  const float* w;
+  int B, S, S_kv, H, D, topk;
+  int64_t q_tok_rows, q_b_rows;
+  int64_t k_row_stride, k_b_stride;
+  int* status;
+  uint64_t limit_ns;
+};
+
 // One exchange slot of the forward: two receivers x six block buffers x
 // 16.5 KB (the partial scores of 128 heads x 64 slots as int16 mantissas
 // with one int32 power-of-two exponent per head).
@@ -103,6 +120,8 @@ cudaError_t launch_fwd(const CUtensorMap& tm_q, const CUtensorMap& tm_o, const F
 cudaError_t launch_bwd_main(const CUtensorMap& tm_q, const CUtensorMap& tm_do,
                             const CUtensorMap& tm_dq, const BwdParams& p, int tokens,
                             cudaStream_t stream);
+cudaError_t launch_indexer_bwd(const CUtensorMap& tm_q, const CUtensorMap& tm_dq,
+                               const IdxParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* dout,
                                   float* delta, float* dkv_acc, int64_t rows, int D,
                                   int64_t acc_elems, cudaStream_t stream);

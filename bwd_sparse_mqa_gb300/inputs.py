@@ -30,7 +30,8 @@ from typing import Optional
 
 import torch
 
-__all__ = ["SMQAConfig", "CONFIGS", "make_inputs", "make_indices", "by_name"]
+__all__ = ["SMQAConfig", "CONFIGS", "make_inputs", "make_indices", "by_name",
+           "INDEXER_CONFIGS", "make_indexer_inputs", "indexer_custom"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -183,3 +184,53 @@ def custom(B: int, S: int, S_kv: int, H: int, D: int, topk: int, recipe: str = "
     """Inputs for an arbitrary shape (tests use this for edge cases)."""
     cfg = SMQAConfig("custom", B, S, S_kv, H, D, topk, recipe, "fwd+bwd", seed, device)
     return make_inputs(cfg)
+
+
+# ---------------------------------------------------------------------------
+# Lightning-indexer backward (tilelang_indexer_bwd page): index_q [S,H,D]
+# bf16, weights [S,H] fp32, index_k [S_kv,D] bf16, topk_indices [S,topk]
+# int32, grad_scores [S,topk] fp32 per batch element.  The page measures
+# nothing; the workload uses the DeepSeek-V4 indexer's head count and width
+# (64 heads of 128) with the attention workloads' sequence length and topk.
+# ---------------------------------------------------------------------------
+INDEXER_CONFIGS = [
+    SMQAConfig("indexer_h64_d128_k2048_s8192", 1, 8192, 8192, 64, 128, 2048, "causal_uniform",
+               "indexer_bwd", 5, "cuda"),
+]
+
+
+def indexer_by_name(name: str) -> SMQAConfig:
+    for c in INDEXER_CONFIGS:
+        if c.name == name:
+            return c
+    raise KeyError(name)
+
+
+def make_indexer_inputs(cfg: SMQAConfig, device: Optional[str] = None,
+                        batched_layout: bool = False) -> dict:
+    """Seeded indexer inputs drawn in the order index_q, index_k, weights,
+    grad_scores, topk_indices (all N(0,1) but the indices).  Per-element
+    layouts ([B,S,H,D], [B,S_kv,D], [B,S,H]) unless ``batched_layout``, which
+    gives the page's batched ones: index_q [S,B,H,D], weights [S,B,H],
+    index_k [S_kv,B,D]; topk_indices and grad_scores are [B,S,topk] in both."""
+    dev = torch.device(device or cfg.device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(cfg.seed)
+    q = torch.randn((cfg.B, cfg.S, cfg.H, cfg.D), generator=gen, device=dev).to(torch.bfloat16)
+    k = torch.randn((cfg.B, cfg.S_kv, cfg.D), generator=gen, device=dev).to(torch.bfloat16)
+    w = torch.randn((cfg.B, cfg.S, cfg.H), generator=gen, device=dev, dtype=torch.float32)
+    g = torch.randn((cfg.B, cfg.S, cfg.topk), generator=gen, device=dev, dtype=torch.float32)
+    idx = make_indices(cfg.recipe, cfg.B, cfg.S, cfg.S_kv, cfg.topk, gen, dev)
+    if batched_layout:
+        q = q.permute(1, 0, 2, 3)
+        k = k.permute(1, 0, 2)
+        w = w.permute(1, 0, 2)
+    return {"index_q": q.contiguous(), "weights": w.contiguous(), "index_k": k.contiguous(),
+            "topk_indices": idx.contiguous(), "grad_scores": g.contiguous()}
+
+
+def indexer_custom(B: int, S: int, S_kv: int, H: int, D: int, topk: int,
+                   recipe: str = "causal_uniform", seed: int = 0, device: str = "cpu",
+                   batched_layout: bool = False) -> dict:
+    cfg = SMQAConfig("indexer_custom", B, S, S_kv, H, D, topk, recipe, "indexer_bwd", seed, device)
+    return make_indexer_inputs(cfg, batched_layout=batched_layout)

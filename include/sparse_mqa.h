@@ -315,6 +315,43 @@ smqa_status smqa_bwd_sink_grad(const float* attn_sink, const float* lse, const f
                                smqa_shape shape, float* dsink, cudaStream_t stream);
 
 /*
+ * Lightning-indexer backward (tilelang_indexer_bwd: `indexer_bwd_interface`,
+ * "backward interface for a single batch element").  The page gives the
+ * tensors, not the formula; the library computes the gradient with respect
+ * to index_q of the lightning indexer's scores
+ *     score[t,j] = sum_h weights[t,h] * ReLU(<index_q[t,h,:], index_k[idx[t,j],:]>)
+ * given grad_scores, that is
+ *     dq[t,h,:] = weights[t,h] * sum_j grad_scores[t,j] * [<q[t,h,:], k_j> > 0] * k_j
+ * over the slots whose index lies in [0, S_kv) (others are masked; a slot
+ * listed twice counts twice; the ReLU's slope is taken as 0 at 0).
+ *   index_q      bf16 [S, H, D]       weights      fp32 [S, H]
+ *   index_k      bf16 [S_kv, D]       topk_indices int32 [S, topk]
+ *   grad_scores  fp32 [S, topk]       dq           bf16 [S, H, D] (output)
+ * shape.B must be 1; 1 <= H <= 128, D in {64, 128}.  The logits are formed
+ * in fp32 by the tensor core, so where <q, k_j> lies within fp32 rounding of
+ * 0 the gate may differ from an exact evaluation.  grad_scores enter the
+ * tensor core as bf16.  Device pointers; asynchronous on `stream`; nothing
+ * is allocated.  Not a function of the attention pages.
+ */
+smqa_status smqa_indexer_bwd(const void* index_q, const float* weights, const void* index_k,
+                             const int32_t* topk_indices, const float* grad_scores,
+                             smqa_shape shape, void* dq, cudaStream_t stream);
+
+/*
+ * The same for a batch in the page's `batched_indexer_bwd` layouts (which
+ * the page describes as looping over the batch; here every batch element
+ * runs in the same launch):
+ *   index_q      bf16 [S, B, H, D]    weights      fp32 [S, B, H]
+ *   index_k      bf16 [S_kv, B, D]    topk_indices int32 [B, S, topk]
+ *   grad_scores  fp32 [B, S, topk]    dq           bf16 [S, B, H, D] (output)
+ * Indices address rows of the same batch element.
+ */
+smqa_status smqa_batched_indexer_bwd(const void* index_q, const float* weights,
+                                     const void* index_k, const int32_t* topk_indices,
+                                     const float* grad_scores, smqa_shape shape, void* dq,
+                                     cudaStream_t stream);
+
+/*
  * Reads the device status word that kernels set when a bounded wait runs out
  * (SMQA_OK if none did).  Synchronizes the current device first.  A nonzero
  * `clear` resets the word afterwards.
