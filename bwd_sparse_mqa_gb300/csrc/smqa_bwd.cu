@@ -311,11 +311,14 @@ struct BwdLayout {
   static constexpr uint32_t kOffCtrl = kOffDs + kPBytes;
   static constexpr int kBarKvFull = 0;
   static constexpr int kBarKvEmpty = kBarKvFull + kStages;
-  static constexpr int kBarSdpFull = kBarKvEmpty + kStages;
-  static constexpr int kBarSdpFree = kBarSdpFull + 1;
-  static constexpr int kBarPdsFull = kBarSdpFree + 1;
-  static constexpr int kBarPdsFree = kBarPdsFull + 1;
-  static constexpr int kBarDkvFull = kBarPdsFree + 1;
+  // The P / dS groups alternate blocks (group = block parity), so the
+  // barriers between them and the MMA issuer come one per parity: a group
+  // only ever waits on phases of its own blocks.
+  static constexpr int kBarSdpFull = kBarKvEmpty + kStages;  // [2]
+  static constexpr int kBarSdpFree = kBarSdpFull + 2;        // [2]
+  static constexpr int kBarPdsFull = kBarSdpFree + 2;        // [2]
+  static constexpr int kBarPdsFree = kBarPdsFull + 2;        // [2]
+  static constexpr int kBarDkvFull = kBarPdsFree + 2;
   static constexpr int kBarDkvFree = kBarDkvFull + 1;
   static constexpr int kBarRecvFull = kBarDkvFree + 1;  // [2], by block parity
   static constexpr int kBarSendOk = kBarRecvFull + 2;    // [2]
@@ -341,11 +344,13 @@ struct BwdLayout {
   static constexpr uint32_t kTmemUsed = kTmemDkv + kNE * kBI;
   static constexpr uint32_t kTmemCols = kTmemUsed <= 256 ? 256 : 512;
   static_assert(kTmemUsed <= 512, "TMEM budget");
-  // warps 0-7: P / dS (thread = head row 32 (warp % 4) + lane and slot half
-  // warp / 4 of each block; for D split across the pair they also send this
-  // CTA's partial S / dP of their slots to the peer); 8-11: dKV drain
-  // (thread = head-dim row); 12-13: gather; 14: TMEM owner + MMA issuer.
+  // warps 0-7: P / dS in two groups of four (group g = warp / 4 handles the
+  // blocks of parity g; thread = head row 32 (warp % 4) + lane, all 64 slots
+  // of a block; for D split across the pair they also send this CTA's
+  // partial S / dP to the peer); 8-11: dKV drain (thread = head-dim row);
+  // 12-13: gather; 14: TMEM owner + MMA issuer.
   static constexpr int kPdsThreads = 256;
+  static constexpr int kGroupThreads = 128;
   static constexpr int kDrainWarp0 = 8;
   static constexpr int kProducerWarp0 = 12;
   static constexpr int kMmaWarp = 14;
@@ -420,17 +425,19 @@ __global__ void __launch_bounds__(480, 1)
       mbar_init(bar(L::kBarKvFull + s), 64);  // every gather thread arrives
       mbar_init(bar(L::kBarKvEmpty + s), 1);
     }
-    mbar_init(bar(L::kBarSdpFull), 1);
-    mbar_init(bar(L::kBarSdpFree), L::kPdsThreads);
-    mbar_init(bar(L::kBarPdsFull), L::kPdsThreads);
-    mbar_init(bar(L::kBarPdsFree), 1);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(bar(L::kBarSdpFull + g), 1);
+      mbar_init(bar(L::kBarSdpFree + g), L::kGroupThreads);
+      mbar_init(bar(L::kBarPdsFull + g), L::kGroupThreads);
+      mbar_init(bar(L::kBarPdsFree + g), 1);
+    }
     mbar_init(bar(L::kBarDkvFull), 1);
     mbar_init(bar(L::kBarDkvFree), 128);
-    // Exchange: the peer's eight P / dS warps each signal a filled buffer
-    // and, later, a consumed one.
+    // Exchange buffer i serves the blocks of parity i: the four warps of the
+    // peer's group i each signal it filled and, later, consumed.
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(L::kBarRecvFull + i), L::kPdsThreads / 32);
-      mbar_init(bar(L::kBarSendOk + i), L::kPdsThreads / 32);
+      mbar_init(bar(L::kBarRecvFull + i), L::kGroupThreads / 32);
+      mbar_init(bar(L::kBarSendOk + i), L::kGroupThreads / 32);
     }
     mbar_init(bar(L::kBarQdoFull), 1);
     mbar_init(bar(L::kBarDqDone), 1);
@@ -579,7 +586,7 @@ __global__ void __launch_bounds__(480, 1)
                    idesc_sdp, acc);
           }
         }
-        mma_commit(bar(L::kBarSdpFull));
+        mma_commit(bar(L::kBarSdpFull + (i & 1)));
       };
       // Gradients of block j: dQ += dS'.K (M = 128 heads, N = DC, K = 64
       // slots); dKV^T[e] = Q^T[e].dS' + dO^T[e].P (M = 128 dims, N = 64
@@ -591,6 +598,9 @@ __global__ void __launch_bounds__(480, 1)
         for (int k = 0; k < L::kBI / 16; ++k)
           mma_ss(tmem + L::kTmemDq, d_ds + (k * 32u >> 4), dkv + (k * 2048u >> 4), idesc_dq,
                  (j > 0 || k > 0) ? 1u : 0u);
+        // Only dQ reads the kv stage: the gather may refill it once these
+        // MMAs are done, while the dKV^T MMAs still run.
+        mma_commit(bar(L::kBarKvEmpty + sj));
 #pragma unroll
         for (int e = 0; e < L::kNE; ++e) {
           const uint32_t d_tm = tmem + L::kTmemDkv + e * L::kBI;
@@ -603,8 +613,7 @@ __global__ void __launch_bounds__(480, 1)
             mma_ss(d_tm, d_dot + ((2 * e * L::kQChunkBytes + k * 2048u) >> 4),
                    d_pmn + (k * 2048u >> 4), idesc_dkv, 1u);
         }
-        mma_commit(bar(L::kBarPdsFree));
-        mma_commit(bar(L::kBarKvEmpty + sj));
+        mma_commit(bar(L::kBarPdsFree + (j & 1)));
         mma_commit(bar(L::kBarDkvFull));
       };
       // Event loop (non-blocking tests), oldest work first: the gradients
@@ -616,14 +625,15 @@ __global__ void __launch_bounds__(480, 1)
       PollState ps = poll_start();
       uint32_t spins = 0;
       while (ok && ng < nblk) {
-        if (ng < ns && mbar_probe(bar(L::kBarPdsFull), ng & 1) &&
+        if (ng < ns && mbar_probe(bar(L::kBarPdsFull + (ng & 1)), (ng >> 1) & 1) &&
             (ng == 0 || mbar_probe(bar(L::kBarDkvFree), (ng - 1) & 1))) {
           tc_fence_after();
           issue_grad(ng);
           ++ng;
         } else if (ns < nblk &&
                    mbar_probe(bar(L::kBarKvFull + ns % L::kStages), (ns / L::kStages) & 1) &&
-                   (ns == 0 || mbar_probe(bar(L::kBarSdpFree), (ns - 1) & 1))) {
+                   (ns == 0 ||
+                    mbar_probe(bar(L::kBarSdpFree + ((ns - 1) & 1)), ((ns - 1) >> 1) & 1))) {
           // The kv tile was written by cp.async (generic proxy): order it
           // before the tensor core's (async proxy) reads.
           fence_proxy_async_smem();
@@ -727,153 +737,176 @@ __global__ void __launch_bounds__(480, 1)
     }
   } else {
     // ------------------------------------------------------------ P / dS
-    // Thread = head row h and slot half hh: per block the full S and dP of
-    // the row's 32 slots (for D = 512 this CTA's partial plus the peer's,
-    // both in block floating point), then
+    // Two groups of four warps alternate blocks (group g takes the blocks of
+    // parity g), so one block's latency chain -- read the S / dP tile, round
+    // and send this CTA's partials, wait for the peer's, decode, write P and
+    // dS' -- overlaps the next block's.  Thread = head row h, all 64 slots
+    // of the block: the full S and dP of the row (for D = 512 this CTA's
+    // partial plus the peer's, both in block floating point), then
     //   P = 2^(S - lse2),  dS' = P (sm_scale dP - sm_scale Delta),
-    // written bf16 for the gradient MMAs, 8 slots at a time.  For D = 512 the
-    // same thread first rounds its partial and writes it into the peer's
-    // exchange buffer, so each partial is rounded once and read from TMEM
-    // once.
+    // written bf16 for the gradient MMAs, 8 slots at a time.  The single
+    // P / dS buffer is written only once the gradients of the previous block
+    // (the other group's) have read it.
     const int h = (warp & 3) * 32 + lane;
-    const int hh = warp >> 2;
+    const int grp = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t t_s = tmem + lane_base + L::kTmemS + 32 * hh;
-    const uint32_t t_dp = tmem + lane_base + L::kTmemDp + 32 * hh;
+    const uint32_t t_s = tmem + lane_base + L::kTmemS;
+    const uint32_t t_dp = tmem + lane_base + L::kTmemDp;
     const float lse2 = h < p.H ? __ldg(p.lse + static_cast<size_t>(t) * p.H + h) : INFINITY;
     const float dlt_s =
         h < p.H ? __ldg(p.delta + static_cast<size_t>(t) * p.H + h) * p.scale : 0.f;
-    const uint32_t peer_full = NC == 2 ? mapa_shared(bar(L::kBarRecvFull), rank ^ 1u) : 0u;
-    const uint32_t peer_sendok = NC == 2 ? mapa_shared(bar(L::kBarSendOk), rank ^ 1u) : 0u;
-    // This CTA's receive buffers, and the peer's (which this thread fills).
-    const uint8_t* recv0 =
-        NC == 2 ? p.exch + (static_cast<size_t>(slot) * 2 + rank) * (2 * L::kXchgBytes) : nullptr;
-    uint8_t* send0 = NC == 2 ? p.exch + (static_cast<size_t>(slot) * 2 + (rank ^ 1u)) *
-                                            (2 * L::kXchgBytes)
-                             : nullptr;
+    const uint32_t peer_full = NC == 2 ? mapa_shared(bar(L::kBarRecvFull + grp), rank ^ 1u) : 0u;
+    const uint32_t peer_sendok = NC == 2 ? mapa_shared(bar(L::kBarSendOk + grp), rank ^ 1u) : 0u;
+    // This group's receive buffer, and the peer's (which this group fills).
+    const uint8_t* recv = NC == 2 ? p.exch + (static_cast<size_t>(slot) * 2 + rank) *
+                                                 (2 * L::kXchgBytes) +
+                                        grp * L::kXchgBytes
+                                  : nullptr;
+    uint8_t* send = NC == 2 ? p.exch + (static_cast<size_t>(slot) * 2 + (rank ^ 1u)) *
+                                           (2 * L::kXchgBytes) +
+                                  grp * L::kXchgBytes
+                            : nullptr;
     const uint32_t row128 = static_cast<uint32_t>(h) * 128u;
     const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
-    auto load_idx = [&](int blk) -> int {
-      const int j = blk * L::kBI + 32 * hh + lane;
-      return j < p.topk ? __ldg(idx_row + j) : -1;
+    auto load_idx = [&](int blk, int half) -> int {
+      const int j = blk * L::kBI + 32 * half + lane;
+      return (blk < nblk && j < p.topk) ? __ldg(idx_row + j) : -1;
     };
-    // P and dS' of the half's slots 8c .. 8c+7 (c = 0..3) from their scores
-    // zs and scaled dP zp (slot validity: bit 8c + k of msk).
-    auto emit = [&](int c, uint32_t msk, const float* zs, const float* zp) {
+    // P and dS' of slots 8 ch .. 8 ch + 7 (ch = 0..7) from their scores zs
+    // and scaled dP zp (slot validity: bit (8 ch + k) % 32 of msk).
+    auto emit = [&](int ch, uint32_t msk, const float* zs, const float* zp) {
       uint32_t pp[4], pd[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const float2 e = add2(make_float2(zs[2 * k], zs[2 * k + 1]), make_float2(-lse2, -lse2));
         const float2 g = add2(make_float2(zp[2 * k], zp[2 * k + 1]), make_float2(-dlt_s, -dlt_s));
-        const int jj = 8 * c + 2 * k;
+        const int jj = (8 * ch + 2 * k) & 31;
         const float2 pv = make_float2(((msk >> jj) & 1u) ? fast_exp2(e.x) : 0.f,
                                       ((msk >> (jj + 1)) & 1u) ? fast_exp2(e.y) : 0.f);
         const float2 dv = mul2(pv, g);
         pp[k] = pack_bf16x2(pv.x, pv.y);
         pd[k] = pack_bf16x2(dv.x, dv.y);
       }
-      const uint32_t chunk = static_cast<uint32_t>(4 * hh + c);
-      const uint32_t off = row128 + ((chunk ^ static_cast<uint32_t>(h & 7)) << 4);
+      const uint32_t off = row128 + ((static_cast<uint32_t>(ch) ^ static_cast<uint32_t>(h & 7)) << 4);
       st_shared_v4(base + L::kOffP + off, pp[0], pp[1], pp[2], pp[3]);
       st_shared_v4(base + L::kOffDs + off, pd[0], pd[1], pd[2], pd[3]);
     };
-    int r_next = load_idx(0);
+    int r0 = load_idx(grp, 0), r1 = load_idx(grp, 1);
     bool ok = *abort_flag == 0;
-    for (int i = 0; ok && i < nblk; ++i) {
-      const int sb = i & 1;
-      // Valid-slot mask of this half of the block (prefetched index).
-      const uint32_t msk =
-          __ballot_sync(0xffffffffu, static_cast<unsigned>(r_next) < static_cast<unsigned>(p.S_kv));
-      if (i + 1 < nblk) r_next = load_idx(i + 1);
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSdpFull), i & 1, ctl));
+    for (int i = grp; ok && i < nblk; i += 2) {
+      const int n = i >> 1;  // this group's block count
+      // Valid-slot masks of the block's two 32-slot halves (prefetched).
+      const uint32_t m0 = __ballot_sync(0xffffffffu, static_cast<unsigned>(r0) < static_cast<unsigned>(p.S_kv));
+      const uint32_t m1 = __ballot_sync(0xffffffffu, static_cast<unsigned>(r1) < static_cast<unsigned>(p.S_kv));
+      r0 = load_idx(i + 2, 0);
+      r1 = load_idx(i + 2, 1);
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSdpFull + grp), n & 1, ctl));
       if (!ok) break;
       tc_fence_after();
       if constexpr (NC == 2) {
-        uint32_t hs[16], hp[16];
-        const uint32_t own_exps = own_partials_bfp(t_s, t_dp, p.scale_log2, p.scale, hs, hp);
+        uint32_t hs[2][16], hp[2][16], own_exps[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+          own_exps[hh] = own_partials_bfp(t_s + 32 * hh, t_dp + 32 * hh, p.scale_log2, p.scale,
+                                          hs[hh], hp[hh]);
         tc_fence_before();
-        mbar_arrive(bar(L::kBarSdpFree));
-        // Send: the peer has consumed block i-2 from this buffer.
-        if (i >= 2) {
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait<true>(bar(L::kBarSendOk + sb), ((i >> 1) - 1) & 1, ctl));
+        mbar_arrive(bar(L::kBarSdpFree + grp));
+        // Send: the peer has consumed this group's previous block from the
+        // buffer.
+        if (n >= 1) {
+          ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarSendOk + grp), (n - 1) & 1, ctl));
           if (!ok) break;
         }
         {
-          uint8_t* buf = send0 + sb * L::kXchgBytes;
-          uint4* dst = reinterpret_cast<uint4*>(buf) + h;
+          uint4* dst = reinterpret_cast<uint4*>(send) + h;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              dst[(4 * hh + c) * L::kHPad] = make_uint4(hs[hh][4 * c], hs[hh][4 * c + 1],
+                                                        hs[hh][4 * c + 2], hs[hh][4 * c + 3]);
+              dst[(8 + 4 * hh + c) * L::kHPad] = make_uint4(hp[hh][4 * c], hp[hh][4 * c + 1],
+                                                            hp[hh][4 * c + 2], hp[hh][4 * c + 3]);
+            }
+          uint32_t* ex = reinterpret_cast<uint32_t*>(send + L::kXchgScaleOff);
+          ex[h] = own_exps[0];
+          ex[L::kHPad + h] = own_exps[1];
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(peer_full);
+        }
+        // The P / dS buffer was last read by the gradient MMAs of block i-1.
+        if (i >= 1) {
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(bar(L::kBarPdsFree + ((i - 1) & 1)), ((i - 1) >> 1) & 1, ctl));
+          if (!ok) break;
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull + grp), n & 1, ctl));
+        if (!ok) break;
+        const uint4* src = reinterpret_cast<const uint4*>(recv) + h;
+        const unsigned int* pex = reinterpret_cast<const unsigned int*>(recv + L::kXchgScaleOff);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint32_t peer_exps = __ldcg(pex + hh * L::kHPad + h);
+          const float us = bfp16_unit<false>(own_exps[hh]), up = bfp16_unit<true>(own_exps[hh]);
+          const float vs = bfp16_unit<false>(peer_exps), vp = bfp16_unit<true>(peer_exps);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            dst[(4 * hh + c) * L::kHPad] =
-                make_uint4(hs[4 * c], hs[4 * c + 1], hs[4 * c + 2], hs[4 * c + 3]);
-            dst[(8 + 4 * hh + c) * L::kHPad] =
-                make_uint4(hp[4 * c], hp[4 * c + 1], hp[4 * c + 2], hp[4 * c + 3]);
-          }
-          reinterpret_cast<uint32_t*>(buf + L::kXchgScaleOff)[hh * L::kHPad + h] = own_exps;
-          __syncwarp();
-          if (lane == 0) mbar_arrive_remote(peer_full + 8u * static_cast<uint32_t>(sb));
-        }
-        // P / dS buffers were last read by the gradient MMAs of block i-1.
-        if (i >= 1) {
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarPdsFree), (i - 1) & 1, ctl));
-          if (!ok) break;
-        }
-        ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull + sb), (i >> 1) & 1, ctl));
-        if (!ok) break;
-        const uint8_t* buf = recv0 + sb * L::kXchgBytes;
-        const uint4* src = reinterpret_cast<const uint4*>(buf) + h;
-        const uint32_t peer_exps =
-            __ldcg(reinterpret_cast<const unsigned int*>(buf + L::kXchgScaleOff) + hh * L::kHPad + h);
-        const float us = bfp16_unit<false>(own_exps), up = bfp16_unit<true>(own_exps);
-        const float vs = bfp16_unit<false>(peer_exps), vp = bfp16_unit<true>(peer_exps);
+            const uint4 ys = __ldcg(src + (4 * hh + c) * L::kHPad);
+            const uint4 yp = __ldcg(src + (8 + 4 * hh + c) * L::kHPad);
+            const uint32_t ysa[4] = {ys.x, ys.y, ys.z, ys.w};
+            const uint32_t ypa[4] = {yp.x, yp.y, yp.z, yp.w};
+            float zs[8], zp[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 ys = __ldcg(src + (4 * hh + c) * L::kHPad);
-          const uint4 yp = __ldcg(src + (8 + 4 * hh + c) * L::kHPad);
-          const uint32_t ysa[4] = {ys.x, ys.y, ys.z, ys.w};
-          const uint32_t ypa[4] = {yp.x, yp.y, yp.z, yp.w};
-          float zs[8], zp[8];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            // Both decodings are exact; the sum is one rounding and commutes,
-            // so the two CTAs get the same full S and dP.
-            const float2 a = add2(bfp16_unpack(hs[4 * c + k], us), bfp16_unpack(ysa[k], vs));
-            const float2 d = add2(bfp16_unpack(hp[4 * c + k], up), bfp16_unpack(ypa[k], vp));
-            zs[2 * k] = a.x;
-            zs[2 * k + 1] = a.y;
-            zp[2 * k] = d.x;
-            zp[2 * k + 1] = d.y;
+            for (int k = 0; k < 4; ++k) {
+              // Both decodings are exact; the sum is one rounding and
+              // commutes, so the two CTAs get the same full S and dP.
+              const float2 a =
+                  add2(bfp16_unpack(hs[hh][4 * c + k], us), bfp16_unpack(ysa[k], vs));
+              const float2 d =
+                  add2(bfp16_unpack(hp[hh][4 * c + k], up), bfp16_unpack(ypa[k], vp));
+              zs[2 * k] = a.x;
+              zs[2 * k + 1] = a.y;
+              zp[2 * k] = d.x;
+              zp[2 * k + 1] = d.y;
+            }
+            emit(4 * hh + c, hh == 0 ? m0 : m1, zs, zp);
           }
-          emit(c, msk, zs, zp);
         }
         fence_proxy_async_smem();
-        mbar_arrive(bar(L::kBarPdsFull));
-        // The exchange buffer may take the peer's block i+2 (a cluster-scope
-        // release: signalled after P / dS so the gradients need not wait).
+        mbar_arrive(bar(L::kBarPdsFull + grp));
+        // The exchange buffer may take the peer's next block of this parity
+        // (a cluster-scope release: signalled after P / dS so the gradients
+        // need not wait).
         __syncwarp();
-        if (lane == 0 && i + 2 < nblk)
-          mbar_arrive_remote(peer_sendok + 8u * static_cast<uint32_t>(sb));
+        if (lane == 0 && i + 2 < nblk) mbar_arrive_remote(peer_sendok);
       } else {
-        float xs[32], xp[32];
-        tmem_ld32x2(t_s, t_dp, xs, xp);
-        tc_fence_before();
-        mbar_arrive(bar(L::kBarSdpFree));
+        // One CTA per token: the tile holds the full S and dP.  It is read
+        // half by half right before the half is written, so it stays busy
+        // until the P / dS buffer is free.
         if (i >= 1) {
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarPdsFree), (i - 1) & 1, ctl));
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(bar(L::kBarPdsFree + ((i - 1) & 1)), ((i - 1) >> 1) & 1, ctl));
           if (!ok) break;
         }
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          float xs[32], xp[32];
+          tmem_ld32x2(t_s + 32 * hh, t_dp + 32 * hh, xs, xp);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float zs[8], zp[8];
+          for (int c = 0; c < 4; ++c) {
+            float zs[8], zp[8];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            zs[k] = xs[8 * c + k] * p.scale_log2;
-            zp[k] = xp[8 * c + k] * p.scale;
+            for (int k = 0; k < 8; ++k) {
+              zs[k] = xs[8 * c + k] * p.scale_log2;
+              zp[k] = xp[8 * c + k] * p.scale;
+            }
+            emit(4 * hh + c, hh == 0 ? m0 : m1, zs, zp);
           }
-          emit(c, msk, zs, zp);
         }
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarSdpFree + grp));
         fence_proxy_async_smem();
-        mbar_arrive(bar(L::kBarPdsFull));
+        mbar_arrive(bar(L::kBarPdsFull + grp));
       }
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDqDone), 0, ctl));
@@ -881,10 +914,10 @@ __global__ void __launch_bounds__(480, 1)
       tc_fence_after();
       // dQ into shared memory as 64-column tiles in the 128-byte-swizzled
       // layout of dq's tensor map (the kv ring is free: every MMA has
-      // completed); the TMA then writes whole rows.  Slot half hh stages
-      // the tiles cc = hh, hh + 2, ...
+      // completed); the TMA then writes whole rows.  Group g stages the
+      // tiles cc = g, g + 2, ...
 #pragma unroll 1
-      for (int cc = hh; cc < DC / 64; cc += 2) {
+      for (int cc = grp; cc < DC / 64; cc += 2) {
         float v[2][32];
         if (nblk > 0) {
           tmem_ld32x2(tmem + lane_base + L::kTmemDq + cc * 64,

@@ -108,77 +108,89 @@ def test_three_buffers_deadlock():
 
 
 # ---------------------------------------------------------------------------
-# The backward pair (smqa_bwd.cu): one S/dP tile, a two-stage kv ring and
-# NB exchange buffers with an explicit consumed-signal (SendOk).  The P/dS
-# threads both send this CTA's partials and consume the peer's, in this order
-# per block:
+# The backward pair (smqa_bwd.cu): one S/dP tile, a two-stage kv ring, one
+# P/dS shared-memory buffer and NB exchange buffers with an explicit
+# consumed-signal (SendOk).  The P/dS threads both send this CTA's partials
+# and consume the peer's; with G groups, group g handles blocks i = g mod G
+# in order (G = 2: the two groups alternate blocks and overlap).  Per block:
 #   gather(i)    needs kv stage i % 2 free (the gradient MMAs of i - 2 done);
 #   sdp(i)       needs gather(i) and the S/dP tile read by read(i - 1);
-#   read(i)      needs sdp(i) and pds(i - 1) (the same threads, in order);
+#   read(i)      needs sdp(i) and pds(i - G) (the same threads, in order);
 #   send(i)      needs read(i) and, for i >= NB, the peer's SendOk for block
 #                i - NB; writes buffer i % NB of the peer (in flight);
-#   pds(i)       needs send(i), grad(i - 1) (single P/dS buffers) and the
+#   pds(i)       needs send(i), grad(i - 1) (the single P/dS buffer) and the
 #                peer's block i; consumes it and, if i + NB < nblk, sends
 #                SendOk for buffer i % NB to the peer (in flight);
 #   grad(i)      needs pds(i) and drain(i - 1) (single dKV tile);
 #   drain(i)     needs grad(i).
+# A barrier that a group waits on is only ever completed for that group's
+# blocks (per-parity barriers), so the parity tests below check phases per
+# group.
 BWD_ROLES = ("gather", "sdp", "read", "send", "pds", "grad", "drain")
 
 
-def run_bwd_model(NB: int, nblk: int, seed: int):
+def run_bwd_model(NB: int, nblk: int, seed: int, G: int = 1):
     rng = random.Random(seed)
     nxt = [{r: 0 for r in BWD_ROLES} for _ in range(2)]
+    done_set = [{r: set() for r in BWD_ROLES} for _ in range(2)]
     arrived = [set(), set()]
     sendok = [set(), set()]        # consumed-signals received by CTA c (block numbers)
     consumed = [set(), set()]
     recv_ph = [[0] * NB for _ in range(2)]
     ok_ph = [[0] * NB for _ in range(2)]
     in_flight = []                 # (kind, dest, block)
+    # The per-group roles (read, send, pds) keep one cursor per group.
+    gnxt = [[{r: g for r in ("read", "send", "pds")} for g in range(G)] for _ in range(2)]
 
     def done(c, role, i):
-        return i < nxt[c][role]
+        return i in done_set[c][role]
 
     def enabled(c):
         out = []
         n = nxt[c]
         i = n["gather"]
         if i < nblk and (i < 2 or done(c, "grad", i - 2)):
-            out.append("gather")
+            out.append(("gather", i))
         i = n["sdp"]
         if i < nblk and done(c, "gather", i) and (i == 0 or done(c, "read", i - 1)):
-            out.append("sdp")
-        i = n["read"]
-        if i < nblk and done(c, "sdp", i) and (i == 0 or done(c, "pds", i - 1)):
-            out.append("read")
-        i = n["send"]
-        if i < nblk and done(c, "read", i):
-            if i >= NB:
-                assert ok_ph[c][i % NB] <= (i // NB - 1) + 1, ("sendok aliasing", c, i)
-                if (i - NB) in sendok[c]:
-                    out.append("send")
-            else:
-                out.append("send")
-        i = n["pds"]
-        if i < nblk and done(c, "send", i) and (i == 0 or done(c, "grad", i - 1)):
-            assert recv_ph[c][i % NB] <= i // NB + 1, ("recv aliasing", c, i)
-            if i in arrived[c]:
-                out.append("pds")
+            out.append(("sdp", i))
+        for g in range(G):
+            cur = gnxt[c][g]
+            i = cur["read"]
+            if i < nblk and done(c, "sdp", i) and (i < G or done(c, "pds", i - G)):
+                out.append(("read", i))
+            i = cur["send"]
+            if i < nblk and done(c, "read", i):
+                if i >= NB:
+                    assert ok_ph[c][i % NB] <= (i // NB - 1) + 1, ("sendok aliasing", c, i)
+                    if (i - NB) in sendok[c]:
+                        out.append(("send", i))
+                else:
+                    out.append(("send", i))
+            i = cur["pds"]
+            if i < nblk and done(c, "send", i) and (i == 0 or done(c, "grad", i - 1)):
+                assert recv_ph[c][i % NB] <= i // NB + 1, ("recv aliasing", c, i)
+                if i in arrived[c]:
+                    out.append(("pds", i))
         i = n["grad"]
         if i < nblk and done(c, "pds", i) and (i == 0 or done(c, "drain", i - 1)):
-            out.append("grad")
+            out.append(("grad", i))
         i = n["drain"]
         if i < nblk and done(c, "grad", i):
-            out.append("drain")
+            out.append(("drain", i))
         return out
 
-    while any(nxt[c][r] < nblk for c in range(2) for r in BWD_ROLES):
-        choices = [(c, r) for c in range(2) for r in enabled(c)]
+    def finished():
+        return all(len(done_set[c]["drain"]) == nblk for c in range(2))
+
+    while not finished():
+        choices = [(c, e) for c in range(2) for e in enabled(c)]
         choices += [("deliver", k) for k in range(len(in_flight))]
         if not choices:
             return "deadlock"
-        c, r = rng.choice(choices)
+        c, e = rng.choice(choices)
         if c == "deliver":
-            kind, dest, blk = in_flight.pop(r)
+            kind, dest, blk = in_flight.pop(e)
             if kind == "data":
                 arrived[dest].add(blk)
                 recv_ph[dest][blk % NB] += 1
@@ -186,7 +198,7 @@ def run_bwd_model(NB: int, nblk: int, seed: int):
                 sendok[dest].add(blk)
                 ok_ph[dest][blk % NB] += 1
             continue
-        i = nxt[c][r]
+        r, i = e
         peer = 1 - c
         if r == "send":
             if i >= NB:
@@ -196,11 +208,16 @@ def run_bwd_model(NB: int, nblk: int, seed: int):
             consumed[c].add(i)
             if i + NB < nblk:
                 in_flight.append(("ok", peer, i))
-        nxt[c][r] += 1
+        done_set[c][r].add(i)
+        if r in ("read", "send", "pds"):
+            gnxt[c][i % G][r] += G
+        else:
+            nxt[c][r] += 1
     return "ok"
 
 
+@pytest.mark.parametrize("G", [1, 2])
 @pytest.mark.parametrize("NB", [2, 3, 4])
-@pytest.mark.parametrize("seed", range(40))
-def test_backward_exchange_protocol_is_safe_and_live(NB, seed):
-    assert run_bwd_model(NB, nblk=24, seed=seed) == "ok"
+@pytest.mark.parametrize("seed", range(30))
+def test_backward_exchange_protocol_is_safe_and_live(NB, seed, G):
+    assert run_bwd_model(NB, nblk=24, seed=seed, G=G) == "ok"
