@@ -113,7 +113,9 @@ def test_three_buffers_deadlock():
 # consumed-signal (SendOk).  The P/dS threads both send this CTA's partials
 # and consume the peer's; with G groups, group g handles blocks i = g mod G
 # in order (G = 2: the two groups alternate blocks and overlap).  Per block:
-#   gather(i)    needs kv stage i % 2 free (the gradient MMAs of i - 2 done);
+#   gather(i)    needs kv stage i % 2 free (the kernel frees it after the dQ
+#                MMAs of block i - 2; the model waits for all of grad(i - 2),
+#                which is stricter);
 #   sdp(i)       needs gather(i) and the S/dP tile read by read(i - 1);
 #   read(i)      needs sdp(i) and pds(i - G) (the same threads, in order);
 #   send(i)      needs read(i) and, for i >= NB, the peer's SendOk for block
