@@ -39,7 +39,7 @@
 //     absent): warps 8-10 gather this CTA's half of the kv rows with
 //     16-byte cp.async (coalesced 512-byte row pieces written into the
 //     128-byte-swizzled K-major tile; completion signalled per block by
-//     cp.async mbarrier arrivals) into a four-stage ring, and publish each
+//     cp.async mbarrier arrivals) into a five-stage ring, and publish each
 //     block's valid-slot mask; warp 11 owns TMEM and issues the MMAs from
 //     one thread (partial scores into a ring of three 64-column TMEM tiles;
 //     P.V with P, bf16, from a two-buffer ring in TMEM as the A operand);
@@ -71,7 +71,7 @@ struct FwdLayout {
   static constexpr int kHPad = 128;           // MMA M: heads padded to 128
   static constexpr int kBI = 64;              // slots per block (MMA N of the scores)
   static constexpr int kChunks = kDC / 64;    // 64-column (128-byte) swizzle chunks per row
-  static constexpr int kStages = 4;           // kv ring
+  static constexpr int kStages = 5;           // kv ring (five 32 KB stages fill shared memory)
   static constexpr int kSBufs = 3;            // score tiles in TMEM
   static constexpr int kXBufs = kSBufs + 3;   // exchange buffers per receiver
   static constexpr uint32_t kQChunkBytes = kHPad * 128;
@@ -109,7 +109,7 @@ struct FwdLayout {
   static constexpr uint32_t kOffSlot = kOffAbort + 4;
   static constexpr uint32_t kOffWarpLast = kOffSlot + 4;  // int [16]
   static constexpr uint32_t kOffMask = kOffWarpLast + 64;  // uint32 [kStages][2]
-  static constexpr uint32_t kCtrlBytes = 4096;
+  static constexpr uint32_t kCtrlBytes = 512;
   static_assert(kOffMask + 8 * kStages - kOffCtrl <= kCtrlBytes, "control block overflow");
   static constexpr uint32_t kSmemBytes = kOffCtrl + kCtrlBytes + 1024;  // +1024: realignment
   static_assert(kSmemBytes <= 232448, "shared memory budget");

@@ -12,7 +12,7 @@
 //
 // One CTA per (token, batch element), two CTAs per SM.  Per 64-slot block:
 //   gather (warps 4-5)  the block's key rows, 16-byte cp.async into a
-//                       128-byte-swizzled K-major tile (two-stage ring), and
+//                       128-byte-swizzled K-major tile (three-stage ring), and
 //                       its grad_scores with masked slots set to 0;
 //   MMA (warp 6)        L = Q.K^T (M = 128 head rows, N = 64 slots, K = D)
 //                       into one of two TMEM tiles, and once the block's gate
@@ -20,7 +20,9 @@
 //                       the same key tile read MN-major) into a TMEM
 //                       accumulator that lives for the whole token;
 //   gate (warps 0-3)    thread = head row: G[h,j] = g_j if L[h,j] > 0 else 0,
-//                       written bf16 as the K-major A operand of dq += G.K.
+//                       written bf16 as the K-major A operand of dq += G.K
+//                       (one buffer, rewritten once the previous block's dq
+//                       MMAs have read it).
 // At the end warps 0-3 scale the accumulator by w[t,h], round it to bf16 and
 // stage it in shared memory for TMA tensor stores.  Head rows H..127 of Q
 // are zero, so their rows of dq are never stored.
@@ -31,12 +33,14 @@
 
 namespace smqa {
 
-template <int D>
+template <int D, int STAGES = 2, int GBUFS = 2, int CTAS = 2>
 struct IdxLayout {
   static constexpr int kHPad = 128;
   static constexpr int kBI = 64;                    // slots per block
   static constexpr int kChunks = D / 64;            // 64-column (128-byte) chunks
-  static constexpr int kStages = 2;
+  static constexpr int kStages = STAGES;            // key-tile ring
+  static constexpr int kGateBufs = GBUFS;           // gate operand buffers
+  static constexpr int kCtasPerSm = CTAS;
   static constexpr uint32_t kQChunkBytes = kHPad * 128;   // 16 KB
   static constexpr uint32_t kQBytes = kChunks * kQChunkBytes;
   static constexpr uint32_t kKvChunkBytes = kBI * 128;    // 8 KB
@@ -44,16 +48,16 @@ struct IdxLayout {
   static constexpr uint32_t kGateBytes = kHPad * kBI * 2; // 16 KB (bf16, 128-byte rows)
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffKv = kOffQ + kQBytes;
-  static constexpr uint32_t kOffGate = kOffKv + kStages * kKvStageBytes;  // [2]
-  static constexpr uint32_t kOffG = kOffGate + 2 * kGateBytes;           // fp32 [kStages][64]
+  static constexpr uint32_t kOffGate = kOffKv + kStages * kKvStageBytes;  // [kGateBufs]
+  static constexpr uint32_t kOffG = kOffGate + kGateBufs * kGateBytes;   // fp32 [kStages][64]
   static constexpr uint32_t kOffCtrl = kOffG + kStages * kBI * 4;
   static constexpr int kBarKvFull = 0;
   static constexpr int kBarKvEmpty = kBarKvFull + kStages;
   static constexpr int kBarLFull = kBarKvEmpty + kStages;  // [2]
   static constexpr int kBarLFree = kBarLFull + 2;          // [2]
-  static constexpr int kBarGFull = kBarLFree + 2;          // [2] gate operand written
-  static constexpr int kBarGFree = kBarGFull + 2;          // [2] gate operand read by the MMA
-  static constexpr int kBarQFull = kBarGFree + 2;
+  static constexpr int kBarGFull = kBarLFree + 2;          // [kGateBufs] gate operand written
+  static constexpr int kBarGFree = kBarGFull + kGateBufs;  // [kGateBufs] gate operand read
+  static constexpr int kBarQFull = kBarGFree + kGateBufs;
   static constexpr int kBarDqDone = kBarQFull + 1;
   static constexpr int kBarDrain = kBarDqDone + 1;
   static constexpr int kBarStaged = kBarDrain + 1;
@@ -64,24 +68,24 @@ struct IdxLayout {
   static constexpr uint32_t kCtrlBytes = 256;
   static_assert(kOffWarpLast + 32 - kOffCtrl <= kCtrlBytes, "control block overflow");
   static constexpr uint32_t kSmemBytes = kOffCtrl + kCtrlBytes + 1024;
-  // Two CTAs per SM.
-  static_assert(2 * (kSmemBytes + 1024) <= 233472, "shared memory budget (two CTAs per SM)");
+  static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 233472, "shared memory budget");
   static_assert(kChunks * kQChunkBytes <= kStages * kKvStageBytes, "dq staging fits the ring");
   // TMEM: two L tiles, then the dq accumulator.
   static constexpr uint32_t kTmemL = 0;
   static constexpr uint32_t kTmemDq = 2 * kBI;
   static constexpr uint32_t kTmemCols = 256;
+  static_assert(kCtasPerSm * kTmemCols <= 512, "TMEM budget of the resident CTAs");
   static_assert(kTmemDq + D <= kTmemCols, "TMEM budget");
   static constexpr int kGatherWarp0 = 4;
   static constexpr int kMmaWarp = 6;
   static constexpr int kThreads = 224;
 };
 
-template <int D>
-__global__ void __launch_bounds__(224, 2)
+template <int D, int ST, int GB, int CT>
+__global__ void __launch_bounds__(224, CT)
     smqa_indexer_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                             const __grid_constant__ CUtensorMap tm_dq, const IdxParams p) {
-  using L = IdxLayout<D>;
+  using L = IdxLayout<D, ST, GB, CT>;
   extern __shared__ uint8_t smem_raw[];
   uint32_t base = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (base & 1023u)) & 1023u;
@@ -110,6 +114,8 @@ __global__ void __launch_bounds__(224, 2)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(L::kBarLFull + i), 1);
       mbar_init(bar(L::kBarLFree + i), 128);
+    }
+    for (int i = 0; i < L::kGateBufs; ++i) {
       mbar_init(bar(L::kBarGFull + i), 128);
       mbar_init(bar(L::kBarGFree + i), 1);
     }
@@ -215,13 +221,14 @@ __global__ void __launch_bounds__(224, 2)
       auto issue_dq = [&](int j) {
         const int st = j % L::kStages;
         const uint64_t dk = d_kvmn + ((static_cast<uint32_t>(st) * L::kKvStageBytes) >> 4);
-        const uint64_t dg = d_gate + ((static_cast<uint32_t>(j & 1) * L::kGateBytes) >> 4);
+        const uint64_t dg =
+            d_gate + ((static_cast<uint32_t>(j % L::kGateBufs) * L::kGateBytes) >> 4);
 #pragma unroll
         for (int k = 0; k < L::kBI / 16; ++k)
           mma_ss(tmem + L::kTmemDq, dg + (k * 32u >> 4), dk + (k * 2048u >> 4), idesc_dq,
                  (j > 0 || k > 0) ? 1u : 0u);
         mma_commit(bar(L::kBarKvEmpty + st));
-        mma_commit(bar(L::kBarGFree + (j & 1)));
+        mma_commit(bar(L::kBarGFree + j % L::kGateBufs));
       };
       // Event loop (non-blocking tests), oldest work first: dq of block n2
       // once its gate operand is written; L of block n1 once its key rows
@@ -231,7 +238,8 @@ __global__ void __launch_bounds__(224, 2)
       PollState ps = poll_start();
       uint32_t spins = 0;
       while (ok && n2 < nblk) {
-        if (n2 < n1 && mbar_probe(bar(L::kBarGFull + (n2 & 1)), (n2 >> 1) & 1)) {
+        if (n2 < n1 &&
+            mbar_probe(bar(L::kBarGFull + n2 % L::kGateBufs), (n2 / L::kGateBufs) & 1)) {
           tc_fence_after();
           issue_dq(n2);
           ++n2;
@@ -268,23 +276,25 @@ __global__ void __launch_bounds__(224, 2)
     const uint32_t row128 = static_cast<uint32_t>(h) * 128u;
     bool ok = *abort_flag == 0;
     for (int i = 0; ok && i < nblk; ++i) {
-      const int gb = i & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarLFull + gb), (i >> 1) & 1, ctl));
+      const int lb = i & 1;                // logit tile
+      const int gb = i % L::kGateBufs;     // gate operand buffer
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarLFull + lb), (i >> 1) & 1, ctl));
       if (!ok) break;
       tc_fence_after();
       float x[64];
-      const uint32_t t_l = tmem + lane_base + L::kTmemL + static_cast<uint32_t>(gb) * L::kBI;
+      const uint32_t t_l = tmem + lane_base + L::kTmemL + static_cast<uint32_t>(lb) * L::kBI;
       tmem_ld32x2(t_l, t_l + 32, *reinterpret_cast<float(*)[32]>(x),
                   *reinterpret_cast<float(*)[32]>(x + 32));
       tc_fence_before();
-      mbar_arrive(bar(L::kBarLFree + gb));
+      mbar_arrive(bar(L::kBarLFree + lb));
       // The block's grad_scores (its key tile, and so the L tile, came after
       // them; this wait has completed and only orders the reads).
       const int st = i % L::kStages;
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarKvFull + st), (i / L::kStages) & 1, ctl));
       if (!ok) break;
-      if (i >= 2) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarGFree + gb), ((i - 2) >> 1) & 1, ctl));
+      if (i >= L::kGateBufs) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(bar(L::kBarGFree + gb), ((i / L::kGateBufs) - 1) & 1, ctl));
         if (!ok) break;
       }
       const float4* gq = reinterpret_cast<const float4*>(smem + L::kOffG + st * L::kBI * 4);
@@ -361,11 +371,18 @@ __global__ void __launch_bounds__(224, 2)
   }
 }
 
+// Key-tile stages, gate buffers and CTAs per SM of the kernel (measured on
+// the H=64 D=128 topk=2048 S=8192 workload: 2/2/2 1.292 ms, 3/1/2 1.049 ms,
+// 4/2/1 1.685 ms, 6/2/1 1.668 ms; two resident CTAs hide each other's
+// per-token prologue and epilogue, and the third stage outweighs the second
+// gate buffer).
+constexpr int kIdxStages = 3, kIdxGateBufs = 1, kIdxCtas = 2;
+
 template <int D>
 static cudaError_t launch_indexer_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_dq,
                                        const IdxParams& p, int ctas, cudaStream_t stream) {
-  using L = IdxLayout<D>;
-  auto kern = smqa_indexer_bwd_kernel<D>;
+  using L = IdxLayout<D, kIdxStages, kIdxGateBufs, kIdxCtas>;
+  auto kern = smqa_indexer_bwd_kernel<D, kIdxStages, kIdxGateBufs, kIdxCtas>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;

@@ -99,8 +99,9 @@ def run_model(X: int, nblk: int, seed: int, tiles: int = 3, stages: int = 4):
 
 @pytest.mark.parametrize("X", [4, 5, 6])
 @pytest.mark.parametrize("seed", range(40))
-def test_exchange_protocol_is_safe_and_live(X, seed):
-    assert run_model(X, nblk=24, seed=seed) == "ok"
+@pytest.mark.parametrize("stages", [4, 5])
+def test_exchange_protocol_is_safe_and_live(X, seed, stages):
+    assert run_model(X, nblk=24, seed=seed, stages=stages) == "ok"
 
 
 def test_three_buffers_deadlock():
