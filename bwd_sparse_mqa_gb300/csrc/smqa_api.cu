@@ -526,6 +526,7 @@ smqa_status indexer_impl(const void* q, const float* w, const void* k, const int
   p.k_b_stride = batched ? s.D : 0;
   p.status = st;
   p.limit_ns = wait_limit_ns();
+  p.stall_cta = g_stall_cta.load(std::memory_order_relaxed);
   e = smqa::launch_indexer_bwd(tq, tdq, p, stream);
   if (e != cudaSuccess) return cuda_fail(e, "indexer bwd launch");
   return SMQA_OK;

@@ -252,6 +252,10 @@ __global__ void __launch_bounds__(224, CT)
           tc_fence_after();
           issue_l(n1);
           ++n1;
+          if (static_cast<int>(blockIdx.x) == p.stall_cta) {  // test hook only
+            ok = stall_until_limit(ctl);
+            break;
+          }
         } else {
           if ((++spins & 63u) == 0u && !poll_check(ctl, ps)) {
             ok = false;

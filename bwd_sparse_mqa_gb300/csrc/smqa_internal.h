@@ -75,6 +75,7 @@ struct IdxParams {
   int64_t k_row_stride, k_b_stride;
   int* status;
   uint64_t limit_ns;
+  int stall_cta;         // test hook: this CTA stalls after its first MMA (-1: none)
 };
 
 // One exchange slot of the forward: two receivers x six block buffers x

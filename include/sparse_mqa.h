@@ -371,8 +371,9 @@ smqa_status smqa_device_status(int clear);
 uint64_t smqa_set_wait_limit_ns(uint64_t ns);
 
 /*
- * Test hook for the failure path.  In every forward and backward-main launch
- * after this call, CTA `cta` (a block index of the launch; -1 turns the hook
+ * Test hook for the failure path.  In every forward, backward-main and
+ * indexer-backward launch after this call, CTA `cta` (a block index of the
+ * launch; -1 turns the hook
  * off) stops after issuing its first tensor-core instruction and waits for a
  * condition that never comes true.  The wait is bounded like every other, so
  * after the wait limit the CTA records SMQA_ERR_DEVICE_TIMEOUT, drains its

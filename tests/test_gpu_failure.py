@@ -4,7 +4,8 @@ allows: no fault, trap or endless loop.  The library's test hook
 instruction and wait for a condition that never comes true; with a 50 ms
 wait limit that wait runs out, the CTA records SMQA_ERR_DEVICE_TIMEOUT in the
 device status word, drains its copies and MMAs, frees TMEM and exits, and its
-peer CTA (D = 512) gives up waiting for the exchange.  The test checks that the call returns, that the
+peer CTA (D = 512) gives up waiting for the exchange.  The lightning-indexer
+backward's kernel is driven through the same path.  The test checks that the call returns, that the
 status is reported (also as an exception with check_status=True, and through
 the autograd wrapper), that later launches skip their work while the word is
 set, that clearing it works, and that afterwards, in the same process and
@@ -79,6 +80,31 @@ for D in (512, 64):
     sparse_mqa_bwd_interface(g["q"], g["kv"], g["attn_sink"], o, g["do"], g["topk_idxs"], lse,
                              check_status=True)
     print("D", D, "after the timeout:", errs)
+
+# The indexer backward's kernel takes the same path.
+from bwd_sparse_mqa_gb300 import indexer_bwd_interface
+import numpy as np
+xi = inputs.indexer_custom(1, 24, 150, 64, 128, 100, recipe="causal_masked10", seed=61)
+gi = {k: v[0].contiguous().cuda() for k, v in xi.items()}
+set_wait_limit_ns(50_000_000)
+lib.smqa_debug_stall(3)
+try:
+    indexer_bwd_interface(gi["index_q"], gi["weights"], gi["index_k"], gi["topk_indices"],
+                          gi["grad_scores"])
+    assert device_status(clear=False) == TIMEOUT, "indexer backward did not time out"
+    assert device_status(clear=True) == TIMEOUT
+finally:
+    lib.smqa_debug_stall(-1)
+    set_wait_limit_ns(0)
+dq = indexer_bwd_interface(gi["index_q"], gi["weights"], gi["index_k"], gi["topk_indices"],
+                           gi["grad_scores"])
+assert device_status(clear=False) == 0
+ref, slack = oracle.indexer_bwd(xi["index_q"][0], xi["weights"][0], xi["index_k"][0],
+                                xi["topk_indices"][0], xi["grad_scores"][0], amb=2.0 ** -12)
+got = dq.float().cpu().numpy().astype(np.float64)
+e = float(np.max(np.maximum(np.abs(got - ref) - slack, 0.0)) / np.max(np.abs(ref)))
+assert e <= 2e-2, e
+print("indexer after the timeout:", e)
 print("OK")
 '''
 
