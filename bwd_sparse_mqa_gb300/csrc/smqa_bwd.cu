@@ -616,24 +616,20 @@ __global__ void __launch_bounds__(480, 1)
         mma_commit(bar(L::kBarPdsFree + (j & 1)));
         mma_commit(bar(L::kBarDkvFull));
       };
-      // Event loop (non-blocking tests), oldest work first: the gradients
-      // of block ng once its P / dS are written and the drain has read the
-      // previous dKV^T tile; S / dP of block ns once its kv rows have landed
-      // and the previous S / dP tile has been read.
+      // Event loop (non-blocking tests): S / dP of block ns as soon as its kv
+      // rows have landed and the previous S / dP tile has been read (first,
+      // so the other P / dS group gets its tile early: 12.67 -> 12.55 ms);
+      // otherwise the gradients of block ng once its P / dS are written and
+      // the drain has read the previous dKV^T tile.
       bool ok = mbar_wait(bar(L::kBarQdoFull), 0, ctl);
       int ns = 0, ng = 0;
       PollState ps = poll_start();
       uint32_t spins = 0;
       while (ok && ng < nblk) {
-        if (ng < ns && mbar_probe(bar(L::kBarPdsFull + (ng & 1)), (ng >> 1) & 1) &&
-            (ng == 0 || mbar_probe(bar(L::kBarDkvFree), (ng - 1) & 1))) {
-          tc_fence_after();
-          issue_grad(ng);
-          ++ng;
-        } else if (ns < nblk &&
-                   mbar_probe(bar(L::kBarKvFull + ns % L::kStages), (ns / L::kStages) & 1) &&
-                   (ns == 0 ||
-                    mbar_probe(bar(L::kBarSdpFree + ((ns - 1) & 1)), ((ns - 1) >> 1) & 1))) {
+        if (ns < nblk &&
+            mbar_probe(bar(L::kBarKvFull + ns % L::kStages), (ns / L::kStages) & 1) &&
+            (ns == 0 ||
+             mbar_probe(bar(L::kBarSdpFree + ((ns - 1) & 1)), ((ns - 1) >> 1) & 1))) {
           // The kv tile was written by cp.async (generic proxy): order it
           // before the tensor core's (async proxy) reads.
           fence_proxy_async_smem();
@@ -644,6 +640,11 @@ __global__ void __launch_bounds__(480, 1)
             ok = stall_until_limit(ctl);
             break;
           }
+        } else if (ng < ns && mbar_probe(bar(L::kBarPdsFull + (ng & 1)), (ng >> 1) & 1) &&
+                   (ng == 0 || mbar_probe(bar(L::kBarDkvFree), (ng - 1) & 1))) {
+          tc_fence_after();
+          issue_grad(ng);
+          ++ng;
         } else {
           if ((++spins & 63u) == 0u && !poll_check(ctl, ps)) {
             ok = false;
@@ -684,7 +685,17 @@ __global__ void __launch_bounds__(480, 1)
         red_add_f32(col + off, v);
       }
     };
+    // The index rows of the next block are loaded while this one is drained,
+    // so their L2 latency stays off the way to DkvFree (12.66 -> 12.36 ms).
+    auto load_r = [&](int blk, int half) -> int {
+      const int slot_j = blk * L::kBI + 32 * half + lane;
+      return (blk < nblk && slot_j < p.topk) ? __ldg(idx_row + slot_j) : -1;
+    };
+    int rn0 = load_r(0, 0), rn1 = load_r(0, 1);
     for (int j = 0; j < nblk; ++j) {
+      const int rc[2] = {rn0, rn1};
+      rn0 = load_r(j + 1, 0);
+      rn1 = load_r(j + 1, 1);
       const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDkvFull), j & 1, ctl));
       if (!ok) break;
       tc_fence_after();
@@ -692,8 +703,7 @@ __global__ void __launch_bounds__(480, 1)
       uint32_t vm[2];
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        const int slot_j = j * L::kBI + 32 * half + lane;
-        const int r = slot_j < p.topk ? __ldg(idx_row + slot_j) : -1;
+        const int r = rc[half];
         const bool v = static_cast<unsigned>(r) < static_cast<unsigned>(p.S_kv);
         vm[half] = __ballot_sync(0xffffffffu, v);
         row[half] = b * p.S_kv + (v ? r : 0);
