@@ -1,5 +1,7 @@
-"""Exact-arithmetic model of the forward's block-floating-point rounding of a
-head's half-D partial scores (the senders' arithmetic in smqa_fwd.cu): the
+"""Exact-arithmetic model of the block-floating-point rounding of a head's
+half-D partial sums that the CTA pairs exchange (the forward's senders in
+smqa_fwd.cu round partial scores this way, the backward's P/dS threads in
+smqa_bwd.cu partial S and sm_scale dP, 32 slots at a time): the
 exponent comes from the fp32 maximum times (1 + 2^-15), every mantissa then
 stays within +-32767 without a clamp, and the absolute error stays within
 2^-15 (1 + 2^-14) of the largest scaled partial.
@@ -80,3 +82,17 @@ def test_maxima_at_power_of_two_boundaries(k):
 def test_all_zero_block():
     n, e, _ = _quantise(np.zeros(64, dtype=np.float32), np.float32(0.09))
     assert e == -100 and all(k == 0 for k in n)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_backward_blocks_at_gradient_scale(seed):
+    """The backward's use: 32-value blocks of partial S (scale sm_scale log2 e)
+    and partial dP (scale sm_scale) at magnitudes from gradient-sized (dO of
+    2^-30 gives partial dP near 1e-9) to large; the bound is relative to the
+    block's largest value, so it holds at every scale down to the exponent
+    clamp at 2^-100."""
+    rng = np.random.default_rng(50 + seed)
+    for s1 in (np.float32(0.04419417 * 1.4426950408889634), np.float32(0.04419417)):
+        for mag in (2.0 ** -60, 2.0 ** -30, 2.0 ** -20, 1.0, 2.0 ** 10):
+            x = (rng.standard_normal(32) * mag).astype(np.float32)
+            _check(x, s1)

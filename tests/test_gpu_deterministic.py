@@ -1,6 +1,8 @@
-"""Deterministic dKV (SMQA_FLAG_DETERMINISTIC_DKV): 32.32 fixed-point integer
-accumulation gives bit-identical dkv from run to run, equal to the oracle
-within the tolerance and to the fp32-atomic path within its rounding."""
+"""Deterministic dKV (SMQA_FLAG_DETERMINISTIC_DKV): 64-bit fixed-point integer
+accumulation (binary point chosen per call from the inputs' magnitudes) gives
+bit-identical dkv from run to run, equal to the oracle within the tolerance
+and to the fp32-atomic path within its rounding.  Gradient-sized and large
+inputs are covered by tests/test_gpu_magnitudes.py."""
 import pytest
 import torch
 
