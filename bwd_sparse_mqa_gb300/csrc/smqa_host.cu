@@ -24,13 +24,22 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 // Chunking: at most about this many chunks per call, none below
-// kMinChunkTokens tokens except a last group of whole batch elements (a
-// chunk's kernels then still fill every SM).  More chunks shorten
-// the copies before the first kernel and after the last one; on the
-// H=128 D=512 topk=2048 S=8192 workload 8, 16 and 24 chunks measured 20.8,
-// 20.1 and 19.8 ms per forward + backward.
+// kMinChunkTokens tokens except the last piece of a batch element's
+// positions or a last group of whole batch elements (a chunk's kernels then
+// still fill every SM).  More chunks shorten the copies before the first
+// kernel and after the last one; on the H=128 D=512 topk=2048 S=8192
+// workload 8, 16 and 24 chunks measured 20.8, 20.1 and 19.8 ms per forward
+// + backward, 32 and 64 no better than 24.  Pieces of S are whole waves --
+// multiples of the tokens one backward launch holds on the GPU at once, half
+// the SM count for D = 512 (a CTA pair per token), the SM count for D = 64
+// -- with the remainder last: a chunk of 4.5 waves leaves half the GPU idle
+// for its last wave, and a short last chunk shortens the final copy of dq
+// (with dout copied next to q: 19.96 -> 19.71 ms; 19.82 with the remainder
+// first).
 constexpr int64_t kTargetChunks = 24;
 constexpr int64_t kMinChunkTokens = 256;
+// The SM count assumed when no device is visible (a GB300).
+constexpr int kDefaultSmCount = 152;
 
 size_t r256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -46,6 +55,17 @@ smqa_status cuda_fail(cudaError_t e, const char* where) {
   return SMQA_ERR_CUDA;
 }
 
+// The SM count of the current device, or kDefaultSmCount when none answers.
+int current_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    (void)cudaGetLastError();
+    return kDefaultSmCount;
+  }
+  return n;
+}
+
 // A run of tokens copied and computed together: batch elements
 // [b0, b0 + nb) x positions [s0, s0 + ns).  nb > 1 only when ns = S, so a
 // chunk's tokens are contiguous in every [B,S,...] tensor.
@@ -53,18 +73,18 @@ struct Chunk {
   int b0, nb, s0, ns;
 };
 
-std::vector<Chunk> plan_chunks(const smqa_shape& s) {
+std::vector<Chunk> plan_chunks(const smqa_shape& s, int sm_count) {
   const int64_t total = static_cast<int64_t>(s.B) * s.S;
-  const int64_t t = std::max((total + kTargetChunks - 1) / kTargetChunks, kMinChunkTokens);
+  const int64_t wave = std::max(1, s.D == 512 ? sm_count / 2 : sm_count);
+  int64_t t = std::max((total + kTargetChunks - 1) / kTargetChunks, kMinChunkTokens);
   std::vector<Chunk> out;
   if (s.S >= t) {
-    const int per = static_cast<int>(s.S / t);  // near-equal pieces of each S, each >= t
+    // Pieces of t tokens rounded up to whole waves, the last piece of each S
+    // the remainder; all of S in one piece when one such piece would not fit.
+    t = std::min<int64_t>((t + wave - 1) / wave * wave, s.S);
     for (int b = 0; b < s.B; ++b)
-      for (int i = 0; i < per; ++i) {
-        const int a = static_cast<int>(static_cast<int64_t>(s.S) * i / per);
-        const int e = static_cast<int>(static_cast<int64_t>(s.S) * (i + 1) / per);
-        out.push_back({b, 1, a, e - a});
-      }
+      for (int64_t a = 0; a < s.S; a += t)
+        out.push_back({b, 1, static_cast<int>(a), static_cast<int>(std::min<int64_t>(t, s.S - a))});
   } else {
     // Whole batch elements, k * S >= t tokens per chunk (the last chunk may
     // hold fewer elements).
@@ -213,9 +233,9 @@ smqa_status enqueue(const HostArgs& a, const Layout& L, uint8_t* ws,
   auto dev = [ws](size_t region, size_t off) { return ws + region + off; };
   const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
 
-  // ---- host -> device: kv and sink, then each chunk's q and idx, with each
-  // chunk's dout one chunk later (the backward of chunk c runs beside the
-  // forward of chunk c+1).
+  // ---- host -> device: kv and sink, then each chunk's q, idx and dout (the
+  // backward is the longer stream: its first chunk starts as soon as the
+  // forward of chunk 0 is done; dout one chunk later measured 0.5 % slower).
   SMQA_TRY(cudaMemcpyAsync(dev(L.kv, 0), a.kv, kvel * 2, h2d, sd.h2d), "kv copy");
   SMQA_TRY(cudaMemcpyAsync(dev(L.sink, 0), a.sink, lse_bytes, h2d, sd.h2d), "sink copy");
   SMQA_TRY(cudaEventRecord(sd.ev[kEvKv], sd.h2d), "event record");
@@ -231,14 +251,10 @@ smqa_status enqueue(const HostArgs& a, const Layout& L, uint8_t* ws,
     SMQA_TRY(cudaMemcpyAsync(dev(L.idx, tok0(c) * idx_bytes), host(a.idx, tok0(c) * idx_bytes),
                              ntok(c) * idx_bytes, h2d, sd.h2d), "topk_idxs copy");
     SMQA_TRY(cudaEventRecord(sd.ev[ev_in(c)], sd.h2d), "event record");
-    if (bwd && c >= 1) {
-      const smqa_status r = copy_dout(c - 1);
+    if (bwd) {
+      const smqa_status r = copy_dout(c);
       if (r != SMQA_OK) return r;
     }
-  }
-  if (bwd) {
-    const smqa_status r = copy_dout(n - 1);
-    if (r != SMQA_OK) return r;
   }
 
   // ---- forward, chunk by chunk, on the caller's stream.
@@ -404,7 +420,10 @@ smqa_status run(const HostArgs& a, void* workspace, size_t workspace_bytes, cuda
     if (p && !is_host_pointer(p))
       return fail(SMQA_ERR_INVALID_ARG, "a tensor argument is device memory (host buffers expected)");
 
-  const std::vector<Chunk> ch = plan_chunks(a.s);
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  const std::vector<Chunk> ch = plan_chunks(a.s, sms);
   Side& sd = g_side[dev];
   std::lock_guard<std::mutex> lk(sd.m);
   smqa_status r = side_prepare(sd, kEvFixed + 4 * ch.size());
@@ -436,7 +455,7 @@ extern "C" {
 
 int smqa_host_chunk_plan(smqa_shape shape, int32_t* out, int max_chunks) {
   if (smqa::validate_shape(shape) != SMQA_OK) return 0;
-  const std::vector<Chunk> ch = plan_chunks(shape);
+  const std::vector<Chunk> ch = plan_chunks(shape, current_sm_count());
   const int n = static_cast<int>(ch.size());
   for (int c = 0; out && c < n && c < max_chunks; ++c) {
     out[4 * c] = ch[c].b0;

@@ -275,7 +275,9 @@ size_t smqa_fwd_host_workspace_bytes(smqa_shape shape);
  * (b0, nb, s0, ns) -- batch elements [b0, b0 + nb) x positions [s0, s0 + ns),
  * nb > 1 only with s0 = 0 and ns = S -- into `out` (4 int32 per chunk; may be
  * NULL) and returns the number of chunks, or 0 for an unsupported shape.
- * Host only: no CUDA call. */
+ * Pieces of S are whole multiples of the tokens one backward launch holds on
+ * the GPU at once, so the plan reads the current device's SM count (152, a
+ * GB300's, when no device is visible); it launches and allocates nothing. */
 int smqa_host_chunk_plan(smqa_shape shape, int32_t* out, int max_chunks);
 size_t smqa_fwd_bwd_host_workspace_bytes(smqa_shape shape, unsigned flags);
 smqa_status smqa_fwd_host(const void* q, const void* kv, const float* attn_sink,

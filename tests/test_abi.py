@@ -266,9 +266,11 @@ def test_product_package_does_not_import_oracle():
 def test_host_chunk_plan_partitions_the_tokens(lib, B, S):
     """The host entry's chunk plan covers every (b, s) exactly once, in
     order, with contiguous tokens per chunk, at least 256 tokens per chunk
-    (except a last group of whole batch elements, or a smaller problem),
-    and at most about 24 chunks."""
-    shp = _lib.Shape(B, S, 64, 16, 64, 8)
+    (except the last piece of a batch element's positions, a last group of
+    whole batch elements, or a smaller problem), pieces of S in whole waves
+    of 76 tokens (D = 512 on 152 SMs, no device here) but the last one, and
+    at most about 24 chunks."""
+    shp = _lib.Shape(B, S, 64, 16, 512, 8)
     n = lib.smqa_host_chunk_plan(shp, None, 0)
     assert n >= 1
     buf = (ctypes.c_int32 * (4 * n))()
@@ -280,7 +282,10 @@ def test_host_chunk_plan_partitions_the_tokens(lib, B, S):
         if nb > 1:
             assert s0 == 0 and ns == S
         flat.extend(range(b0 * S + s0, b0 * S + s0 + nb * ns))
-        assert nb * ns >= min(256, B * S) or (b0 + nb == B and s0 == 0 and ns == S)
+        last_piece = nb == 1 and s0 + ns == S
+        assert nb * ns >= min(256, B * S) or last_piece or (b0 + nb == B and s0 == 0 and ns == S)
+        if nb == 1 and not last_piece:
+            assert ns % 76 == 0
     assert flat == list(range(B * S))
     assert n <= 25
     assert lib.smqa_host_chunk_plan(_lib.Shape(B, S, 64, 16, 100, 8), None, 0) == 0

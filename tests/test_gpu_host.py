@@ -11,9 +11,10 @@ import oracle
 from bwd_sparse_mqa_gb300 import (_lib, inputs, sparse_mqa_fwd_bwd_host, sparse_mqa_fwd_host)
 from tests import _parity as P
 
-# (B, S, S_kv, H, D, topk, recipe): chunks of at least 256 tokens (the
-# minimum decides at these sizes; smqa_host_chunk_plan gives the plan) --
-#   1 x 1100 -> four pieces of S (275 tokens each);
+# (B, S, S_kv, H, D, topk, recipe): chunks of at least 256 tokens rounded up
+# to whole waves (the minimum decides at these sizes; smqa_host_chunk_plan
+# gives the plan) -- on a 152-SM GB300
+#   1 x 1100 -> three pieces of S of 304 tokens and a last one of 188;
 #   2 x 600  -> two pieces per batch element (kv and dKV offsets per b);
 #   5 x 100  -> whole batch elements, three in a chunk and a last chunk of two.
 CASES = [(1, 1100, 500, 32, 512, 96, "causal_masked10"),
