@@ -138,6 +138,8 @@ size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // slots.
 constexpr size_t kExchFlagBytes = 4096;
 constexpr int kExchSlots = 96;
+// The slot flags, then the backward's token counter, fit the flag block.
+static_assert((kExchSlots + 1) * sizeof(int) <= kExchFlagBytes, "exchange flag block");
 
 size_t exchange_bytes(const smqa_shape& s) {
   return s.D == 512 ? kExchFlagBytes + static_cast<size_t>(kExchSlots) * smqa::kBwdSlotBytes : 0;
@@ -156,15 +158,15 @@ smqa_status bwd_main_impl(const void* q, const void* kv, const void* dout, const
   int* st = status_ptr(&e);
   if (!st) return cuda_fail(e, "status word");
   if (exchange_bytes(s) != 0) {
-    // Every slot free at launch (the kernel's pairs claim and release them).
-    e = cudaMemsetAsync(exch, 0, kExchSlots * sizeof(int), stream);
+    // Every slot free at launch (the kernel's pairs claim and release them),
+    // and the token counter the pairs take their tokens from at zero.
+    e = cudaMemsetAsync(exch, 0, (kExchSlots + 1) * sizeof(int), stream);
     if (e != cudaSuccess) return cuda_fail(e, "exchange flags clear");
   }
-  CUtensorMap tq, tdo, tdq;
+  CUtensorMap tq, tdo;
   const uint64_t T = static_cast<uint64_t>(s.B) * s.S;
   if (!encode_bf16_2d(&tq, q, s.D, T * s.H, 64, static_cast<uint32_t>(s.H)) ||
-      !encode_bf16_2d(&tdo, dout, s.D, T * s.H, 64, static_cast<uint32_t>(s.H)) ||
-      !encode_bf16_2d(&tdq, dq, s.D, T * s.H, 64, static_cast<uint32_t>(s.H)))
+      !encode_bf16_2d(&tdo, dout, s.D, T * s.H, 64, static_cast<uint32_t>(s.H)))
     return SMQA_ERR_CUDA;
   smqa::BwdParams p{};
   p.kv = static_cast<const __nv_bfloat16*>(kv);
@@ -190,8 +192,9 @@ smqa_status bwd_main_impl(const void* q, const void* kv, const void* dout, const
     p.slot_flags = static_cast<int*>(exch);
     p.exch = static_cast<uint8_t*>(exch) + kExchFlagBytes;
     p.nslots = kExchSlots;
+    p.tok_counter = static_cast<int*>(exch) + kExchSlots;
   }
-  e = smqa::launch_bwd_main(tq, tdo, tdq, p, static_cast<int>(T), stream);
+  e = smqa::launch_bwd_main(tq, tdo, p, static_cast<int>(T), stream);
   if (e != cudaSuccess) return cuda_fail(e, "bwd main launch");
   return SMQA_OK;
 }

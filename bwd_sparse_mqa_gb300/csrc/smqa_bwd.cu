@@ -13,15 +13,18 @@
 // Three kernels, as on the page:
 //   preprocess   Delta[t,h] in fp32 (one warp per row) and zeroing of the
 //                fp32 dKV accumulator, fused into one launch;
-//   main         per token (a CTA pair for D = 512, each CTA owning half of
-//                D): S = Q.K^T and dP = dO.V^T on the tensor core over 64-slot
+//   main         persistent CTAs (a CTA pair for D = 512, each CTA owning
+//                half of D) that take tokens one after another: per token,
+//                S = Q.K^T and dP = dO.V^T on the tensor core over 64-slot
 //                blocks, the pair's half-D partial sums traded in block
 //                floating point through an L2-resident exchange slot (two
 //                buffers per receiver, freed by a consumed-signal), P and dS
 //                on CUDA cores, then dQ += dS.K accumulated in TMEM over all
 //                blocks and dKV^T = Q^T.dS + dO^T.P per block, which a drain
 //                warpgroup reads from TMEM and scatters with fp32
-//                red.global.add into the accumulator;
+//                red.global.add into the accumulator; the next token's
+//                gathers, scores and exchange start while the current one
+//                finishes;
 //   postprocess  fp32 accumulator -> bf16 (round to nearest even).
 // dKV^T (lanes = head-dim rows, columns = slots) keeps M = 128 for the
 // 64-slot blocks and lets each warp's 32 lanes add to 32 consecutive floats
@@ -296,6 +299,7 @@ struct BwdLayout {
   static constexpr int kChunks = DC / 64;
   static constexpr int kNE = DC >= 128 ? DC / 128 : 1;  // 128-row halves of dKV^T
   static constexpr int kStages = NC == 2 ? 2 : 4;
+  static constexpr int kTokRing = 4;             // live-block counts published ahead
   static constexpr uint32_t kQChunkBytes = kHPad * 128;          // 16 KB
   static constexpr uint32_t kQBytes = kChunks * kQChunkBytes;
   static constexpr uint32_t kKvChunkBytes = kBI * 128;           // 8 KB
@@ -311,9 +315,10 @@ struct BwdLayout {
   static constexpr uint32_t kOffCtrl = kOffDs + kPBytes;
   static constexpr int kBarKvFull = 0;
   static constexpr int kBarKvEmpty = kBarKvFull + kStages;
-  // The P / dS groups alternate blocks (group = block parity), so the
-  // barriers between them and the MMA issuer come one per parity: a group
-  // only ever waits on phases of its own blocks.
+  // The P / dS groups alternate blocks (group = parity of the block's index
+  // in the CTA's whole sequence), so the barriers between them and the MMA
+  // issuer come one per parity: a group only ever waits on phases of its own
+  // blocks.
   static constexpr int kBarSdpFull = kBarKvEmpty + kStages;  // [2]
   static constexpr int kBarSdpFree = kBarSdpFull + 2;        // [2]
   static constexpr int kBarPdsFull = kBarSdpFree + 2;        // [2]
@@ -322,20 +327,29 @@ struct BwdLayout {
   static constexpr int kBarDkvFree = kBarDkvFull + 1;
   static constexpr int kBarRecvFull = kBarDkvFree + 1;  // [2], by block parity
   static constexpr int kBarSendOk = kBarRecvFull + 2;    // [2]
-  static constexpr int kBarQdoFull = kBarSendOk + 2;
-  static constexpr int kBarDqDone = kBarQdoFull + 1;
-  static constexpr int kBarDrain = kBarDqDone + 1;
-  static constexpr int kBarDqStaged = kBarDrain + 1;  // dQ tile in shared memory
-  static constexpr int kNumBars = kBarDqStaged + 1;
+  static constexpr int kBarQdoFull = kBarSendOk + 2;     // one phase per token with blocks
+  static constexpr int kBarQdoFree = kBarQdoFull + 1;    // its MMAs are done with Q and dO
+  static constexpr int kBarDqDone = kBarQdoFree + 1;     // its dQ is complete in TMEM
+  static constexpr int kBarDqFree = kBarDqDone + 1;      // ... and has been read out
+  static constexpr int kBarTokFull = kBarDqFree + 1;     // [kTokRing]
+  static constexpr int kBarTokEmpty = kBarTokFull + kTokRing;  // [kTokRing]
+  // The pair's token sequence: rank 0 takes each token from the counter and
+  // hands it to both CTAs (IdFull), rank 1 frees an entry again (IdEmpty,
+  // on rank 0) once its readers are done with it.
+  static constexpr int kBarIdFull = kBarTokEmpty + kTokRing;   // [kTokRing]
+  static constexpr int kBarIdEmpty = kBarIdFull + kTokRing;    // [kTokRing]
+  static constexpr int kBarDrain = kBarIdEmpty + kTokRing;
+  static constexpr int kNumBars = kBarDrain + 1;
   static constexpr uint32_t kOffTmemHolder = kOffCtrl + 8 * kNumBars;
   static constexpr uint32_t kOffAbort = kOffTmemHolder + 4;
   static constexpr uint32_t kOffSlot = kOffAbort + 4;
-  static constexpr uint32_t kOffWarpLast = kOffSlot + 4;  // int [16]
+  static constexpr uint32_t kOffTokLast = kOffSlot + 4;           // int [kTokRing][2]
+  static constexpr uint32_t kOffTokId = kOffTokLast + 8 * kTokRing;  // int [kTokRing], handed over
+  static constexpr uint32_t kOffTokT = kOffTokId + 4 * kTokRing;     // int [kTokRing], published
   static constexpr uint32_t kCtrlBytes = 512;
-  static_assert(kOffWarpLast + 64 - kOffCtrl <= kCtrlBytes, "control block overflow");
+  static_assert(kOffTokT + 4 * kTokRing - kOffCtrl <= kCtrlBytes, "control block overflow");
   static constexpr uint32_t kSmemBytes = kOffCtrl + kCtrlBytes + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert((DC / 64) * kQChunkBytes <= kStages * kKvStageBytes, "dQ staging fits the kv ring");
   // TMEM: dQ, S, dP, dKV^T (one tile each).
   static constexpr uint32_t kTmemDq = 0;
   static constexpr uint32_t kTmemS = DC;
@@ -347,14 +361,18 @@ struct BwdLayout {
   // warps 0-7: P / dS in two groups of four (group g = warp / 4 handles the
   // blocks of parity g; thread = head row 32 (warp % 4) + lane, all 64 slots
   // of a block; for D split across the pair they also send this CTA's
-  // partial S / dP to the peer); 8-11: dKV drain (thread = head-dim row);
-  // 12-13: gather; 14: TMEM owner + MMA issuer.
+  // partial S / dP to the peer); 8-11: dKV drain (thread = head-dim row) and
+  // each token's dQ read-out (thread = head row); 12-13: gather and each
+  // token's live-block count; 14: TMEM owner + MMA issuer + Q / dO loads.
   static constexpr int kPdsThreads = 256;
   static constexpr int kGroupThreads = 128;
   static constexpr int kDrainWarp0 = 8;
   static constexpr int kProducerWarp0 = 12;
   static constexpr int kMmaWarp = 14;
   static constexpr int kThreads = 480;
+  // Readers of a published live-block count: the MMA thread, the eight
+  // P / dS warps and the four drain warps (one arrival each).
+  static constexpr int kTokReaders = 1 + 8 + 4;
   // Exchange buffer of one receiver and block parity: 16 pieces of 16 bytes
   // per head (8 of S, 8 of dP, each the 16-bit block-floating-point fields
   // of 8 slots), piece-major, then per slot half and head one packed pair of
@@ -397,11 +415,19 @@ __device__ __forceinline__ float bfp16_unit(uint32_t exps) {
   return pow2f(e - 14);
 }
 
+// Persistent: each CTA (pair) of the grid's p.clusters handles a sequence of
+// tokens -- taken one at a time from p.tok_counter by the pair's rank 0 (so
+// faster pairs take more), or c, c + p.clusters, ... without a counter -- as
+// one sequence of 64-slot blocks (G counts them over the CTA's whole life),
+// so that the next token's gathers, scores and exchange overlap the last
+// blocks and the dQ read-out of the current one; only Q / dO (one buffer)
+// wait for the previous token's gradient MMAs.  Every barrier phase follows
+// G, or the token count k.  Ring entry k % kTokRing publishes token k's index
+// (-1: no more tokens) and live-block count.
 template <int DC, int NC, bool DET>
 __global__ void __launch_bounds__(480, 1)
     smqa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
-                    const __grid_constant__ CUtensorMap tm_do,
-                    const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
   using L = BwdLayout<DC, NC>;
   extern __shared__ uint8_t smem_raw[];
   uint32_t base = smem_u32(smem_raw);
@@ -411,14 +437,22 @@ __global__ void __launch_bounds__(480, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x / NC;
+  const int cl = static_cast<int>(blockIdx.x) / NC;  // this CTA's (pair's) index
   const uint32_t rank = NC == 2 ? cluster_ctarank() : 0u;
-  const int b = t / p.S;
+  auto token_of = [&](int k) -> int { return cl + k * p.clusters; };  // k-th token of the CTA
   auto bar = [&](int i) -> uint32_t { return base + L::kOffCtrl + 8u * static_cast<uint32_t>(i); };
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(smem + L::kOffTmemHolder);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
   volatile int* slot_smem = reinterpret_cast<volatile int*>(smem + L::kOffSlot);
+  volatile int* tok_last = reinterpret_cast<volatile int*>(smem + L::kOffTokLast);
+  volatile int* tok_id = reinterpret_cast<volatile int*>(smem + L::kOffTokId);
+  volatile int* tok_t = reinterpret_cast<volatile int*>(smem + L::kOffTokT);
   const WaitCtl ctl{abort_flag, p.status, p.limit_ns};
+  // Live blocks of the token in ring entry e (after its full barrier).
+  auto tok_blocks = [&](int e) -> int {
+    const int last = max(tok_last[2 * e], tok_last[2 * e + 1]);
+    return last < 0 ? 0 : last / L::kBI + 1;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < L::kStages; ++s) {
@@ -440,18 +474,24 @@ __global__ void __launch_bounds__(480, 1)
       mbar_init(bar(L::kBarSendOk + i), L::kGroupThreads / 32);
     }
     mbar_init(bar(L::kBarQdoFull), 1);
+    mbar_init(bar(L::kBarQdoFree), 1);
     mbar_init(bar(L::kBarDqDone), 1);
+    mbar_init(bar(L::kBarDqFree), 128);
+    for (int e = 0; e < L::kTokRing; ++e) {
+      mbar_init(bar(L::kBarTokFull + e), 2);  // one per gather warp
+      mbar_init(bar(L::kBarTokEmpty + e), L::kTokReaders);
+      mbar_init(bar(L::kBarIdFull + e), 1);
+      mbar_init(bar(L::kBarIdEmpty + e), 1);
+    }
     mbar_init(bar(L::kBarDrain), 1);
-    mbar_init(bar(L::kBarDqStaged), L::kPdsThreads);
     *abort_flag = *reinterpret_cast<volatile int*>(p.status) != 0 ? 1 : 0;
     *slot_smem = -1;
     if (NC == 2 && rank == 0 && *abort_flag == 0) {
       // Claim an exchange slot for the pair (bounded; released at exit).
-      const int c = static_cast<int>(blockIdx.x / NC);
       const uint64_t t0 = globaltimer_ns();
       int got = -1;
       for (uint32_t it = 0; got < 0; ++it) {
-        const int s = static_cast<int>((static_cast<uint32_t>(c) + it) % static_cast<uint32_t>(p.nslots));
+        const int s = static_cast<int>((static_cast<uint32_t>(cl) + it) % static_cast<uint32_t>(p.nslots));
         if (atomicCAS(p.slot_flags + s, 0, 1) == 0) {
           got = s;
         } else if ((it % static_cast<uint32_t>(p.nslots)) == static_cast<uint32_t>(p.nslots) - 1u &&
@@ -464,13 +504,6 @@ __global__ void __launch_bounds__(480, 1)
       *slot_smem = got;
     }
     fence_mbar_init();
-    // Q and dO slices, issued before the index scan so the loads overlap.
-    mbar_arrive_expect_tx(bar(L::kBarQdoFull), 2u * static_cast<uint32_t>(p.H) * 128u * L::kChunks);
-    for (int c = 0; c < L::kChunks; ++c) {
-      const int x = static_cast<int>(rank) * DC + c * 64;
-      tma_load_2d(base + L::kOffQ + c * L::kQChunkBytes, &tm_q, x, t * p.H, bar(L::kBarQdoFull));
-      tma_load_2d(base + L::kOffDo + c * L::kQChunkBytes, &tm_do, x, t * p.H, bar(L::kBarQdoFull));
-    }
   }
   if (warp == L::kMmaWarp) {
     if (lane == 0) {
@@ -479,6 +512,8 @@ __global__ void __launch_bounds__(480, 1)
     }
     tmem_alloc(base + L::kOffTmemHolder, L::kTmemCols);
   }
+  // Heads beyond H are zero rows of the Q / dO operands (the TMA box covers
+  // H rows, so later loads leave them zero).
   if (threadIdx.x < L::kHPad && static_cast<int>(threadIdx.x) >= p.H) {
     const uint32_t h = threadIdx.x;
 #pragma unroll
@@ -490,15 +525,11 @@ __global__ void __launch_bounds__(480, 1)
       }
     fence_proxy_async_smem();
   }
-  volatile int* warp_last = reinterpret_cast<volatile int*>(smem + L::kOffWarpLast);
-  scan_last_valid(p.idx + static_cast<size_t>(t) * p.topk, p.topk, p.S_kv, warp_last);
   tc_fence_before();
   __syncthreads();
   if (NC == 2) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  // Blocks up to the last one holding a valid slot (0: no valid slot).
-  const int nblk = live_blocks(warp_last, L::kBI);
   // The pair's exchange slot (claimed by rank 0); without one, nothing runs.
   int slot = -1;
   if (NC == 2) {
@@ -508,9 +539,11 @@ __global__ void __launch_bounds__(480, 1)
 
   if (warp >= L::kProducerWarp0 && warp < L::kMmaWarp) {
     // ------------------------------------------------------------ gather
-    // Warp pw copies slots [32 pw, 32 pw + 32) of each 64-slot block; one
-    // warp instruction moves kRpi whole rows of this CTA's D slice (32 lanes
-    // x 16 bytes, coalesced) into the 128-byte-swizzled tile with cp.async.
+    // Per token: the index row's last valid slot (each warp scans half the
+    // row) into ring entry k % kTokRing, then the token's live blocks.  Warp
+    // pw copies slots [32 pw, 32 pw + 32) of each 64-slot block; one warp
+    // instruction moves kRpi whole rows of this CTA's D slice (32 lanes x 16
+    // bytes, coalesced) into the 128-byte-swizzled tile with cp.async.
     const int pw = warp - L::kProducerWarp0;
     constexpr int kCpr = DC / 8;
     constexpr int kRpi = 32 / kCpr;
@@ -518,41 +551,131 @@ __global__ void __launch_bounds__(480, 1)
     const int cc = lane % kCpr;
     const uint32_t lane_off = static_cast<uint32_t>(cc / 8) * L::kKvChunkBytes;
     const uint32_t c16 = static_cast<uint32_t>(cc % 8);
-    const __nv_bfloat16* kv_col = p.kv + static_cast<size_t>(rank) * DC + cc * 8;
-    const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
-    auto load_idx = [&](int blk) -> int {
-      const int j = blk * L::kBI + 32 * pw + lane;
-      return j < p.topk ? __ldg(idx_row + j) : -1;
-    };
-    int r_next = load_idx(0);
-    for (int i = 0; i < nblk; ++i) {
-      const int s = i % L::kStages;
-      const int r = r_next;
-      if (i + 1 < nblk) r_next = load_idx(i + 1);
-      const bool v = static_cast<unsigned>(r) < static_cast<unsigned>(p.S_kv);
-      const int row = b * p.S_kv + (v ? r : 0);
-      if (i >= L::kStages) {
-        const bool ok = mbar_wait(bar(L::kBarKvEmpty + s), ((i / L::kStages) - 1) & 1, ctl);
-        if (!__all_sync(0xffffffffu, ok)) break;
-      } else if (*abort_flag) {
+    bool ok = *abort_flag == 0;
+    int G = 0;
+    for (int k = 0; ok; ++k) {
+      const int e = k % L::kTokRing;
+      if (k >= L::kTokRing) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarTokEmpty + e),
+                                               ((k / L::kTokRing) - 1) & 1, ctl));
+        if (!ok) break;
+      }
+      int t;
+      if (NC == 2 && p.tok_counter != nullptr) {
+        // The pair's k-th token: rank 0 takes it from the counter and writes
+        // it into both CTAs' entry e (the peer's only once the peer has
+        // freed it); both read it after IdFull.
+        if (pw == 0 && lane == 0) {
+          if (rank == 1 && k >= L::kTokRing) {
+            mbar_arrive_remote(mapa_shared(bar(L::kBarIdEmpty + e), 0u));
+          } else if (rank == 0) {
+            bool free_ok = true;
+            if (k >= L::kTokRing)
+              free_ok = mbar_wait<true>(bar(L::kBarIdEmpty + e), ((k / L::kTokRing) - 1) & 1, ctl);
+            if (free_ok) {
+              int nt = atomicAdd(p.tok_counter, 1);
+              if (nt >= p.tokens) nt = -1;
+              tok_id[e] = nt;
+              st_shared_cluster_s32(mapa_shared(base + L::kOffTokId + 4u * e, 1u), nt);
+              mbar_arrive_remote(mapa_shared(bar(L::kBarIdFull + e), 1u));
+              mbar_arrive(bar(L::kBarIdFull + e));
+            }
+          }
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarIdFull + e), (k / L::kTokRing) & 1, ctl));
+        if (!ok) break;
+        t = tok_id[e];
+      } else {
+        t = token_of(k) < p.tokens ? token_of(k) : -1;
+      }
+      if (t < 0) {
+        // No more tokens: publish the end.
+        if (lane == 0) {
+          if (pw == 0) tok_t[e] = -1;
+          tok_last[2 * e + pw] = -1;
+          mbar_arrive(bar(L::kBarTokFull + e));
+        }
         break;
       }
-      const uint32_t stage = base + L::kOffKv + s * L::kKvStageBytes + lane_off;
-#pragma unroll
-      for (int k = 0; k < 32 / kRpi; ++k) {
-        const int rw = k * kRpi + rsub;  // row within this warp's 32
-        const int rr = __shfl_sync(0xffffffffu, row, rw);
-        const uint32_t srow = static_cast<uint32_t>(32 * pw + rw);
-        cp_async_16(stage + srow * 128u + ((c16 ^ (srow & 7u)) << 4),
-                    kv_col + static_cast<size_t>(rr) * p.D);
+      const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
+      // 16-byte loads issued eight at a time before any compare, so one
+      // round of memory latency covers a 2048-slot row (the scalar scan it
+      // replaces, eight dependent rounds, held up the token's first gathers
+      // and cost 0.25 us per block).
+      int last = -1;
+      const int tid = 32 * pw + lane;
+      if ((p.topk & 3) == 0 && (reinterpret_cast<uintptr_t>(idx_row) & 15u) == 0) {
+        const int4* row4 = reinterpret_cast<const int4*>(idx_row);
+        const unsigned skv = static_cast<unsigned>(p.S_kv);
+#pragma unroll 8
+        for (int q = tid; q < p.topk / 4; q += 64) {
+          const int4 v = __ldg(row4 + q);
+          if (static_cast<unsigned>(v.x) < skv) last = 4 * q;
+          if (static_cast<unsigned>(v.y) < skv) last = 4 * q + 1;
+          if (static_cast<unsigned>(v.z) < skv) last = 4 * q + 2;
+          if (static_cast<unsigned>(v.w) < skv) last = 4 * q + 3;
+        }
+      } else {
+#pragma unroll 8
+        for (int j = tid; j < p.topk; j += 64)
+          if (static_cast<unsigned>(__ldg(idx_row + j)) < static_cast<unsigned>(p.S_kv)) last = j;
       }
-      // Arrives on the stage's full barrier once this thread's copies of the
-      // block have landed; the MMA thread fences them into the async proxy.
-      cp_async_arrive_noinc(bar(L::kBarKvFull + s));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, off));
+      if (lane == 0) {
+        if (pw == 0) tok_t[e] = t;
+        tok_last[2 * e + pw] = last;
+        mbar_arrive(bar(L::kBarTokFull + e));
+        // The token's Q / dO slices into L2: the MMA thread loads them once
+        // the previous token's gradients are done, right at the token
+        // boundary (12.54 -> 12.50 ms).
+        if (k > 0) {
+          for (int c = 2 * pw; c < 2 * pw + 2 && c < L::kChunks; ++c) {
+            tma_prefetch_l2_2d(&tm_q, static_cast<int>(rank) * DC + c * 64, t * p.H);
+            tma_prefetch_l2_2d(&tm_do, static_cast<int>(rank) * DC + c * 64, t * p.H);
+          }
+        }
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarTokFull + e), (k / L::kTokRing) & 1, ctl));
+      if (!ok) break;
+      const int nblk = tok_blocks(e);
+      const int b = t / p.S;
+      const __nv_bfloat16* kv_col =
+          p.kv + static_cast<size_t>(b) * p.S_kv * p.D + static_cast<size_t>(rank) * DC + cc * 8;
+      auto load_idx = [&](int blk) -> int {
+        const int j = blk * L::kBI + 32 * pw + lane;
+        return j < p.topk ? __ldg(idx_row + j) : -1;
+      };
+      int r_next = nblk > 0 ? load_idx(0) : -1;
+      for (int i = 0; i < nblk; ++i, ++G) {
+        const int s = G % L::kStages;
+        const int r = r_next;
+        if (i + 1 < nblk) r_next = load_idx(i + 1);
+        const int row = static_cast<unsigned>(r) < static_cast<unsigned>(p.S_kv) ? r : 0;
+        if (G >= L::kStages) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarKvEmpty + s), ((G / L::kStages) - 1) & 1, ctl));
+          if (!ok) break;
+        } else if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        const uint32_t stage = base + L::kOffKv + s * L::kKvStageBytes + lane_off;
+#pragma unroll
+        for (int kk = 0; kk < 32 / kRpi; ++kk) {
+          const int rw = kk * kRpi + rsub;  // row within this warp's 32
+          const int rr = __shfl_sync(0xffffffffu, row, rw);
+          const uint32_t srow = static_cast<uint32_t>(32 * pw + rw);
+          cp_async_16(stage + srow * 128u + ((c16 ^ (srow & 7u)) << 4),
+                      kv_col + static_cast<size_t>(rr) * p.D);
+        }
+        // Arrives on the stage's full barrier once this thread's copies of
+        // the block have landed; the MMA thread fences them into the async
+        // proxy.
+        cp_async_arrive_noinc(bar(L::kBarKvFull + s));
+      }
     }
     // Let every copy this warp started land before the CTA can exit.
     cp_async_wait_all();
-    if (warp == L::kProducerWarp0 && lane == 0) mbar_wait_drain(bar(L::kBarQdoFull), 0);
   } else if (warp == L::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -570,9 +693,9 @@ __global__ void __launch_bounds__(480, 1)
       const uint64_t d_dot = smem_desc(base + L::kOffDo, L::kQChunkBytes, 1024u, kSwizzle128B);
       const uint64_t d_dsmn = smem_desc(base + L::kOffDs, L::kPBytes, 1024u, kSwizzle128B);
       const uint64_t d_pmn = smem_desc(base + L::kOffP, L::kPBytes, 1024u, kSwizzle128B);
-      // S and dP of block i (M = 128 heads, N = 64 slots, K = this CTA's D slice).
-      auto issue_sdp = [&](int i) {
-        const int s = i % L::kStages;
+      // S and dP of block G (M = 128 heads, N = 64 slots, K = this CTA's D slice).
+      auto issue_sdp = [&](int G) {
+        const int s = G % L::kStages;
         const uint64_t dk = d_kv + ((static_cast<uint32_t>(s) * L::kKvStageBytes) >> 4);
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c) {
@@ -586,18 +709,19 @@ __global__ void __launch_bounds__(480, 1)
                    idesc_sdp, acc);
           }
         }
-        mma_commit(bar(L::kBarSdpFull + (i & 1)));
+        mma_commit(bar(L::kBarSdpFull + (G & 1)));
       };
-      // Gradients of block j: dQ += dS'.K (M = 128 heads, N = DC, K = 64
-      // slots); dKV^T[e] = Q^T[e].dS' + dO^T[e].P (M = 128 dims, N = 64
-      // slots, K = 128 heads).
-      auto issue_grad = [&](int j) {
-        const int sj = j % L::kStages;
+      // Gradients of block G (block i of its token): dQ += dS'.K (M = 128
+      // heads, N = DC, K = 64 slots; the token's first block overwrites);
+      // dKV^T[e] = Q^T[e].dS' + dO^T[e].P (M = 128 dims, N = 64 slots, K =
+      // 128 heads).
+      auto issue_grad = [&](int G, int i) {
+        const int sj = G % L::kStages;
         const uint64_t dkv = d_kvmn + ((static_cast<uint32_t>(sj) * L::kKvStageBytes) >> 4);
 #pragma unroll
         for (int k = 0; k < L::kBI / 16; ++k)
           mma_ss(tmem + L::kTmemDq, d_ds + (k * 32u >> 4), dkv + (k * 2048u >> 4), idesc_dq,
-                 (j > 0 || k > 0) ? 1u : 0u);
+                 (i > 0 || k > 0) ? 1u : 0u);
         // Only dQ reads the kv stage: the gather may refill it once these
         // MMAs are done, while the dKV^T MMAs still run.
         mma_commit(bar(L::kBarKvEmpty + sj));
@@ -613,38 +737,113 @@ __global__ void __launch_bounds__(480, 1)
             mma_ss(d_tm, d_dot + ((2 * e * L::kQChunkBytes + k * 2048u) >> 4),
                    d_pmn + (k * 2048u >> 4), idesc_dkv, 1u);
         }
-        mma_commit(bar(L::kBarPdsFree + (j & 1)));
+        mma_commit(bar(L::kBarPdsFree + (G & 1)));
         mma_commit(bar(L::kBarDkvFull));
       };
-      // Event loop (non-blocking tests): S / dP of block ns as soon as its kv
-      // rows have landed and the previous S / dP tile has been read (first,
-      // so the other P / dS group gets its tile early: 12.67 -> 12.55 ms);
-      // otherwise the gradients of block ng once its P / dS are written and
-      // the drain has read the previous dKV^T tile.
-      bool ok = mbar_wait(bar(L::kBarQdoFull), 0, ctl);
-      int ns = 0, ng = 0;
+      // Three cursors over the CTA's tokens: Q / dO loads (token lk; one per
+      // token with blocks, into the single buffer once the previous such
+      // token's MMAs have completed), S / dP (token sk, its block si,
+      // sequence index sG) and gradients (gk, gi, gG).  Each caches its
+      // token's live-block count (-1: not read yet) and touches the published
+      // counts only at token boundaries, so an iteration stays short.  Event
+      // loop (non-blocking tests): S / dP of the next block as soon as its kv
+      // rows have landed, the previous S / dP tile has been read and its
+      // token's Q / dO are in (first, so the other P / dS group gets its
+      // tile early: 12.67 -> 12.55 ms); otherwise the gradients of the oldest
+      // block once its P / dS are written and the drain has read the previous
+      // dKV^T tile (and, for a token's first block, the previous token's dQ
+      // has been read out); otherwise the next Q / dO load.
+      auto tok_known = [&](int k) -> bool {
+        return mbar_probe(bar(L::kBarTokFull + k % L::kTokRing), (k / L::kTokRing) & 1);
+      };
+      auto nblk_of = [&](int k) -> int { return tok_blocks(k % L::kTokRing); };
+      int lk = 0, lnb = -1, la = 0, lt = -1;        // load cursor (token lt), loads issued
+      bool l_end = false;                            // the load cursor met the end
+      int sk = 0, si = 0, snb = -1, sG = 0, sa = 0;  // sa: load index of token sk
+      int gk = 0, gi = 0, gnb = -1, gG = 0, ga = 0;  // ga: load index of token gk
+      int qfree = 0;                                 // Q / dO releases committed
+      bool ok = *abort_flag == 0;
       PollState ps = poll_start();
       uint32_t spins = 0;
-      while (ok && ng < nblk) {
-        if (ns < nblk &&
-            mbar_probe(bar(L::kBarKvFull + ns % L::kStages), (ns / L::kStages) & 1) &&
-            (ns == 0 ||
-             mbar_probe(bar(L::kBarSdpFree + ((ns - 1) & 1)), ((ns - 1) >> 1) & 1))) {
+      while (ok) {
+        // ---- cursor bookkeeping (does work only at token boundaries).  The
+        // next load's count is read only once the buffer is about to be free
+        // (its previous token's last gradients issued), so that an iteration
+        // in mid-token probes nothing but the events.
+        if (lnb < 0 && !l_end && qfree >= la && tok_known(lk)) {
+          lt = tok_t[lk % L::kTokRing];
+          if (lt < 0) {
+            l_end = true;
+          } else {
+            lnb = nblk_of(lk);
+            if (lnb == 0) {  // nothing to load: on to the next token
+              ++lk;
+              lnb = -1;
+              continue;
+            }
+          }
+        }
+        if (snb < 0 && sk < lk) snb = nblk_of(sk);  // published: the load cursor passed it
+        if (snb >= 0 && si == snb) {                  // token sk done (or without blocks)
+          if (snb > 0) ++sa;
+          ++sk;
+          si = 0;
+          snb = -1;
+          continue;
+        }
+        if (gnb < 0 && gk < lk) gnb = nblk_of(gk);
+        if (gnb >= 0 && gi == gnb && gk < sk) {       // token gk done: release its count
+          mbar_arrive(bar(L::kBarTokEmpty + gk % L::kTokRing));
+          if (gnb > 0) ++ga;
+          ++gk;
+          gi = 0;
+          gnb = -1;
+          continue;
+        }
+        if (l_end && gk == lk) break;  // every token done
+        // ---- events
+        if (si < snb &&
+            mbar_probe(bar(L::kBarKvFull + sG % L::kStages), (sG / L::kStages) & 1) &&
+            (sG == 0 || mbar_probe(bar(L::kBarSdpFree + ((sG - 1) & 1)), ((sG - 1) >> 1) & 1)) &&
+            (si > 0 || mbar_probe(bar(L::kBarQdoFull), sa & 1))) {
           // The kv tile was written by cp.async (generic proxy): order it
           // before the tensor core's (async proxy) reads.
           fence_proxy_async_smem();
           tc_fence_after();
-          issue_sdp(ns);
-          ++ns;
-          if (static_cast<int>(blockIdx.x) == p.stall_cta) {  // test hook only
+          issue_sdp(sG);
+          ++si;
+          ++sG;
+          if (static_cast<int>(blockIdx.x) == p.stall_cta && sG == 1) {  // test hook only
             ok = stall_until_limit(ctl);
             break;
           }
-        } else if (ng < ns && mbar_probe(bar(L::kBarPdsFull + (ng & 1)), (ng >> 1) & 1) &&
-                   (ng == 0 || mbar_probe(bar(L::kBarDkvFree), (ng - 1) & 1))) {
+        } else if (gG < sG && mbar_probe(bar(L::kBarPdsFull + (gG & 1)), (gG >> 1) & 1) &&
+                   (gG == 0 || mbar_probe(bar(L::kBarDkvFree), (gG - 1) & 1)) &&
+                   (gi > 0 || ga == 0 || mbar_probe(bar(L::kBarDqFree), (ga - 1) & 1))) {
           tc_fence_after();
-          issue_grad(ng);
-          ++ng;
+          issue_grad(gG, gi);
+          ++gi;
+          ++gG;
+          if (gi == gnb) {
+            // The token's last gradients: its dQ is complete once they are,
+            // and Q / dO may take the next token.
+            mma_commit(bar(L::kBarDqDone));
+            mma_commit(bar(L::kBarQdoFree));
+            ++qfree;
+          }
+        } else if (lnb > 0 && (la == 0 || mbar_probe(bar(L::kBarQdoFree), (la - 1) & 1))) {
+          // Q and dO slices of token lt into the (free) buffer.
+          const int t = lt;
+          mbar_arrive_expect_tx(bar(L::kBarQdoFull),
+                                2u * static_cast<uint32_t>(p.H) * 128u * L::kChunks);
+          for (int c = 0; c < L::kChunks; ++c) {
+            const int x = static_cast<int>(rank) * DC + c * 64;
+            tma_load_2d(base + L::kOffQ + c * L::kQChunkBytes, &tm_q, x, t * p.H, bar(L::kBarQdoFull));
+            tma_load_2d(base + L::kOffDo + c * L::kQChunkBytes, &tm_do, x, t * p.H, bar(L::kBarQdoFull));
+          }
+          ++la;
+          ++lk;
+          lnb = -1;
         } else {
           if ((++spins & 63u) == 0u && !poll_check(ctl, ps)) {
             ok = false;
@@ -654,28 +853,29 @@ __global__ void __launch_bounds__(480, 1)
         }
         ps.t0 = globaltimer_ns();  // progress: the limit counts from the last issue
       }
-      mma_commit(bar(L::kBarDqDone));
+      // No MMA may still be running when TMEM is released, and no Q / dO
+      // load still landing when the CTA exits.
       mma_commit(bar(L::kBarDrain));
       mbar_wait_drain(bar(L::kBarDrain), 0);
+      if (la > 0) mbar_wait_drain(bar(L::kBarQdoFull), (la - 1) & 1);
     }
     __syncwarp();
   } else if (warp >= L::kDrainWarp0) {
     // ------------------------------------------------------------ dKV drain
     // Thread = head-dim row of one lane quarter; per block 64 slots, read as
     // two 32-slot halves (both 128-row halves of the tile per TMEM trip).
+    // After each token's blocks the same warps read its dQ out of TMEM
+    // (thread = head row of the lane quarter) and store it, bf16.
     const int wq = warp - L::kDrainWarp0;  // TMEM lane quarter
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
     const bool active = (wq * 32) < DC;  // DC = 64: rows 64..127 are padding
     const size_t col0 = static_cast<size_t>(rank) * DC + wq * 32 + lane;
-    float* col = p.dkv_acc + col0;
-    unsigned long long* colx = p.dkv_fix + col0;
     // One contribution to element off of this lane's column: an fp32
     // reduction, or in the deterministic mode the value times 2^k (the
     // call's binary point) rounded to a 64-bit integer and added as an
     // integer, so the sum does not depend on the order of the additions.
     const float fix_scale = DET ? pow2f(__ldg(p.fix_shift)) : 0.f;
-    auto add = [&](size_t off, float v) {
+    auto add = [&](float* col, unsigned long long* colx, size_t off, float v) {
       if constexpr (DET) {
         const long long n = __float2ll_rn(v * fix_scale);
         asm volatile("red.global.add.u64 [%0], %1;" ::"l"(colx + off),
@@ -685,74 +885,129 @@ __global__ void __launch_bounds__(480, 1)
         red_add_f32(col + off, v);
       }
     };
-    // The index rows of the next block are loaded while this one is drained,
-    // so their L2 latency stays off the way to DkvFree (12.66 -> 12.36 ms).
-    auto load_r = [&](int blk, int half) -> int {
-      const int slot_j = blk * L::kBI + 32 * half + lane;
-      return (blk < nblk && slot_j < p.topk) ? __ldg(idx_row + slot_j) : -1;
-    };
-    int rn0 = load_r(0, 0), rn1 = load_r(0, 1);
-    for (int j = 0; j < nblk; ++j) {
-      const int rc[2] = {rn0, rn1};
-      rn0 = load_r(j + 1, 0);
-      rn1 = load_r(j + 1, 1);
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDkvFull), j & 1, ctl));
+    const int h = wq * 32 + lane;  // head row of the dQ read-out
+    bool ok = *abort_flag == 0;
+    int G = 0, a = 0;
+    for (int k = 0; ok; ++k) {
+      const int e = k % L::kTokRing;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarTokFull + e), (k / L::kTokRing) & 1, ctl));
       if (!ok) break;
-      tc_fence_after();
-      int row[2];
-      uint32_t vm[2];
+      const int t = tok_t[e];
+      if (t < 0) break;
+      const int nblk = tok_blocks(e);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::kBarTokEmpty + e));
+      const int b = t / p.S;
+      const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
+      float* col = p.dkv_acc + static_cast<size_t>(b) * p.S_kv * p.D + col0;
+      unsigned long long* colx =
+          DET ? p.dkv_fix + static_cast<size_t>(b) * p.S_kv * p.D + col0 : nullptr;
+      // The index rows of the next block are loaded while this one is
+      // drained, so their L2 latency stays off the way to DkvFree (12.66 ->
+      // 12.36 ms).
+      auto load_r = [&](int blk, int half) -> int {
+        const int slot_j = blk * L::kBI + 32 * half + lane;
+        return (blk < nblk && slot_j < p.topk) ? __ldg(idx_row + slot_j) : -1;
+      };
+      int rn0 = load_r(0, 0), rn1 = load_r(0, 1);
+      for (int j = 0; j < nblk; ++j, ++G) {
+        const int rc[2] = {rn0, rn1};
+        rn0 = load_r(j + 1, 0);
+        rn1 = load_r(j + 1, 1);
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDkvFull), G & 1, ctl));
+        if (!ok) break;
+        tc_fence_after();
+        int row[2];
+        uint32_t vm[2];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int r = rc[half];
-        const bool v = static_cast<unsigned>(r) < static_cast<unsigned>(p.S_kv);
-        vm[half] = __ballot_sync(0xffffffffu, v);
-        row[half] = b * p.S_kv + (v ? r : 0);
-      }
-      const uint32_t t0 = tmem + lane_base + L::kTmemDkv;
-      if constexpr (L::kNE == 2) {
-#pragma unroll 1
         for (int half = 0; half < 2; ++half) {
-          float x[2][32];
-          tmem_ld32x2(t0 + 32 * half, t0 + L::kBI + 32 * half, x[0], x[1]);
-          if (half == 1) {  // the whole tile is in registers: let the MMAs reuse it
-            tc_fence_before();
-            mbar_arrive(bar(L::kBarDkvFree));
-          }
-          if (active) {
+          const int r = rc[half];
+          const bool v = static_cast<unsigned>(r) < static_cast<unsigned>(p.S_kv);
+          vm[half] = __ballot_sync(0xffffffffu, v);
+          row[half] = v ? r : 0;
+        }
+        const uint32_t t0 = tmem + lane_base + L::kTmemDkv;
+        if constexpr (L::kNE == 2) {
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            float x[2][32];
+            tmem_ld32x2(t0 + 32 * half, t0 + L::kBI + 32 * half, x[0], x[1]);
+            if (half == 1) {  // the whole tile is in registers: let the MMAs reuse it
+              tc_fence_before();
+              mbar_arrive(bar(L::kBarDkvFree));
+            }
+            if (active) {
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              const int rk = __shfl_sync(0xffffffffu, row[half], k);
-              if ((vm[half] >> k) & 1u) {
-                add(static_cast<size_t>(rk) * p.D, x[0][k]);
-                add(static_cast<size_t>(rk) * p.D + 128, x[1][k]);
+              for (int kk = 0; kk < 32; ++kk) {
+                const int rk = __shfl_sync(0xffffffffu, row[half], kk);
+                if ((vm[half] >> kk) & 1u) {
+                  add(col, colx, static_cast<size_t>(rk) * p.D, x[0][kk]);
+                  add(col, colx, static_cast<size_t>(rk) * p.D + 128, x[1][kk]);
+                }
               }
             }
           }
+        } else {
+          float x[2][32];
+          tmem_ld32x2(t0, t0 + 32, x[0], x[1]);
+          tc_fence_before();
+          mbar_arrive(bar(L::kBarDkvFree));
+          if (active) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+#pragma unroll
+              for (int kk = 0; kk < 32; ++kk) {
+                const int rk = __shfl_sync(0xffffffffu, row[half], kk);
+                if ((vm[half] >> kk) & 1u) add(col, colx, static_cast<size_t>(rk) * p.D, x[half][kk]);
+              }
+          }
         }
-      } else {
-        float x[2][32];
-        tmem_ld32x2(t0, t0 + 32, x[0], x[1]);
+      }
+      if (!ok) break;
+      // dQ of the token, bf16, straight from TMEM to its rows (16-byte
+      // stores; 32 columns per TMEM load -- 64 at a time cost 0.8 %, through
+      // the drain loop's registers); a token without a valid slot gets zeros.
+      if (nblk > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDqDone), a & 1, ctl));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      uint4* dst = reinterpret_cast<uint4*>(p.dq + (static_cast<size_t>(t) * p.H + h) * p.D +
+                                            static_cast<size_t>(rank) * DC);
+#pragma unroll 1
+      for (int c = 0; c < DC / 32; ++c) {
+        float v[32];
+        if (nblk > 0) {
+          tmem_ld32(tmem + lane_base + L::kTmemDq + c * 32, v);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 32; ++kk) v[kk] = 0.f;
+        }
+        if (h < p.H) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            dst[4 * c + kk] = make_uint4(pack_bf16x2(v[8 * kk], v[8 * kk + 1]),
+                                         pack_bf16x2(v[8 * kk + 2], v[8 * kk + 3]),
+                                         pack_bf16x2(v[8 * kk + 4], v[8 * kk + 5]),
+                                         pack_bf16x2(v[8 * kk + 6], v[8 * kk + 7]));
+        }
+      }
+      if (nblk > 0) {
+        // dQ is in registers: the next token's first dQ MMA may overwrite it.
         tc_fence_before();
-        mbar_arrive(bar(L::kBarDkvFree));
-        if (active) {
-#pragma unroll
-          for (int half = 0; half < 2; ++half)
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              const int rk = __shfl_sync(0xffffffffu, row[half], k);
-              if ((vm[half] >> k) & 1u) add(static_cast<size_t>(rk) * p.D, x[half][k]);
-            }
-        }
+        mbar_arrive(bar(L::kBarDqFree));
+        ++a;
       }
     }
   } else {
     // ------------------------------------------------------------ P / dS
     // Two groups of four warps alternate blocks (group g takes the blocks of
-    // parity g), so one block's latency chain -- read the S / dP tile, round
-    // and send this CTA's partials, wait for the peer's, decode, write P and
-    // dS' -- overlaps the next block's.  Thread = head row h, all 64 slots
-    // of the block: the full S and dP of the row (for D = 512 this CTA's
-    // partial plus the peer's, both in block floating point), then
+    // parity g in the CTA's sequence), so one block's latency chain -- read
+    // the S / dP tile, round and send this CTA's partials, wait for the
+    // peer's, decode, write P and dS' -- overlaps the next block's.  Thread
+    // = head row h, all 64 slots of the block: the full S and dP of the row
+    // (for D = 512 this CTA's partial plus the peer's, both in block
+    // floating point), then
     //   P = 2^(S - lse2),  dS' = P (sm_scale dP - sm_scale Delta),
     // written bf16 for the gradient MMAs, 8 slots at a time.  The single
     // P / dS buffer is written only once the gradients of the previous block
@@ -762,9 +1017,6 @@ __global__ void __launch_bounds__(480, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + lane_base + L::kTmemS;
     const uint32_t t_dp = tmem + lane_base + L::kTmemDp;
-    const float lse2 = h < p.H ? __ldg(p.lse + static_cast<size_t>(t) * p.H + h) : INFINITY;
-    const float dlt_s =
-        h < p.H ? __ldg(p.delta + static_cast<size_t>(t) * p.H + h) * p.scale : 0.f;
     const uint32_t peer_full = NC == 2 ? mapa_shared(bar(L::kBarRecvFull + grp), rank ^ 1u) : 0u;
     const uint32_t peer_sendok = NC == 2 ? mapa_shared(bar(L::kBarSendOk + grp), rank ^ 1u) : 0u;
     // This group's receive buffer, and the peer's (which this group fills).
@@ -777,11 +1029,7 @@ __global__ void __launch_bounds__(480, 1)
                                   grp * L::kXchgBytes
                             : nullptr;
     const uint32_t row128 = static_cast<uint32_t>(h) * 128u;
-    const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
-    auto load_idx = [&](int blk, int half) -> int {
-      const int j = blk * L::kBI + 32 * half + lane;
-      return (blk < nblk && j < p.topk) ? __ldg(idx_row + j) : -1;
-    };
+    float lse2 = INFINITY, dlt_s = 0.f;
     // P and dS' of slots 8 ch .. 8 ch + 7 (ch = 0..7) from their scores zs
     // and scaled dP zp (slot validity: bit (8 ch + k) % 32 of msk).
     auto emit = [&](int ch, uint32_t msk, const float* zs, const float* zp) {
@@ -801,169 +1049,146 @@ __global__ void __launch_bounds__(480, 1)
       st_shared_v4(base + L::kOffP + off, pp[0], pp[1], pp[2], pp[3]);
       st_shared_v4(base + L::kOffDs + off, pd[0], pd[1], pd[2], pd[3]);
     };
-    int r0 = load_idx(grp, 0), r1 = load_idx(grp, 1);
     bool ok = *abort_flag == 0;
-    for (int i = grp; ok && i < nblk; i += 2) {
-      const int n = i >> 1;  // this group's block count
-      // Valid-slot masks of the block's two 32-slot halves (prefetched).
-      const uint32_t m0 = __ballot_sync(0xffffffffu, static_cast<unsigned>(r0) < static_cast<unsigned>(p.S_kv));
-      const uint32_t m1 = __ballot_sync(0xffffffffu, static_cast<unsigned>(r1) < static_cast<unsigned>(p.S_kv));
-      r0 = load_idx(i + 2, 0);
-      r1 = load_idx(i + 2, 1);
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSdpFull + grp), n & 1, ctl));
+    int G0 = 0;  // sequence index of the token's first block
+    for (int k = 0; ok; ++k) {
+      const int te = k % L::kTokRing;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarTokFull + te), (k / L::kTokRing) & 1, ctl));
       if (!ok) break;
-      tc_fence_after();
-      if constexpr (NC == 2) {
-        uint32_t hs[2][16], hp[2][16], own_exps[2];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-          own_exps[hh] = own_partials_bfp(t_s + 32 * hh, t_dp + 32 * hh, p.scale_log2, p.scale,
-                                          hs[hh], hp[hh]);
-        tc_fence_before();
-        mbar_arrive(bar(L::kBarSdpFree + grp));
-        // Send: the peer has consumed this group's previous block from the
-        // buffer.
-        if (n >= 1) {
-          ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarSendOk + grp), (n - 1) & 1, ctl));
-          if (!ok) break;
-        }
-        {
-          uint4* dst = reinterpret_cast<uint4*>(send) + h;
+      const int t = tok_t[te];
+      if (t < 0) break;
+      const int nblk = tok_blocks(te);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::kBarTokEmpty + te));
+      int i = ((G0 & 1) == grp) ? 0 : 1;  // this group's first block of the token
+      if (i < nblk) {
+        lse2 = h < p.H ? __ldg(p.lse + static_cast<size_t>(t) * p.H + h) : INFINITY;
+        dlt_s = h < p.H ? __ldg(p.delta + static_cast<size_t>(t) * p.H + h) * p.scale : 0.f;
+      }
+      const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
+      auto load_idx = [&](int blk, int half) -> int {
+        const int j = blk * L::kBI + 32 * half + lane;
+        return (blk < nblk && j < p.topk) ? __ldg(idx_row + j) : -1;
+      };
+      int r0 = load_idx(i, 0), r1 = load_idx(i, 1);
+      for (; ok && i < nblk; i += 2) {
+        const int G = G0 + i;
+        const int n = G >> 1;  // this group's block count
+        // Valid-slot masks of the block's two 32-slot halves (prefetched).
+        const uint32_t m0 = __ballot_sync(0xffffffffu, static_cast<unsigned>(r0) < static_cast<unsigned>(p.S_kv));
+        const uint32_t m1 = __ballot_sync(0xffffffffu, static_cast<unsigned>(r1) < static_cast<unsigned>(p.S_kv));
+        r0 = load_idx(i + 2, 0);
+        r1 = load_idx(i + 2, 1);
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSdpFull + grp), n & 1, ctl));
+        if (!ok) break;
+        tc_fence_after();
+        if constexpr (NC == 2) {
+          uint32_t hs[2][16], hp[2][16], own_exps[2];
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh)
+            own_exps[hh] = own_partials_bfp(t_s + 32 * hh, t_dp + 32 * hh, p.scale_log2, p.scale,
+                                            hs[hh], hp[hh]);
+          tc_fence_before();
+          mbar_arrive(bar(L::kBarSdpFree + grp));
+          // Send: the peer has consumed this group's previous block from the
+          // buffer.
+          if (n >= 1) {
+            ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarSendOk + grp), (n - 1) & 1, ctl));
+            if (!ok) break;
+          }
+          {
+            uint4* dst = reinterpret_cast<uint4*>(send) + h;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                dst[(4 * hh + c) * L::kHPad] = make_uint4(hs[hh][4 * c], hs[hh][4 * c + 1],
+                                                          hs[hh][4 * c + 2], hs[hh][4 * c + 3]);
+                dst[(8 + 4 * hh + c) * L::kHPad] = make_uint4(hp[hh][4 * c], hp[hh][4 * c + 1],
+                                                              hp[hh][4 * c + 2], hp[hh][4 * c + 3]);
+              }
+            uint32_t* ex = reinterpret_cast<uint32_t*>(send + L::kXchgScaleOff);
+            ex[h] = own_exps[0];
+            ex[L::kHPad + h] = own_exps[1];
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(peer_full);
+          }
+          // The P / dS buffer was last read by the gradient MMAs of block G-1.
+          if (G >= 1) {
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(bar(L::kBarPdsFree + ((G - 1) & 1)), ((G - 1) >> 1) & 1, ctl));
+            if (!ok) break;
+          }
+          ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull + grp), n & 1, ctl));
+          if (!ok) break;
+          const uint4* src = reinterpret_cast<const uint4*>(recv) + h;
+          const unsigned int* pex = reinterpret_cast<const unsigned int*>(recv + L::kXchgScaleOff);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint32_t peer_exps = __ldcg(pex + hh * L::kHPad + h);
+            const float us = bfp16_unit<false>(own_exps[hh]), up = bfp16_unit<true>(own_exps[hh]);
+            const float vs = bfp16_unit<false>(peer_exps), vp = bfp16_unit<true>(peer_exps);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-              dst[(4 * hh + c) * L::kHPad] = make_uint4(hs[hh][4 * c], hs[hh][4 * c + 1],
-                                                        hs[hh][4 * c + 2], hs[hh][4 * c + 3]);
-              dst[(8 + 4 * hh + c) * L::kHPad] = make_uint4(hp[hh][4 * c], hp[hh][4 * c + 1],
-                                                            hp[hh][4 * c + 2], hp[hh][4 * c + 3]);
+              const uint4 ys = __ldcg(src + (4 * hh + c) * L::kHPad);
+              const uint4 yp = __ldcg(src + (8 + 4 * hh + c) * L::kHPad);
+              const uint32_t ysa[4] = {ys.x, ys.y, ys.z, ys.w};
+              const uint32_t ypa[4] = {yp.x, yp.y, yp.z, yp.w};
+              float zs[8], zp[8];
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                // Both decodings are exact; the sum is one rounding and
+                // commutes, so the two CTAs get the same full S and dP.
+                const float2 a =
+                    add2(bfp16_unpack(hs[hh][4 * c + kk], us), bfp16_unpack(ysa[kk], vs));
+                const float2 d =
+                    add2(bfp16_unpack(hp[hh][4 * c + kk], up), bfp16_unpack(ypa[kk], vp));
+                zs[2 * kk] = a.x;
+                zs[2 * kk + 1] = a.y;
+                zp[2 * kk] = d.x;
+                zp[2 * kk + 1] = d.y;
+              }
+              emit(4 * hh + c, hh == 0 ? m0 : m1, zs, zp);
             }
-          uint32_t* ex = reinterpret_cast<uint32_t*>(send + L::kXchgScaleOff);
-          ex[h] = own_exps[0];
-          ex[L::kHPad + h] = own_exps[1];
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(bar(L::kBarPdsFull + grp));
+          // The exchange buffer may take the peer's next block of this
+          // parity (a cluster-scope release: signalled after P / dS so the
+          // gradients need not wait; the last one is never waited for).
           __syncwarp();
-          if (lane == 0) mbar_arrive_remote(peer_full);
-        }
-        // The P / dS buffer was last read by the gradient MMAs of block i-1.
-        if (i >= 1) {
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(bar(L::kBarPdsFree + ((i - 1) & 1)), ((i - 1) >> 1) & 1, ctl));
-          if (!ok) break;
-        }
-        ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull + grp), n & 1, ctl));
-        if (!ok) break;
-        const uint4* src = reinterpret_cast<const uint4*>(recv) + h;
-        const unsigned int* pex = reinterpret_cast<const unsigned int*>(recv + L::kXchgScaleOff);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const uint32_t peer_exps = __ldcg(pex + hh * L::kHPad + h);
-          const float us = bfp16_unit<false>(own_exps[hh]), up = bfp16_unit<true>(own_exps[hh]);
-          const float vs = bfp16_unit<false>(peer_exps), vp = bfp16_unit<true>(peer_exps);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint4 ys = __ldcg(src + (4 * hh + c) * L::kHPad);
-            const uint4 yp = __ldcg(src + (8 + 4 * hh + c) * L::kHPad);
-            const uint32_t ysa[4] = {ys.x, ys.y, ys.z, ys.w};
-            const uint32_t ypa[4] = {yp.x, yp.y, yp.z, yp.w};
-            float zs[8], zp[8];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              // Both decodings are exact; the sum is one rounding and
-              // commutes, so the two CTAs get the same full S and dP.
-              const float2 a =
-                  add2(bfp16_unpack(hs[hh][4 * c + k], us), bfp16_unpack(ysa[k], vs));
-              const float2 d =
-                  add2(bfp16_unpack(hp[hh][4 * c + k], up), bfp16_unpack(ypa[k], vp));
-              zs[2 * k] = a.x;
-              zs[2 * k + 1] = a.y;
-              zp[2 * k] = d.x;
-              zp[2 * k + 1] = d.y;
-            }
-            emit(4 * hh + c, hh == 0 ? m0 : m1, zs, zp);
+          if (lane == 0) mbar_arrive_remote(peer_sendok);
+        } else {
+          // One CTA per token: the tile holds the full S and dP.  It is read
+          // half by half right before the half is written, so it stays busy
+          // until the P / dS buffer is free.
+          if (G >= 1) {
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(bar(L::kBarPdsFree + ((G - 1) & 1)), ((G - 1) >> 1) & 1, ctl));
+            if (!ok) break;
           }
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(bar(L::kBarPdsFull + grp));
-        // The exchange buffer may take the peer's next block of this parity
-        // (a cluster-scope release: signalled after P / dS so the gradients
-        // need not wait).
-        __syncwarp();
-        if (lane == 0 && i + 2 < nblk) mbar_arrive_remote(peer_sendok);
-      } else {
-        // One CTA per token: the tile holds the full S and dP.  It is read
-        // half by half right before the half is written, so it stays busy
-        // until the P / dS buffer is free.
-        if (i >= 1) {
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(bar(L::kBarPdsFree + ((i - 1) & 1)), ((i - 1) >> 1) & 1, ctl));
-          if (!ok) break;
-        }
 #pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          float xs[32], xp[32];
-          tmem_ld32x2(t_s + 32 * hh, t_dp + 32 * hh, xs, xp);
+          for (int hh = 0; hh < 2; ++hh) {
+            float xs[32], xp[32];
+            tmem_ld32x2(t_s + 32 * hh, t_dp + 32 * hh, xs, xp);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float zs[8], zp[8];
+            for (int c = 0; c < 4; ++c) {
+              float zs[8], zp[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              zs[k] = xs[8 * c + k] * p.scale_log2;
-              zp[k] = xp[8 * c + k] * p.scale;
+              for (int kk = 0; kk < 8; ++kk) {
+                zs[kk] = xs[8 * c + kk] * p.scale_log2;
+                zp[kk] = xp[8 * c + kk] * p.scale;
+              }
+              emit(4 * hh + c, hh == 0 ? m0 : m1, zs, zp);
             }
-            emit(4 * hh + c, hh == 0 ? m0 : m1, zs, zp);
           }
-        }
-        tc_fence_before();
-        mbar_arrive(bar(L::kBarSdpFree + grp));
-        fence_proxy_async_smem();
-        mbar_arrive(bar(L::kBarPdsFull + grp));
-      }
-    }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDqDone), 0, ctl));
-    if (ok) {
-      tc_fence_after();
-      // dQ into shared memory as 64-column tiles in the 128-byte-swizzled
-      // layout of dq's tensor map (the kv ring is free: every MMA has
-      // completed); the TMA then writes whole rows.  Group g stages the
-      // tiles cc = g, g + 2, ...
-#pragma unroll 1
-      for (int cc = grp; cc < DC / 64; cc += 2) {
-        float v[2][32];
-        if (nblk > 0) {
-          tmem_ld32x2(tmem + lane_base + L::kTmemDq + cc * 64,
-                      tmem + lane_base + L::kTmemDq + cc * 64 + 32, v[0], v[1]);
-        } else {  // no valid slot: dQ was never written, the gradient is 0
-#pragma unroll
-          for (int k = 0; k < 32; ++k) v[0][k] = v[1][k] = 0.f;
-        }
-        const uint32_t row = base + L::kOffKv + static_cast<uint32_t>(cc) * L::kQChunkBytes +
-                             static_cast<uint32_t>(h) * 128u;
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          uint32_t w[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(v[u][2 * k], v[u][2 * k + 1]);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t piece = static_cast<uint32_t>(4 * u + k);
-            st_shared_v4(row + ((piece ^ (static_cast<uint32_t>(h) & 7u)) << 4), w[4 * k],
-                         w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-          }
+          tc_fence_before();
+          mbar_arrive(bar(L::kBarSdpFree + grp));
+          fence_proxy_async_smem();
+          mbar_arrive(bar(L::kBarPdsFull + grp));
         }
       }
-    }
-    // Every P / dS thread arrives (also after a failed wait, so that the
-    // storing thread never waits in vain); one thread ships the tiles.
-    fence_proxy_async_smem();
-    mbar_arrive(bar(L::kBarDqStaged));
-    if (threadIdx.x == 0) {
-      if (mbar_wait(bar(L::kBarDqStaged), 0, ctl) && *abort_flag == 0) {
-        for (int cc = 0; cc < DC / 64; ++cc)
-          tma_store_2d(&tm_dq, base + L::kOffKv + static_cast<uint32_t>(cc) * L::kQChunkBytes,
-                       static_cast<int>(rank) * DC + cc * 64, t * p.H);
-        bulk_commit_group();
-        bulk_wait_group0();  // complete before the CTA (and its shared memory) goes away
-      }
+      G0 += nblk;
     }
   }
 
@@ -981,17 +1206,43 @@ __global__ void __launch_bounds__(480, 1)
   }
 }
 
+// Clusters (pairs, or single CTAs for D = 64) of one instantiation that fit
+// on the device at once, per device (the persistent grid's size).
+template <int DC, int NC, bool DET>
+static int bwd_resident_clusters(cudaLaunchConfig_t cfg) {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] > 0) return cached[dev];
+  int n = 0;
+  auto kern = smqa_bwd_kernel<DC, NC, DET>;
+  if (NC > 1) {
+    cfg.gridDim = dim3(NC, 1, 1);
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  } else {
+    int per_sm = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, static_cast<int>(cfg.blockDim.x),
+                                                      cfg.dynamicSmemBytes) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      n = per_sm * sms;
+  }
+  if (n <= 0) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  cached[dev] = n;
+  return n;
+}
+
 template <int DC, int NC, bool DET>
 static cudaError_t launch_bwd_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_do,
-                                   const CUtensorMap& tm_dq, const BwdParams& p, int tokens,
-                                   cudaStream_t stream) {
+                                   const BwdParams& p0, int tokens, cudaStream_t stream) {
   using L = BwdLayout<DC, NC>;
   auto kern = smqa_bwd_kernel<DC, NC, DET>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(tokens) * NC, 1, 1);
   cfg.blockDim = dim3(L::kThreads, 1, 1);
   cfg.dynamicSmemBytes = L::kSmemBytes;
   cfg.stream = stream;
@@ -1002,20 +1253,25 @@ static cudaError_t launch_bwd_impl(const CUtensorMap& tm_q, const CUtensorMap& t
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tm_q, tm_do, tm_dq, p);
+  const int resident = bwd_resident_clusters<DC, NC, DET>(cfg);
+  if (resident <= 0) return cudaErrorInvalidConfiguration;
+  BwdParams p = p0;
+  p.tokens = tokens;
+  p.clusters = tokens < resident ? tokens : resident;
+  cfg.gridDim = dim3(static_cast<unsigned>(p.clusters) * NC, 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, tm_q, tm_do, p);
 }
 
 cudaError_t launch_bwd_main(const CUtensorMap& tm_q, const CUtensorMap& tm_do,
-                            const CUtensorMap& tm_dq, const BwdParams& p, int tokens,
-                            cudaStream_t stream) {
+                            const BwdParams& p, int tokens, cudaStream_t stream) {
   // The deterministic mode is a separate instantiation, so the default
   // kernel's reduction loop carries no branch for it.
   if (p.D == 512)
-    return p.det ? launch_bwd_impl<256, 2, true>(tm_q, tm_do, tm_dq, p, tokens, stream)
-                 : launch_bwd_impl<256, 2, false>(tm_q, tm_do, tm_dq, p, tokens, stream);
+    return p.det ? launch_bwd_impl<256, 2, true>(tm_q, tm_do, p, tokens, stream)
+                 : launch_bwd_impl<256, 2, false>(tm_q, tm_do, p, tokens, stream);
   if (p.D == 64)
-    return p.det ? launch_bwd_impl<64, 1, true>(tm_q, tm_do, tm_dq, p, tokens, stream)
-                 : launch_bwd_impl<64, 1, false>(tm_q, tm_do, tm_dq, p, tokens, stream);
+    return p.det ? launch_bwd_impl<64, 1, true>(tm_q, tm_do, p, tokens, stream)
+                 : launch_bwd_impl<64, 1, false>(tm_q, tm_do, p, tokens, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -25,6 +25,12 @@ struct FwdParams {
   int* status;           // device status word
   uint64_t limit_ns;     // bounded-wait limit
   int stall_cta;         // test hook: this CTA stalls after its first MMA (-1: none)
+  // Persistent grid: `clusters` CTAs (pairs for D = 512) over `tokens`
+  // tokens (set at launch).  With tok_counter (zero before the launch) a
+  // pair takes its next token from it; without, cluster c takes tokens
+  // c, c + clusters, ...
+  int tokens, clusters;
+  int* tok_counter;
   // D split across a CTA pair: the pairs trade their partial scores through
   // an L2-resident pool of nslots slots (kFwdSlotBytes each); slot_flags[s]
   // is 1 while a pair holds slot s (all zero before the launch).
@@ -52,6 +58,12 @@ struct BwdParams {
   int* status;
   uint64_t limit_ns;
   int stall_cta;         // test hook: this CTA stalls after its first MMA (-1: none)
+  // Persistent grid: `clusters` CTAs (pairs for D = 512) over `tokens`
+  // tokens (set at launch).  With tok_counter (zero before the launch) a
+  // pair takes its next token from it; without, cluster c takes tokens
+  // c, c + clusters, ...
+  int tokens, clusters;
+  int* tok_counter;
   // D split across a CTA pair: the pairs trade their partial S / dP through
   // an L2-resident pool of nslots slots (kBwdSlotBytes each); slot_flags[s]
   // is 1 while a pair holds slot s (all zero before the launch).
@@ -119,7 +131,7 @@ void set_last_error(const char* msg);
 cudaError_t launch_fwd(const CUtensorMap& tm_q, const CUtensorMap& tm_o, const FwdParams& p,
                        int tokens, cudaStream_t stream);
 cudaError_t launch_bwd_main(const CUtensorMap& tm_q, const CUtensorMap& tm_do,
-                            const CUtensorMap& tm_dq, const BwdParams& p, int tokens,
+                            const BwdParams& p, int tokens,
                             cudaStream_t stream);
 cudaError_t launch_indexer_bwd(const CUtensorMap& tm_q, const CUtensorMap& tm_dq,
                                const IdxParams& p, cudaStream_t stream);
