@@ -261,14 +261,14 @@ smqa_status smqa_fwd(const void* q, const void* kv, const float* attn_sink,
   cudaError_t e;
   int* st = status_ptr(&e);
   if (!st) return cuda_fail(e, "status word");
-  CUtensorMap tq, to;
+  CUtensorMap tq;
   const uint64_t T = static_cast<uint64_t>(shape.B) * shape.S;
-  if (!encode_bf16_2d(&tq, q, shape.D, T * shape.H, 64, static_cast<uint32_t>(shape.H)) ||
-      !encode_bf16_2d(&to, o, shape.D, T * shape.H, 64, static_cast<uint32_t>(shape.H)))
+  if (!encode_bf16_2d(&tq, q, shape.D, T * shape.H, 64, static_cast<uint32_t>(shape.H)))
     return SMQA_ERR_CUDA;
   if (need != 0) {
-    // Every slot free at launch (the kernel's pairs claim and release them).
-    e = cudaMemsetAsync(workspace, 0, kExchSlots * sizeof(int), stream);
+    // Every slot free at launch (the kernel's pairs claim and release them),
+    // and the token counter the pairs take their tokens from at zero.
+    e = cudaMemsetAsync(workspace, 0, (kExchSlots + 1) * sizeof(int), stream);
     if (e != cudaSuccess) return cuda_fail(e, "exchange flags clear");
   }
   const float scale = effective_scale(sm_scale, shape.D);
@@ -294,8 +294,9 @@ smqa_status smqa_fwd(const void* q, const void* kv, const float* attn_sink,
     p.slot_flags = static_cast<int*>(workspace);
     p.exch = static_cast<uint8_t*>(workspace) + kExchFlagBytes;
     p.nslots = kExchSlots;
+    p.tok_counter = static_cast<int*>(workspace) + kExchSlots;
   }
-  e = smqa::launch_fwd(tq, to, p, static_cast<int>(T), stream);
+  e = smqa::launch_fwd(tq, p, static_cast<int>(T), stream);
   if (e != cudaSuccess) return cuda_fail(e, "fwd launch");
   return SMQA_OK;
 }

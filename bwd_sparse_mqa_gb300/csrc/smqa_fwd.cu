@@ -34,7 +34,12 @@
 //     goes into the buffer of block j only after its own CTA has received
 //     block j + 3 (six buffers rather than the four this needs at least, so
 //     that a sender waits for the peer's block i - 3 rather than i - 1).
-//   * D = 64: one CTA per token, no exchange.
+//   * Persistent CTAs (pairs): each takes tokens one after another from a
+//     counter (rank 0 hands each to its peer), so the next token's gathers,
+//     scores, exchange and softmax run while the current one's last P.V and
+//     O read-out finish; O goes from TMEM straight to global memory with
+//     32-byte stores.
+//   * D = 64: one CTA per token (static order), no exchange.
 //   * Warp roles (D = 512; for D = 64 the combiner and sender warps are
 //     absent): warps 8-10 gather this CTA's half of the kv rows with
 //     16-byte cp.async (coalesced 512-byte row pieces written into the
@@ -78,11 +83,9 @@ struct FwdLayout {
   static constexpr uint32_t kQBytes = kChunks * kQChunkBytes;
   static constexpr uint32_t kKvChunkBytes = kBI * 128;   // kBI rows x 128 B
   static constexpr uint32_t kStageBytes = kChunks * kKvChunkBytes;
+  static constexpr int kTokRing = 4;          // tokens published ahead
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffKv = kOffQ + kQBytes;
-  // The epilogue stages O in the (then idle) kv ring: 64-column tiles of
-  // 128 rows x 128 bytes.
-  static constexpr uint32_t kOTileBytes = kHPad * 128;
   // Exchange buffer of one receiver and block: each head's 64 partial scores
   // as int16 with one power-of-two scale (block floating point), in 8 pieces
   // of 16 bytes per head, piece-major (a warp's 32 heads are 512 contiguous
@@ -100,20 +103,29 @@ struct FwdLayout {
   static constexpr int kBarRecvFull = kBarSFree + kSBufs;    // [kXBufs] peer's partial arrived
   static constexpr int kBarPFull = kBarRecvFull + kXBufs;    // [2] P of block i in buffer i % 2
   static constexpr int kBarODone = kBarPFull + 2;            // [2] P.V of block i done
-  static constexpr int kBarQFull = kBarODone + 2;
-  static constexpr int kBarDrain = kBarQFull + 1;
-  static constexpr int kBarOStaged = kBarDrain + 1;          // O tile in shared memory
-  static constexpr int kNumBars = kBarOStaged + 1;
+  static constexpr int kBarQFull = kBarODone + 2;            // one phase per token with blocks
+  static constexpr int kBarQFree = kBarQFull + 1;            // its scores MMAs are done with Q
+  static constexpr int kBarOFree = kBarQFree + 1;            // its O has been read out
+  static constexpr int kBarTokFull = kBarOFree + 1;          // [kTokRing] token published
+  static constexpr int kBarTokEmpty = kBarTokFull + kTokRing;  // [kTokRing] ... and read
+  // The pair's token sequence: rank 0 takes each token from the counter and
+  // hands it to both CTAs (IdFull); rank 1 frees an entry again (IdEmpty, on
+  // rank 0) once its readers are done with it.
+  static constexpr int kBarIdFull = kBarTokEmpty + kTokRing;   // [kTokRing]
+  static constexpr int kBarIdEmpty = kBarIdFull + kTokRing;    // [kTokRing]
+  static constexpr int kBarDrain = kBarIdEmpty + kTokRing;
+  static constexpr int kNumBars = kBarDrain + 1;
   static constexpr uint32_t kOffTmemHolder = kOffCtrl + 8 * kNumBars;
   static constexpr uint32_t kOffAbort = kOffTmemHolder + 4;
   static constexpr uint32_t kOffSlot = kOffAbort + 4;
-  static constexpr uint32_t kOffWarpLast = kOffSlot + 4;  // int [16]
-  static constexpr uint32_t kOffMask = kOffWarpLast + 64;  // uint32 [kStages][2]
-  static constexpr uint32_t kCtrlBytes = 512;
-  static_assert(kOffMask + 8 * kStages - kOffCtrl <= kCtrlBytes, "control block overflow");
+  static constexpr uint32_t kOffMask = kOffSlot + 4;  // uint32 [kStages][2]
+  static constexpr uint32_t kOffTokLast = kOffMask + 8 * kStages;  // int [kTokRing][kGatherWarps]
+  static constexpr uint32_t kOffTokId = kOffTokLast + 4 * 3 * kTokRing;  // int [kTokRing], handed over
+  static constexpr uint32_t kOffTokT = kOffTokId + 4 * kTokRing;         // int [kTokRing], published
+  static constexpr uint32_t kCtrlBytes = 640;
+  static_assert(kOffTokT + 4 * kTokRing - kOffCtrl <= kCtrlBytes, "control block overflow");
   static constexpr uint32_t kSmemBytes = kOffCtrl + kCtrlBytes + 1024;  // +1024: realignment
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert((kDC / 64) * kOTileBytes <= kStages * kStageBytes, "O staging fits the kv ring");
   // TMEM: O, the ring of score tiles, then two P buffers (bf16 pairs, 32
   // columns each).
   static constexpr uint32_t kTmemO = 0;
@@ -134,6 +146,10 @@ struct FwdLayout {
   static constexpr int kMmaWarp = kGatherWarp0 + kGatherWarps;
   static constexpr int kSendWarp0 = kMmaWarp + 1;
   static constexpr int kThreads = (kSendWarp0 + (NSPLIT == 2 ? 4 : 0)) * 32;
+  // Readers of a published token: the MMA thread, the softmax warps and (D
+  // split only) the combiner and sender warps (one arrival each).
+  static constexpr int kTokReaders = 1 + 4 + (NSPLIT == 2 ? 8 : 0);
+  static_assert(kGatherWarps == 3, "token ring entries hold three gather warps' scans");
   static_assert(2 * kXBufs * kXchgBytes == kFwdSlotBytes, "exchange slot size");
 };
 
@@ -162,10 +178,19 @@ __device__ __forceinline__ void gather_block(uint32_t stage, const __nv_bfloat16
   }
 }
 
+// Persistent: each CTA (pair) of the grid's p.clusters handles a sequence of
+// tokens -- taken one at a time from p.tok_counter by the pair's rank 0 (so
+// faster pairs take more), or c, c + p.clusters, ... without a counter -- as
+// one sequence of 64-slot blocks (G counts them over the CTA's whole life),
+// so that the next token's gathers, scores, exchange and softmax overlap the
+// current one's last P.V and O read-out; Q (one buffer) waits only for the
+// current token's last scores MMA, the next token's first P.V for the O
+// read-out.  Every barrier phase follows G, or the token count k.  Ring entry
+// k % kTokRing publishes token k's index (-1: no more tokens) and its last
+// valid slot as scanned by the three gather warps.
 template <int D, int NSPLIT>
 __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
-    smqa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
-                    const FwdParams p) {
+    smqa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const FwdParams p) {
   using L = FwdLayout<D, NSPLIT>;
   constexpr int DC = L::kDC;
   extern __shared__ uint8_t smem_raw[];
@@ -176,16 +201,23 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x / NSPLIT;
+  const int cl = static_cast<int>(blockIdx.x) / NSPLIT;  // this CTA's (pair's) index
   const uint32_t rank = NSPLIT == 2 ? cluster_ctarank() : 0u;
-  const int b = t / p.S;
-  const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
+  auto token_of = [&](int k) -> int { return cl + k * p.clusters; };  // k-th token, no counter
   auto bar = [&](int i) -> uint32_t { return base + L::kOffCtrl + 8u * static_cast<uint32_t>(i); };
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(smem + L::kOffTmemHolder);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
   volatile int* slot_smem = reinterpret_cast<volatile int*>(smem + L::kOffSlot);
   volatile uint32_t* vmask = reinterpret_cast<volatile uint32_t*>(smem + L::kOffMask);
+  volatile int* tok_last = reinterpret_cast<volatile int*>(smem + L::kOffTokLast);
+  volatile int* tok_id = reinterpret_cast<volatile int*>(smem + L::kOffTokId);
+  volatile int* tok_t = reinterpret_cast<volatile int*>(smem + L::kOffTokT);
   const WaitCtl ctl{abort_flag, p.status, p.limit_ns};
+  // Live blocks of the token in ring entry e (after its full barrier).
+  auto tok_blocks = [&](int e) -> int {
+    const int last = max(max(tok_last[3 * e], tok_last[3 * e + 1]), tok_last[3 * e + 2]);
+    return last < 0 ? 0 : last / L::kBI + 1;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < L::kStages; ++s) {
@@ -207,8 +239,15 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
       mbar_init(bar(L::kBarODone + s), 1);
     }
     mbar_init(bar(L::kBarQFull), 1);
+    mbar_init(bar(L::kBarQFree), 1);
+    mbar_init(bar(L::kBarOFree), L::kSoftmaxThreads);
+    for (int e = 0; e < L::kTokRing; ++e) {
+      mbar_init(bar(L::kBarTokFull + e), L::kGatherWarps);
+      mbar_init(bar(L::kBarTokEmpty + e), L::kTokReaders);
+      mbar_init(bar(L::kBarIdFull + e), 1);
+      mbar_init(bar(L::kBarIdEmpty + e), 1);
+    }
     mbar_init(bar(L::kBarDrain), 1);
-    mbar_init(bar(L::kBarOStaged), L::kSoftmaxThreads);
     *abort_flag = *reinterpret_cast<volatile int*>(p.status) != 0 ? 1 : 0;
     *slot_smem = -1;
     if (NSPLIT == 2 && rank == 0 && *abort_flag == 0) {
@@ -216,7 +255,7 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
       const uint64_t t0 = globaltimer_ns();
       int got = -1;
       for (uint32_t it = 0; got < 0; ++it) {
-        const int s = static_cast<int>((static_cast<uint32_t>(t) + it) % static_cast<uint32_t>(p.nslots));
+        const int s = static_cast<int>((static_cast<uint32_t>(cl) + it) % static_cast<uint32_t>(p.nslots));
         if (atomicCAS(p.slot_flags + s, 0, 1) == 0) {
           got = s;
         } else if ((it % static_cast<uint32_t>(p.nslots)) == static_cast<uint32_t>(p.nslots) - 1u &&
@@ -229,15 +268,13 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
       *slot_smem = got;
     }
     fence_mbar_init();
-    // This CTA's column half of Q, issued before anything else waits on
-    // memory (the index scan below overlaps it).
-    mbar_arrive_expect_tx(bar(L::kBarQFull), static_cast<uint32_t>(p.H) * 128u * L::kChunks);
-    for (int c = 0; c < L::kChunks; ++c)
-      tma_load_2d(base + L::kOffQ + c * L::kQChunkBytes, &tm_q, static_cast<int>(rank) * DC + c * 64,
-                  t * p.H, bar(L::kBarQFull));
   }
-  if (warp == L::kMmaWarp) tmem_alloc(base + L::kOffTmemHolder, L::kTmemCols);
-  // Heads beyond H are zero rows of the smem A operand (the TMA box covers H rows).
+  if (warp == L::kMmaWarp) {
+    if (lane == 0) tma_prefetch_desc(&tm_q);
+    tmem_alloc(base + L::kOffTmemHolder, L::kTmemCols);
+  }
+  // Heads beyond H are zero rows of the smem A operand (the TMA box covers H
+  // rows, so later loads leave them zero).
   if (threadIdx.x < L::kHPad && static_cast<int>(threadIdx.x) >= p.H) {
     const uint32_t h = threadIdx.x;
 #pragma unroll
@@ -247,16 +284,11 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
         st_shared_v4(base + L::kOffQ + c * L::kQChunkBytes + h * 128u + k * 16u, 0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
   }
-  volatile int* warp_last = reinterpret_cast<volatile int*>(smem + L::kOffWarpLast);
-  scan_last_valid(idx_row, p.topk, p.S_kv, warp_last);
   tc_fence_before();
   __syncthreads();
   if (NSPLIT == 2) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  // Blocks up to the last one holding a valid slot (0: no valid slot); both
-  // CTAs of a pair read the same index row, so they agree on it.
-  const int nblk = live_blocks(warp_last, L::kBI);
   // The pair's exchange slot (claimed by rank 0); without one, nothing runs.
   int slot = -1;
   if (NSPLIT == 2) {
@@ -268,42 +300,124 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
 
   if (warp >= L::kGatherWarp0 && warp < L::kMmaWarp) {
     // ------------------------------------------------------------ gather
+    // Per token: its index (handed over within the pair), the index row's
+    // last valid slot (each warp scans a third) into ring entry k %
+    // kTokRing, then its live blocks.  (An L2 prefetch of the token's Q
+    // here cost 1 %.)
     const int w = warp - L::kGatherWarp0;
-    auto load_idx = [&](int blk, int half) -> int {
-      const int j = blk * L::kBI + 32 * half + lane;
-      return j < p.topk ? __ldg(idx_row + j) : -1;
-    };
     const int col0 = static_cast<int>(rank) * DC;
-    int n0 = load_idx(0, 0), n1 = load_idx(0, 1);
-    for (int i = 0; run && i < nblk; ++i) {
-      const int s = i % L::kStages;
-      const int r0 = n0, r1 = n1;
-      if (i + 1 < nblk) {
-        n0 = load_idx(i + 1, 0);
-        n1 = load_idx(i + 1, 1);
+    bool ok = run;
+    int G = 0;
+    for (int k = 0; ok; ++k) {
+      const int e = k % L::kTokRing;
+      if (k >= L::kTokRing) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarTokEmpty + e),
+                                               ((k / L::kTokRing) - 1) & 1, ctl));
+        if (!ok) break;
       }
-      const int row0 = b * p.S_kv + (static_cast<unsigned>(r0) < static_cast<unsigned>(p.S_kv) ? r0 : 0);
-      const int row1 = b * p.S_kv + (static_cast<unsigned>(r1) < static_cast<unsigned>(p.S_kv) ? r1 : 0);
-      if (i >= L::kStages) {
-        const bool ok = mbar_wait(bar(L::kBarKvEmpty + s), ((i / L::kStages) - 1) & 1, ctl);
-        if (!__all_sync(0xffffffffu, ok)) break;
+      int t;
+      if (NSPLIT == 2 && p.tok_counter != nullptr) {
+        // The pair's k-th token: rank 0 takes it from the counter and writes
+        // it into both CTAs' entry e (the peer's only once the peer has
+        // freed it); both read it after IdFull.
+        if (w == 0 && lane == 0) {
+          if (rank == 1 && k >= L::kTokRing) {
+            mbar_arrive_remote(mapa_shared(bar(L::kBarIdEmpty + e), 0u));
+          } else if (rank == 0) {
+            bool free_ok = true;
+            if (k >= L::kTokRing)
+              free_ok = mbar_wait<true>(bar(L::kBarIdEmpty + e), ((k / L::kTokRing) - 1) & 1, ctl);
+            if (free_ok) {
+              int nt = atomicAdd(p.tok_counter, 1);
+              if (nt >= p.tokens) nt = -1;
+              tok_id[e] = nt;
+              st_shared_cluster_s32(mapa_shared(base + L::kOffTokId + 4u * e, 1u), nt);
+              mbar_arrive_remote(mapa_shared(bar(L::kBarIdFull + e), 1u));
+              mbar_arrive(bar(L::kBarIdFull + e));
+            }
+          }
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarIdFull + e), (k / L::kTokRing) & 1, ctl));
+        if (!ok) break;
+        t = tok_id[e];
+      } else {
+        t = token_of(k) < p.tokens ? token_of(k) : -1;
       }
-      // The block's valid-slot mask (bit j of word h: slot 32h + j), read by
-      // the softmax once this stage's full barrier has completed.
-      const uint32_t m0 = __ballot_sync(0xffffffffu, static_cast<unsigned>(r0) < static_cast<unsigned>(p.S_kv));
-      const uint32_t m1 = __ballot_sync(0xffffffffu, static_cast<unsigned>(r1) < static_cast<unsigned>(p.S_kv));
-      gather_block<L::kChunks, D, L::kGatherWarps>(base + L::kOffKv + static_cast<uint32_t>(s) * L::kStageBytes,
-                                  p.kv, col0, row0, row1, w, lane);
-      cp_async_arrive_noinc(bar(L::kBarKvFull + s));
-      if (w == 0 && lane == 0) {
-        vmask[2 * s] = m0;
-        vmask[2 * s + 1] = m1;
-        mbar_arrive(bar(L::kBarKvFull + s));
+      if (t < 0) {
+        // No more tokens: publish the end.
+        if (lane == 0) {
+          if (w == 0) tok_t[e] = -1;
+          tok_last[3 * e + w] = -1;
+          mbar_arrive(bar(L::kBarTokFull + e));
+        }
+        break;
+      }
+      const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
+      // 16-byte loads issued before any compare: one round of memory
+      // latency covers a 2048-slot row.
+      int last = -1;
+      const int tid = 32 * w + lane;
+      if ((p.topk & 3) == 0 && (reinterpret_cast<uintptr_t>(idx_row) & 15u) == 0) {
+        const int4* row4 = reinterpret_cast<const int4*>(idx_row);
+        const unsigned skv = static_cast<unsigned>(p.S_kv);
+#pragma unroll 8
+        for (int q = tid; q < p.topk / 4; q += 32 * L::kGatherWarps) {
+          const int4 v = __ldg(row4 + q);
+          if (static_cast<unsigned>(v.x) < skv) last = 4 * q;
+          if (static_cast<unsigned>(v.y) < skv) last = 4 * q + 1;
+          if (static_cast<unsigned>(v.z) < skv) last = 4 * q + 2;
+          if (static_cast<unsigned>(v.w) < skv) last = 4 * q + 3;
+        }
+      } else {
+#pragma unroll 8
+        for (int j = tid; j < p.topk; j += 32 * L::kGatherWarps)
+          if (static_cast<unsigned>(__ldg(idx_row + j)) < static_cast<unsigned>(p.S_kv)) last = j;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, off));
+      if (lane == 0) {
+        if (w == 0) tok_t[e] = t;
+        tok_last[3 * e + w] = last;
+        mbar_arrive(bar(L::kBarTokFull + e));
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarTokFull + e), (k / L::kTokRing) & 1, ctl));
+      if (!ok) break;
+      const int nblk = tok_blocks(e);
+      const int b = t / p.S;
+      auto load_idx = [&](int blk, int half) -> int {
+        const int j = blk * L::kBI + 32 * half + lane;
+        return j < p.topk ? __ldg(idx_row + j) : -1;
+      };
+      int n0 = nblk > 0 ? load_idx(0, 0) : -1, n1 = nblk > 0 ? load_idx(0, 1) : -1;
+      for (int i = 0; i < nblk; ++i, ++G) {
+        const int s = G % L::kStages;
+        const int r0 = n0, r1 = n1;
+        if (i + 1 < nblk) {
+          n0 = load_idx(i + 1, 0);
+          n1 = load_idx(i + 1, 1);
+        }
+        const int row0 = b * p.S_kv + (static_cast<unsigned>(r0) < static_cast<unsigned>(p.S_kv) ? r0 : 0);
+        const int row1 = b * p.S_kv + (static_cast<unsigned>(r1) < static_cast<unsigned>(p.S_kv) ? r1 : 0);
+        if (G >= L::kStages) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarKvEmpty + s), ((G / L::kStages) - 1) & 1, ctl));
+          if (!ok) break;
+        }
+        // The block's valid-slot mask (bit j of word h: slot 32h + j), read by
+        // the softmax once this stage's full barrier has completed.
+        const uint32_t m0 = __ballot_sync(0xffffffffu, static_cast<unsigned>(r0) < static_cast<unsigned>(p.S_kv));
+        const uint32_t m1 = __ballot_sync(0xffffffffu, static_cast<unsigned>(r1) < static_cast<unsigned>(p.S_kv));
+        gather_block<L::kChunks, D, L::kGatherWarps>(base + L::kOffKv + static_cast<uint32_t>(s) * L::kStageBytes,
+                                    p.kv, col0, row0, row1, w, lane);
+        cp_async_arrive_noinc(bar(L::kBarKvFull + s));
+        if (w == 0 && lane == 0) {
+          vmask[2 * s] = m0;
+          vmask[2 * s + 1] = m1;
+          mbar_arrive(bar(L::kBarKvFull + s));
+        }
       }
     }
     // Let every copy this warp started land before the CTA can exit.
     cp_async_wait_all();
-    if (w == 0 && lane == 0) mbar_wait_drain(bar(L::kBarQFull), 0);
   } else if (warp == L::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -327,58 +441,137 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
                    dk + ((c * L::kKvChunkBytes + k * 32u) >> 4), idesc_s, (c | k) ? 1u : 0u);
         mma_commit(bar(L::kBarSFull + i % L::kSBufs));
       };
-      // O += P.V for block j; P (A operand) from TMEM buffer j % 2, V = this
-      // CTA's columns of the block, MN-major.
-      auto issue_pv = [&](int j) {
+      // O += P.V for block j (block jt of its token: the first overwrites);
+      // P (A operand) from TMEM buffer j % 2, V = this CTA's columns of the
+      // block, MN-major.
+      auto issue_pv = [&](int j, int jt) {
         const int sj = j % L::kStages;
         const uint64_t dv = d_v + ((static_cast<uint32_t>(sj) * L::kStageBytes) >> 4);
         const uint32_t a_tm = tmem + L::kTmemP + static_cast<uint32_t>(j & 1) * (L::kBI / 2);
 #pragma unroll
         for (int k = 0; k < L::kBI / 16; ++k)
           mma_ts(tmem + L::kTmemO, a_tm + k * 8, dv + (k * 2048u >> 4), idesc_o,
-                 (j > 0 || k > 0) ? 1u : 0u);
+                 (jt > 0 || k > 0) ? 1u : 0u);
         mma_commit(bar(L::kBarKvEmpty + sj));
         mma_commit(bar(L::kBarODone + (j & 1)));
       };
-      // Event loop (non-blocking tests, so that waiting on one kind of work
-      // never delays the other), oldest work first: P.V of block npv once
-      // its P is written; scores of block ns once its kv rows have landed
-      // and its score tile has been read by the softmax (block ns - kSBufs).
-      bool ok = run && mbar_wait(bar(L::kBarQFull), 0, ctl);
-      int ns = 0, npv = 0;
+      // Three cursors over the CTA's tokens: Q loads (token lk, one per
+      // token with blocks, into the single buffer once the previous such
+      // token's last scores MMA has completed), scores (token sk, its block
+      // si, sequence index sG) and P.V (vk, vi, vG).  Each caches its
+      // token's live-block count (-1: not read yet) and touches the
+      // published counts only at token boundaries.  Event loop
+      // (non-blocking tests, so that waiting on one kind of work never
+      // delays the other), oldest work first: P.V of block vG once its P is
+      // written (and, for a token's first block, the previous token's O has
+      // been read out); scores of block sG once its kv rows have landed, its
+      // score tile has been read by the softmax (block sG - kSBufs) and its
+      // token's Q is in; otherwise the next Q load.
+      auto tok_known = [&](int k) -> bool {
+        return mbar_probe(bar(L::kBarTokFull + k % L::kTokRing), (k / L::kTokRing) & 1);
+      };
+      auto nblk_of = [&](int k) -> int { return tok_blocks(k % L::kTokRing); };
+      int lk = 0, lnb = -1, la = 0, lt = -1;         // load cursor (token lt), loads issued
+      bool l_end = false;                             // the load cursor met the end
+      int sk = 0, si = 0, snb = -1, sG = 0, sa = 0;   // sa: load index of token sk
+      int vk = 0, vi = 0, vnb = -1, vG = 0, va = 0;   // va: load index of token vk
+      int qfree = 0;                                  // Q releases committed
+      bool ok = run;
       PollState ps = poll_start();
       uint32_t spins = 0;
-      while (ok && npv < nblk) {
-        if (npv < ns && mbar_probe(bar(L::kBarPFull + (npv & 1)), (npv >> 1) & 1)) {
-          tc_fence_after();
-          issue_pv(npv);
-          ++npv;
-        } else if (ns < nblk &&
-                   mbar_probe(bar(L::kBarKvFull + ns % L::kStages), (ns / L::kStages) & 1) &&
-                   (ns < L::kSBufs ||
-                    mbar_probe(bar(L::kBarSFree + ns % L::kSBufs), ((ns / L::kSBufs) - 1) & 1))) {
-          // The kv tile was written by cp.async (generic proxy): order it
-          // before the tensor core's (async proxy) reads.
-          fence_proxy_async_smem();
-          tc_fence_after();
-          issue_s(ns);
-          ++ns;
-          if (static_cast<int>(blockIdx.x) == p.stall_cta) {  // test hook only
-            ok = stall_until_limit(ctl);
-            break;
+      while (ok) {
+        // ---- cursor bookkeeping (does work only at token boundaries)
+        if (lnb < 0 && !l_end && qfree >= la && tok_known(lk)) {
+          lt = tok_t[lk % L::kTokRing];
+          if (lt < 0) {
+            l_end = true;
+          } else {
+            lnb = nblk_of(lk);
+            if (lnb == 0) {  // nothing to load: on to the next token
+              ++lk;
+              lnb = -1;
+              continue;
+            }
           }
-        } else {
-          if ((++spins & 63u) == 0u && !poll_check(ctl, ps)) {
+        }
+        if (snb < 0 && sk < lk) snb = nblk_of(sk);  // published: the load cursor passed it
+        if (snb >= 0 && si == snb) {                  // token sk done (or without blocks)
+          if (snb > 0) ++sa;
+          ++sk;
+          si = 0;
+          snb = -1;
+          continue;
+        }
+        if (vnb < 0 && vk < lk) vnb = nblk_of(vk);
+        if (vnb >= 0 && vi == vnb && vk < sk) {       // token vk done: release its entry
+          mbar_arrive(bar(L::kBarTokEmpty + vk % L::kTokRing));
+          if (vnb > 0) ++va;
+          ++vk;
+          vi = 0;
+          vnb = -1;
+          continue;
+        }
+        if (l_end && vk == lk) break;  // every token done
+        // ---- events, within the current tokens: back to the bookkeeping
+        // only at a token boundary or after a Q load, so that a mid-token
+        // iteration tests nothing but the events.
+        const bool want_load = lnb > 0;
+        const bool need_book = !want_load && lnb < 0 && !l_end && qfree >= la;
+        for (;;) {
+          if (vG < sG && vi < vnb && mbar_probe(bar(L::kBarPFull + (vG & 1)), (vG >> 1) & 1) &&
+              (vi > 0 || va == 0 || mbar_probe(bar(L::kBarOFree), (va - 1) & 1))) {
+            tc_fence_after();
+            issue_pv(vG, vi);
+            ++vi;
+            ++vG;
+            ps.t0 = globaltimer_ns();  // progress: the limit counts from the last issue
+            if (vi == vnb) break;
+          } else if (si < snb &&
+                     mbar_probe(bar(L::kBarKvFull + sG % L::kStages), (sG / L::kStages) & 1) &&
+                     (sG < L::kSBufs ||
+                      mbar_probe(bar(L::kBarSFree + sG % L::kSBufs), ((sG / L::kSBufs) - 1) & 1)) &&
+                     (si > 0 || mbar_probe(bar(L::kBarQFull), sa & 1))) {
+            // The kv tile was written by cp.async (generic proxy): order it
+            // before the tensor core's (async proxy) reads.
+            fence_proxy_async_smem();
+            tc_fence_after();
+            issue_s(sG);
+            ++si;
+            ++sG;
+            ps.t0 = globaltimer_ns();
+            if (static_cast<int>(blockIdx.x) == p.stall_cta && sG == 1) {  // test hook only
+              ok = stall_until_limit(ctl);
+              break;
+            }
+            if (si == snb) {  // the token's last scores: Q may take the next token
+              mma_commit(bar(L::kBarQFree));
+              ++qfree;
+              break;
+            }
+          } else if (want_load && (la == 0 || mbar_probe(bar(L::kBarQFree), (la - 1) & 1))) {
+            // This CTA's column half of token lt's Q into the (free) buffer.
+            mbar_arrive_expect_tx(bar(L::kBarQFull), static_cast<uint32_t>(p.H) * 128u * L::kChunks);
+            for (int c = 0; c < L::kChunks; ++c)
+              tma_load_2d(base + L::kOffQ + c * L::kQChunkBytes, &tm_q,
+                          static_cast<int>(rank) * DC + c * 64, lt * p.H, bar(L::kBarQFull));
+            ++la;
+            ++lk;
+            lnb = -1;
+            ps.t0 = globaltimer_ns();
+            break;
+          } else if (need_book && tok_known(lk)) {  // the next token is published
+            break;
+          } else if ((++spins & 63u) == 0u && !poll_check(ctl, ps)) {
             ok = false;
             break;
           }
-          continue;
         }
-        ps.t0 = globaltimer_ns();  // progress: the limit counts from the last issue
       }
-      // No MMA may still be running when TMEM is released.
+      // No MMA may still be running when TMEM is released, and no Q load
+      // still landing when the CTA exits.
       mma_commit(bar(L::kBarDrain));
       mbar_wait_drain(bar(L::kBarDrain), 0);
+      if (la > 0) mbar_wait_drain(bar(L::kBarQFull), (la - 1) & 1);
     }
     __syncwarp();
   } else if (NSPLIT == 2 && warp >= L::kSendWarp0) {
@@ -394,10 +587,20 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
     const uint32_t peer_full = mapa_shared(bar(L::kBarRecvFull), rank ^ 1u);
     uint8_t* peer0 = p.exch + (static_cast<size_t>(slot) * 2 + (rank ^ 1u)) *
                                   (L::kXBufs * L::kXchgBytes);
-    for (int i = 0; run && i < nblk; ++i) {
+    bool ok = run;
+    int G = 0;
+    for (int k = 0; ok; ++k) {
+     const int te = k % L::kTokRing;
+     ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarTokFull + te), (k / L::kTokRing) & 1, ctl));
+     if (!ok || tok_t[te] < 0) break;
+     const int nblk = tok_blocks(te);
+     __syncwarp();
+     if (lane == 0) mbar_arrive(bar(L::kBarTokEmpty + te));
+     for (int ib = 0; ib < nblk; ++ib, ++G) {
+      const int i = G;  // position in the CTA's block sequence
       const int sb = i % L::kSBufs;
       const int xb = i % L::kXBufs;
-      bool ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + sb), (i / L::kSBufs) & 1, ctl));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + sb), (i / L::kSBufs) & 1, ctl));
       if (!ok) break;
       tc_fence_after();
       const uint32_t tile = tmem + lane_base + L::kTmemS + sb * L::kBI;
@@ -438,6 +641,7 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
       mbar_arrive(bar(L::kBarSRead + sb));
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(peer_full + 8u * static_cast<uint32_t>(xb));
+     }
     }
   } else if (NSPLIT == 2 && warp >= L::kCombWarp0 && warp < L::kGatherWarp0) {
     // ------------------------------------------------------------ combiner
@@ -452,11 +656,21 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
     const uint32_t lane_base = static_cast<uint32_t>(sq * 32) << 16;
     const uint8_t* recv0 = p.exch + (static_cast<size_t>(slot) * 2 + rank) *
                                         (L::kXBufs * L::kXchgBytes);
-    for (int i = 0; run && i < nblk; ++i) {
+    bool ok = run;
+    int G = 0;
+    for (int k = 0; ok; ++k) {
+     const int te = k % L::kTokRing;
+     ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarTokFull + te), (k / L::kTokRing) & 1, ctl));
+     if (!ok || tok_t[te] < 0) break;
+     const int nblk = tok_blocks(te);
+     __syncwarp();
+     if (lane == 0) mbar_arrive(bar(L::kBarTokEmpty + te));
+     for (int ib = 0; ib < nblk; ++ib, ++G) {
+      const int i = G;  // position in the CTA's block sequence
       const int sb = i % L::kSBufs;
       const int xb = i % L::kXBufs;
-      bool ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull + xb),
-                                                        (i / L::kXBufs) & 1, ctl));
+      ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull + xb),
+                                                   (i / L::kXBufs) & 1, ctl));
       if (!ok) break;
       const uint8_t* buf = recv0 + static_cast<size_t>(xb) * L::kXchgBytes;
       const uint4* src = reinterpret_cast<const uint4*>(buf) + h;
@@ -490,6 +704,7 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
       // The peer's values are consumed (see the flow-control note above).
       tc_fence_before();
       mbar_arrive(bar(L::kBarSSum + sb));
+     }
     }
   } else if (warp < L::kSoftmaxThreads / 32) {
     // ------------------------------------------------------------ softmax
@@ -502,10 +717,24 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
     // With the D split the tile already holds s1 * score.
     const float s1 = NSPLIT == 2 ? 1.f : (p.ref_round ? p.scale : p.scale_log2);
     const float s2 = p.ref_round ? 1.4426950408889634f : 1.f;
-    float m_run = -INFINITY;
-    float l_run = 0.f;
+    // O rows start 32-byte aligned when the tensor does (row and half
+    // offsets are multiples of 64 bytes).
+    const bool o32 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
     bool ok = run;
-    for (int i = 0; ok && i < nblk; ++i) {
+    int G = 0;  // blocks so far
+    for (int tk = 0; ok; ++tk) {
+     const int te = tk % L::kTokRing;
+     ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarTokFull + te), (tk / L::kTokRing) & 1, ctl));
+     if (!ok) break;
+     const int t = tok_t[te];
+     if (t < 0) break;
+     const int nblk = tok_blocks(te);
+     __syncwarp();
+     if (lane == 0) mbar_arrive(bar(L::kBarTokEmpty + te));
+     float m_run = -INFINITY;
+     float l_run = 0.f;
+     for (int ib = 0; ib < nblk; ++ib, ++G) {
+      const int i = G;  // position in the CTA's block sequence
       const int sb = i % L::kSBufs;
       ok = __all_sync(0xffffffffu, mbar_wait(bar((NSPLIT == 2 ? L::kBarSSum : L::kBarSFull) + sb),
                                              (i / L::kSBufs) & 1, ctl));
@@ -575,7 +804,7 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
       // completed, rescale this row before P.V of block i may start (whole
       // warp, since TMEM accesses are warp-collective; rows without a bump
       // use 1).
-      const bool need_rescale = bump && alpha != 0.f && i > 0;
+      const bool need_rescale = bump && alpha != 0.f && ib > 0;
       if (__any_sync(0xffffffffu, need_rescale)) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + ((i - 1) & 1)),
                                                ((i - 1) >> 1) & 1, ctl));
@@ -593,62 +822,56 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
       }
       tc_fence_before();
       mbar_arrive(bar(L::kBarPFull + (i & 1)));
-    }
-    if (ok && nblk > 0)
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + ((nblk - 1) & 1)),
-                                             ((nblk - 1) >> 1) & 1, ctl));
-    if (ok) {
-      tc_fence_after();
-      const float sink2 = h < p.H ? __ldg(p.sink + h) * 1.4426950408889634f : 0.f;
-      const float m_fin = fmaxf(m_run, sink2);
-      const float so = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_fin);
-      const float Z = l_run * so + fast_exp2(sink2 - m_fin);
-      const float inv = so / Z;
-      // O, scaled, into shared memory as 64-column tiles in the
-      // 128-byte-swizzled layout of the output's tensor map (the kv ring is
-      // free: every MMA has completed); the TMA then writes whole rows.
+     }
+     if (!ok) break;
+     // The token's last P.V, then O (normalised, bf16) straight from TMEM
+     // to its rows with 16-byte stores (the kv ring, which used to stage it
+     // for a TMA store, already holds the next token's rows), and the LSE.
+     if (nblk > 0) {
+       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + ((G - 1) & 1)),
+                                              ((G - 1) >> 1) & 1, ctl));
+       if (!ok) break;
+       tc_fence_after();
+     }
+     const float sink2 = h < p.H ? __ldg(p.sink + h) * 1.4426950408889634f : 0.f;
+     const float m_fin = fmaxf(m_run, sink2);
+     const float so = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_fin);
+     const float Z = l_run * so + fast_exp2(sink2 - m_fin);
+     const float inv = so / Z;
+     __nv_bfloat16* orow = p.o + (static_cast<size_t>(t) * p.H + h) * D + static_cast<size_t>(rank) * DC;
 #pragma unroll 1
-      for (int cc = 0; cc < DC / 64; ++cc) {
-        float v[2][32];
-        if (nblk > 0) {
-          tmem_ld32x2(tmem + lane_base + L::kTmemO + cc * 64,
-                      tmem + lane_base + L::kTmemO + cc * 64 + 32, v[0], v[1]);
-        } else {  // no valid slot: O was never written, the output is 0
+     for (int c = 0; c < DC / 32; ++c) {
+       float v[32];
+       if (nblk > 0) {
+         tmem_ld32(tmem + lane_base + L::kTmemO + c * 32, v);
+       } else {  // no valid slot: O was never written, the output is 0
 #pragma unroll
-          for (int k = 0; k < 32; ++k) v[0][k] = v[1][k] = 0.f;
-        }
-        const uint32_t row = base + L::kOffKv + static_cast<uint32_t>(cc) * L::kOTileBytes +
-                             static_cast<uint32_t>(h) * 128u;
+         for (int kk = 0; kk < 32; ++kk) v[kk] = 0.f;
+       }
+       if (h < p.H) {
+         uint32_t w[16];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          uint32_t w[16];
+         for (int u = 0; u < 16; ++u) {
+           const float2 y = mul2(make_float2(v[2 * u], v[2 * u + 1]), make_float2(inv, inv));
+           w[u] = pack_bf16x2(y.x, y.y);
+         }
+         if (o32) {  // 32-byte stores: half the transactions of 16-byte ones
+           st_global_v8(orow + 32 * c, *reinterpret_cast<const uint32_t(*)[8]>(w));
+           st_global_v8(orow + 32 * c + 16, *reinterpret_cast<const uint32_t(*)[8]>(w + 8));
+         } else {
+           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float2 y = mul2(make_float2(v[u][2 * k], v[u][2 * k + 1]), make_float2(inv, inv));
-            w[k] = pack_bf16x2(y.x, y.y);
-          }
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t piece = static_cast<uint32_t>(4 * u + k);
-            st_shared_v4(row + ((piece ^ (static_cast<uint32_t>(h) & 7u)) << 4), w[4 * k],
-                         w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-          }
-        }
-      }
-      if (rank == 0 && h < p.H) p.lse[static_cast<size_t>(t) * p.H + h] = m_fin + log2f(Z);
-    }
-    // Every softmax thread arrives (also after a failed wait, so that the
-    // storing thread never waits in vain); one thread ships the tiles.
-    fence_proxy_async_smem();
-    mbar_arrive(bar(L::kBarOStaged));
-    if (threadIdx.x == 0) {
-      if (mbar_wait(bar(L::kBarOStaged), 0, ctl) && *abort_flag == 0) {
-        for (int cc = 0; cc < DC / 64; ++cc)
-          tma_store_2d(&tm_o, base + L::kOffKv + static_cast<uint32_t>(cc) * L::kOTileBytes,
-                       static_cast<int>(rank) * DC + cc * 64, t * p.H);
-        bulk_commit_group();
-        bulk_wait_group0();  // complete before the CTA (and its shared memory) goes away
-      }
+           for (int kk = 0; kk < 4; ++kk)
+             dst[kk] = make_uint4(w[4 * kk], w[4 * kk + 1], w[4 * kk + 2], w[4 * kk + 3]);
+         }
+       }
+     }
+     if (nblk > 0) {
+       // O is in registers: the next token's first P.V may overwrite it.
+       tc_fence_before();
+       mbar_arrive(bar(L::kBarOFree));
+     }
+     if (rank == 0 && h < p.H) p.lse[static_cast<size_t>(t) * p.H + h] = m_fin + log2f(Z);
     }
   }
 
@@ -666,16 +889,43 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
   }
 }
 
+// Clusters (pairs, or single CTAs for D = 64) of one instantiation that fit
+// on the device at once, per device (the persistent grid's size).
 template <int D, int NSPLIT>
-static cudaError_t launch_fwd_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_o,
-                                   const FwdParams& p, int tokens, cudaStream_t stream) {
+static int fwd_resident_clusters(cudaLaunchConfig_t cfg) {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] > 0) return cached[dev];
+  int n = 0;
+  auto kern = smqa_fwd_kernel<D, NSPLIT>;
+  if (NSPLIT > 1) {
+    cfg.gridDim = dim3(NSPLIT, 1, 1);
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  } else {
+    int per_sm = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, static_cast<int>(cfg.blockDim.x),
+                                                      cfg.dynamicSmemBytes) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      n = per_sm * sms;
+  }
+  if (n <= 0) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  cached[dev] = n;
+  return n;
+}
+
+template <int D, int NSPLIT>
+static cudaError_t launch_fwd_impl(const CUtensorMap& tm_q, const FwdParams& p0, int tokens,
+                                   cudaStream_t stream) {
   using L = FwdLayout<D, NSPLIT>;
   auto kern = smqa_fwd_kernel<D, NSPLIT>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(tokens) * NSPLIT, 1, 1);
   cfg.blockDim = dim3(L::kThreads, 1, 1);
   cfg.dynamicSmemBytes = L::kSmemBytes;
   cfg.stream = stream;
@@ -686,13 +936,19 @@ static cudaError_t launch_fwd_impl(const CUtensorMap& tm_q, const CUtensorMap& t
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tm_q, tm_o, p);
+  const int resident = fwd_resident_clusters<D, NSPLIT>(cfg);
+  if (resident <= 0) return cudaErrorInvalidConfiguration;
+  FwdParams p = p0;
+  p.tokens = tokens;
+  p.clusters = tokens < resident ? tokens : resident;
+  cfg.gridDim = dim3(static_cast<unsigned>(p.clusters) * NSPLIT, 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, tm_q, p);
 }
 
-cudaError_t launch_fwd(const CUtensorMap& tm_q, const CUtensorMap& tm_o, const FwdParams& p,
-                       int tokens, cudaStream_t stream) {
-  if (p.D == 512) return launch_fwd_impl<512, 2>(tm_q, tm_o, p, tokens, stream);
-  if (p.D == 64) return launch_fwd_impl<64, 1>(tm_q, tm_o, p, tokens, stream);
+cudaError_t launch_fwd(const CUtensorMap& tm_q, const FwdParams& p, int tokens,
+                       cudaStream_t stream) {
+  if (p.D == 512) return launch_fwd_impl<512, 2>(tm_q, p, tokens, stream);
+  if (p.D == 64) return launch_fwd_impl<64, 1>(tm_q, p, tokens, stream);
   return cudaErrorInvalidValue;
 }
 

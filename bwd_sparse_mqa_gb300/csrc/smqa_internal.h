@@ -128,8 +128,8 @@ inline size_t det_stats_offset(const smqa_shape& s) {
 // Records `msg` as the text smqa_last_error() returns on this thread.
 void set_last_error(const char* msg);
 
-cudaError_t launch_fwd(const CUtensorMap& tm_q, const CUtensorMap& tm_o, const FwdParams& p,
-                       int tokens, cudaStream_t stream);
+cudaError_t launch_fwd(const CUtensorMap& tm_q, const FwdParams& p, int tokens,
+                       cudaStream_t stream);
 cudaError_t launch_bwd_main(const CUtensorMap& tm_q, const CUtensorMap& tm_do,
                             const BwdParams& p, int tokens,
                             cudaStream_t stream);
