@@ -801,57 +801,67 @@ __global__ void __launch_bounds__(480, 1)
           continue;
         }
         if (l_end && gk == lk) break;  // every token done
-        // ---- events
-        if (si < snb &&
-            mbar_probe(bar(L::kBarKvFull + sG % L::kStages), (sG / L::kStages) & 1) &&
-            (sG == 0 || mbar_probe(bar(L::kBarSdpFree + ((sG - 1) & 1)), ((sG - 1) >> 1) & 1)) &&
-            (si > 0 || mbar_probe(bar(L::kBarQdoFull), sa & 1))) {
-          // The kv tile was written by cp.async (generic proxy): order it
-          // before the tensor core's (async proxy) reads.
-          fence_proxy_async_smem();
-          tc_fence_after();
-          issue_sdp(sG);
-          ++si;
-          ++sG;
-          if (static_cast<int>(blockIdx.x) == p.stall_cta && sG == 1) {  // test hook only
-            ok = stall_until_limit(ctl);
+        // ---- events, within the current tokens: back to the bookkeeping
+        // only at a token boundary or after a Q / dO load, so that a
+        // mid-token iteration tests nothing but the events.
+        const bool want_load = lnb > 0;
+        const bool need_book = !want_load && lnb < 0 && !l_end && qfree >= la;
+        for (;;) {
+          if (si < snb &&
+              mbar_probe(bar(L::kBarKvFull + sG % L::kStages), (sG / L::kStages) & 1) &&
+              (sG == 0 || mbar_probe(bar(L::kBarSdpFree + ((sG - 1) & 1)), ((sG - 1) >> 1) & 1)) &&
+              (si > 0 || mbar_probe(bar(L::kBarQdoFull), sa & 1))) {
+            // The kv tile was written by cp.async (generic proxy): order it
+            // before the tensor core's (async proxy) reads.
+            fence_proxy_async_smem();
+            tc_fence_after();
+            issue_sdp(sG);
+            ++si;
+            ++sG;
+            ps.t0 = globaltimer_ns();  // progress: the limit counts from the last issue
+            if (static_cast<int>(blockIdx.x) == p.stall_cta && sG == 1) {  // test hook only
+              ok = stall_until_limit(ctl);
+              break;
+            }
+            if (si == snb) break;
+          } else if (gG < sG && gi < gnb && mbar_probe(bar(L::kBarPdsFull + (gG & 1)), (gG >> 1) & 1) &&
+                     (gG == 0 || mbar_probe(bar(L::kBarDkvFree), (gG - 1) & 1)) &&
+                     (gi > 0 || ga == 0 || mbar_probe(bar(L::kBarDqFree), (ga - 1) & 1))) {
+            tc_fence_after();
+            issue_grad(gG, gi);
+            ++gi;
+            ++gG;
+            ps.t0 = globaltimer_ns();
+            if (gi == gnb) {
+              // The token's last gradients: its dQ is complete once they
+              // are, and Q / dO may take the next token.
+              mma_commit(bar(L::kBarDqDone));
+              mma_commit(bar(L::kBarQdoFree));
+              ++qfree;
+              break;
+            }
+          } else if (want_load && (la == 0 || mbar_probe(bar(L::kBarQdoFree), (la - 1) & 1))) {
+            // Q and dO slices of token lt into the (free) buffer.
+            const int t = lt;
+            mbar_arrive_expect_tx(bar(L::kBarQdoFull),
+                                  2u * static_cast<uint32_t>(p.H) * 128u * L::kChunks);
+            for (int c = 0; c < L::kChunks; ++c) {
+              const int x = static_cast<int>(rank) * DC + c * 64;
+              tma_load_2d(base + L::kOffQ + c * L::kQChunkBytes, &tm_q, x, t * p.H, bar(L::kBarQdoFull));
+              tma_load_2d(base + L::kOffDo + c * L::kQChunkBytes, &tm_do, x, t * p.H, bar(L::kBarQdoFull));
+            }
+            ++la;
+            ++lk;
+            lnb = -1;
+            ps.t0 = globaltimer_ns();
             break;
-          }
-        } else if (gG < sG && mbar_probe(bar(L::kBarPdsFull + (gG & 1)), (gG >> 1) & 1) &&
-                   (gG == 0 || mbar_probe(bar(L::kBarDkvFree), (gG - 1) & 1)) &&
-                   (gi > 0 || ga == 0 || mbar_probe(bar(L::kBarDqFree), (ga - 1) & 1))) {
-          tc_fence_after();
-          issue_grad(gG, gi);
-          ++gi;
-          ++gG;
-          if (gi == gnb) {
-            // The token's last gradients: its dQ is complete once they are,
-            // and Q / dO may take the next token.
-            mma_commit(bar(L::kBarDqDone));
-            mma_commit(bar(L::kBarQdoFree));
-            ++qfree;
-          }
-        } else if (lnb > 0 && (la == 0 || mbar_probe(bar(L::kBarQdoFree), (la - 1) & 1))) {
-          // Q and dO slices of token lt into the (free) buffer.
-          const int t = lt;
-          mbar_arrive_expect_tx(bar(L::kBarQdoFull),
-                                2u * static_cast<uint32_t>(p.H) * 128u * L::kChunks);
-          for (int c = 0; c < L::kChunks; ++c) {
-            const int x = static_cast<int>(rank) * DC + c * 64;
-            tma_load_2d(base + L::kOffQ + c * L::kQChunkBytes, &tm_q, x, t * p.H, bar(L::kBarQdoFull));
-            tma_load_2d(base + L::kOffDo + c * L::kQChunkBytes, &tm_do, x, t * p.H, bar(L::kBarQdoFull));
-          }
-          ++la;
-          ++lk;
-          lnb = -1;
-        } else {
-          if ((++spins & 63u) == 0u && !poll_check(ctl, ps)) {
+          } else if (need_book && tok_known(lk)) {  // the next token is published
+            break;
+          } else if ((++spins & 63u) == 0u && !poll_check(ctl, ps)) {
             ok = false;
             break;
           }
-          continue;
         }
-        ps.t0 = globaltimer_ns();  // progress: the limit counts from the last issue
       }
       // No MMA may still be running when TMEM is released, and no Q / dO
       // load still landing when the CTA exits.
@@ -886,6 +896,8 @@ __global__ void __launch_bounds__(480, 1)
       }
     };
     const int h = wq * 32 + lane;  // head row of the dQ read-out
+    // dQ rows start 32-byte aligned when the tensor does.
+    const bool dq32 = (reinterpret_cast<uintptr_t>(p.dq) & 31u) == 0;
     bool ok = *abort_flag == 0;
     int G = 0, a = 0;
     for (int k = 0; ok; ++k) {
@@ -972,8 +984,7 @@ __global__ void __launch_bounds__(480, 1)
         if (!ok) break;
         tc_fence_after();
       }
-      uint4* dst = reinterpret_cast<uint4*>(p.dq + (static_cast<size_t>(t) * p.H + h) * p.D +
-                                            static_cast<size_t>(rank) * DC);
+      __nv_bfloat16* qrow = p.dq + (static_cast<size_t>(t) * p.H + h) * p.D + static_cast<size_t>(rank) * DC;
 #pragma unroll 1
       for (int c = 0; c < DC / 32; ++c) {
         float v[32];
@@ -984,12 +995,18 @@ __global__ void __launch_bounds__(480, 1)
           for (int kk = 0; kk < 32; ++kk) v[kk] = 0.f;
         }
         if (h < p.H) {
+          uint32_t w[16];
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            dst[4 * c + kk] = make_uint4(pack_bf16x2(v[8 * kk], v[8 * kk + 1]),
-                                         pack_bf16x2(v[8 * kk + 2], v[8 * kk + 3]),
-                                         pack_bf16x2(v[8 * kk + 4], v[8 * kk + 5]),
-                                         pack_bf16x2(v[8 * kk + 6], v[8 * kk + 7]));
+          for (int u = 0; u < 16; ++u) w[u] = pack_bf16x2(v[2 * u], v[2 * u + 1]);
+          if (dq32) {  // 32-byte stores: half the transactions of 16-byte ones
+            st_global_v8(qrow + 32 * c, *reinterpret_cast<const uint32_t(*)[8]>(w));
+            st_global_v8(qrow + 32 * c + 16, *reinterpret_cast<const uint32_t(*)[8]>(w + 8));
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(qrow + 32 * c);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              dst[kk] = make_uint4(w[4 * kk], w[4 * kk + 1], w[4 * kk + 2], w[4 * kk + 3]);
+          }
         }
       }
       if (nblk > 0) {
