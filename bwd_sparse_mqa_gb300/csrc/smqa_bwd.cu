@@ -582,6 +582,9 @@ __global__ void __launch_bounds__(480, 1)
             }
           }
         }
+        // The whole warp again before anyone waits (lanes suspended in a wait
+        // while lane 0 hands the token over slow the handover down).
+        __syncwarp();
         ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarIdFull + e), (k / L::kTokRing) & 1, ctl));
         if (!ok) break;
         t = tok_id[e];

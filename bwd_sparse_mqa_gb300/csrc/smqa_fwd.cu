@@ -306,83 +306,96 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
     // here cost 1 %.)
     const int w = warp - L::kGatherWarp0;
     const int col0 = static_cast<int>(rank) * DC;
-    bool ok = run;
-    int G = 0;
-    for (int k = 0; ok; ++k) {
+    // Token k's setup: wait until ring entry k % kTokRing is free, learn the
+    // token (for D = 512 rank 0 takes it from the counter and writes it into
+    // both CTAs' entry, the peer's only once the peer has freed it), scan its
+    // index row (16-byte loads issued before any compare) and publish it.
+    auto setup = [&](int k) -> bool {
       const int e = k % L::kTokRing;
-      if (k >= L::kTokRing) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarTokEmpty + e),
-                                               ((k / L::kTokRing) - 1) & 1, ctl));
-        if (!ok) break;
-      }
+      if (k >= L::kTokRing &&
+          !__all_sync(0xffffffffu, mbar_wait(bar(L::kBarTokEmpty + e), ((k / L::kTokRing) - 1) & 1, ctl)))
+        return false;
       int t;
       if (NSPLIT == 2 && p.tok_counter != nullptr) {
-        // The pair's k-th token: rank 0 takes it from the counter and writes
-        // it into both CTAs' entry e (the peer's only once the peer has
-        // freed it); both read it after IdFull.
-        if (w == 0 && lane == 0) {
-          if (rank == 1 && k >= L::kTokRing) {
-            mbar_arrive_remote(mapa_shared(bar(L::kBarIdEmpty + e), 0u));
-          } else if (rank == 0) {
-            bool free_ok = true;
-            if (k >= L::kTokRing)
-              free_ok = mbar_wait<true>(bar(L::kBarIdEmpty + e), ((k / L::kTokRing) - 1) & 1, ctl);
-            if (free_ok) {
-              int nt = atomicAdd(p.tok_counter, 1);
-              if (nt >= p.tokens) nt = -1;
-              tok_id[e] = nt;
-              st_shared_cluster_s32(mapa_shared(base + L::kOffTokId + 4u * e, 1u), nt);
-              mbar_arrive_remote(mapa_shared(bar(L::kBarIdFull + e), 1u));
-              mbar_arrive(bar(L::kBarIdFull + e));
+        if (w == 0) {
+          if (lane == 0) {
+            if (rank == 1 && k >= L::kTokRing) {
+              mbar_arrive_remote(mapa_shared(bar(L::kBarIdEmpty + e), 0u));
+            } else if (rank == 0) {
+              bool free_ok = true;
+              if (k >= L::kTokRing)
+                free_ok = mbar_wait<true>(bar(L::kBarIdEmpty + e), ((k / L::kTokRing) - 1) & 1, ctl);
+              if (free_ok) {
+                int nt = atomicAdd(p.tok_counter, 1);
+                if (nt >= p.tokens) nt = -1;
+                tok_id[e] = nt;
+                st_shared_cluster_s32(mapa_shared(base + L::kOffTokId + 4u * e, 1u), nt);
+                mbar_arrive_remote(mapa_shared(bar(L::kBarIdFull + e), 1u));
+                mbar_arrive(bar(L::kBarIdFull + e));
+              }
             }
           }
+          // The whole warp again before anyone waits: lanes suspended in a
+          // wait while lane 0 hands the token over slowed the handover by
+          // thousands of cycles.
+          __syncwarp();
         }
-        ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarIdFull + e), (k / L::kTokRing) & 1, ctl));
-        if (!ok) break;
+        if (!__all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarIdFull + e), (k / L::kTokRing) & 1, ctl)))
+          return false;
         t = tok_id[e];
       } else {
         t = token_of(k) < p.tokens ? token_of(k) : -1;
       }
-      if (t < 0) {
-        // No more tokens: publish the end.
-        if (lane == 0) {
-          if (w == 0) tok_t[e] = -1;
-          tok_last[3 * e + w] = -1;
-          mbar_arrive(bar(L::kBarTokFull + e));
-        }
-        break;
-      }
-      const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
-      // 16-byte loads issued before any compare: one round of memory
-      // latency covers a 2048-slot row.
       int last = -1;
-      const int tid = 32 * w + lane;
-      if ((p.topk & 3) == 0 && (reinterpret_cast<uintptr_t>(idx_row) & 15u) == 0) {
-        const int4* row4 = reinterpret_cast<const int4*>(idx_row);
-        const unsigned skv = static_cast<unsigned>(p.S_kv);
+      if (t >= 0) {
+        const int32_t* row = p.idx + static_cast<size_t>(t) * p.topk;
+        const int tid = 32 * w + lane;
+        if ((p.topk & 3) == 0 && (reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
+          const int4* row4 = reinterpret_cast<const int4*>(row);
+          const unsigned skv = static_cast<unsigned>(p.S_kv);
 #pragma unroll 8
-        for (int q = tid; q < p.topk / 4; q += 32 * L::kGatherWarps) {
-          const int4 v = __ldg(row4 + q);
-          if (static_cast<unsigned>(v.x) < skv) last = 4 * q;
-          if (static_cast<unsigned>(v.y) < skv) last = 4 * q + 1;
-          if (static_cast<unsigned>(v.z) < skv) last = 4 * q + 2;
-          if (static_cast<unsigned>(v.w) < skv) last = 4 * q + 3;
+          for (int q = tid; q < p.topk / 4; q += 32 * L::kGatherWarps) {
+            const int4 v = __ldg(row4 + q);
+            if (static_cast<unsigned>(v.x) < skv) last = 4 * q;
+            if (static_cast<unsigned>(v.y) < skv) last = 4 * q + 1;
+            if (static_cast<unsigned>(v.z) < skv) last = 4 * q + 2;
+            if (static_cast<unsigned>(v.w) < skv) last = 4 * q + 3;
+          }
+        } else {
+#pragma unroll 8
+          for (int j = tid; j < p.topk; j += 32 * L::kGatherWarps)
+            if (static_cast<unsigned>(__ldg(row + j)) < static_cast<unsigned>(p.S_kv)) last = j;
         }
-      } else {
-#pragma unroll 8
-        for (int j = tid; j < p.topk; j += 32 * L::kGatherWarps)
-          if (static_cast<unsigned>(__ldg(idx_row + j)) < static_cast<unsigned>(p.S_kv)) last = j;
-      }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, off));
+        for (int off = 16; off > 0; off >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, off));
+      }
       if (lane == 0) {
         if (w == 0) tok_t[e] = t;
         tok_last[3 * e + w] = last;
         mbar_arrive(bar(L::kBarTokFull + e));
       }
+      return true;
+    };
+    // The next token is set up once a couple of the current token's blocks
+    // are issued (the gather waits for free kv stages then anyway), so that
+    // its index, count and Q are known before the current token ends: set
+    // up at the token boundary instead, the next token's first scores came
+    // ~15,000 cycles after the current token's last.
+    bool ok = run && setup(0);
+    int G = 0;
+    for (int k = 0; ok; ++k) {
+      const int e = k % L::kTokRing;
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarTokFull + e), (k / L::kTokRing) & 1, ctl));
       if (!ok) break;
+      const int t = tok_t[e];
+      if (t < 0) break;  // no more tokens
       const int nblk = tok_blocks(e);
+      const int pre = nblk < 2 ? nblk : 2;  // blocks issued before the next token's setup
+      if (pre == 0) {
+        ok = setup(k + 1);
+        if (!ok) break;
+      }
+      const int32_t* idx_row = p.idx + static_cast<size_t>(t) * p.topk;
       const int b = t / p.S;
       auto load_idx = [&](int blk, int half) -> int {
         const int j = blk * L::kBI + 32 * half + lane;
@@ -413,6 +426,10 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
           vmask[2 * s] = m0;
           vmask[2 * s + 1] = m1;
           mbar_arrive(bar(L::kBarKvFull + s));
+        }
+        if (i + 1 == pre) {
+          ok = setup(k + 1);
+          if (!ok) break;
         }
       }
     }
