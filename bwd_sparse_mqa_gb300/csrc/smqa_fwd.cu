@@ -607,58 +607,58 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
     bool ok = run;
     int G = 0;
     for (int k = 0; ok; ++k) {
-     const int te = k % L::kTokRing;
-     ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarTokFull + te), (k / L::kTokRing) & 1, ctl));
-     if (!ok || tok_t[te] < 0) break;
-     const int nblk = tok_blocks(te);
-     __syncwarp();
-     if (lane == 0) mbar_arrive(bar(L::kBarTokEmpty + te));
-     for (int ib = 0; ib < nblk; ++ib, ++G) {
-      const int i = G;  // position in the CTA's block sequence
-      const int sb = i % L::kSBufs;
-      const int xb = i % L::kXBufs;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + sb), (i / L::kSBufs) & 1, ctl));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t tile = tmem + lane_base + L::kTmemS + sb * L::kBI;
-      float x[64];
-      tmem_ld32x2(tile, tile + 32, *reinterpret_cast<float(*)[32]>(x),
-                  *reinterpret_cast<float(*)[32]>(x + 32));
-      const int ex = bfp16_exponent(__fmul_rn(__fmul_rn(absmax_fold_n<64>(x), s1), kExpMargin));
-      const float f = __fmul_rn(s1, pow2f(14 - ex)), inv = pow2f(ex - 14);
-      uint32_t w[32];
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float2 r = bfp16_round2(make_float2(x[2 * k], x[2 * k + 1]), f);
-        w[k] = bfp16_pack(r.x, r.y);
-        const float2 v = bfp16_value2(r, inv);
-        x[2 * k] = v.x;
-        x[2 * k + 1] = v.y;
-      }
-      // The peer has read block i - kXBufs from this buffer once its block
-      // i - kXBufs + kSBufs has arrived here (it computed that block into
-      // the score tile it freed after reading block i - kXBufs).
-      if (i >= L::kXBufs) {
-        const int j = i - L::kXBufs + L::kSBufs;
-        ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull + j % L::kXBufs),
-                                                     (j / L::kXBufs) & 1, ctl));
-        if (!ok) break;
-      }
-      // The stores first, so that their way to L2 overlaps the write-back.
-      uint8_t* buf = peer0 + static_cast<size_t>(xb) * L::kXchgBytes;
-      uint4* dst = reinterpret_cast<uint4*>(buf) + h;
-#pragma unroll
-      for (int c = 0; c < L::kPieces; ++c)
-        dst[c * L::kHPad] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-      reinterpret_cast<int*>(buf + L::kXchgScaleOff)[h] = ex;
-      // The tile now gets this CTA's partial as the peer will see it.
-      tmem_st32(tile, *reinterpret_cast<float(*)[32]>(x));
-      tmem_st32(tile + 32, *reinterpret_cast<float(*)[32]>(x + 32));
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarSRead + sb));
+      const int te = k % L::kTokRing;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarTokFull + te), (k / L::kTokRing) & 1, ctl));
+      if (!ok || tok_t[te] < 0) break;
+      const int nblk = tok_blocks(te);
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote(peer_full + 8u * static_cast<uint32_t>(xb));
-     }
+      if (lane == 0) mbar_arrive(bar(L::kBarTokEmpty + te));
+      for (int ib = 0; ib < nblk; ++ib, ++G) {
+        const int i = G;  // position in the CTA's block sequence
+        const int sb = i % L::kSBufs;
+        const int xb = i % L::kXBufs;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + sb), (i / L::kSBufs) & 1, ctl));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t tile = tmem + lane_base + L::kTmemS + sb * L::kBI;
+        float x[64];
+        tmem_ld32x2(tile, tile + 32, *reinterpret_cast<float(*)[32]>(x),
+                    *reinterpret_cast<float(*)[32]>(x + 32));
+        const int ex = bfp16_exponent(__fmul_rn(__fmul_rn(absmax_fold_n<64>(x), s1), kExpMargin));
+        const float f = __fmul_rn(s1, pow2f(14 - ex)), inv = pow2f(ex - 14);
+        uint32_t w[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float2 r = bfp16_round2(make_float2(x[2 * k], x[2 * k + 1]), f);
+          w[k] = bfp16_pack(r.x, r.y);
+          const float2 v = bfp16_value2(r, inv);
+          x[2 * k] = v.x;
+          x[2 * k + 1] = v.y;
+        }
+        // The peer has read block i - kXBufs from this buffer once its block
+        // i - kXBufs + kSBufs has arrived here (it computed that block into
+        // the score tile it freed after reading block i - kXBufs).
+        if (i >= L::kXBufs) {
+          const int j = i - L::kXBufs + L::kSBufs;
+          ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull + j % L::kXBufs),
+                                                       (j / L::kXBufs) & 1, ctl));
+          if (!ok) break;
+        }
+        // The stores first, so that their way to L2 overlaps the write-back.
+        uint8_t* buf = peer0 + static_cast<size_t>(xb) * L::kXchgBytes;
+        uint4* dst = reinterpret_cast<uint4*>(buf) + h;
+#pragma unroll
+        for (int c = 0; c < L::kPieces; ++c)
+          dst[c * L::kHPad] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        reinterpret_cast<int*>(buf + L::kXchgScaleOff)[h] = ex;
+        // The tile now gets this CTA's partial as the peer will see it.
+        tmem_st32(tile, *reinterpret_cast<float(*)[32]>(x));
+        tmem_st32(tile + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarSRead + sb));
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(peer_full + 8u * static_cast<uint32_t>(xb));
+      }
     }
   } else if (NSPLIT == 2 && warp >= L::kCombWarp0 && warp < L::kGatherWarp0) {
     // ------------------------------------------------------------ combiner
@@ -676,52 +676,52 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
     bool ok = run;
     int G = 0;
     for (int k = 0; ok; ++k) {
-     const int te = k % L::kTokRing;
-     ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarTokFull + te), (k / L::kTokRing) & 1, ctl));
-     if (!ok || tok_t[te] < 0) break;
-     const int nblk = tok_blocks(te);
-     __syncwarp();
-     if (lane == 0) mbar_arrive(bar(L::kBarTokEmpty + te));
-     for (int ib = 0; ib < nblk; ++ib, ++G) {
-      const int i = G;  // position in the CTA's block sequence
-      const int sb = i % L::kSBufs;
-      const int xb = i % L::kXBufs;
-      ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull + xb),
-                                                   (i / L::kXBufs) & 1, ctl));
-      if (!ok) break;
-      const uint8_t* buf = recv0 + static_cast<size_t>(xb) * L::kXchgBytes;
-      const uint4* src = reinterpret_cast<const uint4*>(buf) + h;
-      uint4 y[L::kPieces];
+      const int te = k % L::kTokRing;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarTokFull + te), (k / L::kTokRing) & 1, ctl));
+      if (!ok || tok_t[te] < 0) break;
+      const int nblk = tok_blocks(te);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::kBarTokEmpty + te));
+      for (int ib = 0; ib < nblk; ++ib, ++G) {
+        const int i = G;  // position in the CTA's block sequence
+        const int sb = i % L::kSBufs;
+        const int xb = i % L::kXBufs;
+        ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::kBarRecvFull + xb),
+                                                     (i / L::kXBufs) & 1, ctl));
+        if (!ok) break;
+        const uint8_t* buf = recv0 + static_cast<size_t>(xb) * L::kXchgBytes;
+        const uint4* src = reinterpret_cast<const uint4*>(buf) + h;
+        uint4 y[L::kPieces];
 #pragma unroll
-      for (int c = 0; c < L::kPieces; ++c) y[c] = __ldcg(src + c * L::kHPad);
-      const float pinv = pow2f(__ldcg(reinterpret_cast<const int*>(buf + L::kXchgScaleOff) + h) - 14);
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSRead + sb), (i / L::kSBufs) & 1, ctl));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t tile = tmem + lane_base + L::kTmemS + sb * L::kBI;
+        for (int c = 0; c < L::kPieces; ++c) y[c] = __ldcg(src + c * L::kHPad);
+        const float pinv = pow2f(__ldcg(reinterpret_cast<const int*>(buf + L::kXchgScaleOff) + h) - 14);
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSRead + sb), (i / L::kSBufs) & 1, ctl));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t tile = tmem + lane_base + L::kTmemS + sb * L::kBI;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float x[32];
-        tmem_ld32(tile + 32 * half, x);
+        for (int half = 0; half < 2; ++half) {
+          float x[32];
+          tmem_ld32(tile + 32 * half, x);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 yc = y[4 * half + c];
-          const uint32_t ya[4] = {yc.x, yc.y, yc.z, yc.w};
+          for (int c = 0; c < 4; ++c) {
+            const uint4 yc = y[4 * half + c];
+            const uint32_t ya[4] = {yc.x, yc.y, yc.z, yc.w};
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 pv = bfp16_unpack(ya[k], pinv);
-            const int j = 8 * c + 2 * k;
-            const float2 sum = add2(make_float2(x[j], x[j + 1]), pv);
-            x[j] = sum.x;
-            x[j + 1] = sum.y;
+            for (int k = 0; k < 4; ++k) {
+              const float2 pv = bfp16_unpack(ya[k], pinv);
+              const int j = 8 * c + 2 * k;
+              const float2 sum = add2(make_float2(x[j], x[j + 1]), pv);
+              x[j] = sum.x;
+              x[j + 1] = sum.y;
+            }
           }
+          tmem_st32(tile + 32 * half, x);
         }
-        tmem_st32(tile + 32 * half, x);
+        // The peer's values are consumed (see the flow-control note above).
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarSSum + sb));
       }
-      // The peer's values are consumed (see the flow-control note above).
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarSSum + sb));
-     }
     }
   } else if (warp < L::kSoftmaxThreads / 32) {
     // ------------------------------------------------------------ softmax
@@ -740,155 +740,155 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
     bool ok = run;
     int G = 0;  // blocks so far
     for (int tk = 0; ok; ++tk) {
-     const int te = tk % L::kTokRing;
-     ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarTokFull + te), (tk / L::kTokRing) & 1, ctl));
-     if (!ok) break;
-     const int t = tok_t[te];
-     if (t < 0) break;
-     const int nblk = tok_blocks(te);
-     __syncwarp();
-     if (lane == 0) mbar_arrive(bar(L::kBarTokEmpty + te));
-     float m_run = -INFINITY;
-     float l_run = 0.f;
-     for (int ib = 0; ib < nblk; ++ib, ++G) {
-      const int i = G;  // position in the CTA's block sequence
-      const int sb = i % L::kSBufs;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar((NSPLIT == 2 ? L::kBarSSum : L::kBarSFull) + sb),
-                                             (i / L::kSBufs) & 1, ctl));
+      const int te = tk % L::kTokRing;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarTokFull + te), (tk / L::kTokRing) & 1, ctl));
       if (!ok) break;
-      tc_fence_after();
-      // The scores imply that the block's kv stage (and its valid-slot mask)
-      // has landed; its full barrier is tested only to order the mask read.
-      const int st = i % L::kStages;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarKvFull + st), (i / L::kStages) & 1, ctl));
-      if (!ok) break;
-      const uint32_t msk0 = vmask[2 * st];
-      const uint32_t msk1 = vmask[2 * st + 1];
-      float x[64];
-      tmem_ld32x2(tmem + lane_base + L::kTmemS + sb * L::kBI,
-                  tmem + lane_base + L::kTmemS + sb * L::kBI + 32,
-                  *reinterpret_cast<float(*)[32]>(x), *reinterpret_cast<float(*)[32]>(x + 32));
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarSFree + sb));
-      // Scale (unless the tile already holds the exp2 argument), then mask
-      // (a block whose 64 slots are all valid has nothing to mask).
-      if (NSPLIT == 1 || p.ref_round) {
-#pragma unroll
-        for (int j = 0; j < 64; ++j) x[j] = (x[j] * s1) * s2;
-      }
-      if ((msk0 & msk1) != 0xffffffffu) {
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const uint32_t bit = ((j < 32 ? msk0 : msk1) >> (j & 31)) & 1u;
-          x[j] = bit ? x[j] : -INFINITY;
-        }
-      }
-      const float mloc = max_n<64>(x);
-      const float m_new = fmaxf(m_run, mloc);
-      const bool bump = (m_run == -INFINITY) ? (m_new != -INFINITY) : (m_new > m_run + 8.f);
-      float alpha = 1.f;
-      if (bump) {
-        alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_new);
-        l_run *= alpha;
-        m_run = m_new;
-      }
-      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      const float2 nm2 = make_float2(-m_use, -m_use);
-      // P buffer i % 2 was last read by P.V of block i-2.
-      if (i >= 2) {
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(bar(L::kBarODone + (i & 1)), ((i - 2) >> 1) & 1, ctl));
+      const int t = tok_t[te];
+      if (t < 0) break;
+      const int nblk = tok_blocks(te);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::kBarTokEmpty + te));
+      float m_run = -INFINITY;
+      float l_run = 0.f;
+      for (int ib = 0; ib < nblk; ++ib, ++G) {
+        const int i = G;  // position in the CTA's block sequence
+        const int sb = i % L::kSBufs;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar((NSPLIT == 2 ? L::kBarSSum : L::kBarSFull) + sb),
+                                               (i / L::kSBufs) & 1, ctl));
         if (!ok) break;
         tc_fence_after();
-      }
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int w = 0; w < 16; ++w) {
-          const float2 d = add2(make_float2(x[32 * half + 2 * w], x[32 * half + 2 * w + 1]), nm2);
-          const float p0 = fast_exp2(d.x);
-          const float p1 = fast_exp2(d.y);
-          pk[w] = pack_bf16x2(p0, p1);
-          rs[w & 3] += p0 + p1;  // fp32 probabilities: the LSE must not carry bf16 rounding
-        }
-        tmem_st16u(tmem + lane_base + L::kTmemP + static_cast<uint32_t>(i & 1) * (L::kBI / 2) +
-                       16 * half, pk);
-      }
-      l_run += (rs[0] + rs[1]) + (rs[2] + rs[3]);
-      // O was accumulated against the old max: once P.V of block i-1 has
-      // completed, rescale this row before P.V of block i may start (whole
-      // warp, since TMEM accesses are warp-collective; rows without a bump
-      // use 1).
-      const bool need_rescale = bump && alpha != 0.f && ib > 0;
-      if (__any_sync(0xffffffffu, need_rescale)) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + ((i - 1) & 1)),
-                                               ((i - 1) >> 1) & 1, ctl));
+        // The scores imply that the block's kv stage (and its valid-slot mask)
+        // has landed; its full barrier is tested only to order the mask read.
+        const int st = i % L::kStages;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarKvFull + st), (i / L::kStages) & 1, ctl));
         if (!ok) break;
-        tc_fence_after();
-        const float a = need_rescale ? alpha : 1.f;
-#pragma unroll 1
-        for (int c = 0; c < DC / 32; ++c) {
-          float v[32];
-          tmem_ld32(tmem + lane_base + L::kTmemO + c * 32, v);
+        const uint32_t msk0 = vmask[2 * st];
+        const uint32_t msk1 = vmask[2 * st + 1];
+        float x[64];
+        tmem_ld32x2(tmem + lane_base + L::kTmemS + sb * L::kBI,
+                    tmem + lane_base + L::kTmemS + sb * L::kBI + 32,
+                    *reinterpret_cast<float(*)[32]>(x), *reinterpret_cast<float(*)[32]>(x + 32));
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarSFree + sb));
+        // Scale (unless the tile already holds the exp2 argument), then mask
+        // (a block whose 64 slots are all valid has nothing to mask).
+        if (NSPLIT == 1 || p.ref_round) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] *= a;
-          tmem_st32(tmem + lane_base + L::kTmemO + c * 32, v);
+          for (int j = 0; j < 64; ++j) x[j] = (x[j] * s1) * s2;
         }
-      }
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarPFull + (i & 1)));
-     }
-     if (!ok) break;
-     // The token's last P.V, then O (normalised, bf16) straight from TMEM
-     // to its rows with 16-byte stores (the kv ring, which used to stage it
-     // for a TMA store, already holds the next token's rows), and the LSE.
-     if (nblk > 0) {
-       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + ((G - 1) & 1)),
-                                              ((G - 1) >> 1) & 1, ctl));
-       if (!ok) break;
-       tc_fence_after();
-     }
-     const float sink2 = h < p.H ? __ldg(p.sink + h) * 1.4426950408889634f : 0.f;
-     const float m_fin = fmaxf(m_run, sink2);
-     const float so = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_fin);
-     const float Z = l_run * so + fast_exp2(sink2 - m_fin);
-     const float inv = so / Z;
-     __nv_bfloat16* orow = p.o + (static_cast<size_t>(t) * p.H + h) * D + static_cast<size_t>(rank) * DC;
+        if ((msk0 & msk1) != 0xffffffffu) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            const uint32_t bit = ((j < 32 ? msk0 : msk1) >> (j & 31)) & 1u;
+            x[j] = bit ? x[j] : -INFINITY;
+          }
+        }
+        const float mloc = max_n<64>(x);
+        const float m_new = fmaxf(m_run, mloc);
+        const bool bump = (m_run == -INFINITY) ? (m_new != -INFINITY) : (m_new > m_run + 8.f);
+        float alpha = 1.f;
+        if (bump) {
+          alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_new);
+          l_run *= alpha;
+          m_run = m_new;
+        }
+        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        const float2 nm2 = make_float2(-m_use, -m_use);
+        // P buffer i % 2 was last read by P.V of block i-2.
+        if (i >= 2) {
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(bar(L::kBarODone + (i & 1)), ((i - 2) >> 1) & 1, ctl));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        float rs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int w = 0; w < 16; ++w) {
+            const float2 d = add2(make_float2(x[32 * half + 2 * w], x[32 * half + 2 * w + 1]), nm2);
+            const float p0 = fast_exp2(d.x);
+            const float p1 = fast_exp2(d.y);
+            pk[w] = pack_bf16x2(p0, p1);
+            rs[w & 3] += p0 + p1;  // fp32 probabilities: the LSE must not carry bf16 rounding
+          }
+          tmem_st16u(tmem + lane_base + L::kTmemP + static_cast<uint32_t>(i & 1) * (L::kBI / 2) +
+                         16 * half, pk);
+        }
+        l_run += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+        // O was accumulated against the old max: once P.V of block i-1 has
+        // completed, rescale this row before P.V of block i may start (whole
+        // warp, since TMEM accesses are warp-collective; rows without a bump
+        // use 1).
+        const bool need_rescale = bump && alpha != 0.f && ib > 0;
+        if (__any_sync(0xffffffffu, need_rescale)) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + ((i - 1) & 1)),
+                                                 ((i - 1) >> 1) & 1, ctl));
+          if (!ok) break;
+          tc_fence_after();
+          const float a = need_rescale ? alpha : 1.f;
 #pragma unroll 1
-     for (int c = 0; c < DC / 32; ++c) {
-       float v[32];
-       if (nblk > 0) {
-         tmem_ld32(tmem + lane_base + L::kTmemO + c * 32, v);
-       } else {  // no valid slot: O was never written, the output is 0
+          for (int c = 0; c < DC / 32; ++c) {
+            float v[32];
+            tmem_ld32(tmem + lane_base + L::kTmemO + c * 32, v);
 #pragma unroll
-         for (int kk = 0; kk < 32; ++kk) v[kk] = 0.f;
-       }
-       if (h < p.H) {
-         uint32_t w[16];
+            for (int k = 0; k < 32; ++k) v[k] *= a;
+            tmem_st32(tmem + lane_base + L::kTmemO + c * 32, v);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarPFull + (i & 1)));
+      }
+      if (!ok) break;
+      // The token's last P.V, then O (normalised, bf16) straight from TMEM
+      // to its rows with 16-byte stores (the kv ring, which used to stage it
+      // for a TMA store, already holds the next token's rows), and the LSE.
+      if (nblk > 0) {
+         ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + ((G - 1) & 1)),
+                                                ((G - 1) >> 1) & 1, ctl));
+         if (!ok) break;
+         tc_fence_after();
+      }
+      const float sink2 = h < p.H ? __ldg(p.sink + h) * 1.4426950408889634f : 0.f;
+      const float m_fin = fmaxf(m_run, sink2);
+      const float so = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_fin);
+      const float Z = l_run * so + fast_exp2(sink2 - m_fin);
+      const float inv = so / Z;
+      __nv_bfloat16* orow = p.o + (static_cast<size_t>(t) * p.H + h) * D + static_cast<size_t>(rank) * DC;
+#pragma unroll 1
+      for (int c = 0; c < DC / 32; ++c) {
+         float v[32];
+         if (nblk > 0) {
+           tmem_ld32(tmem + lane_base + L::kTmemO + c * 32, v);
+         } else {  // no valid slot: O was never written, the output is 0
 #pragma unroll
-         for (int u = 0; u < 16; ++u) {
-           const float2 y = mul2(make_float2(v[2 * u], v[2 * u + 1]), make_float2(inv, inv));
-           w[u] = pack_bf16x2(y.x, y.y);
+           for (int kk = 0; kk < 32; ++kk) v[kk] = 0.f;
          }
-         if (o32) {  // 32-byte stores: half the transactions of 16-byte ones
-           st_global_v8(orow + 32 * c, *reinterpret_cast<const uint32_t(*)[8]>(w));
-           st_global_v8(orow + 32 * c + 16, *reinterpret_cast<const uint32_t(*)[8]>(w + 8));
-         } else {
-           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+         if (h < p.H) {
+           uint32_t w[16];
 #pragma unroll
-           for (int kk = 0; kk < 4; ++kk)
-             dst[kk] = make_uint4(w[4 * kk], w[4 * kk + 1], w[4 * kk + 2], w[4 * kk + 3]);
+           for (int u = 0; u < 16; ++u) {
+             const float2 y = mul2(make_float2(v[2 * u], v[2 * u + 1]), make_float2(inv, inv));
+             w[u] = pack_bf16x2(y.x, y.y);
+           }
+           if (o32) {  // 32-byte stores: half the transactions of 16-byte ones
+             st_global_v8(orow + 32 * c, *reinterpret_cast<const uint32_t(*)[8]>(w));
+             st_global_v8(orow + 32 * c + 16, *reinterpret_cast<const uint32_t(*)[8]>(w + 8));
+           } else {
+             uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+             for (int kk = 0; kk < 4; ++kk)
+               dst[kk] = make_uint4(w[4 * kk], w[4 * kk + 1], w[4 * kk + 2], w[4 * kk + 3]);
+           }
          }
-       }
-     }
-     if (nblk > 0) {
-       // O is in registers: the next token's first P.V may overwrite it.
-       tc_fence_before();
-       mbar_arrive(bar(L::kBarOFree));
-     }
-     if (rank == 0 && h < p.H) p.lse[static_cast<size_t>(t) * p.H + h] = m_fin + log2f(Z);
+      }
+      if (nblk > 0) {
+         // O is in registers: the next token's first P.V may overwrite it.
+         tc_fence_before();
+         mbar_arrive(bar(L::kBarOFree));
+      }
+      if (rank == 0 && h < p.H) p.lse[static_cast<size_t>(t) * p.H + h] = m_fin + log2f(Z);
     }
   }
 
