@@ -93,12 +93,13 @@ typedef struct {
 
 /*
  * Bytes of device workspace smqa_fwd needs for `shape`: 0 when D = 64; for
- * D = 512 the exchange pool (4 KB of slot flags + 96 slots of 198 KB).  For
- * D = 512 each token is handled by a pair of CTAs that own one half of D
- * each; every 64-slot block they trade their partial scores through a slot
- * of this pool (it stays in L2).  The contents need no initialisation:
- * smqa_fwd clears the slot flags on its stream.  Returns 0 for an
- * unsupported shape.
+ * D = 512 the exchange pool (4 KB of slot flags and the token counter + 96
+ * slots of 198 KB).  For D = 512 pairs of CTAs that own one half of D each
+ * work through the tokens, taking them one at a time from the counter;
+ * every 64-slot block a pair trades its partial scores through its slot of
+ * this pool (it stays in L2).  The contents need no initialisation:
+ * smqa_fwd clears the slot flags and the counter on its stream.  Returns 0
+ * for an unsupported shape.
  */
 size_t smqa_fwd_workspace_bytes(smqa_shape shape);
 
@@ -144,14 +145,15 @@ size_t smqa_bwd_workspace_bytes(smqa_shape shape, unsigned flags);
 
 /*
  * Bytes of the exchange pool the main backward kernel uses for `shape`
- * (0 when D = 64; 4 KB of slot flags + 96 slots of 132 KB when D = 512).
- * For D = 512 each token is handled by a pair of CTAs that own one half of D
- * each; every 64-slot block they trade their partial scores and dP, in block
+ * (0 when D = 64; 4 KB of slot flags and the token counter + 96 slots of
+ * 132 KB when D = 512).  For D = 512 pairs of CTAs that own one half of D
+ * each work through the tokens, taking them one at a time from the counter;
+ * every 64-slot block a pair trades its partial scores and dP, in block
  * floating point (16-bit mantissas with one power-of-two exponent per head
  * and block, so the precision is relative to the block's largest value at any
- * magnitude), through a slot of this pool (it stays in L2).  The pool's contents need no
- * initialisation: smqa_bwd_main clears the slot flags on its stream.
- * Returns 0 for an unsupported shape.
+ * magnitude), through its slot of this pool (it stays in L2).  The pool's
+ * contents need no initialisation: smqa_bwd_main clears the slot flags and
+ * the counter on its stream.  Returns 0 for an unsupported shape.
  */
 size_t smqa_bwd_exchange_bytes(smqa_shape shape);
 
