@@ -11,9 +11,9 @@
 // Design.  The token's H heads are the M = 128 rows of every MMA (heads
 // beyond H are zero rows), so the heads sharing one gathered kv block form a
 // real GEMM for the tcgen05 tensor core.  Slots go in blocks of 64.
-//   * D = 512: a cluster of two CTAs per token.  CTA r owns the column half
-//     [256r, 256r+256) of Q, of every gathered kv row and of O (its O
-//     accumulator, 128 x 256 fp32, is half of TMEM).  Per block it computes
+//   * D = 512: a cluster of two CTAs works on each token.  CTA r owns the
+//     column half [256r, 256r+256) of Q, of every gathered kv row and of O
+//     (its O accumulator, 128 x 256 fp32, is half of TMEM).  Per block it computes
 //     the partial scores over its half, S_r = Q_r.K_r^T, and the pair trades
 //     them through an L2-resident exchange slot: each CTA scales its partial
 //     into the exp2 domain and sends it in block floating point (per head
@@ -39,7 +39,8 @@
 //     scores, exchange and softmax run while the current one's last P.V and
 //     O read-out finish; O goes from TMEM straight to global memory with
 //     32-byte stores.
-//   * D = 64: one CTA per token (static order), no exchange.
+//   * D = 64: single persistent CTAs, no exchange; CTA c takes tokens c,
+//     c + grid, ... (static order, no counter).
 //   * Warp roles (D = 512; for D = 64 the combiner and sender warps are
 //     absent): warps 8-10 gather this CTA's half of the kv rows with
 //     16-byte cp.async (coalesced 512-byte row pieces written into the
