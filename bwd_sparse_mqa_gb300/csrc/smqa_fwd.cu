@@ -843,13 +843,15 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
       }
       if (!ok) break;
       // The token's last P.V, then O (normalised, bf16) straight from TMEM
-      // to its rows with 16-byte stores (the kv ring, which used to stage it
+      // to its rows with 32-byte stores (the kv ring, which used to stage it
       // for a TMA store, already holds the next token's rows), and the LSE.
+      // 64 columns per TMEM trip (one wait for two loads; 32 at a time:
+      // 4.65 against 4.60 ms on the headline workload).
       if (nblk > 0) {
-         ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + ((G - 1) & 1)),
-                                                ((G - 1) >> 1) & 1, ctl));
-         if (!ok) break;
-         tc_fence_after();
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + ((G - 1) & 1)),
+                                               ((G - 1) >> 1) & 1, ctl));
+        if (!ok) break;
+        tc_fence_after();
       }
       const float sink2 = h < p.H ? __ldg(p.sink + h) * 1.4426950408889634f : 0.f;
       const float m_fin = fmaxf(m_run, sink2);
@@ -858,36 +860,42 @@ __global__ void __launch_bounds__(NSPLIT == 2 ? 512 : 256, 1)
       const float inv = so / Z;
       __nv_bfloat16* orow = p.o + (static_cast<size_t>(t) * p.H + h) * D + static_cast<size_t>(rank) * DC;
 #pragma unroll 1
-      for (int c = 0; c < DC / 32; ++c) {
-         float v[32];
-         if (nblk > 0) {
-           tmem_ld32(tmem + lane_base + L::kTmemO + c * 32, v);
-         } else {  // no valid slot: O was never written, the output is 0
+      for (int c2 = 0; c2 < DC / 64; ++c2) {
+        float v2[2][32];
+        if (nblk > 0) {
+          tmem_ld32x2(tmem + lane_base + L::kTmemO + c2 * 64,
+                      tmem + lane_base + L::kTmemO + c2 * 64 + 32, v2[0], v2[1]);
+        } else {  // no valid slot: O was never written, the output is 0
 #pragma unroll
-           for (int kk = 0; kk < 32; ++kk) v[kk] = 0.f;
-         }
-         if (h < p.H) {
-           uint32_t w[16];
+          for (int kk = 0; kk < 32; ++kk) v2[0][kk] = v2[1][kk] = 0.f;
+        }
 #pragma unroll
-           for (int u = 0; u < 16; ++u) {
-             const float2 y = mul2(make_float2(v[2 * u], v[2 * u + 1]), make_float2(inv, inv));
-             w[u] = pack_bf16x2(y.x, y.y);
-           }
-           if (o32) {  // 32-byte stores: half the transactions of 16-byte ones
-             st_global_v8(orow + 32 * c, *reinterpret_cast<const uint32_t(*)[8]>(w));
-             st_global_v8(orow + 32 * c + 16, *reinterpret_cast<const uint32_t(*)[8]>(w + 8));
-           } else {
-             uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * c2 + cc;
+          const float* v = v2[cc];
+          if (h < p.H) {
+            uint32_t w[16];
 #pragma unroll
-             for (int kk = 0; kk < 4; ++kk)
-               dst[kk] = make_uint4(w[4 * kk], w[4 * kk + 1], w[4 * kk + 2], w[4 * kk + 3]);
-           }
-         }
+            for (int u = 0; u < 16; ++u) {
+              const float2 y = mul2(make_float2(v[2 * u], v[2 * u + 1]), make_float2(inv, inv));
+              w[u] = pack_bf16x2(y.x, y.y);
+            }
+            if (o32) {  // 32-byte stores: half the transactions of 16-byte ones
+              st_global_v8(orow + 32 * c, *reinterpret_cast<const uint32_t(*)[8]>(w));
+              st_global_v8(orow + 32 * c + 16, *reinterpret_cast<const uint32_t(*)[8]>(w + 8));
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                dst[kk] = make_uint4(w[4 * kk], w[4 * kk + 1], w[4 * kk + 2], w[4 * kk + 3]);
+            }
+          }
+        }
       }
       if (nblk > 0) {
-         // O is in registers: the next token's first P.V may overwrite it.
-         tc_fence_before();
-         mbar_arrive(bar(L::kBarOFree));
+        // O is in registers: the next token's first P.V may overwrite it.
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarOFree));
       }
       if (rank == 0 && h < p.H) p.lse[static_cast<size_t>(t) * p.H + h] = m_fin + log2f(Z);
     }
