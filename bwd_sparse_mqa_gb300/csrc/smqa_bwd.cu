@@ -979,9 +979,10 @@ __global__ void __launch_bounds__(480, 1)
         }
       }
       if (!ok) break;
-      // dQ of the token, bf16, straight from TMEM to its rows (16-byte
-      // stores; 32 columns per TMEM load -- 64 at a time cost 0.8 %, through
-      // the drain loop's registers); a token without a valid slot gets zeros.
+      // dQ of the token, bf16, straight from TMEM to its rows (32-byte
+      // stores, 16-byte ones when dq is not 32-byte aligned; 32 columns per
+      // TMEM load -- 64 at a time cost 0.8 %, through the drain loop's
+      // registers); a token without a valid slot gets zeros.
       if (nblk > 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDqDone), a & 1, ctl));
         if (!ok) break;
